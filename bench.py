@@ -1,0 +1,380 @@
+"""Benchmark: causal GQA + RoPE attention, forward + backward, TFLOP/s.
+
+One step = forward + backward of every layer of the GPU-pipeline workload (B=16,
+T=512, Hq=12, Hkv=4, D=64, bf16, 16 layers with distinct buffers, so the 16 x 115 MB
+working set is far larger than L2 and every step reads from HBM).  FLOPs per layer
+count exact causal pairs: 14 * D * T(T+1)/2 * B * Hq (4 D forward, 10 D backward).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the
+attention of independent sequences needs no exchange); the timed region is bracketed
+by a barrier and the max over ranks is reported.  `--impl reference` times the fp64
+CPU oracle on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal GQA+RoPE attn fwd+bwd TFLOP/s (B16 T512 Hq12/Hkv4 D64 bf16), % of peak"
+KERNELS_PER_LAYER = 4          # forward, Delta preprocess, backward main, dQ epilogue
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", type=int, default=2, help="workload id (see synthetic.WORKLOADS)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ distributed harness
+class Harness:
+    """Rank bookkeeping.  Collectives here only synchronise the timing (barrier, max
+    of the step time); the attention itself never communicates."""
+
+    def __init__(self, backend: str):
+        import torch.distributed as dist
+        self.dist = dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        if self.world > 1 and not dist.is_initialized():
+            dist.init_process_group(backend)
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1 and self.dist.is_initialized():
+            self.dist.destroy_process_group()
+
+
+def shard_layers(layers: int, world: int, rank: int):
+    """Replicas: every rank runs all layers on its own copy (weak scaling)."""
+    return list(range(layers))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks / profile data
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": d.get("bf16_tflops"), "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d.get("hbm_gbs"), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(kernel_source: str, key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current source of the kernel (matched by the source file's sha256)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(key)
+    if not ent:
+        return None
+    with open(kernel_source, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return ent["dram_bytes_per_launch"] if ent.get("source_sha256") == sha else None
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample(w, rows: int = 4):
+    """A bounded sample of the workload for the CPU oracle: the first `rows` batch rows
+    of layer 0, every head (so the oracle's OpenMP loops over (batch, head) and
+    (batch, kv head) have 48 and 16 independent units)."""
+    from causal_gqa_flash_attention_gb300 import synthetic
+    q, k, v, dO = synthetic.make_inputs(w, layer=0, batch=slice(0, rows))
+    arrs = [t.double().numpy() for t in (q, k, v, dO)]
+    flops = 14 * w.D * w.pairs * rows * w.Hq
+    desc = f"layer 0, batch rows 0..{rows - 1}, all {w.Hq} query / {w.Hkv} kv heads, T={w.T}, D={w.D}, fp64"
+    return arrs, flops, desc
+
+
+def cpu_baseline(w, seconds_target=10.0):
+    """The fp64 oracle, as it stands, on a bounded sample (forward + backward),
+    repeated until ~seconds_target of host time."""
+    import oracle
+    oracle.build()
+    (qn, kn, vn, dn), flops, desc = oracle_sample(w)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attn_fwd(qn, kn, vn, w.theta)
+        oracle.attn_bwd(qn, kn, vn, dn, w.theta)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target or n >= 1000:
+            break
+    return {"value": flops * n / el / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{desc}; fwd+bwd x{n} in {el:.1f} s"}
+
+
+def run_reference(args, w):
+    """--impl reference: the fp64 CPU oracle on the host cores, timed per step on a
+    bounded sample of the workload (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    (q, k, v, dO), flops, sample = oracle_sample(w)
+    for _ in range(args.warmup):
+        oracle.attn_fwd(q, k, v, w.theta)
+        oracle.attn_bwd(q, k, v, dO, w.theta)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attn_fwd(q, k, v, w.theta)
+        oracle.attn_bwd(q, k, v, dO, w.theta)
+    el = time.perf_counter() - t0
+    val = flops * args.steps / el / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": sample},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, w):
+    import torch
+
+    import causal_gqa_flash_attention_gb300 as ne
+    from causal_gqa_flash_attention_gb300 import _build, synthetic
+
+    hz = Harness("nccl")
+    torch.cuda.set_device(hz.local_rank)
+    dev = torch.device("cuda", hz.local_rank)
+    if hz.local_rank == 0:
+        _build.build()
+    hz.barrier()
+    ne.load()
+    layers = shard_layers(w.layers, hz.world, hz.rank)
+    dt = w.torch_dtype
+
+    # Inputs resident in HBM (device arm) and pinned host copies (end-to-end arm).
+    host, devs = [], []
+    for L in layers:
+        q, k, v, dO = synthetic.make_inputs(w, layer=L)
+        hq = [t.contiguous().pin_memory() for t in (q, k, v, dO)]
+        host.append(hq)
+        d = [t.to(dev, non_blocking=False) for t in hq]
+        o = torch.empty_like(d[0])
+        lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
+        ws = ne.alloc_workspace(w.B, w.T, w.Hq, w.Hkv, w.D, dev)
+        dq, dk, dv = torch.empty_like(d[0]), torch.empty_like(d[1]), torch.empty_like(d[2])
+        devs.append(dict(q=d[0], k=d[1], v=d[2], dO=d[3], o=o, lse=lse, ws=ws, dq=dq, dk=dk, dv=dv))
+    grads_host = [[torch.empty_like(t).pin_memory() for t in (h[0], h[1], h[2])] for h in host]
+    stream = torch.cuda.current_stream(dev)
+    fw_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in layers]
+    bw_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in layers]
+    fwd_ms, bwd_ms = [], []
+
+    def step(record=False):
+        for i, b in enumerate(devs):
+            if record:
+                fw_ev[i][0].record(stream)
+            ne.attn_fwd(b["q"], b["k"], b["v"], w.theta, o=b["o"], lse=b["lse"])
+            if record:
+                fw_ev[i][1].record(stream)
+                bw_ev[i][0].record(stream)
+            ne.attn_bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["dO"], w.theta, workspace=b["ws"],
+                        dq=b["dq"], dk=b["dk"], dv=b["dv"])
+            if record:
+                bw_ev[i][1].record(stream)
+
+    def step_e2e():
+        for i, b in enumerate(devs):
+            for name, h in zip(("q", "k", "v", "dO"), host[i]):
+                b[name].copy_(h, non_blocking=True)
+            ne.attn_fwd(b["q"], b["k"], b["v"], w.theta, o=b["o"], lse=b["lse"])
+            ne.attn_bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["dO"], w.theta, workspace=b["ws"],
+                        dq=b["dq"], dk=b["dk"], dv=b["dv"])
+            for h, name in zip(grads_host[i], ("dq", "dk", "dv")):
+                h.copy_(b[name], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if ne.get_device_error() != ne.NE_OK:
+        raise RuntimeError("device error during warm-up: " + ne.last_error())
+
+    clocks = ClockSampler(hz.local_rank)
+    clocks.start()
+    hz.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)     # per-layer events; the last step's values are read below
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    hz.barrier()
+    clk = clocks.stop()
+    ms_local = e0.elapsed_time(e1) / args.steps
+    for i in range(len(layers)):
+        fwd_ms.append(fw_ev[i][0].elapsed_time(fw_ev[i][1]))
+        bwd_ms.append(bw_ev[i][0].elapsed_time(bw_ev[i][1]))
+    if ne.get_device_error() != ne.NE_OK:
+        raise RuntimeError("device error during timing: " + ne.last_error())
+    ms = hz.max(ms_local, dev)
+
+    # End-to-end: host buffers, H2D of the inputs and D2H of the gradients inside the step.
+    for _ in range(2):
+        step_e2e()
+    torch.cuda.synchronize(dev)
+    hz.barrier()
+    e2 = max(2, args.steps // 2)
+    t0 = time.perf_counter()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(e2):
+        step_e2e()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    hz.barrier()
+    e2e_ms = hz.max(g0.elapsed_time(g1) / e2, dev)
+
+    flops_step = w.flops() * len(layers)
+    total_flops = flops_step * hz.world
+    value = total_flops / (ms * 1e-3) / 1e12
+    e2e_val = total_flops / (e2e_ms * 1e-3) / 1e12
+    es = 2 if w.dtype == "bf16" else 4
+    h2d = sum(t.numel() * es for h in host for t in h)
+    d2h = sum(t.numel() * es for g in grads_host for t in g)
+
+    peaks = measured_peaks()
+    # Dominant kernel: the backward call (Delta + main + dQ epilogue; the main kernel
+    # dominates it).  Algorithmic FLOPs per launch = 10 D T(T+1)/2 B Hq.
+    bwd_avg = statistics.mean(bwd_ms)
+    fwd_avg = statistics.mean(fwd_ms)
+    peak = peaks["bf16_tflops"]
+    achieved = w.flops_bwd() / (bwd_avg * 1e-3) / 1e12
+    traffic = profiled_traffic(os.path.join(ROOT, "causal_gqa_flash_attention_gb300", "csrc", "attn_bwd.cu"),
+                               f"attn_bwd_kernel:{w.name}")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": hz.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1), layer-distinct buffers)",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "layers_per_step": len(layers), "rope_theta": w.theta,
+                   "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets "
+                         f"({sum(b['q'].numel() + b['k'].numel() * 2 + b['dO'].numel() for b in devs) * es / 1e6:.0f} MB of inputs)",
+                   "parallelism": f"replicas x{hz.world}"},
+        "pct_of_peak": value / hz.world / peak,
+        "roofline": {"kernel": "attn_bwd call (Delta preprocess + main + dQ epilogue)", "bound": "tensor",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{peaks['source']} bf16 burst", "traffic": traffic,
+                     "per_launch_ms": bwd_avg},
+        "kernels": {"attn_fwd_ms": fwd_avg, "attn_fwd_tflops": w.flops_fwd() / (fwd_avg * 1e-3) / 1e12,
+                    "attn_bwd_ms": bwd_avg, "attn_bwd_tflops": achieved},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": KERNELS_PER_LAYER * len(layers) * args.steps,
+        "clocks": clk,
+    }
+    if hz.rank == 0 and not args.no_cpu_baseline and hz.world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    elif hz.rank == 0 and hz.world == 1:
+        line["cpu_baseline"] = None
+    if hz.rank == 0:
+        print(json.dumps(line), flush=True)
+    hz.close()
+
+
+def main():
+    args = parse()
+    from causal_gqa_flash_attention_gb300 import synthetic
+    w = synthetic.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,180 @@
-"""libneattn binding (placeholder until the C-ABI lands)."""
+"""Python binding of libneattn (causal GQA + RoPE flash attention for sm_103a).
+
+Argument marshalling only: every function checks dtypes, shapes and devices, then
+calls the C ABI declared in include/neattn.h with raw device pointers and the
+current torch CUDA stream.  All arithmetic runs in the library's CUDA kernels.  There
+is no CPU fallback: if libneattn.so is missing or no sm_103 device is present the
+calls raise.
+
+Layouts: q, o, dO, dq are [B, T, Hq, D]; k, v, dk, dv are [B, T, Hkv, D]; lse is
+[B, Hq, T] fp32.  bf16 tensors run on bf16 tensor cores, fp32 tensors on TF32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import synthetic  # noqa: F401  (seeded inputs; no attention arithmetic)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libneattn.so")
+_lock = threading.Lock()
+_lib = None
+
+NE_OK, NE_ERR_INVALID_ARG, NE_ERR_UNSUPPORTED, NE_ERR_CUDA, NE_ERR_DEVICE_TIMEOUT, NE_ERR_NO_DEVICE = range(6)
+
+# Every symbol include/neattn.h declares (checked by the tests).
+EXPORTS = (
+    "ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd_workspace_size", "ne_attn_bwd",
+    "ne_attn_bwd_f32", "ne_status_string", "ne_last_error", "ne_get_device_error",
+    "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown",
+)
+
+
+class NeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} [status {status}]")
+        self.status = status
+
+
+def load(path: str | None = None):
+    """Load libneattn.so (built by ``_build.build()``).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"libneattn.so not found at {p}; run __graft_entry__.build() first")
+        lib = ctypes.CDLL(p)
+        vp, i, d, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
+        lib.ne_rope_table.argtypes = [vp, vp, i, i, d, vp]
+        lib.ne_attn_fwd.argtypes = [vp] * 5 + [i] * 5 + [d, vp]
+        lib.ne_attn_fwd_f32.argtypes = lib.ne_attn_fwd.argtypes
+        lib.ne_attn_bwd_workspace_size.argtypes = [i] * 5
+        lib.ne_attn_bwd_workspace_size.restype = sz
+        lib.ne_attn_bwd.argtypes = [vp] * 9 + [i] * 5 + [d, vp, sz, vp]
+        lib.ne_attn_bwd_f32.argtypes = lib.ne_attn_bwd.argtypes
+        lib.ne_status_string.argtypes = [i]
+        lib.ne_status_string.restype = ctypes.c_char_p
+        lib.ne_last_error.argtypes = []
+        lib.ne_last_error.restype = ctypes.c_char_p
+        lib.ne_get_device_error.argtypes = [vp]
+        lib.ne_set_wait_timeout_ms.argtypes = [ctypes.c_uint32]
+        lib.ne_set_wait_timeout_ms.restype = None
+        lib.ne_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+        lib.ne_shutdown.argtypes = []
+        lib.ne_shutdown.restype = None
+        for f in ("ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd", "ne_attn_bwd_f32",
+                  "ne_get_device_error", "ne_selftest_wait_timeout"):
+            getattr(lib, f).restype = i
+        _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != NE_OK:
+        lib = load()
+        raise NeError(status, f"{lib.ne_status_string(status).decode()}: {lib.ne_last_error().decode()}")
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dims(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, T, H, D]")
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, T, Hkv, D) or tuple(v.shape) != (B, T, Hkv, D):
+        raise ValueError(f"k, v must be [B, T, Hkv, D]; got {tuple(k.shape)}, {tuple(v.shape)}")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("dtype must be bfloat16 or float32")
+    return B, T, Hq, Hkv, D
+
+
+def rope_table(T: int, D: int, theta: float = 10000.0, device="cuda"):
+    """cos, sin [T, D/2] fp32 on ``device`` (ne_rope_table)."""
+    lib = load()
+    c = torch.empty((T, D // 2), dtype=torch.float32, device=device)
+    s = torch.empty_like(c)
+    _check(lib.ne_rope_table(_ptr(c), _ptr(s), T, D, float(theta), _stream(c)))
+    return c, s
+
+
+def attn_fwd(q, k, v, theta: float = 10000.0, o=None, lse=None):
+    """Forward: returns (o [B,T,Hq,D], lse [B,Hq,T] fp32)."""
+    lib = load()
+    B, T, Hq, Hkv, D = _dims(q, k, v)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    fn = lib.ne_attn_fwd if q.dtype == torch.bfloat16 else lib.ne_attn_fwd_f32
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, Hq, Hkv, D, float(theta), _stream(q)))
+    return o, lse
+
+
+def workspace_size(B, T, Hq, Hkv, D) -> int:
+    return int(load().ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D))
+
+
+def alloc_workspace(B, T, Hq, Hkv, D, device="cuda"):
+    n = workspace_size(B, T, Hq, Hkv, D)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def attn_bwd(q, k, v, o, lse, dO, theta: float = 10000.0, workspace=None, dq=None, dk=None, dv=None):
+    """Backward: returns (dq, dk, dv) in the input dtype."""
+    lib = load()
+    B, T, Hq, Hkv, D = _dims(q, k, v)
+    for t in (o, dO):
+        if tuple(t.shape) != tuple(q.shape) or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("o and dO must match q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, T) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, Hq, T]")
+    if workspace is None:
+        workspace = alloc_workspace(B, T, Hq, Hkv, D, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    fn = lib.ne_attn_bwd if q.dtype == torch.bfloat16 else lib.ne_attn_bwd_f32
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+              B, T, Hq, Hkv, D, float(theta), _ptr(workspace), workspace.numel() * workspace.element_size(),
+              _stream(q)))
+    return dq, dk, dv
+
+
+def get_device_error(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device error status."""
+    lib = load()
+    s = torch.cuda.current_stream(device).cuda_stream
+    return int(lib.ne_get_device_error(ctypes.c_void_p(s)))
+
+
+def set_wait_timeout_ms(ms: int):
+    load().ne_set_wait_timeout_ms(int(ms))
+
+
+def selftest_wait_timeout(timeout_ms: int = 50):
+    lib = load()
+    _check(lib.ne_selftest_wait_timeout(int(timeout_ms), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+
+
+def last_error() -> str:
+    return load().ne_last_error().decode()
+
+
+def shutdown():
+    load().ne_shutdown()

@@ -1,0 +1,402 @@
+// api.cu -- the C ABI declared in include/neattn.h: argument validation, status
+// codes, per-device caches (RoPE tables, device error word), TMA tensor-map encoding
+// and kernel launches.  No compute happens here; every step runs in the kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "kernels.h"
+#include "neattn.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ne_status fail(ne_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+ne_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(NE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------------ per-device state
+struct DeviceState {
+    int* err_word = nullptr;                                           // device int
+    std::map<std::tuple<int, int, uint64_t>, float2*> rope;            // (T, D, theta bits)
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+uint32_t g_timeout_ms = 0;   // 0 = default
+
+unsigned long long timeout_ns() {
+    uint32_t ms = g_timeout_ms;
+    if (ms == 0) {
+        const char* env = std::getenv("NE_ATTN_TIMEOUT_MS");
+        long v = env ? std::strtol(env, nullptr, 10) : 0;
+        ms = v > 0 ? (uint32_t)v : 2000u;
+    }
+    return (unsigned long long)ms * 1000000ull;
+}
+
+ne_status current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return fail(NE_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev);
+    if (major != 10 || minor != 3)
+        return fail(NE_ERR_NO_DEVICE, "device %d is sm_%d%d; libneattn is built for sm_103a only", *dev, major,
+                    minor);
+    return NE_OK;
+}
+
+// Device error word of the current device (allocated once).
+ne_status error_word(int dev, int** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& ds = g_dev[dev];
+    if (!ds.err_word) {
+        cudaError_t e = cudaMalloc(&ds.err_word, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+        e = cudaMemset(ds.err_word, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    }
+    *out = ds.err_word;
+    return NE_OK;
+}
+
+// Cached interleaved (cos, sin) table [T, D/2] for the current device.  Built on
+// `st` by the rope kernel the first time; that first build synchronises `st`.
+ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const float2** out) {
+    uint64_t tb;
+    std::memcpy(&tb, &theta, sizeof(tb));
+    const auto key = std::make_tuple(T, D, tb);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto& m = g_dev[dev].rope;
+        auto it = m.find(key);
+        if (it != m.end()) {
+            *out = it->second;
+            return NE_OK;
+        }
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+        return fail(NE_ERR_UNSUPPORTED,
+                    "first call for T=%d D=%d theta=%g on this device happened inside stream capture; "
+                    "make one call before capturing",
+                    T, D, theta);
+    float2* buf = nullptr;
+    size_t bytes = (size_t)T * (D / 2) * sizeof(float2);
+    cudaError_t e = cudaMalloc(&buf, bytes < 16 ? 16 : bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(rope table)");
+    e = ne::launch_rope_table(nullptr, nullptr, buf, T, D, theta, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        cudaFree(buf);
+        return cuda_fail(e, "rope table build");
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto& m = g_dev[dev].rope;
+    auto it = m.find(key);
+    if (it != m.end()) {   // another thread won the race
+        cudaFree(buf);
+        *out = it->second;
+    } else {
+        m[key] = buf;
+        *out = buf;
+    }
+    return NE_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+ne_status encode_fn(EncodeTiledFn* out) {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!fn) return fail(NE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    *out = fn;
+    return NE_OK;
+}
+
+// Tiled map over a [B, T, H, D] tensor: box = (128 bytes of D, 1 head, rows, 1 batch),
+// 128-byte swizzle, zero fill out of bounds (ragged T tails).
+ne_status map_bthd(CUtensorMap* m, const void* ptr, bool f32, int B, int T, int H, int D, int rows) {
+    EncodeTiledFn enc;
+    ne_status s = encode_fn(&enc);
+    if (s != NE_OK) return s;
+    const int es = f32 ? 4 : 2;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es, (cuuint64_t)T * H * D * es};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return NE_OK;
+}
+
+// ------------------------------------------------------------------ validation
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ne_status check_shape(int B, int T, int Hq, int Hkv, int D, double theta, bool f32) {
+    if (B < 0 || T < 0) return fail(NE_ERR_INVALID_ARG, "B and T must be >= 0 (B=%d T=%d)", B, T);
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+        return fail(NE_ERR_INVALID_ARG, "need Hq > 0, Hkv > 0 and Hq %% Hkv == 0 (Hq=%d Hkv=%d)", Hq, Hkv);
+    if (!(theta > 0.0) || !std::isfinite(theta)) return fail(NE_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    if (D <= 0 || D % 2 != 0) return fail(NE_ERR_INVALID_ARG, "D must be even and > 0 (D=%d)", D);
+    if (f32 ? (D != 32 && D != 64) : (D != 64 && D != 128))
+        return fail(NE_ERR_UNSUPPORTED, "head_dim D=%d is not supported for %s (supported: %s)", D,
+                    f32 ? "f32" : "bf16", f32 ? "32, 64" : "64, 128");
+    const long long elems = (long long)B * T * Hq * D;
+    if (elems >= (1LL << 31)) return fail(NE_ERR_INVALID_ARG, "B*T*Hq*D must be < 2^31");
+    return NE_OK;
+}
+
+ne_status check_ptrs(std::initializer_list<const void*> ps) {
+    for (const void* p : ps) {
+        if (!p) return fail(NE_ERR_INVALID_ARG, "null tensor pointer");
+        if (!aligned16(p)) return fail(NE_ERR_INVALID_ARG, "tensor pointer %p is not 16-byte aligned", p);
+    }
+    return NE_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t bwd_ws_bytes(int B, int T, int Hq, int D) {
+    return round_up((size_t)B * Hq * T * sizeof(float), 256) + (size_t)B * T * Hq * D * sizeof(float);
+}
+
+// ------------------------------------------------------------------ forward / backward
+ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
+                        int Hq, int Hkv, int D, double theta, cudaStream_t st) {
+    g_last_error.clear();
+    ne_status s = check_shape(B, T, Hq, Hkv, D, theta, f32);
+    if (s != NE_OK) return s;
+    if (B == 0 || T == 0) return NE_OK;
+    if ((s = check_ptrs({q, k, v, o, lse})) != NE_OK) return s;
+    int dev;
+    if ((s = current_device(&dev)) != NE_OK) return s;
+    int* err;
+    if ((s = error_word(dev, &err)) != NE_OK) return s;
+    const float2* rope;
+    if ((s = rope_cache(dev, T, D, theta, st, &rope)) != NE_OK) return s;
+    CUtensorMap tq, tk, tv, to;
+    const int kv_rows = ne::fwd_kv_box_rows(f32, D);
+    if ((s = map_bthd(&tq, q, f32, B, T, Hq, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tk, k, f32, B, T, Hkv, D, kv_rows)) != NE_OK) return s;
+    if ((s = map_bthd(&tv, v, f32, B, T, Hkv, D, kv_rows)) != NE_OK) return s;
+    if ((s = map_bthd(&to, o, f32, B, T, Hq, D, 128)) != NE_OK) return s;
+    ne::FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.rope = rope;
+    a.T = T;
+    a.Hq = Hq;
+    a.G = Hq / Hkv;
+    a.n_qt = (T + 255) / 256;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    a.err = err;
+    a.timeout_ns = timeout_ns();
+    cudaError_t e = ne::launch_fwd(f32, D, B, tq, tk, tv, to, a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
+    return NE_OK;
+}
+
+ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dO, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
+                        double theta, void* ws, size_t ws_bytes, cudaStream_t st) {
+    g_last_error.clear();
+    ne_status s = check_shape(B, T, Hq, Hkv, D, theta, f32);
+    if (s != NE_OK) return s;
+    if (f32) return fail(NE_ERR_UNSUPPORTED, "the f32 (TF32) backward is not built yet");
+    if (B == 0 || T == 0) return NE_OK;
+    if ((s = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv})) != NE_OK) return s;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return fail(NE_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+    const size_t need = bwd_ws_bytes(B, T, Hq, D);
+    if (ws_bytes < need)
+        return fail(NE_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", ws_bytes, need);
+    int dev;
+    if ((s = current_device(&dev)) != NE_OK) return s;
+    int* err;
+    if ((s = error_word(dev, &err)) != NE_OK) return s;
+    const float2* rope;
+    if ((s = rope_cache(dev, T, D, theta, st, &rope)) != NE_OK) return s;
+    float* delta = static_cast<float*>(ws);
+    float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up((size_t)B * Hq * T * sizeof(float), 256));
+    const long long rows = (long long)B * T * Hq;
+
+    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D};
+    cudaError_t e = ne::launch_bwd_pre(f32, pa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
+
+    CUtensorMap tq, tk, tv, tdo;
+    if ((s = map_bthd(&tq, q, f32, B, T, Hq, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tk, k, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tv, v, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tdo, dO, f32, B, T, Hq, D, 128)) != NE_OK) return s;
+    ne::BwdArgs a;
+    a.lse = lse;
+    a.delta = delta;
+    a.dq_acc = dq_acc;
+    a.dk = dk;
+    a.dv = dv;
+    a.rope = rope;
+    a.T = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.n_kvt = (T + 127) / 128;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    a.scale = (float)(1.0 / std::sqrt((double)D));
+    a.err = err;
+    a.timeout_ns = timeout_ns();
+    e = ne::launch_bwd(f32, D, B, tq, tk, tv, tdo, a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
+
+    ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale};
+    e = ne::launch_bwd_post(f32, qa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dq epilogue launch");
+    return NE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ne_status ne_rope_table(float* cos_out, float* sin_out, int T, int D, double theta, ne_stream_t stream) {
+    g_last_error.clear();
+    if (T < 0 || D <= 0 || D % 2 != 0) return fail(NE_ERR_INVALID_ARG, "need T >= 0 and even D > 0");
+    if (!(theta > 0.0) || !std::isfinite(theta)) return fail(NE_ERR_INVALID_ARG, "theta must be finite and > 0");
+    if (T == 0) return NE_OK;
+    if (!cos_out || !sin_out) return fail(NE_ERR_INVALID_ARG, "null output pointer");
+    int dev;
+    ne_status s = current_device(&dev);
+    if (s != NE_OK) return s;
+    cudaError_t e = ne::launch_rope_table(cos_out, sin_out, nullptr, T, D, theta, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+    return NE_OK;
+}
+
+ne_status ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
+                      int Hkv, int D, double rope_theta, ne_stream_t stream) {
+    return attn_fwd_impl(false, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, (cudaStream_t)stream);
+}
+
+ne_status ne_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int T,
+                          int Hq, int Hkv, int D, double rope_theta, ne_stream_t stream) {
+    return attn_fwd_impl(true, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, (cudaStream_t)stream);
+}
+
+size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D) {
+    if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return 0;
+    return bwd_ws_bytes(B, T, Hq, D);
+}
+
+ne_status ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                      void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                      void* workspace, size_t workspace_bytes, ne_stream_t stream) {
+    return attn_bwd_impl(false, q, k, v, o, lse, dO, dq, dk, dv, B, T, Hq, Hkv, D, rope_theta, workspace,
+                         workspace_bytes, (cudaStream_t)stream);
+}
+
+ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const float* o, const float* lse,
+                          const float* dO, float* dq, float* dk, float* dv, int B, int T, int Hq, int Hkv, int D,
+                          double rope_theta, void* workspace, size_t workspace_bytes, ne_stream_t stream) {
+    return attn_bwd_impl(true, q, k, v, o, lse, dO, dq, dk, dv, B, T, Hq, Hkv, D, rope_theta, workspace,
+                         workspace_bytes, (cudaStream_t)stream);
+}
+
+const char* ne_status_string(ne_status s) {
+    switch (s) {
+        case NE_OK: return "NE_OK";
+        case NE_ERR_INVALID_ARG: return "NE_ERR_INVALID_ARG";
+        case NE_ERR_UNSUPPORTED: return "NE_ERR_UNSUPPORTED";
+        case NE_ERR_CUDA: return "NE_ERR_CUDA";
+        case NE_ERR_DEVICE_TIMEOUT: return "NE_ERR_DEVICE_TIMEOUT";
+        case NE_ERR_NO_DEVICE: return "NE_ERR_NO_DEVICE";
+    }
+    return "NE_UNKNOWN_STATUS";
+}
+
+const char* ne_last_error(void) { return g_last_error.c_str(); }
+
+ne_status ne_get_device_error(ne_stream_t stream) {
+    g_last_error.clear();
+    int dev;
+    ne_status s = current_device(&dev);
+    if (s != NE_OK) return s;
+    int* err;
+    if ((s = error_word(dev, &err)) != NE_OK) return s;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int h = 0;
+    e = cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (h != 0) {
+        e = cudaMemset(err, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+        if (h == ne::SITE_RANGE)
+            return fail(NE_ERR_INVALID_ARG,
+                        "a rotated q or k value exceeded 65504, the fp16 range of the bf16 path's logit operand; "
+                        "the outputs of that call are invalid");
+        return fail(NE_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel ran out (site 0x%x)", h);
+    }
+    return NE_OK;
+}
+
+void ne_set_wait_timeout_ms(uint32_t ms) { g_timeout_ms = ms; }
+
+ne_status ne_selftest_wait_timeout(uint32_t timeout_ms, ne_stream_t stream) {
+    g_last_error.clear();
+    int dev;
+    ne_status s = current_device(&dev);
+    if (s != NE_OK) return s;
+    int* err;
+    if ((s = error_word(dev, &err)) != NE_OK) return s;
+    cudaError_t e = ne::launch_selftest_wait(err, (unsigned long long)timeout_ms * 1000000ull, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+    return NE_OK;
+}
+
+void ne_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_dev) {
+        cudaSetDevice(kv.first);
+        if (kv.second.err_word) cudaFree(kv.second.err_word);
+        for (auto& r : kv.second.rope) cudaFree(r.second);
+    }
+    g_dev.clear();
+    cudaSetDevice(cur);
+}
+
+}  // extern "C"

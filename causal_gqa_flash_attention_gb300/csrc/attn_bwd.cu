@@ -1,0 +1,509 @@
+// attn_bwd.cu -- backward of causal GQA + RoPE attention on tcgen05 tensor cores.
+//
+// The hand-written backward of "NanoEuler: C와 CUDA로 밑바닥부터 구축한 GPT-2 규모의
+// LLM" (검증 및 안정성), for the attention of the same page's 기술 사양 (RoPE, GQA) and
+// 커널 구현 (tiling, no T x T matrix).  With s = 1/sqrt(D), Q' = R Q, K' = R K:
+//   P  = exp(s Q'K'^T - LSE)  (recomputed from the forward's LSE, causal mask)
+//   dV = sum_heads P^T dO,  dP = dO V^T,  dS = P o (dP - Delta),  Delta = rowsum(dO o O)
+//   dK = R^T sum_heads s dS^T Q',  dQ = R^T s dS K'
+// Three kernels on one stream:
+//   bwd_pre   Delta = rowsum(dO o O) (fp32) and zeroing of the fp32 dQ accumulator;
+//   bwd_main  KV-major: one CTA per (batch, kv head, 128-key tile) loops over the G
+//             query heads of its group and every query tile on or after the diagonal.
+//             dK and dV accumulate in TMEM across the whole group (no atomics); each
+//             (head, query tile) step adds its dS K' into the fp32 dQ accumulator;
+//   bwd_post  dQ = s R^T (accumulator), cast to the output dtype.
+//
+// bwd_main warp roles (512 threads):
+//   warp 0      TMA producer: K, V once; Q and dO tiles into a ring.
+//   warp 1      TMEM allocator (all 512 columns) and UMMA issuer.
+//   warps 4-7   RoPE: rotate K once and every Q tile in place.
+//   warps 8-11  thread = key row: P^T and dS^T from S^T, dP^T, LSE, Delta; P^T to TMEM,
+//               dS^T (bf16) to shared memory; at the end dK (inverse rotation) and dV.
+//   warps 12-15 thread = query row: drain dQ from TMEM into the fp32 accumulator.
+#include <cuda_bf16.h>
+#include "kernels.h"
+#include "ptx.cuh"
+#include "rope_smem.cuh"
+
+namespace ne {
+
+namespace {
+
+// ------------------------------------------------------------------------ pre
+// Delta[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]; also zeroes dq_acc.  A group of
+// LPR lanes takes one row (D elements); rows are [B,T,Hq] in memory order.
+template <typename Tin, int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
+    constexpr int EPV = 16 / sizeof(Tin);        // elements per 16-byte vector
+    constexpr int LPR = D / EPV;                 // lanes per row (8 or 16)
+    constexpr int RPW = 32 / LPR;                // rows per warp step
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR, li = lane % LPR;
+    const long long warp_global = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = (gridDim.x * (long long)blockDim.x) >> 5;
+    for (long long r0 = warp_global * RPW; r0 < a.rows; r0 += nwarps * RPW) {
+        const long long row = r0 + sub;
+        float acc = 0.f;
+        if (row < a.rows) {
+            const uint4 ov = reinterpret_cast<const uint4*>(static_cast<const Tin*>(a.o) + row * D)[li];
+            const uint4 gv = reinterpret_cast<const uint4*>(static_cast<const Tin*>(a.dO) + row * D)[li];
+            if constexpr (sizeof(Tin) == 2) {
+                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+                const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 of = __bfloat1622float2(o2[k]), gf = __bfloat1622float2(g2[k]);
+                    acc = fmaf(of.x, gf.x, acc);
+                    acc = fmaf(of.y, gf.y, acc);
+                }
+            } else {
+                acc = __uint_as_float(ov.x) * __uint_as_float(gv.x) + __uint_as_float(ov.y) * __uint_as_float(gv.y) +
+                      __uint_as_float(ov.z) * __uint_as_float(gv.z) + __uint_as_float(ov.w) * __uint_as_float(gv.w);
+            }
+            float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D);
+            for (int k = li; k < D / 4; k += LPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (row < a.rows && li == 0) {
+            const long long t = (row / a.Hq) % a.T, bh = (row / ((long long)a.Hq * a.T)) * a.Hq + row % a.Hq;
+            a.delta[bh * a.T + t] = acc;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------ post
+// dq[row] = s * R_t^T dq_acc[row]; thread = 2 pairs (4 elements).
+template <typename Tout, int D>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const BwdPostArgs a) {
+    const long long n = a.rows * (D / 4);
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long row = idx / (D / 4);
+        const int q4 = (int)(idx % (D / 4));
+        const int t = (int)((row / a.Hq) % a.T);
+        const float4 g = reinterpret_cast<const float4*>(a.dq_acc)[idx];
+        const float4 cs = __ldg(reinterpret_cast<const float4*>(a.rope + (size_t)t * (D / 2) + 2 * q4));
+        const float y0 = a.scale * (g.x * cs.x + g.y * cs.y), y1 = a.scale * (-g.x * cs.y + g.y * cs.x);
+        const float y2 = a.scale * (g.z * cs.z + g.w * cs.w), y3 = a.scale * (-g.z * cs.w + g.w * cs.z);
+        if constexpr (sizeof(Tout) == 2) {
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(y0, y1), p1 = __floats2bfloat162_rn(y2, y3);
+            reinterpret_cast<uint2*>(a.dq)[idx] =
+                make_uint2(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1));
+        } else {
+            reinterpret_cast<float4*>(a.dq)[idx] = make_float4(y0, y1, y2, y3);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------ main
+template <int D>
+struct BwdCfg {
+    static constexpr int ES = 2;
+    static constexpr int BKV = 128;                 // key rows per CTA
+    static constexpr int BQ = 128;                  // query rows per step
+    static constexpr int ROWB = D * ES;
+    static constexpr int NCH = ROWB / 128;
+    static constexpr int EPC = 64;
+    static constexpr int NQS = D <= 64 ? 2 : 1;     // Q/dO stages
+    static constexpr bool DS_ALIASES_Q16 = D > 64;  // dS^T reuses the fp16 Q' buffer
+    static constexpr int KV_BYTES = BKV * ROWB;
+    static constexpr int Q_BYTES = BQ * ROWB;
+    static constexpr int STAGE_BYTES = 3 * Q_BYTES; // Q' (bf16) | Q' (fp16) | dO
+    static constexpr int DS_BYTES = BKV * BQ * 2;   // dS^T bf16 [key][query]
+    static constexpr int SMEM = 1024 + 3 * KV_BYTES + NQS * STAGE_BYTES + (DS_ALIASES_Q16 ? 0 : DS_BYTES);
+    // TMEM columns
+    static constexpr int S_COL = 0;                 // S^T, then P^T (bf16 packed)
+    static constexpr int DP_COL = 128;              // dP^T
+    static constexpr int DV_COL = 256;
+    static constexpr int DK_COL = 256 + D;
+    static constexpr int DQ_COL = D <= 64 ? 256 + 2 * D : 128;  // D = 128 shares dP^T's columns
+    static constexpr bool DQ_ALIASES_DP = D > 64;
+    static constexpr int KSTEPS_D = ROWB / 32;      // K-steps over head_dim
+    static constexpr int KSTEPS_Q = BQ / 16;        // K-steps over query rows
+    static constexpr int KSTEPS_KV = BKV / 16;      // K-steps over key rows
+    static constexpr int THREADS = 512;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(DS_BYTES == Q_BYTES || !DS_ALIASES_Q16, "alias needs equal sizes");
+};
+
+template <int D>
+__global__ void __launch_bounds__(512, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs a) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = smem;                            // K' bf16 (rotated in place)
+    uint8_t* sK16 = sK + C::KV_BYTES;              // K' fp16 (logit operand)
+    uint8_t* sV = sK16 + C::KV_BYTES;
+    uint8_t* sStage = sV + C::KV_BYTES;            // NQS x (Q' bf16 | Q' fp16 | dO)
+    uint8_t* sdS = C::DS_ALIASES_Q16 ? sStage + C::Q_BYTES : sStage + C::NQS * C::STAGE_BYTES;
+    auto stage_q = [&](int s) { return sStage + s * C::STAGE_BYTES; };
+    auto stage_q16 = [&](int s) { return sStage + s * C::STAGE_BYTES + C::Q_BYTES; };
+    auto stage_do = [&](int s) { return sStage + s * C::STAGE_BYTES + 2 * C::Q_BYTES; };
+
+    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_s_full, bar_dp_full, bar_ds_ready,
+        bar_ds_free, bar_dq_full, bar_dq_free, bar_dkv_full, bar_final;
+    __shared__ __align__(8) uint64_t bar_qdo_full[C::NQS], bar_q_ready[C::NQS], bar_qdo_empty[C::NQS];
+    __shared__ __align__(8) uint64_t bar_rows[2];   // LSE/Delta of a query tile staged (double buffer)
+    __shared__ float s_lse[2][C::BQ], s_delta[2][C::BQ];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hkv = blockIdx.x, b = blockIdx.y, j = blockIdx.z;
+    const int T = a.T, G = a.G;
+    const int kv0 = j * C::BKV;
+    const int n_qt = (T + C::BQ - 1) / C::BQ;
+    const int i_first = kv0 / C::BQ;
+    const int per_head = n_qt - i_first;
+    const int n_it = G * per_head;
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar_kv_full), 1);
+        mbar_init(smem_u32(&bar_k_ready), 128);
+        mbar_init(smem_u32(&bar_s_full), 1);
+        mbar_init(smem_u32(&bar_dp_full), 1);
+        mbar_init(smem_u32(&bar_ds_ready), 128);
+        mbar_init(smem_u32(&bar_ds_free), 1);
+        mbar_init(smem_u32(&bar_dq_full), 1);
+        mbar_init(smem_u32(&bar_dq_free), 128);
+        mbar_init(smem_u32(&bar_dkv_full), 1);
+        mbar_init(smem_u32(&bar_final), 1);
+        mbar_init(smem_u32(&bar_rows[0]), 128);
+        mbar_init(smem_u32(&bar_rows[1]), 128);
+        for (int s = 0; s < C::NQS; ++s) {
+            mbar_init(smem_u32(&bar_qdo_full[s]), 1);
+            mbar_init(smem_u32(&bar_q_ready[s]), 128);
+            mbar_init(smem_u32(&bar_qdo_empty[s]), 1);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(smem_u32(&tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_slot;
+    const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+            const uint32_t kvf = smem_u32(&bar_kv_full);
+            mbar_arrive_expect_tx(kvf, 2 * C::KV_BYTES);
+            for (int c = 0; c < C::NCH; ++c) {
+                tma_load_4d(smem_u32(sK + c * C::BKV * 128), &tm_k, kvf, c * C::EPC, hkv, kv0, b);
+                tma_load_4d(smem_u32(sV + c * C::BKV * 128), &tm_v, kvf, c * C::EPC, hkv, kv0, b);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % C::NQS;
+                const int h = hkv * G + it / per_head;
+                const int q0 = (i_first + it % per_head) * C::BQ;
+                if (it >= C::NQS &&
+                    !mbar_wait(smem_u32(&bar_qdo_empty[s]), ((it / C::NQS) - 1) & 1, w, SITE_BWD_QDO_EMPTY))
+                    break;
+                const uint32_t f = smem_u32(&bar_qdo_full[s]);
+                mbar_arrive_expect_tx(f, 2 * C::Q_BYTES);
+                for (int c = 0; c < C::NCH; ++c) {
+                    tma_load_4d(smem_u32(stage_q(s) + c * C::BQ * 128), &tm_q, f, c * C::EPC, h, q0, b);
+                    tma_load_4d(smem_u32(stage_do(s) + c * C::BQ * 128), &tm_do, f, c * C::EPC, h, q0, b);
+                }
+                ++issued;
+            }
+            mbar_wait_drain(kvf, 0, w, SITE_BWD_DRAIN);
+            for (int it = max(0, issued - C::NQS); it < issued; ++it)
+                mbar_wait_drain(smem_u32(&bar_qdo_full[it % C::NQS]), (it / C::NQS) & 1, w, SITE_BWD_DRAIN);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ UMMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_make(FMT_F16, 128, C::BQ, false, false);   // S^T (fp16 Q', K')
+            constexpr uint32_t id_dp = idesc_make(FMT_BF16, 128, C::BQ, false, false); // dP^T
+            constexpr uint32_t id_dv = idesc_make(FMT_BF16, 128, D, false, true);      // dV, dK (B MN-major)
+            constexpr uint32_t id_dq = idesc_make(FMT_BF16, 128, D, true, true);       // dQ (A, B MN-major)
+            const uint32_t sK_a = smem_u32(sK), sK16_a = smem_u32(sK16), sV_a = smem_u32(sV);
+            bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % C::NQS;
+                const uint32_t sdS_a = smem_u32(C::DS_ALIASES_Q16 ? stage_q16(s) : sdS);
+                if (!mbar_wait(smem_u32(&bar_q_ready[s]), (it / C::NQS) & 1, w, SITE_BWD_Q_READY)) break;
+                tc_fence_after();
+                const uint32_t q_a = smem_u32(stage_q(s)), q16_a = smem_u32(stage_q16(s)), do_a = smem_u32(stage_do(s));
+                // S^T = K' Q'^T   [keys x queries], K = head_dim, fp16 operands
+#pragma unroll
+                for (int ks = 0; ks < C::KSTEPS_D; ++ks) {
+                    const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
+                    const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
+                    umma_ss<false>(tm + C::S_COL, sdesc(sK16_a + off, 16, 1024), sdesc(q16_a + offq, 16, 1024), id_s,
+                                   ks > 0);
+                }
+                umma_commit(smem_u32(&bar_s_full));
+                if constexpr (C::DQ_ALIASES_DP) {
+                    if (it > 0 && !mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE)) break;
+                    tc_fence_after();
+                }
+                // dP^T = V dO^T   [keys x queries]
+#pragma unroll
+                for (int ks = 0; ks < C::KSTEPS_D; ++ks) {
+                    const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
+                    const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
+                    umma_ss<false>(tm + C::DP_COL, sdesc(sV_a + off, 16, 1024), sdesc(do_a + offq, 16, 1024), id_dp,
+                                   ks > 0);
+                }
+                umma_commit(smem_u32(&bar_dp_full));
+                if (!mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY)) break;
+                tc_fence_after();
+                // dV += P^T dO    (P^T from TMEM, dO MN-major), K = queries
+#pragma unroll
+                for (int ks = 0; ks < C::KSTEPS_Q; ++ks)
+                    umma_ts<false>(tm + C::DV_COL, tm + C::S_COL + ks * 8,
+                                   sdesc(do_a + ks * 16 * 128, C::BQ * 128, 1024), id_dv, (it > 0 || ks > 0) ? 1u : 0u);
+                // dK' += dS^T Q'  (dS^T K-major in smem, Q' bf16 MN-major), K = queries
+#pragma unroll
+                for (int ks = 0; ks < C::KSTEPS_Q; ++ks) {
+                    const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
+                    umma_ss<false>(tm + C::DK_COL, sdesc(sdS_a + off, 16, 1024),
+                                   sdesc(q_a + ks * 16 * 128, C::BQ * 128, 1024), id_dv, (it > 0 || ks > 0) ? 1u : 0u);
+                }
+                umma_commit(smem_u32(&bar_qdo_empty[s]));
+                if constexpr (!C::DQ_ALIASES_DP) {
+                    if (it > 0 && !mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE)) break;
+                    tc_fence_after();
+                }
+                // dQ'_part = dS K'  (dS = MN-major view of dS^T, K' bf16 MN-major), K = keys
+#pragma unroll
+                for (int ks = 0; ks < C::KSTEPS_KV; ++ks)
+                    umma_ss<false>(tm + C::DQ_COL, sdesc(sdS_a + ks * 16 * 128, C::BKV * 128, 1024),
+                                   sdesc(sK_a + ks * 16 * 128, C::BKV * 128, 1024), id_dq, ks > 0);
+                umma_commit(smem_u32(&bar_dq_full));
+                umma_commit(smem_u32(&bar_ds_free));
+            }
+            umma_commit(smem_u32(&bar_dkv_full));
+            umma_commit(smem_u32(&bar_final));
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ RoPE rotation
+        const int rt = tid - 128;
+        bool ovf = false;
+        if (mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV)) {
+            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_BF16_F16>(sK, sK16, kv0, T, rt, a.rope);
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_k_ready));
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % C::NQS;
+                const int q0 = (i_first + it % per_head) * C::BQ;
+                if (!mbar_wait_warp(smem_u32(&bar_qdo_full[s]), (it / C::NQS) & 1, w, SITE_BWD_QDO_FULL)) break;
+                // With dS^T living in the fp16 Q' buffer, the previous step's dK/dQ MMAs
+                // must be done with it before it is overwritten.
+                if (C::DS_ALIASES_Q16 && it > 0 &&
+                    !mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE))
+                    break;
+                ovf |= rope_tile_smem<D, C::BQ, 128, ROPE_BF16_F16>(stage_q(s), stage_q16(s), q0, T, rt, a.rope);
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bar_q_ready[s]));
+            }
+        }
+        if (ovf) atomicCAS(a.err, 0, SITE_RANGE);
+    } else if (warp >= 8 && warp < 12) {
+        // ------------------------------------------------------------ P^T, dS^T; dK, dV epilogue
+        const int r = tid - 256;                       // key row = TMEM lane
+        const int kvpos = kv0 + r;
+        const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sl2 = a.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int h = hkv * G + it / per_head;
+            const int q0 = (i_first + it % per_head) * C::BQ;
+            const int sb = it & 1;
+            uint8_t* dsb = C::DS_ALIASES_Q16 ? stage_q16(it % C::NQS) : sdS;
+            {
+                const int qpos = q0 + r;
+                const size_t rix = ((size_t)b * a.Hq + h) * T + qpos;
+                s_lse[sb][r] = qpos < T ? a.lse[rix] * 1.4426950408889634f : 0.f;
+                s_delta[sb][r] = qpos < T ? a.delta[rix] : 0.f;
+            }
+            // Staged values are visible to the group once all 128 have arrived.  Buffer sb
+            // is rewritten two steps later, after every thread has passed this step.
+            mbar_arrive(smem_u32(&bar_rows[sb]));
+            if (!mbar_wait_warp(smem_u32(&bar_rows[sb]), (it >> 1) & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
+            const bool diag = kv0 + C::BKV - 1 > q0;
+            if (!mbar_wait_warp(smem_u32(&bar_s_full), it & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
+            if (!mbar_wait_warp(smem_u32(&bar_dp_full), it & 1, w, SITE_BWD_DP_FULL)) { ok = false; break; }
+            if (it > 0 && !mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < C::BQ; c += 32) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(lt + C::S_COL + c, sr);
+                tmem_ld32(lt + C::DP_COL + c, dr);
+                tmem_wait_ld();
+                reg_fence32(sr);
+                reg_fence32(dr);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float p0 = exp2f(fmaf(__uint_as_float(sr[e]), sl2, -s_lse[sb][c + e]));
+                    float p1 = exp2f(fmaf(__uint_as_float(sr[e + 1]), sl2, -s_lse[sb][c + e + 1]));
+                    if (diag && kvpos > q0 + c + e) p0 = 0.f;
+                    if (diag && kvpos > q0 + c + e + 1) p1 = 0.f;
+                    const float d0 = p0 * (__uint_as_float(dr[e]) - s_delta[sb][c + e]);
+                    const float d1 = p1 * (__uint_as_float(dr[e + 1]) - s_delta[sb][c + e + 1]);
+                    pk[e >> 1] = pack_bf162(p0, p1);
+                    dk[e >> 1] = pack_bf162(d0, d1);
+                }
+                tmem_st16(lt + C::S_COL + (c >> 1), pk);
+                uint8_t* base = dsb + (c >> 6) * C::BKV * 128;
+                const int u0 = (c & 63) >> 3;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4*>(base + sw128_offset(r, u0 + k)) =
+                        make_uint4(dk[4 * k], dk[4 * k + 1], dk[4 * k + 2], dk[4 * k + 3]);
+            }
+            fence_proxy_async_smem();
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_ds_ready));
+        }
+        // dK = s R^T dK', dV: key row r of this CTA's tile
+        if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
+            tc_fence_after();
+            const bool valid = kvpos < T;
+            const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t kr[32], vr[32];
+                tmem_ld32(lt + C::DK_COL + c, kr);
+                tmem_ld32(lt + C::DV_COL + c, vr);
+                tmem_wait_ld();
+                reg_fence32(kr);
+                reg_fence32(vr);
+                if (!valid) continue;
+                uint32_t kp[16], vp[16];
+                const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)kvpos * (D / 2) + c / 2);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 cs = __ldg(tab + e / 4);
+                    const float g0 = __uint_as_float(kr[e]) * a.scale, g1 = __uint_as_float(kr[e + 1]) * a.scale;
+                    const float g2 = __uint_as_float(kr[e + 2]) * a.scale, g3 = __uint_as_float(kr[e + 3]) * a.scale;
+                    kp[e >> 1] = pack_bf162(g0 * cs.x + g1 * cs.y, -g0 * cs.y + g1 * cs.x);
+                    kp[(e >> 1) + 1] = pack_bf162(g2 * cs.z + g3 * cs.w, -g2 * cs.w + g3 * cs.z);
+                    vp[e >> 1] = pack_bf162(__uint_as_float(vr[e]), __uint_as_float(vr[e + 1]));
+                    vp[(e >> 1) + 1] = pack_bf162(__uint_as_float(vr[e + 2]), __uint_as_float(vr[e + 3]));
+                }
+                uint4* dkp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + orow + c);
+                uint4* dvp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + orow + c);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    dkp[e] = make_uint4(kp[4 * e], kp[4 * e + 1], kp[4 * e + 2], kp[4 * e + 3]);
+                    dvp[e] = make_uint4(vp[4 * e], vp[4 * e + 1], vp[4 * e + 2], vp[4 * e + 3]);
+                }
+            }
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ dQ drain
+        const int r = tid - 384;                       // query row = TMEM lane
+        const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
+        for (int it = 0; it < n_it; ++it) {
+            const int h = hkv * G + it / per_head;
+            const int qpos = (i_first + it % per_head) * C::BQ + r;
+            if (!mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, w, SITE_BWD_DQ_FULL)) break;
+            tc_fence_after();
+            float* dst = a.dq_acc + (((size_t)b * T + (qpos < T ? qpos : 0)) * a.Hq + h) * D;
+            uint32_t v[D];
+            tmem_ld_cols<D / 32>(lt + C::DQ_COL, v);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_dq_free));
+            if (qpos < T) {
+#pragma unroll
+                for (int e = 0; e < D; e += 4)
+                    atomicAdd(reinterpret_cast<float4*>(dst + e),
+                              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                          __uint_as_float(v[e + 3])));
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        mbar_wait_drain(smem_u32(&bar_final), 0, w, SITE_BWD_DRAIN);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tm, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+    using C = BwdCfg<D>;
+    auto kfn = attn_bwd_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.Hkv, B, a.n_kvt);
+    kfn<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, a);
+    return cudaGetLastError();
+}
+
+int grid_for(long long work, int per_block) {
+    long long blocks = (work + per_block - 1) / per_block;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st) {
+    if (a.rows == 0) return cudaSuccess;
+    const long long warps_needed = (a.rows + 3) / 4;
+    const int blocks = grid_for(warps_needed * 32, 256);
+    if (!tf32) {
+        if (a.D == 64) bwd_pre_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, st>>>(a);
+        else if (a.D == 128) bwd_pre_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, st>>>(a);
+        else return cudaErrorInvalidValue;
+    } else {
+        if (a.D == 32) bwd_pre_kernel<float, 32><<<blocks, 256, 0, st>>>(a);
+        else if (a.D == 64) bwd_pre_kernel<float, 64><<<blocks, 256, 0, st>>>(a);
+        else return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st) {
+    if (a.rows == 0) return cudaSuccess;
+    const int blocks = grid_for(a.rows * (a.D / 4), 256);
+    if (!tf32) {
+        if (a.D == 64) bwd_post_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, st>>>(a);
+        else if (a.D == 128) bwd_post_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, st>>>(a);
+        else return cudaErrorInvalidValue;
+    } else {
+        if (a.D == 32) bwd_post_kernel<float, 32><<<blocks, 256, 0, st>>>(a);
+        else if (a.D == 64) bwd_post_kernel<float, 64><<<blocks, 256, 0, st>>>(a);
+        else return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+    if (tf32) return cudaErrorNotSupported;
+    if (D == 64) return launch_bwd_t<64>(B, tq, tk, tv, tdo, a, st);
+    if (D == 128) return launch_bwd_t<128>(B, tq, tk, tv, tdo, a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ne

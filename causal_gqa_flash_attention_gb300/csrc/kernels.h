@@ -1,0 +1,79 @@
+// kernels.h -- internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ne {
+
+// Device error codes written by bounded waits (first writer wins).  The low byte is
+// the wait site; the host maps any nonzero word to NE_ERR_DEVICE_TIMEOUT.
+enum WaitSite : int {
+    SITE_FWD_Q = 0x101, SITE_FWD_KV_FULL, SITE_FWD_KV_EMPTY, SITE_FWD_K_READY, SITE_FWD_S_FULL,
+    SITE_FWD_P_READY, SITE_FWD_O_DONE, SITE_FWD_DRAIN,
+    SITE_BWD_KV = 0x201, SITE_BWD_QDO_FULL, SITE_BWD_QDO_EMPTY, SITE_BWD_Q_READY, SITE_BWD_S_FULL,
+    SITE_BWD_DP_FULL, SITE_BWD_DS_READY, SITE_BWD_DS_FREE, SITE_BWD_DQ_FULL, SITE_BWD_DQ_FREE,
+    SITE_BWD_DKV, SITE_BWD_DRAIN,
+    SITE_SELFTEST = 0x301,
+    // Not a wait: a rotated q/k value exceeded the fp16 range of the logit operand.
+    SITE_RANGE = 0x401,
+};
+
+struct FwdArgs {
+    void* o;                 // [B,T,Hq,D], input dtype
+    float* lse;              // [B,Hq,T]
+    const float2* rope;      // [T, D/2] (cos, sin)
+    int T, Hq, G, n_qt;      // n_qt = ceil(T / 256): pairs of 128-row query tiles
+    float scale_log2;        // log2(e) / sqrt(D)
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+struct BwdPreArgs {
+    const void* o;           // [B,T,Hq,D]
+    const void* dO;          // [B,T,Hq,D]
+    float* delta;            // [B,Hq,T]
+    float* dq_acc;           // [B,T,Hq,D] fp32, zeroed here
+    long long rows;          // B*T*Hq
+    int T, Hq, D;
+};
+
+struct BwdArgs {
+    const float* lse;        // [B,Hq,T]
+    const float* delta;      // [B,Hq,T]
+    float* dq_acc;           // [B,T,Hq,D] fp32 accumulator of R dQ / s
+    void* dk;                // [B,T,Hkv,D]
+    void* dv;                // [B,T,Hkv,D]
+    const float2* rope;      // [T, D/2]
+    int T, Hq, Hkv, G, n_kvt;
+    float scale_log2;        // log2(e) / sqrt(D)
+    float scale;             // 1 / sqrt(D)
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+struct BwdPostArgs {
+    const float* dq_acc;     // [B,T,Hq,D]
+    void* dq;                // [B,T,Hq,D]
+    const float2* rope;
+    long long rows;          // B*T*Hq
+    int T, Hq, D;
+    float scale;
+};
+
+// Tile rows of the key/value tensor maps the forward kernel expects.
+int fwd_kv_box_rows(bool tf32, int D);
+// Launchers: return cudaSuccess or the launch error.
+cudaError_t launch_rope_table(float* cos_out, float* sin_out, float2* interleaved, int T, int D,
+                              double theta, cudaStream_t st);
+cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st);
+cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                       cudaStream_t st);
+cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st);
+cudaError_t launch_selftest_wait(int* err, unsigned long long timeout_ns, cudaStream_t st);
+
+}  // namespace ne

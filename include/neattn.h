@@ -1,0 +1,132 @@
+/*
+ * neattn.h -- C ABI of libneattn: fused causal grouped-query self-attention with
+ * rotary position embeddings (RoPE), forward and backward, on sm_103a tensor cores.
+ *
+ * What is computed (page title, section):
+ *   - causal self-attention, each position attending to itself and earlier
+ *     positions ("Tiny hackable CUDA language model implementation", Core Mechanics,
+ *     causal self-attention bullet);
+ *   - grouped-query attention: Hkv key/value heads, each shared by G = Hq / Hkv
+ *     query heads; query head h reads key/value head h / G ("NanoEuler: C와 CUDA로
+ *     밑바닥부터 구축한 GPT-2 규모의 LLM", 기술 사양, GQA bullet, and 모델 구성);
+ *   - RoPE on queries and keys (same page, 기술 사양, RoPE bullet): adjacent pairs
+ *     (2i, 2i+1) of a row at position t are rotated by the angle t * theta^(-2i/D),
+ *     (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos), positions t = 0 .. T-1;
+ *   - FlashAttention-style tiling with an online softmax, so the T x T score matrix
+ *     is never stored (same page, 커널 구현);
+ *   - the hand-written backward pass (same page, 검증 및 안정성).
+ *   O = softmax(s * Q' K'^T + causal mask) V with s = 1/sqrt(D), Q' = R Q, K' = R K.
+ *   LSE[b,h,t] = natural log of sum_j exp(s * q'_t . k'_j) over j <= t.
+ *
+ * Layouts (all row-major, dense, no padding):
+ *   q, o, dO, dq : [B, T, Hq,  D]      k, v, dk, dv : [B, T, Hkv, D]
+ *   lse          : [B, Hq, T] fp32     rope tables  : [T, D/2] fp32
+ * The bf16 entry points take __nv_bfloat16 tensors and compute with bf16 tensor-core
+ * inputs and fp32 accumulation; the *_f32 entry points take fp32 tensors and use TF32
+ * tensor cores with fp32 accumulation.  Outputs have the input dtype, lse is fp32.
+ *
+ * Supported shapes: B >= 0, T >= 0 (any T, ragged tails included), Hq % Hkv == 0,
+ * D in {64, 128} for bf16 and {32, 64} for f32 (others return NE_ERR_UNSUPPORTED),
+ * B * T * max(Hq, 1) * D < 2^31.  Every tensor pointer must be 16-byte aligned.
+ *
+ * Ownership: the caller owns every tensor and the backward workspace.  The library
+ * owns only small per-device caches (RoPE tables per (T, D, theta), one device error
+ * word), created on first use and released by ne_shutdown().  All pointers are device
+ * pointers unless stated otherwise.
+ *
+ * Streams: every call enqueues its kernels on `stream` (NULL = legacy default stream)
+ * and returns without synchronising, except that the first call for a new
+ * (device, T, D, theta) builds its RoPE table and synchronises `stream` once; make
+ * that first call before any stream capture.  Argument errors return before anything
+ * is enqueued.  Device-side failures (a bounded wait inside a kernel that ran out,
+ * see ne_get_device_error) are reported asynchronously.
+ *
+ * Threading: calls are thread-safe; ne_last_error() is per thread.
+ */
+#ifndef NEATTN_H
+#define NEATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* ne_stream_t;
+
+typedef enum {
+    NE_OK = 0,
+    NE_ERR_INVALID_ARG = 1,     /* bad pointer, shape or size; nothing was enqueued */
+    NE_ERR_UNSUPPORTED = 2,     /* valid but not implemented (e.g. head_dim) */
+    NE_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed; see ne_last_error() */
+    NE_ERR_DEVICE_TIMEOUT = 4,  /* a kernel's bounded wait ran out (ne_get_device_error) */
+    NE_ERR_NO_DEVICE = 5        /* no CUDA device, or not an sm_103 device */
+} ne_status;
+
+/* RoPE cos/sin table (the rotation of the RoPE bullet, same page): for t < T and
+ * i < D/2, cos_out[t*(D/2)+i] = cos(t * theta^(-2i/D)) and likewise sin_out.  Angles
+ * are formed in fp64 on the device and stored as fp32.  cos_out/sin_out: device
+ * pointers to T*D/2 floats each.  D must be even and > 0, theta > 0. */
+ne_status ne_rope_table(float* cos_out, float* sin_out, int T, int D, double theta,
+                        ne_stream_t stream);
+
+/* Forward (커널 구현: tiling + online softmax).  q [B,T,Hq,D], k and v [B,T,Hkv,D] in,
+ * o [B,T,Hq,D] and lse [B,Hq,T] (fp32) out.  bf16 tensors. */
+ne_status ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                      ne_stream_t stream);
+/* Same with fp32 tensors on TF32 tensor cores. */
+ne_status ne_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                          int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                          ne_stream_t stream);
+
+/* Bytes of device workspace ne_attn_bwd needs for this shape (0 on a bad shape).
+ * Layout: Delta fp32 [B,Hq,T] at offset 0, then (256-byte aligned) the fp32 dQ
+ * accumulator [B,T,Hq,D].  Both are rewritten by every call. */
+size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D);
+
+/* Backward (검증 및 안정성: the hand-written backward), the vector-Jacobian product of
+ * <dO, O> for the forward above.  Inputs q, k, v, o, lse, dO as the forward wrote or
+ * read them; outputs dq [B,T,Hq,D], dk and dv [B,T,Hkv,D] in the input dtype.  The
+ * gradient of every kv head is summed over its G query heads.  `workspace` must hold
+ * ne_attn_bwd_workspace_size() bytes (256-byte aligned); it is caller-owned scratch. */
+ne_status ne_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                      int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                      void* workspace, size_t workspace_bytes, ne_stream_t stream);
+ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const float* o,
+                          const float* lse, const float* dO, float* dq, float* dk, float* dv,
+                          int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                          void* workspace, size_t workspace_bytes, ne_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* ne_status_string(ne_status s);
+/* Detail of the last error on the calling thread ("" if none). */
+const char* ne_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns NE_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out since the last
+ * check (the kernel then skipped the rest of its work and its outputs are invalid),
+ * NE_ERR_CUDA if the synchronisation failed, else NE_OK. */
+ne_status ne_get_device_error(ne_stream_t stream);
+
+/* Wall-clock limit of every bounded wait inside the kernels (default 2000 ms, or
+ * NE_ATTN_TIMEOUT_MS from the environment).  0 restores the default. */
+void ne_set_wait_timeout_ms(uint32_t ms);
+
+/* Diagnostic: launches one tiny kernel whose bounded wait can never be satisfied, so
+ * it runs out after `timeout_ms` and records NE_ERR_DEVICE_TIMEOUT in the device error
+ * word, exactly as a stalled attention kernel would.  Used to test the error path
+ * without faulting or hanging the GPU. */
+ne_status ne_selftest_wait_timeout(uint32_t timeout_ms, ne_stream_t stream);
+
+/* Releases the library's per-device caches (RoPE tables, error words). */
+void ne_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NEATTN_H */

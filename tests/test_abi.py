@@ -1,0 +1,79 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every symbol the
+header declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_gqa_flash_attention_gb300 as ne
+from causal_gqa_flash_attention_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "neattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ne.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ne_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_symbols() == sorted(ne.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    names = [lib.ne_status_string(i).decode() for i in range(6)]
+    assert names == ["NE_OK", "NE_ERR_INVALID_ARG", "NE_ERR_UNSUPPORTED", "NE_ERR_CUDA",
+                     "NE_ERR_DEVICE_TIMEOUT", "NE_ERR_NO_DEVICE"]
+
+
+def test_workspace_size_formula(lib):
+    B, T, Hq, Hkv, D = 16, 512, 12, 4, 64
+    delta = B * Hq * T * 4
+    delta_al = (delta + 255) // 256 * 256
+    assert lib.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D) == delta_al + B * T * Hq * D * 4
+    assert lib.ne_attn_bwd_workspace_size(1, 8, 3, 2, 64) == 0   # Hq % Hkv != 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((1, 8, 3, 2, 64, 10000.0), ne.NE_ERR_INVALID_ARG),    # Hq % Hkv
+    ((1, 8, 4, 2, 63, 10000.0), ne.NE_ERR_INVALID_ARG),    # odd D
+    ((1, 8, 4, 2, 64, -1.0), ne.NE_ERR_INVALID_ARG),       # theta
+    ((-1, 8, 4, 2, 64, 10000.0), ne.NE_ERR_INVALID_ARG),   # B
+    ((1, 8, 4, 2, 96, 10000.0), ne.NE_ERR_UNSUPPORTED),    # head_dim
+    ((1, 8, 4, 0, 64, 10000.0), ne.NE_ERR_INVALID_ARG),    # Hkv
+])
+def test_forward_rejects_bad_shapes_before_any_device_work(lib, args, expect):
+    null = ctypes.c_void_p(0)
+    B, T, Hq, Hkv, D, theta = args
+    st = lib.ne_attn_fwd(null, null, null, null, null, B, T, Hq, Hkv, D, theta, null)
+    assert st == expect
+    assert lib.ne_last_error().decode() != ""
+
+
+def test_empty_problem_is_a_no_op(lib):
+    null = ctypes.c_void_p(0)
+    assert lib.ne_attn_fwd(null, null, null, null, null, 0, 128, 4, 2, 64, 10000.0, null) == ne.NE_OK
+    assert lib.ne_attn_fwd(null, null, null, null, null, 2, 0, 4, 2, 64, 10000.0, null) == ne.NE_OK
+
+
+def test_backward_rejects_small_workspace_and_misalignment(lib):
+    vp = ctypes.c_void_p
+    p = vp(4096)   # never dereferenced: validation fails first
+    st = lib.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 8, 4, 2, 64, 10000.0, vp(4096), 16, vp(0))
+    assert st == ne.NE_ERR_INVALID_ARG and "workspace" in lib.ne_last_error().decode()
+    q = vp(4096 + 8)
+    st = lib.ne_attn_bwd(q, p, p, p, p, p, p, p, p, 1, 8, 4, 2, 64, 10000.0, vp(4096), 1 << 20, vp(0))
+    assert st == ne.NE_ERR_INVALID_ARG and "aligned" in lib.ne_last_error().decode()
