@@ -149,7 +149,8 @@ __global__ void __launch_bounds__(512, 1)
         bar_ds_free, bar_dq_full, bar_dq_free, bar_dkv_full, bar_final;
     __shared__ __align__(8) uint64_t bar_qdo_full[C::NQS], bar_q_ready[C::NQS], bar_qdo_empty[C::NQS];
     __shared__ __align__(8) uint64_t bar_rows[2];   // LSE/Delta of a query tile staged (double buffer)
-    __shared__ float s_lse[2][C::BQ], s_delta[2][C::BQ];
+    __shared__ __align__(16) float s_lse[2][C::BQ];
+    __shared__ __align__(16) float s_delta[2][C::BQ];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -353,16 +354,23 @@ __global__ void __launch_bounds__(512, 1)
                 reg_fence32(sr);
                 reg_fence32(dr);
                 uint32_t pk[16], dk[16];
+                const float4* l4 = reinterpret_cast<const float4*>(&s_lse[sb][c]);
+                const float4* d4 = reinterpret_cast<const float4*>(&s_delta[sb][c]);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p0 = exp2f(fmaf(__uint_as_float(sr[e]), sl2, -s_lse[sb][c + e]));
-                    float p1 = exp2f(fmaf(__uint_as_float(sr[e + 1]), sl2, -s_lse[sb][c + e + 1]));
-                    if (diag && kvpos > q0 + c + e) p0 = 0.f;
-                    if (diag && kvpos > q0 + c + e + 1) p1 = 0.f;
-                    const float d0 = p0 * (__uint_as_float(dr[e]) - s_delta[sb][c + e]);
-                    const float d1 = p1 * (__uint_as_float(dr[e + 1]) - s_delta[sb][c + e + 1]);
-                    pk[e >> 1] = pack_bf162(p0, p1);
-                    dk[e >> 1] = pack_bf162(d0, d1);
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 lv = l4[e >> 2], dv = d4[e >> 2];   // broadcast reads
+                    const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv.x, dv.y, dv.z, dv.w};
+                    float p[4], g[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
+                        if (diag && kvpos > q0 + c + e + k) p[k] = 0.f;
+                        g[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
+                    }
+                    pk[e >> 1] = pack_bf162(p[0], p[1]);
+                    pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
+                    dk[e >> 1] = pack_bf162(g[0], g[1]);
+                    dk[(e >> 1) + 1] = pack_bf162(g[2], g[3]);
                 }
                 tmem_st16(lt + C::S_COL + (c >> 1), pk);
                 uint8_t* base = dsb + (c >> 6) * C::BKV * 128;

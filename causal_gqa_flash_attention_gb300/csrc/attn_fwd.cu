@@ -275,13 +275,20 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t sr[C::BN];
             tmem_ld_cols<C::BN / 32>(lt + s_col, sr);
             const int kv0 = j * C::BN;
-            const bool diag = kv0 + C::BN - 1 > qsub0;
-            float mx = kNegInf;
+            if (kv0 + C::BN - 1 > qsub0) {          // tile crosses the diagonal: mask j > i
 #pragma unroll
-            for (int e = 0; e < C::BN; ++e) {
-                if (diag && kv0 + e > qpos) sr[e] = __float_as_uint(kNegInf);
-                mx = fmaxf(mx, __uint_as_float(sr[e]));
+                for (int e = 0; e < C::BN; ++e)
+                    if (kv0 + e > qpos) sr[e] = __float_as_uint(kNegInf);
             }
+            // Row max over 8 independent chains (one warp per SMSP runs this: a single
+            // dependent chain of BN maxes would serialise on the FMNMX latency).
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = __uint_as_float(sr[k]);
+#pragma unroll
+            for (int e = 8; e < C::BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float m_tile = mx * sl2;
             // A row whose max grew by more than 2^8 rescales l and its O row; the others
             // keep their max (p <= 2^8 stays exact).  TMEM access is warp-collective, so
@@ -290,7 +297,7 @@ __global__ void __launch_bounds__(384, 1)
             const bool need = j > 0 && m_tile > m_used + 8.f;
             if (j == 0) m_used = m_tile;
             if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? exp2f(m_used - m_tile) : 1.f;
+                const float alpha = need ? ex2(m_used - m_tile) : 1.f;
                 l *= alpha;
                 if (need) m_used = m_tile;
                 if (!mbar_wait_warp(smem_u32(&bar_o_done[u]), (j - 1) & 1, w, SITE_FWD_O_DONE)) { ok = false; break; }
@@ -304,15 +311,16 @@ __global__ void __launch_bounds__(384, 1)
                     tmem_st32(lt + o_col + c, orow);
                 }
             }
-            float sum = 0.f;
+            float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float neg_m = -m_used;
 #pragma unroll
             for (int c = 0; c < C::BN; c += 32) {
                 if constexpr (TF32) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p = exp2f(fmaf(__uint_as_float(sr[c + e]), sl2, -m_used));
-                        sum += p;
+                        const float p = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, neg_m));
+                        s8[e & 7] += p;
                         pk[e] = f32_to_tf32_rna(p);
                     }
                     tmem_st32(lt + s_col + c, pk);
@@ -320,15 +328,16 @@ __global__ void __launch_bounds__(384, 1)
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float p0 = exp2f(fmaf(__uint_as_float(sr[c + e]), sl2, -m_used));
-                        const float p1 = exp2f(fmaf(__uint_as_float(sr[c + e + 1]), sl2, -m_used));
-                        sum += p0 + p1;
+                        const float p0 = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, neg_m));
+                        const float p1 = ex2(fmaf(__uint_as_float(sr[c + e + 1]), sl2, neg_m));
+                        s8[e & 7] += p0;
+                        s8[(e + 1) & 7] += p1;
                         pk[e >> 1] = pack_bf162(p0, p1);
                     }
                     tmem_st16(lt + s_col + (c >> 1), pk);
                 }
             }
-            l += sum;
+            l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_p_ready[u]));

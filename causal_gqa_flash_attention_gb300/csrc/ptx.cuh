@@ -48,6 +48,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Same test, but a thread whose phase is not complete is suspended (not spinning, so
+// it takes no issue slots from working warps) until the phase completes or
+// `suspend_ns` elapses.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
 
 // Error/abort context shared by the waits of one CTA.  Every wait is bounded: after
 // `timeout_ns` of wall-clock time it records `code` in the device error word (first
@@ -67,8 +80,7 @@ __device__ __forceinline__ void raise_error(const WaitCtx& w, int code) {
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, int code) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
         if (*w.abort_smem) return false;
         if (globaltimer_ns() - t0 > w.timeout_ns) {
             raise_error(w, code);
@@ -94,8 +106,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
 static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const WaitCtx& w, int code) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
         if (globaltimer_ns() - t0 > w.timeout_ns) {
             raise_error(w, code);
             return false;
@@ -324,6 +335,13 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef NE_R8
 #undef NE_P8
 #undef NE_S8
+
+// 2^x on the special-function unit (flush-to-zero; exp2(-inf) = 0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Offset of 16-byte unit `u` (0..7) of row `r` inside a 128-byte-swizzled region
 // whose rows are 128 bytes apart.
