@@ -30,7 +30,7 @@ NE_OK, NE_ERR_INVALID_ARG, NE_ERR_UNSUPPORTED, NE_ERR_CUDA, NE_ERR_DEVICE_TIMEOU
 EXPORTS = (
     "ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd_workspace_size", "ne_attn_bwd",
     "ne_attn_bwd_f32", "ne_status_string", "ne_last_error", "ne_get_device_error",
-    "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown",
+    "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown", "ne_attn_bwd_noalloc",
 )
 
 
@@ -66,10 +66,11 @@ def load(path: str | None = None):
         lib.ne_set_wait_timeout_ms.argtypes = [ctypes.c_uint32]
         lib.ne_set_wait_timeout_ms.restype = None
         lib.ne_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+        lib.ne_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 5 + [d, vp]
         lib.ne_shutdown.argtypes = []
         lib.ne_shutdown.restype = None
         for f in ("ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd", "ne_attn_bwd_f32",
-                  "ne_get_device_error", "ne_selftest_wait_timeout"):
+                  "ne_get_device_error", "ne_selftest_wait_timeout", "ne_attn_bwd_noalloc"):
             getattr(lib, f).restype = i
         _lib = lib
     return _lib

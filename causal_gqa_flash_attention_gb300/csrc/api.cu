@@ -287,6 +287,34 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     return NE_OK;
 }
 
+// ------------------------------------------------------------------ allocation-free backward
+// Scratch of ne_attn_bwd_noalloc: a file-scope device array (every GPU that loads the
+// library holds it until the process exits).  Layout per call: RoPE table
+// [T, D/2] float2 | Delta [B, Hq, T] fp32 | dQ accumulator [B, T, Hq, D] fp32, each
+// part starting on a 256-byte boundary.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch per device ordinal.  In host code the array's
+// name is only a host-side stand-in, so the address comes from cudaGetSymbolAddress,
+// taken once per device with that device current.
+constexpr int kMaxDevices = 64;
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+ne_status noalloc_scratch(int dev, void** out) {
+    if (dev < 0 || dev >= kMaxDevices) return fail(NE_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return NE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -397,6 +425,67 @@ void ne_shutdown(void) {
     }
     g_dev.clear();
     cudaSetDevice(cur);
+}
+
+ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dO, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
+                              double rope_theta, ne_stream_t stream) {
+    g_last_error.clear();
+    cudaStream_t st = (cudaStream_t)stream;
+    ne_status s = check_shape(B, T, Hq, Hkv, D, rope_theta, false);
+    if (s != NE_OK) return s;
+    if (B == 0 || T == 0) return NE_OK;
+    if ((s = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv})) != NE_OK) return s;
+    const size_t rope_bytes = round_up((size_t)T * (D / 2) * sizeof(float2), 256);
+    const size_t delta_bytes = round_up((size_t)B * Hq * T * sizeof(float), 256);
+    const size_t acc_bytes = (size_t)B * T * Hq * D * sizeof(float);
+    if (rope_bytes + delta_bytes + acc_bytes > kNoAllocScratchBytes)
+        return fail(NE_ERR_INVALID_ARG,
+                    "ne_attn_bwd_noalloc: this shape needs %zu bytes of scratch, above its fixed maximum of %zu "
+                    "(%zu MiB); use ne_attn_bwd with a caller-allocated workspace",
+                    rope_bytes + delta_bytes + acc_bytes, kNoAllocScratchBytes, kNoAllocScratchBytes >> 20);
+    int dev;
+    if ((s = current_device(&dev)) != NE_OK) return s;
+    void* base;
+    if ((s = noalloc_scratch(dev, &base)) != NE_OK) return s;
+    float2* rope = static_cast<float2*>(base);
+    float* delta = reinterpret_cast<float*>(static_cast<char*>(base) + rope_bytes);
+    float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(base) + rope_bytes + delta_bytes);
+    const long long rows = (long long)B * T * Hq;
+
+    // The table is rebuilt on every call: the scratch keeps whatever the last call left.
+    cudaError_t e = ne::launch_rope_table(nullptr, nullptr, rope, T, D, rope_theta, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D};   // also zeroes dq_acc
+    e = ne::launch_bwd_pre(false, pa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
+    CUtensorMap tq, tk, tv, tdo;
+    if ((s = map_bthd(&tq, q, false, B, T, Hq, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tk, k, false, B, T, Hkv, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tv, v, false, B, T, Hkv, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tdo, dO, false, B, T, Hq, D, 128)) != NE_OK) return s;
+    ne::BwdArgs a;
+    a.lse = lse;
+    a.delta = delta;
+    a.dq_acc = dq_acc;
+    a.dk = dk;
+    a.dv = dv;
+    a.rope = rope;
+    a.T = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.n_kvt = (T + 127) / 128;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    a.scale = (float)(1.0 / std::sqrt((double)D));
+    a.err = nullptr;            // no error word: that would need an allocation
+    a.timeout_ns = timeout_ns();
+    e = ne::launch_bwd(false, D, B, tq, tk, tv, tdo, a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
+    ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale};
+    e = ne::launch_bwd_post(false, qa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dq epilogue launch");
+    return NE_OK;
 }
 
 }  // extern "C"

@@ -101,6 +101,33 @@ ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const 
                           int B, int T, int Hq, int Hkv, int D, double rope_theta,
                           void* workspace, size_t workspace_bytes, ne_stream_t stream);
 
+/* Backward that allocates nothing (there is no counterpart of this call on the
+ * pages: it is a deployment convenience).  Same computation, arguments and outputs
+ * as ne_attn_bwd for bf16 tensors, but without a workspace argument: its scratch
+ * (RoPE table, Delta, fp32 dQ accumulator) lives in one file-scope device array of
+ * 32 MiB that every GPU loading the library keeps until the process exits.  It is for
+ * callers that cannot call cudaMalloc at this point: code that runs while a stream
+ * is being captured into a CUDA graph (allocation is not allowed there), runtimes
+ * whose own allocator already owns the device's free memory, or real-time loops that
+ * forbid allocation after start-up.  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *  - Limit: round256(T*(D/2)*8) + round256(B*Hq*T*4) + B*T*Hq*D*4 <= 33554432 bytes
+ *    (the GPU-pipeline shape B=16 T=512 Hq=12 D=64 uses 25.7 MB); larger shapes
+ *    return NE_ERR_INVALID_ARG before anything is enqueued.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array, which keeps the last call's contents; every call
+ *    rewrites what it reads.  Calls whose kernels overlap on the GPU (two streams, or
+ *    two threads) race on the scratch and produce wrong gradients: serialise them.
+ *  - The kernels still bound every internal wait, but a wait that runs out is not
+ *    recorded (recording needs the allocated error word): use ne_attn_bwd when that
+ *    report is wanted. */
+ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                              int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                              ne_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* ne_status_string(ne_status s);
 /* Detail of the last error on the calling thread ("" if none). */
