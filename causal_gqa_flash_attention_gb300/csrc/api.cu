@@ -100,10 +100,11 @@ ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const
                     "make one call before capturing",
                     T, D, theta);
     float2* buf = nullptr;
-    size_t bytes = (size_t)T * (D / 2) * sizeof(float2);
-    cudaError_t e = cudaMalloc(&buf, bytes < 16 ? 16 : bytes);
+    const int rows = ne::rope_table_rows(T);
+    size_t bytes = (size_t)rows * (D / 2) * sizeof(float2);
+    cudaError_t e = cudaMalloc(&buf, bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(rope table)");
-    e = ne::launch_rope_table(nullptr, nullptr, buf, T, D, theta, st);
+    e = ne::launch_rope_table(nullptr, nullptr, buf, rows, D, theta, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         cudaFree(buf);
@@ -436,7 +437,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     if (s != NE_OK) return s;
     if (B == 0 || T == 0) return NE_OK;
     if ((s = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv})) != NE_OK) return s;
-    const size_t rope_bytes = round_up((size_t)T * (D / 2) * sizeof(float2), 256);
+    const size_t rope_bytes = round_up((size_t)ne::rope_table_rows(T) * (D / 2) * sizeof(float2), 256);
     const size_t delta_bytes = round_up((size_t)B * Hq * T * sizeof(float), 256);
     const size_t acc_bytes = (size_t)B * T * Hq * D * sizeof(float);
     if (rope_bytes + delta_bytes + acc_bytes > kNoAllocScratchBytes)
@@ -454,7 +455,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     const long long rows = (long long)B * T * Hq;
 
     // The table is rebuilt on every call: the scratch keeps whatever the last call left.
-    cudaError_t e = ne::launch_rope_table(nullptr, nullptr, rope, T, D, rope_theta, st);
+    cudaError_t e = ne::launch_rope_table(nullptr, nullptr, rope, ne::rope_table_rows(T), D, rope_theta, st);
     if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
     ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D};   // also zeroes dq_acc
     e = ne::launch_bwd_pre(false, pa, st);

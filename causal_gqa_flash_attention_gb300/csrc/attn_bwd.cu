@@ -235,21 +235,32 @@ __global__ void __launch_bounds__(512, 1)
             constexpr uint32_t id_dp = idesc_make(FMT_BF16, 128, C::BQ, false, false); // dP^T
             constexpr uint32_t id_dv = idesc_make(FMT_BF16, 128, D, false, true);      // dV, dK (B MN-major)
             constexpr uint32_t id_dq = idesc_make(FMT_BF16, 128, D, true, true);       // dQ (A, B MN-major)
-            const uint32_t sK_a = smem_u32(sK), sK16_a = smem_u32(sK16), sV_a = smem_u32(sV);
+            // Descriptors are built once; per step only the start address moves.
+            const uint64_t dK = sdesc(smem_u32(sK), 16, 1024), dK16 = sdesc(smem_u32(sK16), 16, 1024);
+            const uint64_t dV = sdesc(smem_u32(sV), 16, 1024);
+            const uint64_t dKmn = sdesc(smem_u32(sK), C::BKV * 128, 1024);      // K' as MN-major B of dQ
+            const uint64_t dQ0 = sdesc(smem_u32(stage_q(0)), 16, 1024);
+            const uint64_t dQmn0 = sdesc(smem_u32(stage_q(0)), C::BQ * 128, 1024);
+            const uint64_t dDS0 = sdesc(smem_u32(sdS), 16, 1024);
+            const uint64_t dDSmn0 = sdesc(smem_u32(sdS), C::BKV * 128, 1024);
+            (void)dQ0;
             bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV);
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it % C::NQS;
-                const uint32_t sdS_a = smem_u32(C::DS_ALIASES_Q16 ? stage_q16(s) : sdS);
+                const uint32_t so = s * C::STAGE_BYTES;            // stage offset from stage 0
+                // dS^T lives in its own buffer, or (D = 128) in this stage's fp16 Q' buffer
+                const uint32_t dso = C::DS_ALIASES_Q16 ? so : 0;
                 if (!mbar_wait(smem_u32(&bar_q_ready[s]), (it / C::NQS) & 1, w, SITE_BWD_Q_READY)) break;
                 tc_fence_after();
-                const uint32_t q_a = smem_u32(stage_q(s)), q16_a = smem_u32(stage_q16(s)), do_a = smem_u32(stage_do(s));
+                const uint64_t dQ16 = sdesc_add(dQ0, so + C::Q_BYTES), dO = sdesc_add(dQ0, so + 2 * C::Q_BYTES);
+                const uint64_t dQmn = sdesc_add(dQmn0, so), dOmn = sdesc_add(dQmn0, so + 2 * C::Q_BYTES);
+                const uint64_t dDS = sdesc_add(dDS0, dso), dDSmn = sdesc_add(dDSmn0, dso);
                 // S^T = K' Q'^T   [keys x queries], K = head_dim, fp16 operands
 #pragma unroll
                 for (int ks = 0; ks < C::KSTEPS_D; ++ks) {
                     const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
                     const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
-                    umma_ss<false>(tm + C::S_COL, sdesc(sK16_a + off, 16, 1024), sdesc(q16_a + offq, 16, 1024), id_s,
-                                   ks > 0);
+                    umma_ss<false>(tm + C::S_COL, sdesc_add(dK16, off), sdesc_add(dQ16, offq), id_s, ks > 0);
                 }
                 umma_commit(smem_u32(&bar_s_full));
                 if constexpr (C::DQ_ALIASES_DP) {
@@ -261,8 +272,7 @@ __global__ void __launch_bounds__(512, 1)
                 for (int ks = 0; ks < C::KSTEPS_D; ++ks) {
                     const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
                     const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
-                    umma_ss<false>(tm + C::DP_COL, sdesc(sV_a + off, 16, 1024), sdesc(do_a + offq, 16, 1024), id_dp,
-                                   ks > 0);
+                    umma_ss<false>(tm + C::DP_COL, sdesc_add(dV, off), sdesc_add(dO, offq), id_dp, ks > 0);
                 }
                 umma_commit(smem_u32(&bar_dp_full));
                 if (!mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY)) break;
@@ -270,14 +280,14 @@ __global__ void __launch_bounds__(512, 1)
                 // dV += P^T dO    (P^T from TMEM, dO MN-major), K = queries
 #pragma unroll
                 for (int ks = 0; ks < C::KSTEPS_Q; ++ks)
-                    umma_ts<false>(tm + C::DV_COL, tm + C::S_COL + ks * 8,
-                                   sdesc(do_a + ks * 16 * 128, C::BQ * 128, 1024), id_dv, (it > 0 || ks > 0) ? 1u : 0u);
+                    umma_ts<false>(tm + C::DV_COL, tm + C::S_COL + ks * 8, sdesc_add(dOmn, ks * 16 * 128), id_dv,
+                                   (it > 0 || ks > 0) ? 1u : 0u);
                 // dK' += dS^T Q'  (dS^T K-major in smem, Q' bf16 MN-major), K = queries
 #pragma unroll
                 for (int ks = 0; ks < C::KSTEPS_Q; ++ks) {
                     const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
-                    umma_ss<false>(tm + C::DK_COL, sdesc(sdS_a + off, 16, 1024),
-                                   sdesc(q_a + ks * 16 * 128, C::BQ * 128, 1024), id_dv, (it > 0 || ks > 0) ? 1u : 0u);
+                    umma_ss<false>(tm + C::DK_COL, sdesc_add(dDS, off), sdesc_add(dQmn, ks * 16 * 128), id_dv,
+                                   (it > 0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(smem_u32(&bar_qdo_empty[s]));
                 if constexpr (!C::DQ_ALIASES_DP) {
@@ -287,8 +297,8 @@ __global__ void __launch_bounds__(512, 1)
                 // dQ'_part = dS K'  (dS = MN-major view of dS^T, K' bf16 MN-major), K = keys
 #pragma unroll
                 for (int ks = 0; ks < C::KSTEPS_KV; ++ks)
-                    umma_ss<false>(tm + C::DQ_COL, sdesc(sdS_a + ks * 16 * 128, C::BKV * 128, 1024),
-                                   sdesc(sK_a + ks * 16 * 128, C::BKV * 128, 1024), id_dq, ks > 0);
+                    umma_ss<false>(tm + C::DQ_COL, sdesc_add(dDSmn, ks * 16 * 128), sdesc_add(dKmn, ks * 16 * 128),
+                                   id_dq, ks > 0);
                 umma_commit(smem_u32(&bar_dq_full));
                 umma_commit(smem_u32(&bar_ds_free));
             }

@@ -6,13 +6,14 @@
 // j <= i ("Tiny hackable CUDA language model implementation", Core Mechanics).
 //
 // One CTA owns two consecutive 128-row query subtiles (u = 0, 1) of one (batch, query
-// head) and walks the key/value tiles up to the diagonal; every K/V tile is loaded and
-// rotated once for both subtiles.  Warp roles (384 threads, one CTA per SM):
+// head) and walks 64-key tiles up to the diagonal; every K/V tile is loaded and
+// rotated once for both subtiles.  Warp roles (416 threads, one CTA per SM):
 //   warp 0       TMA producer: Q0, Q1 once, then K/V tiles into an NS-stage ring.
-//   warp 1       TMEM allocator (512 columns) and UMMA issuer.  Order per tile j:
-//                PV0(j), S0(j+1), PV1(j), S1(j+1), so each softmax group works on one
-//                subtile while the tensor core runs the other's MMAs.
-//   warps 2-3    RoPE on every K tile in place (fp16 logit operand; TF32: rounded fp32)
+//   warp 1, 2    UMMA issuer of subtile 0 / 1 (warp 1 also owns the 512 TMEM columns).
+//                One thread issues a tcgen05.mma only every ~100 cycles, so each subtile
+//                gets its own issuer: S_u(j+2) = Q'_u K'_j+2^T into S buffer j % 2 right
+//                after PV_u(j) = P_u(j) V_j, two tiles ahead of the softmax.
+//   warps 3, 12  RoPE on every K tile in place (fp16 logit operand; TF32: rounded fp32)
 //                and, for TF32, V transposed (TF32 UMMA reads K-major operands only).
 //   warps 4-7    softmax of subtile 0; warps 8-11 softmax of subtile 1.  Thread r owns
 //                query row r (TMEM lane r): it rotates its Q row block once, then per
@@ -20,7 +21,7 @@
 //                writes P (bf16, or TF32 fp32) back over S, rescales its O row when m
 //                grew by more than 2^8, and at the end writes O / l (staged in shared
 //                memory, stored by TMA) and LSE.
-// TMEM: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// TMEM: S buffers (u, b) at 64 * (2u + b), b = 0, 1; O_u at 256 + u * D.
 // Every wait is bounded (WaitCtx); a CTA that gives up records an error code, drains
 // its own copies and MMAs, frees its TMEM and exits.
 #include <cuda_bf16.h>
@@ -38,28 +39,33 @@ template <bool TF32, int D>
 struct FwdCfg {
     static constexpr int ES = TF32 ? 4 : 2;            // element bytes
     static constexpr int BM = 128;                     // query rows per subtile
+    static constexpr int BN = 64;                      // key rows per tile
     static constexpr int ROWB = D * ES;                // bytes per row
-    static constexpr int BN = (TF32 && D == 64) ? 64 : 128;  // key rows per tile
     static constexpr int NCH = ROWB / 128;             // 128-byte chunks per row
     static constexpr int EPC = 128 / ES;               // elements per chunk
     static constexpr int Q_BYTES = BM * ROWB;          // one subtile
     static constexpr int KV_BYTES = BN * ROWB;
     static constexpr int VT_BYTES = TF32 ? BN * ROWB : 0;
     static constexpr int STAGE_BYTES = 2 * KV_BYTES + VT_BYTES;
-    static constexpr int NS = (2 * Q_BYTES + 3 * STAGE_BYTES <= 200 * 1024) ? 3 : 2;
+    static constexpr int NS_FIT = (220 * 1024 - 2 * Q_BYTES) / STAGE_BYTES;
+    static constexpr int NS = NS_FIT > 6 ? 6 : NS_FIT; // K/V pipeline stages
     static constexpr int SMEM = 1024 + 2 * Q_BYTES + NS * STAGE_BYTES;
-    static constexpr int O_COL = 256;
+    static constexpr int O_COL = 256;                  // O_u at O_COL + u*D
     static constexpr int S_KSTEPS = ROWB / 32;         // 32-byte K-steps of S = Q K^T
     static constexpr int PV_KSTEPS = BN * ES / 32;     // K-steps of O += P V
     static constexpr int PV_ROWS = 32 / ES;            // key rows per PV K-step
     static constexpr uint32_t FMT_S = TF32 ? FMT_TF32 : FMT_F16;
     static constexpr uint32_t FMT_PV = TF32 ? FMT_TF32 : FMT_BF16;
     static constexpr int MODE = TF32 ? ROPE_TF32 : ROPE_F16;
-    static constexpr int THREADS = 384;
+    static constexpr int THREADS = 416;             // 13 warps
     static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
-    static_assert(D <= 128, "two O subtiles must fit next to two S tiles in 512 TMEM columns");
+    static_assert(D <= 128, "O subtiles must fit next to four S buffers in 512 TMEM columns");
+    static_assert(NS >= 3, "need at least three K/V stages (S runs two tiles ahead)");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
+
+// TMEM column of S buffer `buf` (0/1) of subtile u.
+__device__ __forceinline__ uint32_t s_col(int u, int buf) { return (uint32_t)((u * 2 + buf) * 64); }
 
 // TF32 only: Vt[d][r] = tf32(V[r][d]) for a [ROWS x D] fp32 tile, written K-major (key
 // index contiguous, 32 keys per 128-byte chunk); NT threads.
@@ -82,8 +88,98 @@ __device__ __forceinline__ void transpose_v_tf32(const uint8_t* src, uint8_t* ds
     }
 }
 
+// Per-row online-softmax state of one softmax thread.
+struct RowState {
+    float m_used;   // max (log2 domain, scaled) the exponentials are taken against
+    float l;        // running sum of exp2(x * sl2 - m_used)
+};
+
+// One key tile of one softmax thread: mask, max, rescale decision (and O rescale),
+// exp2, P written back over this tile's S buffer, p_ready arrival.  Returns false
+// when a wait ran out.
 template <bool TF32, int D>
-__global__ void __launch_bounds__(384, 1)
+__device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int u, int qsub0, int qpos, uint32_t lt,
+                                             float sl2, RowState& st, uint64_t* bar_o_done, uint64_t* bar_p_ready,
+                                             const WaitCtx& w) {
+    using C = FwdCfg<TF32, D>;
+    const int kv0 = j * C::BN;
+    if (kv0 + C::BN - 1 > qsub0) {   // tile crosses the diagonal: mask keys after the row
+#pragma unroll
+        for (int e = 0; e < C::BN; ++e)
+            if (kv0 + e > qpos) sr[e] = __float_as_uint(kNegInf);
+    }
+    // Row max over 8 independent chains (a single dependent chain would serialise on
+    // the max latency: one warp per SMSP runs this).
+    float m8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m8[k] = __uint_as_float(sr[k]);
+#pragma unroll
+    for (int e = 8; e < C::BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
+    const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+    const float m_tile = mx * sl2;
+    // An fp16 operand that overflowed (|rotated q or k| > 65504) turns logits into inf or
+    // NaN; a finite row max rules that out for the whole row (masked rows are -inf).
+    if (!(fabsf(mx) < __int_as_float(0x7f800000)) && !(mx == kNegInf)) { if (w.err) atomicCAS(w.err, 0, SITE_RANGE); }
+    // A row whose max grew by more than 2^8 rescales l and its O row; the others keep
+    // their max (p <= 2^8 stays exact).  TMEM access is warp-collective, so a warp
+    // rescales when any lane needs it (alpha = 1 elsewhere).  O is idle once the PV of
+    // tile j-1 is done (it is issued before P of tile j can be consumed).
+    const bool need = j > 0 && m_tile > st.m_used + 8.f;
+    if (j == 0) st.m_used = m_tile;
+    if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2(st.m_used - m_tile) : 1.f;
+        st.l *= alpha;
+        if (need) st.m_used = m_tile;
+        if (!mbar_wait_warp(smem_u32(&bar_o_done[u]), (j - 1) & 1, w, SITE_FWD_O_DONE)) return false;
+        tc_fence_after();
+        const uint32_t oc = C::O_COL + u * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 16) {   // 16 columns at a time: two S tiles are live in registers
+            uint32_t orow[16];
+            tmem_ld16(lt + oc + c, orow);
+            tmem_wait_ld16(orow);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
+            tmem_st16(lt + oc + c, orow);
+        }
+    }
+    float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float neg_m = -st.m_used;
+    const uint32_t sc = lt + s_col(u, j & 1);
+#pragma unroll
+    for (int c = 0; c < C::BN; c += 32) {
+        if constexpr (TF32) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float p = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, neg_m));
+                s8[e & 7] += p;
+                pk[e] = f32_to_tf32_rna(p);
+            }
+            tmem_st32(sc + c, pk);
+        } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, neg_m));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[c + e + 1]), sl2, neg_m));
+                s8[e & 7] += p0;
+                s8[(e + 1) & 7] += p1;
+                pk[e >> 1] = pack_bf162(p0, p1);
+            }
+            tmem_st16(sc + (c >> 1), pk);
+        }
+    }
+    st.l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&bar_p_ready[u * 2 + (j & 1)]));
+    return true;
+}
+
+template <bool TF32, int D>
+__global__ void __launch_bounds__(416, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FwdArgs a) {
@@ -94,7 +190,8 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* sStage = sQ + 2 * C::Q_BYTES;            // NS x (K | V | Vt)
 
     __shared__ __align__(8) uint64_t bar_q_full, bar_final;
-    __shared__ __align__(8) uint64_t bar_q_ready[2], bar_s_full[2], bar_p_ready[2], bar_o_done[2], bar_o_staged[2];
+    __shared__ __align__(8) uint64_t bar_q_ready[2], bar_o_done[2], bar_o_staged[2];
+    __shared__ __align__(8) uint64_t bar_s_full[4], bar_p_ready[4];     // [u * 2 + buffer]
     __shared__ __align__(8) uint64_t bar_kv_full[C::NS], bar_k_ready[C::NS], bar_kv_empty[C::NS];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -116,18 +213,20 @@ __global__ void __launch_bounds__(384, 1)
 
     if (tid == 0) {
         mbar_init(smem_u32(&bar_q_full), 1);
-        mbar_init(smem_u32(&bar_final), 1);
+        mbar_init(smem_u32(&bar_final), 2);              // one commit per UMMA issuer
         for (int u = 0; u < 2; ++u) {
             mbar_init(smem_u32(&bar_q_ready[u]), 128);
-            mbar_init(smem_u32(&bar_s_full[u]), 1);
-            mbar_init(smem_u32(&bar_p_ready[u]), 128);
             mbar_init(smem_u32(&bar_o_done[u]), 1);
             mbar_init(smem_u32(&bar_o_staged[u]), 128);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(smem_u32(&bar_s_full[i]), 1);
+            mbar_init(smem_u32(&bar_p_ready[i]), 128);
         }
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(smem_u32(&bar_kv_full[s]), 1);
             mbar_init(smem_u32(&bar_k_ready[s]), 64);
-            mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+            mbar_init(smem_u32(&bar_kv_empty[s]), 2);    // one commit per UMMA issuer
         }
         abort_flag = 0;
         fence_mbar_init();
@@ -177,78 +276,99 @@ __global__ void __launch_bounds__(384, 1)
             for (int j = max(0, issued - C::NS); j < issued; ++j)
                 mbar_wait_drain(smem_u32(&bar_kv_full[j % C::NS]), (j / C::NS) & 1, w, SITE_FWD_DRAIN);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ UMMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ UMMA issuers
+        // A single thread issues a tcgen05.mma only every ~100 cycles, so each subtile
+        // has its own issuer (lane 0 of warp 1 + u).  S_u(j) goes to S buffer j % 2,
+        // two tiles ahead of the softmax, and overwrites P_u(j-2), whose PV the same
+        // thread issued earlier (one thread's UMMAs execute in order).
+        const int u = warp - 1;
+        const int n = n_u[u];
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_make(C::FMT_S, 128, C::BN, false, false);
             constexpr uint32_t id_o = idesc_make(C::FMT_PV, 128, D, false, !TF32);
-            auto issue_s = [&](int u, int j) {
-                const int s = j % C::NS;
-                const uint32_t qa = smem_u32(sQ + u * C::Q_BYTES), ka = smem_u32(stage_k(s));
+            // Descriptors are built once; a K-step or a stage only moves the start address.
+            const uint64_t dq = sdesc(smem_u32(sQ + u * C::Q_BYTES), 16, 1024);
+            const uint64_t dk0 = sdesc(smem_u32(stage_k(0)), 16, 1024);
+            const uint64_t dv0 = TF32 ? sdesc(smem_u32(stage_vt(0)), 16, 1024)
+                                      : sdesc(smem_u32(stage_v(0)), C::BN * 128, 1024);
+            const uint32_t ocol = tm + C::O_COL + u * D;
+            auto issue_s = [&](int j) {
+                const uint64_t dk = sdesc_add(dk0, (j % C::NS) * C::STAGE_BYTES);
+                const uint32_t dcol = tm + s_col(u, j & 1);
 #pragma unroll
                 for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
                     const uint32_t byte = ks * 32;
-                    umma_ss<TF32>(tm + u * 128, sdesc(qa + (byte >> 7) * C::BM * 128 + (byte & 127), 16, 1024),
-                                  sdesc(ka + (byte >> 7) * C::BN * 128 + (byte & 127), 16, 1024), id_s, ks > 0);
+                    umma_ss<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
+                                  sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
                 }
-                umma_commit(smem_u32(&bar_s_full[u]));
+                umma_commit(smem_u32(&bar_s_full[u * 2 + (j & 1)]));
             };
-            auto issue_pv = [&](int u, int j) -> bool {
-                if (!mbar_wait(smem_u32(&bar_p_ready[u]), j & 1, w, SITE_FWD_P_READY)) return false;
+            auto issue_pv = [&](int j) -> bool {
+                if (!mbar_wait(smem_u32(&bar_p_ready[u * 2 + (j & 1)]), (j >> 1) & 1, w, SITE_FWD_P_READY))
+                    return false;
                 tc_fence_after();
-                const int s = j % C::NS;
+                const uint64_t dv = sdesc_add(dv0, (j % C::NS) * C::STAGE_BYTES);
+                const uint32_t pcol = tm + s_col(u, j & 1);
 #pragma unroll
                 for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
-                    uint64_t bd;
-                    if constexpr (TF32) {
-                        const uint32_t byte = ks * 32;   // V^T [D x BN], K-major, 32 keys per chunk
-                        bd = sdesc(smem_u32(stage_vt(s)) + (byte >> 7) * D * 128 + (byte & 127), 16, 1024);
-                    } else {                            // V [BN x D], MN-major, D chunks BN*128 apart
-                        bd = sdesc(smem_u32(stage_v(s)) + ks * C::PV_ROWS * 128, C::BN * 128, 1024);
-                    }
-                    umma_ts<TF32>(tm + C::O_COL + u * D, tm + u * 128 + ks * 8, bd, id_o, (j > 0 || ks > 0) ? 1u : 0u);
+                    // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
+                    // MN-major, PV_ROWS keys per K-step.
+                    const uint32_t off = TF32 ? ((ks * 32) >> 7) * D * 128 + ((ks * 32) & 127) : ks * C::PV_ROWS * 128;
+                    umma_ts<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(smem_u32(&bar_o_done[u]));
                 return true;
             };
-            bool ok = true;
-            for (int u = 0; u < n_qsub && ok; ++u) ok = mbar_wait(smem_u32(&bar_q_ready[u]), 0, w, SITE_FWD_Q);
-            ok = ok && mbar_wait(smem_u32(&bar_k_ready[0]), 0, w, SITE_FWD_K_READY);
-            if (ok) {
+            auto k_ready = [&](int j) {
+                const bool r = mbar_wait(smem_u32(&bar_k_ready[j % C::NS]), (j / C::NS) & 1, w, SITE_FWD_K_READY);
                 tc_fence_after();
-                if (n_u[0] > 0) issue_s(0, 0);
-                if (n_u[1] > 0) issue_s(1, 0);
+                return r;
+            };
+            // A subtile beyond T (n == 0) issues nothing but still releases every stage.
+            bool ok = n == 0 || mbar_wait(smem_u32(&bar_q_ready[u]), 0, w, SITE_FWD_Q);
+            for (int j = 0; ok && j < 2 && j < n; ++j) {
+                if (!(ok = k_ready(j))) break;
+                issue_s(j);
             }
+            // Every stage of the CTA's key range is released by both issuers.  The
+            // subtile with fewer tiles releases its tail without using it, but only once
+            // the stage really holds that tile (k_ready), so it never runs a phase ahead.
             for (int j = 0; ok && j < n_kv; ++j) {
-                if (j < n_u[0] && !(ok = issue_pv(0, j))) break;
-                const bool nxt = j + 1 < n_kv;
-                if (nxt) {
-                    const int s1 = (j + 1) % C::NS;
-                    if (!(ok = mbar_wait(smem_u32(&bar_k_ready[s1]), ((j + 1) / C::NS) & 1, w, SITE_FWD_K_READY)))
-                        break;
-                    tc_fence_after();
-                    if (j + 1 < n_u[0]) issue_s(0, j + 1);
+                if (j < n) {
+                    if (!(ok = issue_pv(j))) break;
+                    if (j + 2 < n) {
+                        if (!(ok = k_ready(j + 2))) break;
+                        issue_s(j + 2);
+                    }
+                } else if (!(ok = k_ready(j))) {
+                    break;
                 }
-                if (j < n_u[1] && !(ok = issue_pv(1, j))) break;
                 umma_commit(smem_u32(&bar_kv_empty[j % C::NS]));
-                if (nxt && j + 1 < n_u[1]) issue_s(1, j + 1);
             }
             umma_commit(smem_u32(&bar_final));
         }
-    } else if (warp < 4) {
+    } else if (warp == 3 || warp == 12) {
         // ------------------------------------------------------------ RoPE on K (+ V^T)
-        const int rt = tid - 64;
-        bool ovf = false;
+        const int rt = lane + (warp == 12 ? 32 : 0);
+        using Rope = RopeTile<D, C::BN, 64, C::MODE>;
+        Rope rope;
+        rope.init(rt, a.rope);
+        float4 next[Rope::F4];
+        rope.load_base(next, 0, T, a.rope);
         for (int j = 0; j < n_kv; ++j) {
             const int s = j % C::NS;
+            float4 cur[Rope::F4];
+#pragma unroll
+            for (int e = 0; e < Rope::F4; ++e) cur[e] = next[e];
+            if (j + 1 < n_kv) rope.load_base(next, (j + 1) * C::BN, T, a.rope);   // one tile early
             if (!mbar_wait_warp(smem_u32(&bar_kv_full[s]), (j / C::NS) & 1, w, SITE_FWD_KV_FULL)) break;
             if constexpr (TF32) transpose_v_tf32<D, C::BN, 64>(stage_v(s), stage_vt(s), rt);
-            ovf |= rope_tile_smem<D, C::BN, 64, C::MODE>(stage_k(s), nullptr, j * C::BN, T, rt, a.rope);
+            rope.template apply<false>(stage_k(s), nullptr, cur);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready[s]));
         }
-        if (ovf) atomicCAS(a.err, 0, SITE_RANGE);
-    } else {
+    } else if (warp < 12) {
         // ------------------------------------------------------------ softmax (subtile u)
         const int u = (warp - 4) >> 2;
         const int r = tid - 128 - 128 * u;            // query row = TMEM lane
@@ -256,97 +376,33 @@ __global__ void __launch_bounds__(384, 1)
         const int qpos = qsub0 + r;
         const int n = n_u[u];
         const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t s_col = u * 128, o_col = C::O_COL + u * D;
+        const uint32_t o_col = C::O_COL + u * D;
         uint8_t* sQu = sQ + u * C::Q_BYTES;
         const float sl2 = a.scale_log2;
-        float m_used = kNegInf, l = 0.f;
+        RowState st{kNegInf, 0.f};
         bool ok = n > 0;
         if (ok && mbar_wait_warp(smem_u32(&bar_q_full), 0, w, SITE_FWD_Q)) {
-            if (rope_tile_smem<D, C::BM, 128, C::MODE>(sQu, nullptr, qsub0, T, r, a.rope))
-                atomicCAS(a.err, 0, SITE_RANGE);
+            rope_tile_smem<D, C::BM, 128, C::MODE, false>(sQu, nullptr, qsub0, T, r, a.rope);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_q_ready[u]));
         } else {
             ok = false;
         }
         for (int j = 0; ok && j < n; ++j) {
-            if (!mbar_wait_warp(smem_u32(&bar_s_full[u]), j & 1, w, SITE_FWD_S_FULL)) { ok = false; break; }
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[u * 2 + (j & 1)]), (j >> 1) & 1, w, SITE_FWD_S_FULL)))
+                break;
             tc_fence_after();
-            uint32_t sr[C::BN];
-            tmem_ld_cols<C::BN / 32>(lt + s_col, sr);
-            const int kv0 = j * C::BN;
-            if (kv0 + C::BN - 1 > qsub0) {          // tile crosses the diagonal: mask j > i
-#pragma unroll
-                for (int e = 0; e < C::BN; ++e)
-                    if (kv0 + e > qpos) sr[e] = __float_as_uint(kNegInf);
-            }
-            // Row max over 8 independent chains (one warp per SMSP runs this: a single
-            // dependent chain of BN maxes would serialise on the FMNMX latency).
-            float m8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = __uint_as_float(sr[k]);
-#pragma unroll
-            for (int e = 8; e < C::BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            const float m_tile = mx * sl2;
-            // A row whose max grew by more than 2^8 rescales l and its O row; the others
-            // keep their max (p <= 2^8 stays exact).  TMEM access is warp-collective, so
-            // a warp rescales when any lane needs it (alpha = 1 elsewhere).  O is idle
-            // here: the PV of tile j-1 finished before S of tile j was issued.
-            const bool need = j > 0 && m_tile > m_used + 8.f;
-            if (j == 0) m_used = m_tile;
-            if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? ex2(m_used - m_tile) : 1.f;
-                l *= alpha;
-                if (need) m_used = m_tile;
-                if (!mbar_wait_warp(smem_u32(&bar_o_done[u]), (j - 1) & 1, w, SITE_FWD_O_DONE)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t orow[32];
-                    tmem_ld_cols<1>(lt + o_col + c, orow);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
-                    tmem_st32(lt + o_col + c, orow);
-                }
-            }
-            float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            const float neg_m = -m_used;
-#pragma unroll
-            for (int c = 0; c < C::BN; c += 32) {
-                if constexpr (TF32) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float p = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, neg_m));
-                        s8[e & 7] += p;
-                        pk[e] = f32_to_tf32_rna(p);
-                    }
-                    tmem_st32(lt + s_col + c, pk);
-                } else {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(sr[c + e + 1]), sl2, neg_m));
-                        s8[e & 7] += p0;
-                        s8[(e + 1) & 7] += p1;
-                        pk[e >> 1] = pack_bf162(p0, p1);
-                    }
-                    tmem_st16(lt + s_col + (c >> 1), pk);
-                }
-            }
-            l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_p_ready[u]));
+            uint32_t sr[64];
+            tmem_ld_cols<2>(lt + s_col(u, j & 1), sr);
+            if (!(ok = softmax_tile<TF32, D>(sr, j, u, qsub0, qpos, lt, sl2, st, bar_o_done, bar_p_ready, w))) break;
         }
         // Epilogue: O / l staged (swizzled) in this subtile's Q buffer, stored by TMA;
-        // LSE = natural log of the partition sum of the scaled logits.
+        // LSE = natural log of the partition sum of the scaled logits.  The last two
+        // PVs may both be in flight: wait for them in order (parity would alias).
+        if (ok && n >= 2) ok = mbar_wait_warp(smem_u32(&bar_o_done[u]), (n - 2) & 1, w, SITE_FWD_O_DONE);
         if (ok && mbar_wait_warp(smem_u32(&bar_o_done[u]), (n - 1) & 1, w, SITE_FWD_O_DONE)) {
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float inv_l = 1.f / st.l;
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
                 uint32_t orow[32];
@@ -374,7 +430,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_o_staged[u]));
-            if (qpos < T) a.lse[((size_t)b * a.Hq + h) * T + qpos] = (m_used + log2f(l)) * 0.6931471805599453f;
+            if (qpos < T) a.lse[((size_t)b * a.Hq + h) * T + qpos] = (st.m_used + log2f(st.l)) * 0.6931471805599453f;
             if (r == 0 && mbar_wait(smem_u32(&bar_o_staged[u]), 0, w, SITE_FWD_O_DONE)) {
                 for (int c = 0; c < C::NCH; ++c)
                     tma_store_4d(&tm_o, smem_u32(sQu + c * C::BM * 128), c * C::EPC, h, qsub0, b);
@@ -409,7 +465,7 @@ cudaError_t launch_fwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, co
 
 }  // namespace
 
-int fwd_kv_box_rows(bool tf32, int D) { return (tf32 && D == 64) ? 64 : 128; }
+int fwd_kv_box_rows(bool tf32, int D) { return 64; }
 
 cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {

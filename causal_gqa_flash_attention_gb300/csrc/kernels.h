@@ -20,6 +20,12 @@ enum WaitSite : int {
     SITE_RANGE = 0x401,
 };
 
+// Rows of the interleaved RoPE table the kernels read: at least this many (shorter
+// sequences get a padded table), because the in-kernel angle-addition steps read
+// table row RSTEP (at most 32).
+constexpr int kRopeTableMinRows = 64;
+inline int rope_table_rows(int T) { return T > kRopeTableMinRows ? T : kRopeTableMinRows; }
+
 struct FwdArgs {
     void* o;                 // [B,T,Hq,D], input dtype
     float* lse;              // [B,Hq,T]

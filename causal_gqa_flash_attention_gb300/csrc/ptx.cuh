@@ -78,6 +78,8 @@ __device__ __forceinline__ void raise_error(const WaitCtx& w, int code) {
 }
 
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, int code) {
+    for (int i = 0; i < 16; ++i)   // short poll first: a sleeping thread wakes up late
+        if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
@@ -245,6 +247,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, ui
 // Operand formats of the instruction descriptor (kind::f16 takes F16 or BF16,
 // kind::tf32 takes TF32; A and B always share one format).
 enum : uint32_t { FMT_F16 = 0, FMT_BF16 = 1, FMT_TF32 = 2 };
+
+// The start-address field is the descriptor's low 14 bits (address >> 4); moving a
+// descriptor by `bytes` inside the same shared window adds bytes >> 4 to it.  Operand
+// tiles never cross the 256 KB window, so no carry reaches the next field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
 // Instruction descriptor, fp32 accumulate, dense.  a_mn / b_mn select MN-major
 // (transposed) operands.

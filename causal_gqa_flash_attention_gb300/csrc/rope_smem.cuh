@@ -4,10 +4,13 @@
 // (x0, x1) -> (x0 c - x1 s, x0 s + x1 c)).
 //
 // A tile is [ROWS x D] in the 128-byte-swizzled layout TMA writes (one 128-byte chunk
-// of the row per ROWS*128-byte slab).  NT threads split the tile into 16-byte units;
-// each thread loads the cos/sin of a batch of units first (the table lives in L2) and
-// only then rotates, so the table latency is paid once per batch.  Rows at or beyond T
-// hold TMA's zero fill; they use the table row of position 0 and stay zero.
+// of the row per ROWS*128-byte slab), split in 16-byte units.  Thread t of NT always
+// takes the same unit u = t % UPR (so the same PPU frequency pairs) of rows
+// r0 = t / UPR, r0 + RSTEP, r0 + 2*RSTEP, ... with RSTEP = NT / UPR.  Its angles
+// therefore form an arithmetic progression: the cos/sin of the first row come from the
+// table (one load per tile, which the caller can issue a tile early) and every further
+// row is reached by one more rotation by RSTEP*w (angle addition; the step is the
+// table row RSTEP).  Rows at or beyond T hold TMA's zero fill and stay zero.
 //
 // Output forms:
 //   ROPE_F16       bf16 in -> fp16 in place (logit operand: 3 more mantissa bits than
@@ -17,6 +20,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include "kernels.h"
 #include "ptx.cuh"
 
 namespace ne {
@@ -38,53 +42,55 @@ __device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Largest finite fp16 is 65504; a rotated value above it would become inf.
-__device__ __forceinline__ bool f16_overflow(float a) { return fabsf(a) > 65504.f; }
-
-// Rotates rows [pos0, pos0 + ROWS) of a tile; thread t of NT.  Returns true if an
-// fp16 output would have overflowed (the caller reports it).
 template <int D, int ROWS, int NT, int MODE>
-__device__ __forceinline__ bool rope_tile_smem(uint8_t* base, uint8_t* dst16, int pos0, int T, int t,
-                                               const float2* __restrict__ rope) {
-    constexpr int ES = MODE == ROPE_TF32 ? 4 : 2;
-    constexpr int UPR = D * ES / 16;           // 16-byte units per row
-    constexpr int PPU = 16 / ES / 2;           // (cos, sin) pairs per unit: 4 or 2
-    constexpr int F4 = PPU / 2;                // float4 table loads per unit
-    constexpr int TOTAL = ROWS * UPR;
-    static_assert(TOTAL % NT == 0, "tile units must split evenly");
-    constexpr int PER = TOTAL / NT;
-    constexpr int BATCH = PER < 8 ? PER : 8;
-    static_assert(PER % BATCH == 0, "batches must split evenly");
-    bool overflow = false;
+struct RopeTile {
+    static constexpr int ES = MODE == ROPE_TF32 ? 4 : 2;
+    static constexpr int UPR = D * ES / 16;        // 16-byte units per row
+    static constexpr int PPU = 16 / ES / 2;        // (cos, sin) pairs per unit: 4 or 2
+    static constexpr int F4 = PPU / 2;             // float4 table reads per unit
+    static constexpr int RSTEP = NT / UPR;         // rows between a thread's units
+    static constexpr int KSTEPS = ROWS / RSTEP;    // units per thread per tile
+    static_assert(NT % UPR == 0 && ROWS % RSTEP == 0, "thread layout");
+    static_assert(RSTEP < kRopeTableMinRows, "step row must exist in the table");
+
+    int unit, r0;
+    float4 step[F4];                               // (cos, sin) of RSTEP * w for this unit's pairs
+
+    __device__ __forceinline__ void init(int t, const float2* __restrict__ rope) {
+        unit = t % UPR;
+        r0 = t / UPR;
+        const float4* sp = reinterpret_cast<const float4*>(rope + (size_t)RSTEP * (D / 2) + unit * PPU);
 #pragma unroll
-    for (int b0 = 0; b0 < PER; b0 += BATCH) {
-        float4 tab[BATCH][F4];
-        uint4 raw[BATCH];
-        uint32_t off[BATCH];
+        for (int e = 0; e < F4; ++e) step[e] = __ldg(sp + e);
+    }
+    // cos/sin of this thread's first row of the tile starting at position pos0.
+    __device__ __forceinline__ void load_base(float4 (&b)[F4], int pos0, int T,
+                                              const float2* __restrict__ rope) const {
+        const int pos = pos0 + r0 < T ? pos0 + r0 : 0;
+        const float4* bp = reinterpret_cast<const float4*>(rope + (size_t)pos * (D / 2) + unit * PPU);
 #pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-            const int ul = t + (b0 + k) * NT;
-            const int row = ul / UPR, unit = ul % UPR;
-            const int pos = pos0 + row < T ? pos0 + row : 0;
-            off[k] = (unit >> 3) * ROWS * 128 + sw128_offset(row, unit & 7);
-            const float4* tp = reinterpret_cast<const float4*>(rope + (size_t)pos * (D / 2) + unit * PPU);
+        for (int e = 0; e < F4; ++e) b[e] = __ldg(bp + e);
+    }
+    // Rotates the tile; with CHECK, returns true if an fp16 output would have overflowed
+    // (without, the caller detects overflow downstream and this returns false).
+    template <bool CHECK = true>
+    __device__ __forceinline__ bool apply(uint8_t* base, uint8_t* dst16, float4 (&b)[F4]) const {
+        float amax = 0.f;
 #pragma unroll
-            for (int e = 0; e < F4; ++e) tab[k][e] = __ldg(tp + e);
-            raw[k] = *reinterpret_cast<const uint4*>(base + off[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
+        for (int k = 0; k < KSTEPS; ++k) {
+            const int row = r0 + k * RSTEP;
+            const uint32_t off = (unit >> 3) * ROWS * 128 + sw128_offset(row, unit & 7);
+            const uint4 raw = *reinterpret_cast<const uint4*>(base + off);
             if constexpr (MODE == ROPE_TF32) {
-                const float4 cs = tab[k][0];
-                const float x0 = __uint_as_float(raw[k].x), x1 = __uint_as_float(raw[k].y);
-                const float x2 = __uint_as_float(raw[k].z), x3 = __uint_as_float(raw[k].w);
-                *reinterpret_cast<uint4*>(base + off[k]) =
+                const float4 cs = b[0];
+                const float x0 = __uint_as_float(raw.x), x1 = __uint_as_float(raw.y);
+                const float x2 = __uint_as_float(raw.z), x3 = __uint_as_float(raw.w);
+                *reinterpret_cast<uint4*>(base + off) =
                     make_uint4(f32_to_tf32_rna(x0 * cs.x - x1 * cs.y), f32_to_tf32_rna(x0 * cs.y + x1 * cs.x),
                                f32_to_tf32_rna(x2 * cs.z - x3 * cs.w), f32_to_tf32_rna(x2 * cs.w + x3 * cs.z));
             } else {
-                const float cs[8] = {tab[k][0].x, tab[k][0].y, tab[k][0].z, tab[k][0].w,
-                                     tab[k][1].x, tab[k][1].y, tab[k][1].z, tab[k][1].w};
-                const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+                const float cs[8] = {b[0].x, b[0].y, b[0].z, b[0].w, b[1].x, b[1].y, b[1].z, b[1].w};
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
                 uint32_t o16[4], ob[4];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
@@ -92,20 +98,39 @@ __device__ __forceinline__ bool rope_tile_smem(uint8_t* base, uint8_t* dst16, in
                     const float x0 = __low2float(v), x1 = __high2float(v);
                     const float c = cs[2 * p], s = cs[2 * p + 1];
                     const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
-                    overflow |= f16_overflow(y0) | f16_overflow(y1);
+                    if constexpr (CHECK) amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
                     o16[p] = pack_half2(y0, y1);
                     if constexpr (MODE == ROPE_BF16_F16) ob[p] = pack_bf162(y0, y1);
                 }
                 if constexpr (MODE == ROPE_F16) {
-                    *reinterpret_cast<uint4*>(base + off[k]) = make_uint4(o16[0], o16[1], o16[2], o16[3]);
+                    *reinterpret_cast<uint4*>(base + off) = make_uint4(o16[0], o16[1], o16[2], o16[3]);
                 } else {
-                    *reinterpret_cast<uint4*>(base + off[k]) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-                    *reinterpret_cast<uint4*>(dst16 + off[k]) = make_uint4(o16[0], o16[1], o16[2], o16[3]);
+                    *reinterpret_cast<uint4*>(base + off) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                    *reinterpret_cast<uint4*>(dst16 + off) = make_uint4(o16[0], o16[1], o16[2], o16[3]);
+                }
+            }
+            if (k + 1 < KSTEPS) {   // advance every pair's angle by RSTEP * w
+#pragma unroll
+                for (int e = 0; e < F4; ++e) {
+                    const float4 c = b[e], s = step[e];
+                    b[e] = make_float4(c.x * s.x - c.y * s.y, c.y * s.x + c.x * s.y,
+                                       c.z * s.z - c.w * s.w, c.w * s.z + c.z * s.w);
                 }
             }
         }
+        return amax > 65504.f;   // largest finite fp16
     }
-    return overflow;
+};
+
+// One-shot form: rotate rows [pos0, pos0 + ROWS) of a tile with thread t of NT.
+template <int D, int ROWS, int NT, int MODE, bool CHECK = true>
+__device__ __forceinline__ bool rope_tile_smem(uint8_t* base, uint8_t* dst16, int pos0, int T, int t,
+                                               const float2* __restrict__ rope) {
+    RopeTile<D, ROWS, NT, MODE> rt;
+    rt.init(t, rope);
+    float4 b[RopeTile<D, ROWS, NT, MODE>::F4];
+    rt.load_base(b, pos0, T, rope);
+    return rt.template apply<CHECK>(base, dst16, b);
 }
 
 }  // namespace ne

@@ -86,6 +86,7 @@ def check(q, k, v, dO, dtype, theta=10000.0, bwd=True):
     (1, 127, 6, 2, 64),
     (1, 5, 2, 1, 64),
     (3, 1, 4, 2, 64),        # T = 1: every row attends to itself only
+    (1, 600, 4, 1, 64),      # last CTA: second subtile past T while the K/V ring wraps
     (1, 384, 8, 2, 128),     # head_dim 128
     (1, 200, 4, 1, 128),
 ])
