@@ -14,13 +14,17 @@
 //             (head, query tile) step adds its dS K' into the fp32 dQ accumulator;
 //   bwd_post  dQ = s R^T (accumulator), cast to the output dtype.
 //
-// bwd_main warp roles (512 threads):
+// bwd_main warp roles (512 threads).  One thread issues a tcgen05.mma only every
+// ~100 cycles, so three warps issue UMMAs, each for its own accumulators:
 //   warp 0      TMA producer: K, V once; Q and dO tiles into a ring.
-//   warp 1      TMEM allocator (all 512 columns) and UMMA issuer.
-//   warps 4-7   RoPE: rotate K once and every Q tile in place.
-//   warps 8-11  thread = key row: P^T and dS^T from S^T, dP^T, LSE, Delta; P^T to TMEM,
-//               dS^T (bf16) to shared memory; at the end dK (inverse rotation) and dV.
-//   warps 12-15 thread = query row: drain dQ from TMEM into the fp32 accumulator.
+//   warp 1      TMEM allocator (all 512 columns); issuer A: S^T = K'Q'^T (fp16), dP^T = V dO^T.
+//   warp 2      issuer B: dV += P^T dO (P^T from TMEM), dK' += dS^T Q'.
+//   warp 3      issuer C: dQ' partial = dS K'.
+//   warps 4-7   RoPE on K once and on every Q tile; drain of the dQ partial (thread =
+//               query row) into the fp32 accumulator with 16-byte atomics.
+//   warps 8-15  two groups, thread = key row, each on half of the query columns: P^T
+//               and dS^T from S^T, dP^T, LSE, Delta; P^T to TMEM, dS^T (bf16) to shared
+//               memory; at the end group 0 writes dK (inverse rotation), group 1 dV.
 #include <cuda_bf16.h>
 #include "kernels.h"
 #include "ptx.cuh"
@@ -120,6 +124,16 @@ struct BwdCfg {
     static constexpr int DK_COL = 256 + D;
     static constexpr int DQ_COL = D <= 64 ? 256 + 2 * D : 128;  // D = 128 shares dP^T's columns
     static constexpr bool DQ_ALIASES_DP = D > 64;
+    // P^T (bf16, 64 packed columns): its own columns when they fit (D = 64), so the next
+    // step's S^T can be issued before dV has read P^T; over S^T otherwise.
+    static constexpr bool PT_OWN = 256 + 3 * D + 64 <= 512;
+    static constexpr int PT_COL = PT_OWN ? 256 + 3 * D : 0;
+    // Packed P^T column of query column q (TMEM column pair q/2).  Sharing S^T's columns,
+    // each half of the queries is packed into the first half of its own 64 S^T columns,
+    // which its group has already read.
+    static __device__ __forceinline__ int pt_col(int q) {
+        return PT_OWN ? PT_COL + (q >> 1) : S_COL + (q >> 1) + ((q >> 6) << 5);
+    }
     static constexpr int KSTEPS_D = ROWB / 32;      // K-steps over head_dim
     static constexpr int KSTEPS_Q = BQ / 16;        // K-steps over query rows
     static constexpr int KSTEPS_KV = BKV / 16;      // K-steps over key rows
@@ -143,10 +157,9 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t* sdS = C::DS_ALIASES_Q16 ? sStage + C::Q_BYTES : sStage + C::NQS * C::STAGE_BYTES;
     auto stage_q = [&](int s) { return sStage + s * C::STAGE_BYTES; };
     auto stage_q16 = [&](int s) { return sStage + s * C::STAGE_BYTES + C::Q_BYTES; };
-    auto stage_do = [&](int s) { return sStage + s * C::STAGE_BYTES + 2 * C::Q_BYTES; };
 
     __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_s_full, bar_dp_full, bar_ds_ready,
-        bar_ds_free, bar_dq_full, bar_dq_free, bar_dkv_full, bar_final;
+        bar_p_free, bar_ds_free, bar_dq_full, bar_dq_free, bar_dkv_full, bar_final, bar_sdp_read;
     __shared__ __align__(8) uint64_t bar_qdo_full[C::NQS], bar_q_ready[C::NQS], bar_qdo_empty[C::NQS];
     __shared__ __align__(8) uint64_t bar_rows[2];   // LSE/Delta of a query tile staged (double buffer)
     __shared__ __align__(16) float s_lse[2][C::BQ];
@@ -168,18 +181,20 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(smem_u32(&bar_k_ready), 128);
         mbar_init(smem_u32(&bar_s_full), 1);
         mbar_init(smem_u32(&bar_dp_full), 1);
-        mbar_init(smem_u32(&bar_ds_ready), 128);
-        mbar_init(smem_u32(&bar_ds_free), 1);
+        mbar_init(smem_u32(&bar_ds_ready), 256);
+        mbar_init(smem_u32(&bar_p_free), 1);
+        mbar_init(smem_u32(&bar_sdp_read), 256);   // S^T and dP^T of a step are in registers
+        mbar_init(smem_u32(&bar_ds_free), 2);      // dK issuer and dQ issuer
         mbar_init(smem_u32(&bar_dq_full), 1);
         mbar_init(smem_u32(&bar_dq_free), 128);
         mbar_init(smem_u32(&bar_dkv_full), 1);
-        mbar_init(smem_u32(&bar_final), 1);
-        mbar_init(smem_u32(&bar_rows[0]), 128);
-        mbar_init(smem_u32(&bar_rows[1]), 128);
+        mbar_init(smem_u32(&bar_final), 3);        // one commit per issuer
+        mbar_init(smem_u32(&bar_rows[0]), 256);
+        mbar_init(smem_u32(&bar_rows[1]), 256);
         for (int s = 0; s < C::NQS; ++s) {
             mbar_init(smem_u32(&bar_qdo_full[s]), 1);
             mbar_init(smem_u32(&bar_q_ready[s]), 128);
-            mbar_init(smem_u32(&bar_qdo_empty[s]), 1);
+            mbar_init(smem_u32(&bar_qdo_empty[s]), 2);   // dK issuer and dQ issuer
         }
         abort_flag = 0;
         fence_mbar_init();
@@ -194,6 +209,10 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     const uint32_t tm = tmem_slot;
     const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
+
+    // Shared-memory descriptors, built once; a step or a stage only moves the start address.
+    auto kdesc = [](const void* p) { return sdesc(smem_u32(p), 16, 1024); };        // K-major
+    auto mndesc = [](const void* p, uint32_t lbo) { return sdesc(smem_u32(p), lbo, 1024); };  // MN-major
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -220,7 +239,8 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_arrive_expect_tx(f, 2 * C::Q_BYTES);
                 for (int c = 0; c < C::NCH; ++c) {
                     tma_load_4d(smem_u32(stage_q(s) + c * C::BQ * 128), &tm_q, f, c * C::EPC, h, q0, b);
-                    tma_load_4d(smem_u32(stage_do(s) + c * C::BQ * 128), &tm_do, f, c * C::EPC, h, q0, b);
+                    tma_load_4d(smem_u32(stage_q(s) + 2 * C::Q_BYTES + c * C::BQ * 128), &tm_do, f, c * C::EPC, h,
+                                q0, b);
                 }
                 ++issued;
             }
@@ -229,227 +249,297 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_wait_drain(smem_u32(&bar_qdo_full[it % C::NQS]), (it / C::NQS) & 1, w, SITE_BWD_DRAIN);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ UMMA issuer
+        // ------------------------------------------------------------ issuer A: S^T, dP^T
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_make(FMT_F16, 128, C::BQ, false, false);   // S^T (fp16 Q', K')
             constexpr uint32_t id_dp = idesc_make(FMT_BF16, 128, C::BQ, false, false); // dP^T
-            constexpr uint32_t id_dv = idesc_make(FMT_BF16, 128, D, false, true);      // dV, dK (B MN-major)
-            constexpr uint32_t id_dq = idesc_make(FMT_BF16, 128, D, true, true);       // dQ (A, B MN-major)
-            // Descriptors are built once; per step only the start address moves.
-            const uint64_t dK = sdesc(smem_u32(sK), 16, 1024), dK16 = sdesc(smem_u32(sK16), 16, 1024);
-            const uint64_t dV = sdesc(smem_u32(sV), 16, 1024);
-            const uint64_t dKmn = sdesc(smem_u32(sK), C::BKV * 128, 1024);      // K' as MN-major B of dQ
-            const uint64_t dQ0 = sdesc(smem_u32(stage_q(0)), 16, 1024);
-            const uint64_t dQmn0 = sdesc(smem_u32(stage_q(0)), C::BQ * 128, 1024);
-            const uint64_t dDS0 = sdesc(smem_u32(sdS), 16, 1024);
-            const uint64_t dDSmn0 = sdesc(smem_u32(sdS), C::BKV * 128, 1024);
-            (void)dQ0;
+            const uint64_t dK16 = kdesc(sK16), dV = kdesc(sV), dQ0 = kdesc(stage_q(0));
             bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV);
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it % C::NQS;
-                const uint32_t so = s * C::STAGE_BYTES;            // stage offset from stage 0
-                // dS^T lives in its own buffer, or (D = 128) in this stage's fp16 Q' buffer
-                const uint32_t dso = C::DS_ALIASES_Q16 ? so : 0;
-                if (!mbar_wait(smem_u32(&bar_q_ready[s]), (it / C::NQS) & 1, w, SITE_BWD_Q_READY)) break;
+                const uint32_t so = s * C::STAGE_BYTES;
+                if (!(ok = mbar_wait(smem_u32(&bar_q_ready[s]), (it / C::NQS) & 1, w, SITE_BWD_Q_READY))) break;
+                // The previous step's S^T and dP^T must have been read out of TMEM; when P^T
+                // shares S^T's columns, dV must also have read P^T.
+                if (it > 0) {
+                    const uint32_t bar = smem_u32(C::PT_OWN ? &bar_sdp_read : &bar_p_free);
+                    if (!(ok = mbar_wait(bar, (it - 1) & 1, w, SITE_BWD_DS_READY))) break;
+                }
                 tc_fence_after();
                 const uint64_t dQ16 = sdesc_add(dQ0, so + C::Q_BYTES), dO = sdesc_add(dQ0, so + 2 * C::Q_BYTES);
-                const uint64_t dQmn = sdesc_add(dQmn0, so), dOmn = sdesc_add(dQmn0, so + 2 * C::Q_BYTES);
-                const uint64_t dDS = sdesc_add(dDS0, dso), dDSmn = sdesc_add(dDSmn0, dso);
-                // S^T = K' Q'^T   [keys x queries], K = head_dim, fp16 operands
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_D; ++ks) {
+                for (int ks = 0; ks < C::KSTEPS_D; ++ks) {      // S^T = K' Q'^T, K = head_dim
                     const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
                     const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
                     umma_ss<false>(tm + C::S_COL, sdesc_add(dK16, off), sdesc_add(dQ16, offq), id_s, ks > 0);
                 }
                 umma_commit(smem_u32(&bar_s_full));
-                if constexpr (C::DQ_ALIASES_DP) {
-                    if (it > 0 && !mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE)) break;
+                if constexpr (C::DQ_ALIASES_DP) {               // dQ of the previous step sits in dP^T's columns
+                    if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE)))
+                        break;
                     tc_fence_after();
                 }
-                // dP^T = V dO^T   [keys x queries]
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_D; ++ks) {
+                for (int ks = 0; ks < C::KSTEPS_D; ++ks) {      // dP^T = V dO^T
                     const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
                     const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
                     umma_ss<false>(tm + C::DP_COL, sdesc_add(dV, off), sdesc_add(dO, offq), id_dp, ks > 0);
                 }
                 umma_commit(smem_u32(&bar_dp_full));
-                if (!mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY)) break;
+            }
+            umma_commit(smem_u32(&bar_final));
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ issuer B: dV, dK
+        if (lane == 0) {
+            constexpr uint32_t id_dv = idesc_make(FMT_BF16, 128, D, false, true);      // B MN-major
+            const uint64_t dQmn0 = mndesc(stage_q(0), C::BQ * 128), dDS0 = kdesc(sdS);
+            bool ok = true;
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % C::NQS;
+                const uint32_t so = s * C::STAGE_BYTES;
+                const uint64_t dDS = sdesc_add(dDS0, C::DS_ALIASES_Q16 ? so : 0);
+                if (!(ok = mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
                 tc_fence_after();
-                // dV += P^T dO    (P^T from TMEM, dO MN-major), K = queries
+                const uint64_t dOmn = sdesc_add(dQmn0, so + 2 * C::Q_BYTES), dQmn = sdesc_add(dQmn0, so);
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_Q; ++ks)
-                    umma_ts<false>(tm + C::DV_COL, tm + C::S_COL + ks * 8, sdesc_add(dOmn, ks * 16 * 128), id_dv,
+                for (int ks = 0; ks < C::KSTEPS_Q; ++ks)         // dV += P^T dO (P^T from TMEM)
+                    umma_ts<false>(tm + C::DV_COL, tm + C::pt_col(ks * 16), sdesc_add(dOmn, ks * 16 * 128), id_dv,
                                    (it > 0 || ks > 0) ? 1u : 0u);
-                // dK' += dS^T Q'  (dS^T K-major in smem, Q' bf16 MN-major), K = queries
+                umma_commit(smem_u32(&bar_p_free));
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_Q; ++ks) {
+                for (int ks = 0; ks < C::KSTEPS_Q; ++ks) {       // dK' += dS^T Q'
                     const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
                     umma_ss<false>(tm + C::DK_COL, sdesc_add(dDS, off), sdesc_add(dQmn, ks * 16 * 128), id_dv,
                                    (it > 0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit(smem_u32(&bar_qdo_empty[s]));
-                if constexpr (!C::DQ_ALIASES_DP) {
-                    if (it > 0 && !mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE)) break;
-                    tc_fence_after();
-                }
-                // dQ'_part = dS K'  (dS = MN-major view of dS^T, K' bf16 MN-major), K = keys
-#pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_KV; ++ks)
-                    umma_ss<false>(tm + C::DQ_COL, sdesc_add(dDSmn, ks * 16 * 128), sdesc_add(dKmn, ks * 16 * 128),
-                                   id_dq, ks > 0);
-                umma_commit(smem_u32(&bar_dq_full));
                 umma_commit(smem_u32(&bar_ds_free));
             }
             umma_commit(smem_u32(&bar_dkv_full));
             umma_commit(smem_u32(&bar_final));
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------------------ RoPE rotation
-        const int rt = tid - 128;
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ issuer C: dQ
+        if (lane == 0) {
+            constexpr uint32_t id_dq = idesc_make(FMT_BF16, 128, D, true, true);       // A, B MN-major
+            const uint64_t dKmn = mndesc(sK, C::BKV * 128), dDSmn0 = mndesc(sdS, C::BKV * 128);
+            bool ok = true;
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % C::NQS;
+                const uint64_t dDSmn = sdesc_add(dDSmn0, C::DS_ALIASES_Q16 ? s * C::STAGE_BYTES : 0);
+                if (!(ok = mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
+                if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
+                if constexpr (C::DQ_ALIASES_DP) {               // dQ overwrites dP^T: issuer A's dP^T is done
+                    if (!(ok = mbar_wait(smem_u32(&bar_dp_full), it & 1, w, SITE_BWD_DP_FULL))) break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < C::KSTEPS_KV; ++ks)        // dQ'_part = dS K'
+                    umma_ss<false>(tm + C::DQ_COL, sdesc_add(dDSmn, ks * 16 * 128), sdesc_add(dKmn, ks * 16 * 128),
+                                   id_dq, ks > 0);
+                umma_commit(smem_u32(&bar_dq_full));
+                umma_commit(smem_u32(&bar_qdo_empty[s]));
+                umma_commit(smem_u32(&bar_ds_free));
+            }
+            umma_commit(smem_u32(&bar_final));
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ RoPE on K and Q; dQ drain
+        // Thread r: RoPE units of the K tile and of every Q tile, and query row r of the dQ
+        // partial (TMEM lane r), added into the fp32 accumulator.  The Q of step it+1 is
+        // rotated before the dQ of step it is drained.
+        const int r = tid - 128;
+        const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
         bool ovf = false;
-        if (mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV)) {
-            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_BF16_F16>(sK, sK16, kv0, T, rt, a.rope);
+        auto drain = [&](int it) -> bool {
+            const int h = hkv * G + it / per_head;
+            const int qpos = (i_first + it % per_head) * C::BQ + r;
+            if (!mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, w, SITE_BWD_DQ_FULL)) return false;
+            tc_fence_after();
+            float* dst = a.dq_acc + (((size_t)b * T + (qpos < T ? qpos : 0)) * a.Hq + h) * D;
+#pragma unroll
+            for (int c = 0; c < D; c += 64) {
+                uint32_t v[64];
+                tmem_ld_cols<2>(lt + C::DQ_COL + c, v);
+                if (c + 64 >= D) {
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bar_dq_free));
+                }
+                if (qpos < T) {
+#pragma unroll
+                    for (int e = 0; e < 64; e += 4)
+                        atomicAdd(reinterpret_cast<float4*>(dst + c + e),
+                                  make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                              __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
+                }
+            }
+            return true;
+        };
+        bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
+        if (ok) {
+            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_BF16_F16>(sK, sK16, kv0, T, r, a.rope);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready));
-            for (int it = 0; it < n_it; ++it) {
+        }
+        for (int it = 0; ok && it <= n_it; ++it) {
+            if (it < n_it) {
                 const int s = it % C::NQS;
                 const int q0 = (i_first + it % per_head) * C::BQ;
-                if (!mbar_wait_warp(smem_u32(&bar_qdo_full[s]), (it / C::NQS) & 1, w, SITE_BWD_QDO_FULL)) break;
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_qdo_full[s]), (it / C::NQS) & 1, w, SITE_BWD_QDO_FULL))) break;
                 // With dS^T living in the fp16 Q' buffer, the previous step's dK/dQ MMAs
                 // must be done with it before it is overwritten.
                 if (C::DS_ALIASES_Q16 && it > 0 &&
-                    !mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE))
+                    !(ok = mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE)))
                     break;
-                ovf |= rope_tile_smem<D, C::BQ, 128, ROPE_BF16_F16>(stage_q(s), stage_q16(s), q0, T, rt, a.rope);
+                ovf |= rope_tile_smem<D, C::BQ, 128, ROPE_BF16_F16>(stage_q(s), stage_q16(s), q0, T, r, a.rope);
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&bar_q_ready[s]));
             }
+            if (it > 0 && !(ok = drain(it - 1))) break;
         }
         if (ovf) atomicCAS(a.err, 0, SITE_RANGE);
-    } else if (warp >= 8 && warp < 12) {
+    } else {
         // ------------------------------------------------------------ P^T, dS^T; dK, dV epilogue
-        const int r = tid - 256;                       // key row = TMEM lane
+        // Two groups share every key row: group g (warps 8-11 / 12-15) takes query columns
+        // [64g, 64g + 64) of S^T and dP^T, so each SMSP has two such warps to overlap.
+        const int g = (warp - 8) >> 2;
+        const int r = (warp & 3) * 32 + lane;          // key row = TMEM lane
         const int kvpos = kv0 + r;
+        const int cbase = 64 * g;
         const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
         const float sl2 = a.scale_log2;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
+        // LSE/Delta of step it sit in s_lse/s_delta[it & 1]; the rows of step it+1 are
+        // fetched while step it runs and published at its end.  A buffer is rewritten only
+        // after every thread has passed the step that read it (bar_rows of the next step).
+        auto row_vals = [&](int it, float& lv, float& dv) {
             const int h = hkv * G + it / per_head;
+            const int qpos = (i_first + it % per_head) * C::BQ + cbase + (r & 63);
+            const size_t rix = ((size_t)b * a.Hq + h) * T + qpos;
+            lv = qpos < T ? a.lse[rix] * 1.4426950408889634f : 0.f;
+            dv = qpos < T ? a.delta[rix] : 0.f;
+        };
+        auto publish = [&](int it, float lv, float dv) {
+            if (r < 64) {
+                s_lse[it & 1][cbase + r] = lv;
+                s_delta[it & 1][cbase + r] = dv;
+            }
+            mbar_arrive(smem_u32(&bar_rows[it & 1]));
+        };
+        {
+            float lv, dv;
+            if (r < 64) row_vals(0, lv, dv);
+            publish(0, lv, dv);
+        }
+        for (int it = 0; it < n_it; ++it) {
             const int q0 = (i_first + it % per_head) * C::BQ;
             const int sb = it & 1;
             uint8_t* dsb = C::DS_ALIASES_Q16 ? stage_q16(it % C::NQS) : sdS;
-            {
-                const int qpos = q0 + r;
-                const size_t rix = ((size_t)b * a.Hq + h) * T + qpos;
-                s_lse[sb][r] = qpos < T ? a.lse[rix] * 1.4426950408889634f : 0.f;
-                s_delta[sb][r] = qpos < T ? a.delta[rix] : 0.f;
-            }
-            // Staged values are visible to the group once all 128 have arrived.  Buffer sb
-            // is rewritten two steps later, after every thread has passed this step.
-            mbar_arrive(smem_u32(&bar_rows[sb]));
             if (!mbar_wait_warp(smem_u32(&bar_rows[sb]), (it >> 1) & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
+            float lv_n = 0.f, dv_n = 0.f;
+            if (it + 1 < n_it && r < 64) row_vals(it + 1, lv_n, dv_n);    // in flight during this step
             const bool diag = kv0 + C::BKV - 1 > q0;
             if (!mbar_wait_warp(smem_u32(&bar_s_full), it & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
             if (!mbar_wait_warp(smem_u32(&bar_dp_full), it & 1, w, SITE_BWD_DP_FULL)) { ok = false; break; }
             if (it > 0 && !mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < C::BQ; c += 32) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(lt + C::S_COL + c, sr);
-                tmem_ld32(lt + C::DP_COL + c, dr);
-                tmem_wait_ld();
-                reg_fence32(sr);
-                reg_fence32(dr);
-                uint32_t pk[16], dk[16];
-                const float4* l4 = reinterpret_cast<const float4*>(&s_lse[sb][c]);
-                const float4* d4 = reinterpret_cast<const float4*>(&s_delta[sb][c]);
+            // P^T goes to its own columns: dV of the previous step must have read them.
+            if (C::PT_OWN && it > 0 && !mbar_wait_warp(smem_u32(&bar_p_free), (it - 1) & 1, w, SITE_BWD_DS_READY)) {
+                ok = false;
+                break;
+            }
+            // Four 16-query chunks; the TMEM loads of chunk c+1 are in flight while chunk c
+            // is computed.  Once the last chunk is in registers the MMA issuer may overwrite
+            // S^T and dP^T with the next step's.
+            auto chunk = [&](int c, uint32_t (&sr)[16], uint32_t (&dr)[16]) {
+                uint32_t pk[8], dk[8];
+                const float4* l4 = reinterpret_cast<const float4*>(&s_lse[sb][cbase + c]);
+                const float4* d4 = reinterpret_cast<const float4*>(&s_delta[sb][cbase + c]);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
+                for (int e = 0; e < 16; e += 4) {
                     const float4 lv = l4[e >> 2], dv = d4[e >> 2];   // broadcast reads
                     const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv.x, dv.y, dv.z, dv.w};
-                    float p[4], g[4];
+                    float p[4], gg[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
-                        if (diag && kvpos > q0 + c + e + k) p[k] = 0.f;
-                        g[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
+                        if (diag && kvpos > q0 + cbase + c + e + k) p[k] = 0.f;
+                        gg[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
                     }
                     pk[e >> 1] = pack_bf162(p[0], p[1]);
                     pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
-                    dk[e >> 1] = pack_bf162(g[0], g[1]);
-                    dk[(e >> 1) + 1] = pack_bf162(g[2], g[3]);
+                    dk[e >> 1] = pack_bf162(gg[0], gg[1]);
+                    dk[(e >> 1) + 1] = pack_bf162(gg[2], gg[3]);
                 }
-                tmem_st16(lt + C::S_COL + (c >> 1), pk);
-                uint8_t* base = dsb + (c >> 6) * C::BKV * 128;
-                const int u0 = (c & 63) >> 3;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    *reinterpret_cast<uint4*>(base + sw128_offset(r, u0 + k)) =
-                        make_uint4(dk[4 * k], dk[4 * k + 1], dk[4 * k + 2], dk[4 * k + 3]);
+                tmem_st8(lt + C::pt_col(cbase + c), pk);
+                uint8_t* base = dsb + g * C::BKV * 128;
+                const int u0 = c >> 3;
+                *reinterpret_cast<uint4*>(base + sw128_offset(r, u0)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+                *reinterpret_cast<uint4*>(base + sw128_offset(r, u0 + 1)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
+            };
+            uint32_t sa[16], da[16], sb2[16], db2[16];
+            const uint32_t scol = lt + C::S_COL + cbase, dcol = lt + C::DP_COL + cbase;
+            tmem_ld16(scol, sa);
+            tmem_ld16(dcol, da);
+            tmem_wait_ld16(sa);
+            tmem_wait_ld16(da);
+            tmem_ld16(scol + 16, sb2);
+            tmem_ld16(dcol + 16, db2);
+            chunk(0, sa, da);
+            tmem_wait_ld16(sb2);
+            tmem_wait_ld16(db2);
+            tmem_ld16(scol + 32, sa);
+            tmem_ld16(dcol + 32, da);
+            chunk(16, sb2, db2);
+            tmem_wait_ld16(sa);
+            tmem_wait_ld16(da);
+            tmem_ld16(scol + 48, sb2);
+            tmem_ld16(dcol + 48, db2);
+            chunk(32, sa, da);
+            tmem_wait_ld16(sb2);
+            tmem_wait_ld16(db2);
+            if constexpr (C::PT_OWN) {
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bar_sdp_read));
             }
+            chunk(48, sb2, db2);
             fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bar_ds_ready));
+            if (it + 1 < n_it) publish(it + 1, lv_n, dv_n);
         }
-        // dK = s R^T dK', dV: key row r of this CTA's tile
+        // Epilogue, key row r of this CTA's tile: group 0 writes dK = s R^T dK', group 1 dV.
         if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
             tc_fence_after();
             const bool valid = kvpos < T;
             const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
-                uint32_t kr[32], vr[32];
-                tmem_ld32(lt + C::DK_COL + c, kr);
-                tmem_ld32(lt + C::DV_COL + c, vr);
+                uint32_t x[32];
+                tmem_ld32(lt + (g == 0 ? C::DK_COL : C::DV_COL) + c, x);
                 tmem_wait_ld();
-                reg_fence32(kr);
-                reg_fence32(vr);
+                reg_fence32(x);
                 if (!valid) continue;
-                uint32_t kp[16], vp[16];
-                const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)kvpos * (D / 2) + c / 2);
+                uint32_t pk[16];
+                if (g == 0) {
+                    const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)kvpos * (D / 2) + c / 2);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 cs = __ldg(tab + e / 4);
-                    const float g0 = __uint_as_float(kr[e]) * a.scale, g1 = __uint_as_float(kr[e + 1]) * a.scale;
-                    const float g2 = __uint_as_float(kr[e + 2]) * a.scale, g3 = __uint_as_float(kr[e + 3]) * a.scale;
-                    kp[e >> 1] = pack_bf162(g0 * cs.x + g1 * cs.y, -g0 * cs.y + g1 * cs.x);
-                    kp[(e >> 1) + 1] = pack_bf162(g2 * cs.z + g3 * cs.w, -g2 * cs.w + g3 * cs.z);
-                    vp[e >> 1] = pack_bf162(__uint_as_float(vr[e]), __uint_as_float(vr[e + 1]));
-                    vp[(e >> 1) + 1] = pack_bf162(__uint_as_float(vr[e + 2]), __uint_as_float(vr[e + 3]));
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 cs = __ldg(tab + e / 4);
+                        const float g0 = __uint_as_float(x[e]) * a.scale, g1 = __uint_as_float(x[e + 1]) * a.scale;
+                        const float g2 = __uint_as_float(x[e + 2]) * a.scale, g3 = __uint_as_float(x[e + 3]) * a.scale;
+                        pk[e >> 1] = pack_bf162(g0 * cs.x + g1 * cs.y, -g0 * cs.y + g1 * cs.x);
+                        pk[(e >> 1) + 1] = pack_bf162(g2 * cs.z + g3 * cs.w, -g2 * cs.w + g3 * cs.z);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf162(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
                 }
-                uint4* dkp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + orow + c);
-                uint4* dvp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + orow + c);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g == 0 ? a.dk : a.dv) + orow + c);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    dkp[e] = make_uint4(kp[4 * e], kp[4 * e + 1], kp[4 * e + 2], kp[4 * e + 3]);
-                    dvp[e] = make_uint4(vp[4 * e], vp[4 * e + 1], vp[4 * e + 2], vp[4 * e + 3]);
-                }
-            }
-        }
-    } else if (warp >= 12) {
-        // ------------------------------------------------------------ dQ drain
-        const int r = tid - 384;                       // query row = TMEM lane
-        const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
-        for (int it = 0; it < n_it; ++it) {
-            const int h = hkv * G + it / per_head;
-            const int qpos = (i_first + it % per_head) * C::BQ + r;
-            if (!mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, w, SITE_BWD_DQ_FULL)) break;
-            tc_fence_after();
-            float* dst = a.dq_acc + (((size_t)b * T + (qpos < T ? qpos : 0)) * a.Hq + h) * D;
-            uint32_t v[D];
-            tmem_ld_cols<D / 32>(lt + C::DQ_COL, v);
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_dq_free));
-            if (qpos < T) {
-#pragma unroll
-                for (int e = 0; e < D; e += 4)
-                    atomicAdd(reinterpret_cast<float4*>(dst + e),
-                              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                                          __uint_as_float(v[e + 3])));
+                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
             }
         }
     }
