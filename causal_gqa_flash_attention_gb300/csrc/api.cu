@@ -236,7 +236,6 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     g_last_error.clear();
     ne_status s = check_shape(B, T, Hq, Hkv, D, theta, f32);
     if (s != NE_OK) return s;
-    if (f32) return fail(NE_ERR_UNSUPPORTED, "the f32 (TF32) backward is not built yet");
     if (B == 0 || T == 0) return NE_OK;
     if ((s = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv})) != NE_OK) return s;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -259,10 +258,11 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
 
     CUtensorMap tq, tk, tv, tdo;
-    if ((s = map_bthd(&tq, q, f32, B, T, Hq, D, 128)) != NE_OK) return s;
+    const int q_rows = f32 ? ne::bwd_tf32_q_box_rows() : 128;
+    if ((s = map_bthd(&tq, q, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
     if ((s = map_bthd(&tk, k, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tv, v, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
-    if ((s = map_bthd(&tdo, dO, f32, B, T, Hq, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tdo, dO, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
     ne::BwdArgs a;
     a.lse = lse;
     a.delta = delta;
@@ -279,7 +279,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     a.scale = (float)(1.0 / std::sqrt((double)D));
     a.err = err;
     a.timeout_ns = timeout_ns();
-    e = ne::launch_bwd(f32, D, B, tq, tk, tv, tdo, a, st);
+    e = f32 ? ne::launch_bwd_tf32(D, B, tq, tk, tv, tdo, a, st) : ne::launch_bwd(f32, D, B, tq, tk, tv, tdo, a, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
 
     ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale};

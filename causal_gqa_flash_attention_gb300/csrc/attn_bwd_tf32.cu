@@ -1,0 +1,386 @@
+// attn_bwd_tf32.cu -- backward of causal GQA + RoPE attention for fp32 tensors on TF32
+// tensor cores (the hand-written backward of "NanoEuler: C와 CUDA로 밑바닥부터 구축한
+// GPT-2 규모의 LLM", 검증 및 안정성, for the attention of its 기술 사양 and 커널 구현).
+//
+// Same mathematics as the bf16 backward (attn_bwd.cu); the layout differs because TF32
+// UMMAs only read K-major operands.  One CTA per (batch, kv head, 128-key tile) loops
+// over the G query heads and every 64-query tile at or after the diagonal:
+//   S^T  = K' Q'^T           M=128 keys, N=64 queries     A = K', B = Q'
+//   dP^T = V dO^T            M=128, N=64                  A = V,  B = dO
+//   P^T, dS^T (fp32, TF32-rounded) written back to TMEM over S^T and dP^T; dS also to
+//   shared memory as [query][key] (the K-major A of the dQ product)
+//   dV  += P^T dO            A = P^T (TMEM), B = dO^T     (dO transposed in smem)
+//   dK' += dS^T Q'           A = dS^T (TMEM), B = Q'^T    (Q' transposed in smem)
+//   dQ'_part = dS K'         M=64 queries, N=D, K=128 keys; A = dS, B = K'^T
+// The M=64 accumulator puts query row m in TMEM lane 32*(m/16) + m%16.
+// Warp roles (384 threads): warp 0 TMA; warp 1 TMEM allocator and UMMA issuer (all
+// products, in order, so every TMEM and smem reuse is ordered by the one issuer);
+// warps 4-7 RoPE, TF32 rounding and transposes, then the dQ drain; warps 8-11 P^T, dS^T
+// and dS (thread = key row) and the dK/dV epilogue.  One Q/dO stage: TF32 is the
+// precision path, not the throughput path.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "rope_smem.cuh"
+
+namespace ne {
+
+namespace {
+
+template <int D>
+struct BwdTf32Cfg {
+    static constexpr int BKV = 128, BQ = 64;
+    static constexpr int ROWB = D * 4;
+    static constexpr int NCH = ROWB / 128;            // 128-byte chunks per row
+    static constexpr int KV_BYTES = BKV * ROWB;       // K', V, K'^T
+    static constexpr int Q_BYTES = BQ * ROWB;         // Q', Q'^T, dO, dO^T
+    static constexpr int DS_BYTES = BQ * BKV * 4;     // dS [query][key]
+    static constexpr int SMEM = 1024 + 3 * KV_BYTES + 4 * Q_BYTES + DS_BYTES;
+    static constexpr int S_COL = 0, DP_COL = 64, DV_COL = 128, DK_COL = 128 + D, DQ_COL = 128 + 2 * D;
+    static constexpr int TMEM_COLS = 128 + 3 * D <= 256 ? 256 : 512;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// dst[d][r] = src[r][d] for a fp32 tile of ROWS rows x D columns in the 128-byte
+// swizzled layout (both K-major, 32 elements per 128-byte chunk); 128 threads.
+template <int D, int ROWS>
+__device__ __forceinline__ void transpose_f32(const uint8_t* src, uint8_t* dst, int t) {
+    constexpr int UNITS = D * ROWS / 4, UPR = ROWS / 4;
+#pragma unroll 4
+    for (int ul = t; ul < UNITS; ul += 128) {
+        const int d = ul / UPR, r0 = 4 * (ul % UPR);
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = *reinterpret_cast<const uint32_t*>(src + (d >> 5) * ROWS * 128 + sw128_offset(r0 + k, (d & 31) >> 2) +
+                                                      (d & 3) * 4);
+        *reinterpret_cast<uint4*>(dst + (r0 >> 5) * D * 128 + sw128_offset(d, (r0 & 31) >> 2)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Round a fp32 tile to TF32 (nearest) in place; 128 threads.
+template <int BYTES>
+__device__ __forceinline__ void round_tf32(uint8_t* p, int t) {
+#pragma unroll 4
+    for (int i = t; i < BYTES / 16; i += 128) {
+        uint4 v = reinterpret_cast<uint4*>(p)[i];
+        v.x = f32_to_tf32_rna(__uint_as_float(v.x));
+        v.y = f32_to_tf32_rna(__uint_as_float(v.y));
+        v.z = f32_to_tf32_rna(__uint_as_float(v.z));
+        v.w = f32_to_tf32_rna(__uint_as_float(v.w));
+        reinterpret_cast<uint4*>(p)[i] = v;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    attn_bwd_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const BwdArgs a) {
+    using C = BwdTf32Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = smem;                       // K' [128][D]
+    uint8_t* sKT = sK + C::KV_BYTES;          // K'^T [D][128]
+    uint8_t* sV = sKT + C::KV_BYTES;          // V [128][D]
+    uint8_t* sQ = sV + C::KV_BYTES;           // Q' [64][D]
+    uint8_t* sQT = sQ + C::Q_BYTES;           // Q'^T [D][64]
+    uint8_t* sO = sQT + C::Q_BYTES;           // dO [64][D]
+    uint8_t* sOT = sO + C::Q_BYTES;           // dO^T [D][64]
+    uint8_t* sdS = sOT + C::Q_BYTES;          // dS [64][128]
+
+    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_qdo_full, bar_q_ready, bar_qdo_empty, bar_s_full,
+        bar_ds_ready, bar_dq_full, bar_dq_free, bar_dkv_full, bar_final, bar_aux;
+    __shared__ __align__(8) uint64_t bar_rows[2];
+    __shared__ __align__(16) float s_lse[2][C::BQ];
+    __shared__ __align__(16) float s_delta[2][C::BQ];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hkv = blockIdx.x, b = blockIdx.y, j = blockIdx.z;
+    const int T = a.T, G = a.G;
+    const int kv0 = j * C::BKV;
+    const int n_qt = (T + C::BQ - 1) / C::BQ;
+    const int i_first = kv0 / C::BQ;
+    const int per_head = n_qt - i_first;
+    const int n_it = G * per_head;
+    auto step_h = [&](int it) { return hkv * G + it / per_head; };
+    auto step_q0 = [&](int it) { return (i_first + it % per_head) * C::BQ; };
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar_kv_full), 1);
+        mbar_init(smem_u32(&bar_k_ready), 128);
+        mbar_init(smem_u32(&bar_qdo_full), 1);
+        mbar_init(smem_u32(&bar_q_ready), 128);
+        mbar_init(smem_u32(&bar_qdo_empty), 1);
+        mbar_init(smem_u32(&bar_s_full), 1);
+        mbar_init(smem_u32(&bar_ds_ready), 128);
+        mbar_init(smem_u32(&bar_dq_full), 1);
+        mbar_init(smem_u32(&bar_dq_free), 128);
+        mbar_init(smem_u32(&bar_dkv_full), 1);
+        mbar_init(smem_u32(&bar_final), 1);
+        mbar_init(smem_u32(&bar_aux), 128);        // intra-group sync of the RoPE/transpose warps
+        mbar_init(smem_u32(&bar_rows[0]), 128);
+        mbar_init(smem_u32(&bar_rows[1]), 128);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(smem_u32(&tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_slot;
+    const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t kvf = smem_u32(&bar_kv_full);
+            mbar_arrive_expect_tx(kvf, 2 * C::KV_BYTES);
+            for (int c = 0; c < C::NCH; ++c) {
+                tma_load_4d(smem_u32(sK + c * C::BKV * 128), &tm_k, kvf, c * 32, hkv, kv0, b);
+                tma_load_4d(smem_u32(sV + c * C::BKV * 128), &tm_v, kvf, c * 32, hkv, kv0, b);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                if (it > 0 && !mbar_wait(smem_u32(&bar_qdo_empty), (it - 1) & 1, w, SITE_BWD_QDO_EMPTY)) break;
+                const uint32_t f = smem_u32(&bar_qdo_full);
+                mbar_arrive_expect_tx(f, 2 * C::Q_BYTES);
+                for (int c = 0; c < C::NCH; ++c) {
+                    tma_load_4d(smem_u32(sQ + c * C::BQ * 128), &tm_q, f, c * 32, step_h(it), step_q0(it), b);
+                    tma_load_4d(smem_u32(sO + c * C::BQ * 128), &tm_do, f, c * 32, step_h(it), step_q0(it), b);
+                }
+                ++issued;
+            }
+            mbar_wait_drain(kvf, 0, w, SITE_BWD_DRAIN);
+            if (issued > 0) mbar_wait_drain(smem_u32(&bar_qdo_full), (issued - 1) & 1, w, SITE_BWD_DRAIN);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ UMMA issuer (all products)
+        if (lane == 0) {
+            constexpr uint32_t id_sp = idesc_make(FMT_TF32, 128, C::BQ, false, false);   // S^T, dP^T
+            constexpr uint32_t id_vk = idesc_make(FMT_TF32, 128, D, false, false);       // dV, dK
+            constexpr uint32_t id_q = idesc_make(FMT_TF32, 64, D, false, false);         // dQ (M = 64)
+            const uint64_t dK = sdesc(smem_u32(sK), 16, 1024), dKT = sdesc(smem_u32(sKT), 16, 1024);
+            const uint64_t dV = sdesc(smem_u32(sV), 16, 1024), dQ = sdesc(smem_u32(sQ), 16, 1024);
+            const uint64_t dQT = sdesc(smem_u32(sQT), 16, 1024), dO = sdesc(smem_u32(sO), 16, 1024);
+            const uint64_t dOT = sdesc(smem_u32(sOT), 16, 1024), dS = sdesc(smem_u32(sdS), 16, 1024);
+            // K-step ks covers 8 fp32 = 32 bytes of the K dimension: chunk ks/4, offset (ks%4)*32.
+            auto koff = [](int ks, int rows) { return (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32); };
+            bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV);
+            for (int it = 0; ok && it < n_it; ++it) {
+                if (!(ok = mbar_wait(smem_u32(&bar_q_ready), it & 1, w, SITE_BWD_Q_READY))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 8; ++ks)
+                    umma_ss<true>(tm + C::S_COL, sdesc_add(dK, koff(ks, C::BKV)), sdesc_add(dQ, koff(ks, C::BQ)), id_sp,
+                                  ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < D / 8; ++ks)
+                    umma_ss<true>(tm + C::DP_COL, sdesc_add(dV, koff(ks, C::BKV)), sdesc_add(dO, koff(ks, C::BQ)), id_sp,
+                                  ks > 0);
+                umma_commit(smem_u32(&bar_s_full));
+                if (!(ok = mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < C::BQ / 8; ++ks)       // dV += P^T dO, K = queries
+                    umma_ts<true>(tm + C::DV_COL, tm + C::S_COL + ks * 8, sdesc_add(dOT, koff(ks, D)), id_vk,
+                                  (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < C::BQ / 8; ++ks)       // dK' += dS^T Q'
+                    umma_ts<true>(tm + C::DK_COL, tm + C::DP_COL + ks * 8, sdesc_add(dQT, koff(ks, D)), id_vk,
+                                  (it > 0 || ks > 0) ? 1u : 0u);
+                if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < C::BKV / 8; ++ks)      // dQ'_part = dS K', K = keys
+                    umma_ss<true>(tm + C::DQ_COL, sdesc_add(dS, koff(ks, C::BQ)), sdesc_add(dKT, koff(ks, D)), id_q,
+                                  ks > 0);
+                umma_commit(smem_u32(&bar_dq_full));
+                umma_commit(smem_u32(&bar_qdo_empty));
+            }
+            umma_commit(smem_u32(&bar_dkv_full));
+            umma_commit(smem_u32(&bar_final));
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ RoPE, rounding, transposes; dQ drain
+        const int r = tid - 128;
+        const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
+        int aux_uses = 0;
+        // The transposes read rows rotated or rounded by other threads of the group.
+        auto group_sync = [&]() -> bool {
+            mbar_arrive(smem_u32(&bar_aux));
+            return mbar_wait_warp(smem_u32(&bar_aux), (aux_uses++) & 1, w, SITE_BWD_KV);
+        };
+        auto drain = [&](int it) -> bool {
+            if (!mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, w, SITE_BWD_DQ_FULL)) return false;
+            tc_fence_after();
+            uint32_t v[D];
+            tmem_ld_cols<D / 32>(lt + C::DQ_COL, v);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_dq_free));
+            const int qrow = (warp & 3) * 16 + lane;           // M=64 layout: lanes 0-15 of each quarter
+            const int qpos = step_q0(it) + qrow;
+            if (lane < 16 && qpos < T) {
+                float* dst = a.dq_acc + (((size_t)b * T + qpos) * a.Hq + step_h(it)) * D;
+#pragma unroll
+                for (int e = 0; e < D; e += 4)
+                    atomicAdd(reinterpret_cast<float4*>(dst + e),
+                              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                          __uint_as_float(v[e + 3])));
+            }
+            return true;
+        };
+        bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
+        if (ok) {
+            rope_tile_smem<D, C::BKV, 128, ROPE_TF32>(sK, nullptr, kv0, T, r, a.rope);
+            round_tf32<C::KV_BYTES>(sV, r);
+            ok = group_sync();
+        }
+        if (ok) {
+            transpose_f32<D, C::BKV>(sK, sKT, r);
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_k_ready));
+        }
+        for (int it = 0; ok && it <= n_it; ++it) {
+            if (it < n_it) {
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_qdo_full), it & 1, w, SITE_BWD_QDO_FULL))) break;
+                rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(sQ, nullptr, step_q0(it), T, r, a.rope);
+                round_tf32<C::Q_BYTES>(sO, r);
+                if (!(ok = group_sync())) break;
+                transpose_f32<D, C::BQ>(sQ, sQT, r);
+                transpose_f32<D, C::BQ>(sO, sOT, r);
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bar_q_ready));
+            }
+            if (it > 0 && !(ok = drain(it - 1))) break;
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ P^T, dS^T, dS; dK, dV epilogue
+        const int r = tid - 256;                       // key row = TMEM lane
+        const int kvpos = kv0 + r;
+        const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sl2 = a.scale_log2;
+        bool ok = true;
+        auto row_vals = [&](int it, float& lv, float& dv) {
+            const int qpos = step_q0(it) + r;
+            const size_t rix = ((size_t)b * a.Hq + step_h(it)) * T + qpos;
+            lv = qpos < T ? a.lse[rix] * 1.4426950408889634f : 0.f;
+            dv = qpos < T ? a.delta[rix] : 0.f;
+        };
+        auto publish = [&](int it, float lv, float dv) {
+            if (r < C::BQ) {
+                s_lse[it & 1][r] = lv;
+                s_delta[it & 1][r] = dv;
+            }
+            mbar_arrive(smem_u32(&bar_rows[it & 1]));
+        };
+        {
+            float lv = 0.f, dv = 0.f;
+            if (r < C::BQ) row_vals(0, lv, dv);
+            publish(0, lv, dv);
+        }
+        for (int it = 0; it < n_it; ++it) {
+            const int q0 = step_q0(it);
+            const int sb = it & 1;
+            if (!mbar_wait_warp(smem_u32(&bar_rows[sb]), (it >> 1) & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
+            float lv_n = 0.f, dv_n = 0.f;
+            if (it + 1 < n_it && r < C::BQ) row_vals(it + 1, lv_n, dv_n);
+            if (!mbar_wait_warp(smem_u32(&bar_s_full), it & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[64], dr[64];
+            tmem_ld_cols<2>(lt + C::S_COL, sr);
+            tmem_ld_cols<2>(lt + C::DP_COL, dr);
+            const bool diag = kv0 + C::BKV - 1 > q0;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                float p = ex2(fmaf(__uint_as_float(sr[c]), sl2, -s_lse[sb][c]));
+                if (diag && kvpos > q0 + c) p = 0.f;
+                const float g = p * (__uint_as_float(dr[c]) - s_delta[sb][c]);
+                sr[c] = f32_to_tf32_rna(p);
+                dr[c] = f32_to_tf32_rna(g);
+                // dS [query c][key r]: key chunk r/32, 4-byte element (r%32) of row c
+                *reinterpret_cast<uint32_t*>(sdS + (r >> 5) * C::BQ * 128 + sw128_offset(c, (r & 31) >> 2) + (r & 3) * 4) =
+                    dr[c];
+            }
+            tmem_st32(lt + C::S_COL, *reinterpret_cast<uint32_t(*)[32]>(sr));
+            tmem_st32(lt + C::S_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            tmem_st32(lt + C::DP_COL, *reinterpret_cast<uint32_t(*)[32]>(dr));
+            tmem_st32(lt + C::DP_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+            fence_proxy_async_smem();
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_ds_ready));
+            if (it + 1 < n_it) publish(it + 1, lv_n, dv_n);
+        }
+        // dK = s R^T dK', dV (fp32): key row r of this CTA's tile
+        if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
+            tc_fence_after();
+            const bool valid = kvpos < T;
+            const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t kr[32], vr[32];
+                tmem_ld32(lt + C::DK_COL + c, kr);
+                tmem_ld32(lt + C::DV_COL + c, vr);
+                tmem_wait_ld();
+                reg_fence32(kr);
+                reg_fence32(vr);
+                if (!valid) continue;
+                const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)kvpos * (D / 2) + c / 2);
+                float4* dkp = reinterpret_cast<float4*>(static_cast<float*>(a.dk) + orow + c);
+                float4* dvp = reinterpret_cast<float4*>(static_cast<float*>(a.dv) + orow + c);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 cs = __ldg(tab + e / 4);
+                    const float g0 = __uint_as_float(kr[e]) * a.scale, g1 = __uint_as_float(kr[e + 1]) * a.scale;
+                    const float g2 = __uint_as_float(kr[e + 2]) * a.scale, g3 = __uint_as_float(kr[e + 3]) * a.scale;
+                    dkp[e / 4] = make_float4(g0 * cs.x + g1 * cs.y, -g0 * cs.y + g1 * cs.x, g2 * cs.z + g3 * cs.w,
+                                             -g2 * cs.w + g3 * cs.z);
+                    dvp[e / 4] = make_float4(__uint_as_float(vr[e]), __uint_as_float(vr[e + 1]),
+                                             __uint_as_float(vr[e + 2]), __uint_as_float(vr[e + 3]));
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        mbar_wait_drain(smem_u32(&bar_final), 0, w, SITE_BWD_DRAIN);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tm, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+    using C = BwdTf32Cfg<D>;
+    auto kfn = attn_bwd_tf32_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.Hkv, B, a.n_kvt);
+    kfn<<<grid, 384, C::SMEM, st>>>(tq, tk, tv, tdo, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int bwd_tf32_q_box_rows() { return BwdTf32Cfg<64>::BQ; }
+
+cudaError_t launch_bwd_tf32(int D, int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+    if (D == 32) return launch_t<32>(B, tq, tk, tv, tdo, a, st);
+    if (D == 64) return launch_t<64>(B, tq, tk, tv, tdo, a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ne

@@ -80,6 +80,10 @@ cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUt
                        const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
                        cudaStream_t st);
 cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st);
+// fp32 tensors on TF32 tensor cores; its Q and dO tensor maps use bwd_tf32_q_box_rows() rows.
+int bwd_tf32_q_box_rows();
+cudaError_t launch_bwd_tf32(int D, int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_selftest_wait(int* err, unsigned long long timeout_ns, cudaStream_t st);
 
 }  // namespace ne

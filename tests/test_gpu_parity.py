@@ -135,13 +135,20 @@ def test_bf16_deterministic_dk_dv():
 # ---------------------------------------------------------------- f32 (TF32)
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,D", [
-    (4, 128, 4, 2, 32),      # the small CPU-model shape, full size
     (2, 512, 12, 4, 64),     # GPU-pipeline shape, two batch rows
-    (1, 77, 4, 1, 64),
+    (1, 77, 4, 1, 64),       # ragged tail
+    (1, 300, 6, 2, 32),
+    (2, 1, 4, 2, 32),
 ])
-def test_f32_forward_matches_oracle(B, T, Hq, Hkv, D):
+def test_f32_matches_oracle(B, T, Hq, Hkv, D):
     q, k, v, dO = synthetic.make_custom(B, T, Hq, Hkv, D, torch.float32, seed=B * 100 + T + D)
-    check(q, k, v, dO, "f32", bwd=False)
+    check(q, k, v, dO, "f32")
+
+
+def test_f32_small_model_workload_full_size():
+    """The small CPU-model workload (B4 T128 Hq4 Hkv2 D32, fp32 on TF32) at full size."""
+    q, k, v, dO = synthetic.make_inputs(synthetic.WORKLOADS[1])
+    check(q, k, v, dO, "f32")
 
 
 # ---------------------------------------------------------------- RoPE table

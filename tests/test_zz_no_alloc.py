@@ -63,9 +63,10 @@ def test_noalloc_backward_matches_workspace_backward_twice(lib, shape):
         alloc_before = torch.cuda.memory_allocated()
         assert call_noalloc(lib, q, k, v, o, lse, dO, dq, dk, dv) == ne.NE_OK, lib.ne_last_error()
         torch.cuda.synchronize()
+        # Nothing may be allocated by the call (memory freed meanwhile by torch is fine).
         if call == 1:   # the first call may still load the module holding the scratch
-            assert torch.cuda.mem_get_info()[0] == free_before
-        assert torch.cuda.memory_allocated() == alloc_before
+            assert torch.cuda.mem_get_info()[0] >= free_before
+        assert torch.cuda.memory_allocated() <= alloc_before
         for name, got, ref in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
             assert torch.isfinite(got).all(), (call, name)
             e = rel(got, ref)
