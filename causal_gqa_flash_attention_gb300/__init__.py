@@ -31,6 +31,7 @@ EXPORTS = (
     "ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd_workspace_size", "ne_attn_bwd",
     "ne_attn_bwd_f32", "ne_status_string", "ne_last_error", "ne_get_device_error",
     "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown", "ne_attn_bwd_noalloc",
+    "ne_profile_enable", "ne_profile_totals",
 )
 
 
@@ -67,6 +68,10 @@ def load(path: str | None = None):
         lib.ne_set_wait_timeout_ms.restype = None
         lib.ne_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         lib.ne_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 5 + [d, vp]
+        lib.ne_profile_enable.argtypes = [i]
+        lib.ne_profile_enable.restype = None
+        lib.ne_profile_totals.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
+        lib.ne_profile_totals.restype = i
         lib.ne_shutdown.argtypes = []
         lib.ne_shutdown.restype = None
         for f in ("ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd", "ne_attn_bwd_f32",
@@ -171,6 +176,23 @@ def set_wait_timeout_ms(ms: int):
 def selftest_wait_timeout(timeout_ms: int = 50):
     lib = load()
     _check(lib.ne_selftest_wait_timeout(int(timeout_ms), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+
+
+PHASES = ("attn_fwd", "bwd_pre", "attn_bwd", "bwd_post")
+
+
+def profile_enable(on: bool = True):
+    """Diagnostic: record CUDA events around every kernel the calls launch."""
+    load().ne_profile_enable(1 if on else 0)
+
+
+def profile_totals() -> dict:
+    """{phase: (total_ms, launches)} since profile_enable(True); synchronises."""
+    lib = load()
+    ms = (ctypes.c_double * 4)()
+    n = (ctypes.c_int * 4)()
+    _check(lib.ne_profile_totals(ms, n))
+    return {PHASES[i]: (float(ms[i]), int(n[i])) for i in range(4)}
 
 
 def last_error() -> str:

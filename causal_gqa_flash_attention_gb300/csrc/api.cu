@@ -10,6 +10,8 @@
 #include <mutex>
 #include <string>
 #include <tuple>
+#include <utility>
+#include <vector>
 
 #include "kernels.h"
 #include "neattn.h"
@@ -123,6 +125,36 @@ ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const
     return NE_OK;
 }
 
+// ------------------------------------------------------------------ phase timing (diagnostic)
+// Events come from a pool that survives re-enabling, so a timed region pays only the
+// two cudaEventRecord calls per launch once the pool has grown.
+struct PhaseProfile {
+    bool on = false;
+    std::vector<cudaEvent_t> pool;          // 2 per recorded launch
+    std::vector<int> phase;                 // phase of recorded launch i
+    size_t used = 0;                        // launches recorded since enabling
+};
+PhaseProfile g_prof;
+
+// Records `launch` between two events when profiling is on.
+template <typename F>
+cudaError_t timed(int phase, cudaStream_t st, F&& launch) {
+    if (!g_prof.on) return launch();
+    const size_t i = g_prof.used;
+    while (g_prof.pool.size() < 2 * (i + 1)) {
+        cudaEvent_t ev = nullptr;
+        if (cudaEventCreate(&ev) != cudaSuccess) return launch();
+        g_prof.pool.push_back(ev);
+    }
+    if (g_prof.phase.size() < i + 1) g_prof.phase.resize(i + 1);
+    cudaEventRecord(g_prof.pool[2 * i], st);
+    cudaError_t e = launch();
+    cudaEventRecord(g_prof.pool[2 * i + 1], st);
+    g_prof.phase[i] = phase;
+    g_prof.used = i + 1;
+    return e;
+}
+
 // ------------------------------------------------------------------ tensor maps
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -225,7 +257,7 @@ ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, v
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     a.err = err;
     a.timeout_ns = timeout_ns();
-    cudaError_t e = ne::launch_fwd(f32, D, B, tq, tk, tv, to, a, st);
+    cudaError_t e = timed(0, st, [&] { return ne::launch_fwd(f32, D, B, tq, tk, tv, to, a, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
     return NE_OK;
 }
@@ -254,7 +286,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     const long long rows = (long long)B * T * Hq;
 
     ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D};
-    cudaError_t e = ne::launch_bwd_pre(f32, pa, st);
+    cudaError_t e = timed(1, st, [&] { return ne::launch_bwd_pre(f32, pa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
 
     CUtensorMap tq, tk, tv, tdo;
@@ -279,11 +311,13 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     a.scale = (float)(1.0 / std::sqrt((double)D));
     a.err = err;
     a.timeout_ns = timeout_ns();
-    e = f32 ? ne::launch_bwd_tf32(D, B, tq, tk, tv, tdo, a, st) : ne::launch_bwd(f32, D, B, tq, tk, tv, tdo, a, st);
+    e = timed(2, st, [&] {
+        return f32 ? ne::launch_bwd_tf32(D, B, tq, tk, tv, tdo, a, st) : ne::launch_bwd(f32, D, B, tq, tk, tv, tdo, a, st);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
 
     ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale};
-    e = ne::launch_bwd_post(f32, qa, st);
+    e = timed(3, st, [&] { return ne::launch_bwd_post(f32, qa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dq epilogue launch");
     return NE_OK;
 }
@@ -412,6 +446,36 @@ ne_status ne_selftest_wait_timeout(uint32_t timeout_ms, ne_stream_t stream) {
     if ((s = error_word(dev, &err)) != NE_OK) return s;
     cudaError_t e = ne::launch_selftest_wait(err, (unsigned long long)timeout_ms * 1000000ull, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+    return NE_OK;
+}
+
+void ne_profile_enable(int on) {
+    g_prof.used = 0;
+    g_prof.on = on != 0;
+    if (!g_prof.on) {
+        for (cudaEvent_t ev : g_prof.pool) cudaEventDestroy(ev);
+        g_prof.pool.clear();
+        g_prof.phase.clear();
+    }
+}
+
+ne_status ne_profile_totals(double ms_out[4], int launches_out[4]) {
+    g_last_error.clear();
+    if (!ms_out || !launches_out) return fail(NE_ERR_INVALID_ARG, "null output");
+    for (int i = 0; i < 4; ++i) {
+        ms_out[i] = 0.0;
+        launches_out[i] = 0;
+    }
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    for (size_t i = 0; i < g_prof.used; ++i) {
+        float ms = 0.f;
+        const int ph = g_prof.phase[i];
+        if (cudaEventElapsedTime(&ms, g_prof.pool[2 * i], g_prof.pool[2 * i + 1]) == cudaSuccess && ph >= 0 && ph < 4) {
+            ms_out[ph] += ms;
+            launches_out[ph] += 1;
+        }
+    }
     return NE_OK;
 }
 

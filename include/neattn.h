@@ -149,6 +149,16 @@ void ne_set_wait_timeout_ms(uint32_t ms);
  * without faulting or hanging the GPU. */
 ne_status ne_selftest_wait_timeout(uint32_t timeout_ms, ne_stream_t stream);
 
+/* Diagnostic timing of the kernels behind the calls above.  While enabled (on != 0),
+ * every call records a CUDA event before and after each kernel it launches, on the
+ * call's stream; ne_profile_totals() synchronises the current device and returns, per
+ * phase, the summed milliseconds and the number of launches since enabling:
+ * phase 0 forward, 1 backward Delta preprocess, 2 backward main, 3 backward dQ
+ * epilogue.  Enabling again restarts the sums and reuses the events already made;
+ * disabling (on == 0) frees them.  Not thread-safe; off by default. */
+void ne_profile_enable(int on);
+ne_status ne_profile_totals(double ms_out[4], int launches_out[4]);
+
 /* Releases the library's per-device caches (RoPE tables, error words). */
 void ne_shutdown(void);
 
