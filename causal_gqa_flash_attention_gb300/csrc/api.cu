@@ -352,6 +352,16 @@ ne_status noalloc_scratch(int dev, void** out) {
 
 }  // namespace
 
+namespace ne {
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* env = std::getenv("NE_ATTN_PDL");
+        return !(env && env[0] == '0');
+    }();
+    return on;
+}
+}  // namespace ne
+
 extern "C" {
 
 ne_status ne_rope_table(float* cos_out, float* sin_out, int T, int D, double theta, ne_stream_t stream) {

@@ -35,68 +35,131 @@ namespace ne {
 namespace {
 
 // ------------------------------------------------------------------------ pre
-// Delta[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]; also zeroes dq_acc.  A group of
-// LPR lanes takes one row (D elements); rows are [B,T,Hq] in memory order.
+// Delta[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]; also zeroes dq_acc.  A group of LPR
+// lanes takes one row (D elements); rows are [B,T,Hq] in memory order.  Each warp keeps
+// U row units (RPW rows each) in flight per pass and zeroes the accumulator rows of the
+// units it reads: interleaving the zero stores with the loads row by row kept HBM busier
+// than a zeroing sweep followed by the loads.
 template <typename Tin, int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
     constexpr int EPV = 16 / sizeof(Tin);        // elements per 16-byte vector
     constexpr int LPR = D / EPV;                 // lanes per row (8 or 16)
-    constexpr int RPW = 32 / LPR;                // rows per warp step
+    constexpr int RPW = 32 / LPR;                // rows per warp unit
+    constexpr int U = 2;                         // units in flight per pass
+    constexpr int ZPL = D / 4 / LPR;             // 16-byte zero stores per lane per row
+    griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int sub = lane / LPR, li = lane % LPR;
-    const long long warp_global = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-    const long long nwarps = (gridDim.x * (long long)blockDim.x) >> 5;
-    for (long long r0 = warp_global * RPW; r0 < a.rows; r0 += nwarps * RPW) {
-        const long long row = r0 + sub;
-        float acc = 0.f;
-        if (row < a.rows) {
-            const uint4 ov = reinterpret_cast<const uint4*>(static_cast<const Tin*>(a.o) + row * D)[li];
-            const uint4 gv = reinterpret_cast<const uint4*>(static_cast<const Tin*>(a.dO) + row * D)[li];
-            if constexpr (sizeof(Tin) == 2) {
-                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-                const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+    const long long wg = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    const uint4* o4 = static_cast<const uint4*>(a.o);
+    const uint4* g4 = static_cast<const uint4*>(a.dO);
+    for (long long r0 = wg * RPW + sub; r0 - sub < a.rows; r0 += nw * RPW * U) {
+        uint4 ov[U], gv[U];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 of = __bfloat1622float2(o2[k]), gf = __bfloat1622float2(g2[k]);
+        for (int k = 0; k < U; ++k) {
+            const long long row = r0 + k * nw * RPW;
+            if (row < a.rows) {
+                ov[k] = o4[row * LPR + li];
+                gv[k] = g4[row * LPR + li];
+            } else {
+                ov[k] = gv[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const long long row = r0 + k * nw * RPW;
+            if (row < a.rows) {
+                float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D);
+#pragma unroll
+                for (int e = 0; e < ZPL; ++e) z[li + e * LPR] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            float acc = 0.f;
+            if constexpr (sizeof(Tin) == 2) {
+                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[k]);
+                const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[k]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
                     acc = fmaf(of.x, gf.x, acc);
                     acc = fmaf(of.y, gf.y, acc);
                 }
             } else {
-                acc = __uint_as_float(ov.x) * __uint_as_float(gv.x) + __uint_as_float(ov.y) * __uint_as_float(gv.y) +
-                      __uint_as_float(ov.z) * __uint_as_float(gv.z) + __uint_as_float(ov.w) * __uint_as_float(gv.w);
+                acc = __uint_as_float(ov[k].x) * __uint_as_float(gv[k].x) +
+                      __uint_as_float(ov[k].y) * __uint_as_float(gv[k].y) +
+                      __uint_as_float(ov[k].z) * __uint_as_float(gv[k].z) +
+                      __uint_as_float(ov[k].w) * __uint_as_float(gv[k].w);
             }
-            float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D);
-            for (int k = li; k < D / 4; k += LPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
 #pragma unroll
-        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (row < a.rows && li == 0) {
-            const long long t = (row / a.Hq) % a.T, bh = (row / ((long long)a.Hq * a.T)) * a.Hq + row % a.Hq;
-            a.delta[bh * a.T + t] = acc;
+            for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const long long row = r0 + k * nw * RPW;
+            if (row < a.rows && li == 0) {
+                const long long t = (row / a.Hq) % a.T, bh = (row / ((long long)a.Hq * a.T)) * a.Hq + row % a.Hq;
+                a.delta[bh * a.T + t] = acc;
+            }
         }
     }
 }
 
 // ------------------------------------------------------------------------ post
-// dq[row] = s * R_t^T dq_acc[row]; thread = 2 pairs (4 elements).
+// dq[row] = s * R_t^T dq_acc[row].  A thread takes 8 consecutive elements (4 pairs) of
+// a row, U such groups in flight per pass; the (cos, sin) table is L2-resident.
 template <typename Tout, int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdPostArgs a) {
-    const long long n = a.rows * (D / 4);
-    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const long long row = idx / (D / 4);
-        const int q4 = (int)(idx % (D / 4));
-        const int t = (int)((row / a.Hq) % a.T);
-        const float4 g = reinterpret_cast<const float4*>(a.dq_acc)[idx];
-        const float4 cs = __ldg(reinterpret_cast<const float4*>(a.rope + (size_t)t * (D / 2) + 2 * q4));
-        const float y0 = a.scale * (g.x * cs.x + g.y * cs.y), y1 = a.scale * (-g.x * cs.y + g.y * cs.x);
-        const float y2 = a.scale * (g.z * cs.z + g.w * cs.w), y3 = a.scale * (-g.z * cs.w + g.w * cs.z);
-        if constexpr (sizeof(Tout) == 2) {
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(y0, y1), p1 = __floats2bfloat162_rn(y2, y3);
-            reinterpret_cast<uint2*>(a.dq)[idx] =
-                make_uint2(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1));
-        } else {
-            reinterpret_cast<float4*>(a.dq)[idx] = make_float4(y0, y1, y2, y3);
+    constexpr int G8 = D / 8;                    // 8-element groups per row
+    constexpr int U = 2;
+    griddep_launch_dependents();
+    griddep_wait();
+    const long long n = a.rows * G8;
+    const long long tg = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    const long long nt = (long long)gridDim.x * blockDim.x;
+    const float4* acc4 = reinterpret_cast<const float4*>(a.dq_acc);
+    const float4* rope4 = reinterpret_cast<const float4*>(a.rope);
+    for (long long i0 = tg; i0 < n; i0 += nt * U) {
+        float4 g[U][2], cs[U][2];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const long long idx = i0 + k * nt;
+            if (idx < n) {
+                const long long row = idx / G8;
+                const int c8 = (int)(idx % G8);
+                const int t = (int)((row / a.Hq) % a.T);
+                g[k][0] = acc4[idx * 2];
+                g[k][1] = acc4[idx * 2 + 1];
+                cs[k][0] = __ldg(rope4 + (size_t)t * (D / 4) + 2 * c8);
+                cs[k][1] = __ldg(rope4 + (size_t)t * (D / 4) + 2 * c8 + 1);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const long long idx = i0 + k * nt;
+            if (idx >= n) continue;
+            float y[8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 v = g[k][h], c = cs[k][h];
+                y[4 * h + 0] = a.scale * (v.x * c.x + v.y * c.y);
+                y[4 * h + 1] = a.scale * (-v.x * c.y + v.y * c.x);
+                y[4 * h + 2] = a.scale * (v.z * c.z + v.w * c.w);
+                y[4 * h + 3] = a.scale * (-v.z * c.w + v.w * c.z);
+            }
+            if constexpr (sizeof(Tout) == 2) {
+                uint4 o;
+                __nv_bfloat162 p0 = __floats2bfloat162_rn(y[0], y[1]), p1 = __floats2bfloat162_rn(y[2], y[3]);
+                __nv_bfloat162 p2 = __floats2bfloat162_rn(y[4], y[5]), p3 = __floats2bfloat162_rn(y[6], y[7]);
+                o.x = *reinterpret_cast<uint32_t*>(&p0);
+                o.y = *reinterpret_cast<uint32_t*>(&p1);
+                o.z = *reinterpret_cast<uint32_t*>(&p2);
+                o.w = *reinterpret_cast<uint32_t*>(&p3);
+                reinterpret_cast<uint4*>(a.dq)[idx] = o;
+            } else {
+                reinterpret_cast<float4*>(a.dq)[idx * 2] = make_float4(y[0], y[1], y[2], y[3]);
+                reinterpret_cast<float4*>(a.dq)[idx * 2 + 1] = make_float4(y[4], y[5], y[6], y[7]);
+            }
         }
     }
 }
@@ -207,6 +270,8 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_launch_dependents();   // after the TMEM allocation
+    griddep_wait();                // LSE, Delta and the zeroed accumulator are visible
     const uint32_t tm = tmem_slot;
     const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
 
@@ -563,8 +628,7 @@ cudaError_t launch_bwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, co
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Hkv, B, a.n_kvt);
-    kfn<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, a);
-    return cudaGetLastError();
+    return launch_k(kfn, grid, dim3(C::THREADS), C::SMEM, st, tq, tk, tv, tdo, a);
 }
 
 int grid_for(long long work, int per_block) {
@@ -577,33 +641,28 @@ int grid_for(long long work, int per_block) {
 
 cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st) {
     if (a.rows == 0) return cudaSuccess;
-    const long long warps_needed = (a.rows + 3) / 4;
-    const int blocks = grid_for(warps_needed * 32, 256);
+    const dim3 g(grid_for(a.rows * 8, 256)), blk(256);
     if (!tf32) {
-        if (a.D == 64) bwd_pre_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, st>>>(a);
-        else if (a.D == 128) bwd_pre_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, st>>>(a);
-        else return cudaErrorInvalidValue;
+        if (a.D == 64) return launch_k(bwd_pre_kernel<__nv_bfloat16, 64>, g, blk, 0, st, a);
+        if (a.D == 128) return launch_k(bwd_pre_kernel<__nv_bfloat16, 128>, g, blk, 0, st, a);
     } else {
-        if (a.D == 32) bwd_pre_kernel<float, 32><<<blocks, 256, 0, st>>>(a);
-        else if (a.D == 64) bwd_pre_kernel<float, 64><<<blocks, 256, 0, st>>>(a);
-        else return cudaErrorInvalidValue;
+        if (a.D == 32) return launch_k(bwd_pre_kernel<float, 32>, g, blk, 0, st, a);
+        if (a.D == 64) return launch_k(bwd_pre_kernel<float, 64>, g, blk, 0, st, a);
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st) {
     if (a.rows == 0) return cudaSuccess;
-    const int blocks = grid_for(a.rows * (a.D / 4), 256);
+    const dim3 g(grid_for(a.rows * (a.D / 8), 256)), blk(256);
     if (!tf32) {
-        if (a.D == 64) bwd_post_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, st>>>(a);
-        else if (a.D == 128) bwd_post_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, st>>>(a);
-        else return cudaErrorInvalidValue;
+        if (a.D == 64) return launch_k(bwd_post_kernel<__nv_bfloat16, 64>, g, blk, 0, st, a);
+        if (a.D == 128) return launch_k(bwd_post_kernel<__nv_bfloat16, 128>, g, blk, 0, st, a);
     } else {
-        if (a.D == 32) bwd_post_kernel<float, 32><<<blocks, 256, 0, st>>>(a);
-        else if (a.D == 64) bwd_post_kernel<float, 64><<<blocks, 256, 0, st>>>(a);
-        else return cudaErrorInvalidValue;
+        if (a.D == 32) return launch_k(bwd_post_kernel<float, 32>, g, blk, 0, st, a);
+        if (a.D == 64) return launch_k(bwd_post_kernel<float, 64>, g, blk, 0, st, a);
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,

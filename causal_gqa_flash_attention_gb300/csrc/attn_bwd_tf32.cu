@@ -134,6 +134,8 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_launch_dependents();   // after the TMEM allocation
+    griddep_wait();                // LSE, Delta and the zeroed accumulator are visible
     const uint32_t tm = tmem_slot;
     const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
 
@@ -368,8 +370,7 @@ cudaError_t launch_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const 
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Hkv, B, a.n_kvt);
-    kfn<<<grid, 384, C::SMEM, st>>>(tq, tk, tv, tdo, a);
-    return cudaGetLastError();
+    return launch_k(kfn, grid, dim3(384), C::SMEM, st, tq, tk, tv, tdo, a);
 }
 
 }  // namespace

@@ -239,6 +239,8 @@ __global__ void __launch_bounds__(416, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_launch_dependents();   // after the TMEM allocation
+    griddep_wait();                // inputs of earlier kernels on the stream are visible
     const uint32_t tm = tmem_slot;
     const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
     auto stage_k = [&](int s) { return sStage + s * C::STAGE_BYTES; };
@@ -459,8 +461,7 @@ cudaError_t launch_fwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, co
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Hq, B, a.n_qt);
-    kfn<<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, to, a);
-    return cudaGetLastError();
+    return launch_k(kfn, grid, dim3(C::THREADS), C::SMEM, st, tq, tk, tv, to, a);
 }
 
 }  // namespace

@@ -2,6 +2,7 @@
 // translation units.  Not part of the public ABI.
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -67,6 +68,30 @@ struct BwdPostArgs {
     int T, Hq, D;
     float scale;
 };
+
+// Programmatic dependent launch: every kernel of the library is launched with
+// programmatic stream serialization (unless NE_ATTN_PDL=0), so it can be scheduled while
+// the previous kernel on the stream drains.  Each kernel does its on-chip set-up first,
+// then `griddepcontrol.wait` before its first global-memory access; kernels that own
+// TMEM signal `launch_dependents` only after their allocation, so a dependent CTA never
+// holds TMEM that a still-unallocated CTA of its predecessor needs.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Tile rows of the key/value tensor maps the forward kernel expects.
 int fwd_kv_box_rows(bool tf32, int D);

@@ -10,6 +10,8 @@ namespace ne {
 __global__ void rope_table_kernel(float* __restrict__ cos_out, float* __restrict__ sin_out,
                                   float2* __restrict__ interleaved, int T, int half, double theta,
                                   double inv_half) {
+    griddep_launch_dependents();
+    griddep_wait();   // an earlier kernel may still read a table this call overwrites
     const long long n = (long long)T * half;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
          idx += (long long)gridDim.x * blockDim.x) {
@@ -32,9 +34,8 @@ cudaError_t launch_rope_table(float* cos_out, float* sin_out, float2* interleave
     if (n == 0) return cudaSuccess;
     int blocks = (int)((n + 255) / 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
-    rope_table_kernel<<<blocks, 256, 0, st>>>(cos_out, sin_out, interleaved, T, half, theta,
-                                              1.0 / (double)half);
-    return cudaGetLastError();
+    return launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st, cos_out, sin_out, interleaved, T, half,
+                    theta, 1.0 / (double)half);
 }
 
 // A kernel whose only bounded wait can never complete: nothing arrives on its
