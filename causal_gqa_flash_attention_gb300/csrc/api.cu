@@ -289,12 +289,14 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     cudaError_t e = timed(1, st, [&] { return ne::launch_bwd_pre(f32, pa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
 
-    CUtensorMap tq, tk, tv, tdo;
-    const int q_rows = f32 ? ne::bwd_tf32_q_box_rows() : 128;
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    const int q_rows = ne::bwd_q_box_rows(f32, D);
     if ((s = map_bthd(&tq, q, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
     if ((s = map_bthd(&tk, k, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tv, v, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tdo, dO, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
+    std::memset(&tdq, 0, sizeof(tdq));
+    if (!f32 && D == 64 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
     ne::BwdArgs a;
     a.lse = lse;
     a.delta = delta;
@@ -312,7 +314,8 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     a.err = err;
     a.timeout_ns = timeout_ns();
     e = timed(2, st, [&] {
-        return f32 ? ne::launch_bwd_tf32(D, B, tq, tk, tv, tdo, a, st) : ne::launch_bwd(f32, D, B, tq, tk, tv, tdo, a, st);
+        return f32 ? ne::launch_bwd_tf32(D, B, tq, tk, tv, tdo, a, st)
+                   : ne::launch_bwd(f32, D, B, tq, tk, tv, tdo, tdq, a, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
 
@@ -534,11 +537,14 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D};   // also zeroes dq_acc
     e = ne::launch_bwd_pre(false, pa, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
-    CUtensorMap tq, tk, tv, tdo;
-    if ((s = map_bthd(&tq, q, false, B, T, Hq, D, 128)) != NE_OK) return s;
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    const int q_rows = ne::bwd_q_box_rows(false, D);
+    if ((s = map_bthd(&tq, q, false, B, T, Hq, D, q_rows)) != NE_OK) return s;
     if ((s = map_bthd(&tk, k, false, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tv, v, false, B, T, Hkv, D, 128)) != NE_OK) return s;
-    if ((s = map_bthd(&tdo, dO, false, B, T, Hq, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tdo, dO, false, B, T, Hq, D, q_rows)) != NE_OK) return s;
+    std::memset(&tdq, 0, sizeof(tdq));
+    if (D == 64 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
     ne::BwdArgs a;
     a.lse = lse;
     a.delta = delta;
@@ -555,7 +561,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     a.scale = (float)(1.0 / std::sqrt((double)D));
     a.err = nullptr;            // no error word: that would need an allocation
     a.timeout_ns = timeout_ns();
-    e = ne::launch_bwd(false, D, B, tq, tk, tv, tdo, a, st);
+    e = ne::launch_bwd(false, D, B, tq, tk, tv, tdo, tdq, a, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
     ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale};
     e = ne::launch_bwd_post(false, qa, st);

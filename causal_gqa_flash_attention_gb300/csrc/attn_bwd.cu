@@ -665,10 +665,16 @@ cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st) {
     return cudaErrorInvalidValue;
 }
 
+int bwd_q_box_rows(bool tf32, int D) {
+    if (tf32) return bwd_tf32_q_box_rows();
+    return D == 64 ? bwd_d64_q_box_rows() : BwdCfg<128>::BQ;
+}
+
 cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
+                       cudaStream_t st) {
     if (tf32) return cudaErrorNotSupported;
-    if (D == 64) return launch_bwd_t<64>(B, tq, tk, tv, tdo, a, st);
+    if (D == 64) return launch_bwd_d64(B, tq, tk, tv, tdo, tdq, a, st);
     if (D == 128) return launch_bwd_t<128>(B, tq, tk, tv, tdo, a, st);
     return cudaErrorInvalidValue;
 }

@@ -1,0 +1,508 @@
+// attn_bwd_d64.cu -- backward main kernel for head_dim 64 (bf16 tensors): the hand-written
+// backward of "NanoEuler: C와 CUDA로 밑바닥부터 구축한 GPT-2 규모의 LLM" (검증 및 안정성)
+// for the causal GQA + RoPE attention of the same page (기술 사양, 커널 구현).  With
+// s = 1/sqrt(D), Q' = R Q, K' = R K (rows rotated by their positions):
+//   P^T  = exp(s K'Q'^T - LSE)            recomputed per tile from the forward's LSE
+//   dP^T = V dO^T,  dS^T = P^T o (dP^T - Delta)
+//   dV  += P^T dO,  dK' += dS^T Q',  dQ' = dS K'   (dK = s R^T dK', dQ = s R^T dQ')
+//
+// One CTA per (batch, kv head, 128-key tile) loops over the G query heads of its group
+// and every 128-query tile on or after the diagonal; dK and dV stay in TMEM for the whole
+// group (no atomics).  Each query tile is taken as two 64-query half-steps: while the
+// softmax-gradient warps work on half-step i, the tensor core computes S^T and dP^T of
+// i+1 and dV / dK of i-1.  dQ' of a whole 128-query tile is one M = 128 MMA over the two
+// halves' dS; the drain warps stage it in shared memory and one TMA bulk reduce-add per
+// tile adds it into the fp32 accumulator.
+//
+// Two limits shape the pipeline.  (1) A chain of K-step MMAs into one accumulator, plus
+// its commit and the waiter's wake-up, takes ~600 cycles on an idle tensor pipe and more
+// under load, so S^T and dP^T are double-buffered in TMEM: those of half-step i+2 are
+// issued as soon as the softmax-gradient warps hold half-step i's in registers.  (2) An
+// MMA with both operands in shared memory (M = 128, N = 64) reads 6 KB per 32 cycles of
+// math, more than the SM's 128 bytes per clock, and every other warp's shared-memory
+// access then queues behind it; so K' (constant per CTA) is copied into TMEM once and
+// S^T reads only Q' from shared memory, and dV takes P^T from TMEM.  The rest of TMEM
+// holds the accumulators, so V, dS^T (for dK') and dS, K' (for dQ') are read from shared
+// memory.
+//
+// Operand precision: Q', K' and dS are fp16 (logits and dS keep 3 more mantissa bits
+// than bf16; a rotated value or a dS beyond the fp16 range is reported as an error, never
+// silently saturated); P^T, V and dO are bf16.  Every MMA has one operand type.
+//
+// Warp roles (512 threads, one CTA per SM):
+//   warp 0      TMA producer (K, V once; Q, dO half tiles into an NQS ring) and the dQ'
+//               issuer (once per 128-query tile).
+//   warp 1      TMEM allocator; S^T issuer.
+//   warp 2      dP^T issuer.
+//   warp 3      dV and dK' issuer.
+//   warps 4-7   RoPE of K once (then the K' rows copied into TMEM) and of every Q half
+//               tile (in place, to fp16), and the dQ' drain (thread = query row of the
+//               tile = TMEM lane) through the staging tile.
+//   warps 8-15  two groups of 128 threads (thread = key row = TMEM lane), each on 32 of
+//               the 64 query columns of a half-step; at the end group 0 writes dK (inverse
+//               rotation, scale), group 1 writes dV.
+// TMEM: S^T of buffer b at 128b and dP^T at 128b + 64 (64 cols each), K' (fp16) at 256
+// as a packed A operand, packed bf16 P^T at 288, dV at 320, dK' at 384, dQ' at 448.
+// Shared memory: K' (fp16), V, NQS x (Q' half | dO half), two dS^T tiles [key][query], the
+// fp32 dQ' staging tile (two 128-byte-swizzled column chunks, as the reduce's box expects).
+// Every wait is bounded; a CTA that gives up records an error code, drains its own copies
+// and MMAs and frees its TMEM.
+#include <cuda_bf16.h>
+#include "kernels.h"
+#include "ptx.cuh"
+#include "rope_smem.cuh"
+
+namespace ne {
+
+namespace {
+
+struct Bwd64 {
+    static constexpr int D = 64;
+    static constexpr int BKV = 128;                  // key rows per CTA
+    static constexpr int BT = 128;                   // query rows per tile
+    static constexpr int BH = 64;                    // query rows per half-step
+    static constexpr int KV_BYTES = BKV * 128;       // one 128-byte row per key
+    static constexpr int H_BYTES = BH * 128;         // a Q or dO half tile
+    static constexpr int STAGE_BYTES = 2 * H_BYTES;  // Q' | dO
+    static constexpr int NQS = 5;                    // half-step stages
+    static constexpr int DS_TILE = BKV * BT * 2;     // dS^T [key][query] fp16: two 64-query chunks
+    static constexpr int DS_CHUNK = BKV * 128;
+    static constexpr int DQ_STAGE = BT * D * 4;      // fp32 dQ' of a tile: two 32-column chunks
+    static constexpr int SMEM = 1024 + 2 * KV_BYTES + NQS * STAGE_BYTES + 2 * DS_TILE + DQ_STAGE;
+    static constexpr int KA_COL = 256, PT_COL = 288, DV_COL = 320, DK_COL = 384, DQ_COL = 448;
+    static constexpr int THREADS = 512;
+    static constexpr int LOOKAHEAD = 4;              // Q half tiles rotated ahead of the drain
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(LOOKAHEAD <= NQS + 2, "rotation lookahead must not outrun the TMA ring");
+};
+
+__device__ __forceinline__ uint32_t s_col(int b) { return (uint32_t)(128 * b); }
+__device__ __forceinline__ uint32_t dp_col(int b) { return (uint32_t)(128 * b + 64); }
+// Packed P^T: 64 queries in 32 columns, group g's 32 queries at +16g.
+
+__global__ void __launch_bounds__(512, 1)
+    attn_bwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                        const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
+    using C = Bwd64;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = smem;                              // K, rotated in place to fp16
+    uint8_t* sV = sK + C::KV_BYTES;
+    uint8_t* sStage = sV + C::KV_BYTES;              // NQS x (Q half | dO half)
+    uint8_t* sDS = sStage + C::NQS * C::STAGE_BYTES; // two dS^T tiles
+    uint8_t* sDQ = sDS + 2 * C::DS_TILE;             // dQ' staging for the bulk reduce
+    auto stage_q = [&](int s) { return sStage + s * C::STAGE_BYTES; };
+    auto stage_do = [&](int s) { return sStage + s * C::STAGE_BYTES + C::H_BYTES; };
+    auto ds_tile = [&](int tb) { return sDS + tb * C::DS_TILE; };
+
+    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_rot, bar_k_ready, bar_dkv_full, bar_final;
+    __shared__ __align__(8) uint64_t bar_qdo_full[C::NQS], bar_q_ready[C::NQS], bar_qdo_empty[C::NQS];
+    __shared__ __align__(8) uint64_t bar_s_full[2], bar_dp_full[2];   // [S^T/dP^T buffer]: MMA done
+    __shared__ __align__(8) uint64_t bar_sp_read[2];                  // ... read into registers
+    __shared__ __align__(8) uint64_t bar_p_free;                      // P^T read by dV
+    __shared__ __align__(8) uint64_t bar_ds_half[2];   // [half]: P^T and the dS^T half of a half-step written
+    __shared__ __align__(8) uint64_t bar_ds_tile[2];   // [dS^T tile buffer]: both halves written
+    __shared__ __align__(8) uint64_t bar_ds_free[2];   // [dS^T tile buffer]: dK' and dQ' done with it
+    __shared__ __align__(8) uint64_t bar_dq_full, bar_dq_free;          // dQ' TMEM accumulator
+    __shared__ __align__(8) uint64_t bar_stage_free, bar_staged;   // dQ' staging tile
+    __shared__ __align__(16) float s_lse[8][2][32];    // [softmax warp][buffer][query column of its group]
+    __shared__ __align__(16) float s_delta[8][2][32];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hkv = blockIdx.x, b = blockIdx.y, j = blockIdx.z;
+    const int T = a.T, G = a.G;
+    const int kv0 = j * C::BKV;
+    const int n_qt = (T + C::BT - 1) / C::BT;
+    const int per_head = n_qt - j;                   // 128-query tiles on or after the diagonal
+    const int n_tiles = G * per_head;
+    const int n_hs = 2 * n_tiles;
+    auto tile_head = [&](int tau) { return hkv * G + tau / per_head; };
+    auto tile_q0 = [&](int tau) { return (j + tau % per_head) * C::BT; };
+    auto hs_q0 = [&](int hs) { return tile_q0(hs >> 1) + (hs & 1) * C::BH; };
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar_kv_full), 1);
+        mbar_init(smem_u32(&bar_k_rot), 128);
+        mbar_init(smem_u32(&bar_k_ready), 128);
+        mbar_init(smem_u32(&bar_p_free), 1);
+        mbar_init(smem_u32(&bar_dkv_full), 1);
+        mbar_init(smem_u32(&bar_final), 4);          // one commit per UMMA issuer
+        for (int s = 0; s < C::NQS; ++s) {
+            mbar_init(smem_u32(&bar_qdo_full[s]), 1);
+            mbar_init(smem_u32(&bar_q_ready[s]), 128);
+            mbar_init(smem_u32(&bar_qdo_empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bar_s_full[i]), 1);
+            mbar_init(smem_u32(&bar_dp_full[i]), 1);
+            mbar_init(smem_u32(&bar_sp_read[i]), 256);
+            mbar_init(smem_u32(&bar_ds_half[i]), 256);
+            mbar_init(smem_u32(&bar_ds_tile[i]), 256);
+            mbar_init(smem_u32(&bar_ds_free[i]), 2);  // dK' issuer (after the odd half) and dQ' issuer
+        }
+        mbar_init(smem_u32(&bar_stage_free), 1);
+        mbar_init(smem_u32(&bar_dq_full), 1);
+        mbar_init(smem_u32(&bar_dq_free), 128);
+        mbar_init(smem_u32(&bar_staged), 128);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(smem_u32(&tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    griddep_launch_dependents();   // after the TMEM allocation
+    griddep_wait();                // LSE, Delta and the zeroed accumulator are visible
+    const uint32_t tm = tmem_slot;
+    const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
+
+    auto kdesc = [](const void* p) { return sdesc(smem_u32(p), 16, 1024); };                 // K-major
+    auto mndesc = [](const void* p, uint32_t lbo) { return sdesc(smem_u32(p), lbo, 1024); };  // MN-major
+
+    // The issuing warps (0-3) run their loops with all 32 lanes, so that descriptors and
+    // loop state stay warp-uniform; elect.sync picks the lane that issues each MMA and
+    // commit, and lane 0 issues the TMA copies.
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer + dQ' issuer
+        const uint32_t kvf = smem_u32(&bar_kv_full);
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+            mbar_arrive_expect_tx(kvf, 2 * C::KV_BYTES);
+            tma_load_4d(smem_u32(sK), &tm_k, kvf, 0, hkv, kv0, b);
+            tma_load_4d(smem_u32(sV), &tm_v, kvf, 0, hkv, kv0, b);
+        }
+        int issued = 0;
+        auto load = [&](int hs) -> bool {
+            const int s = hs % C::NQS;
+            if (hs >= C::NQS &&
+                !mbar_wait_warp(smem_u32(&bar_qdo_empty[s]), ((hs / C::NQS) - 1) & 1, w, SITE_BWD_QDO_EMPTY))
+                return false;
+            if (lane == 0) {
+                const uint32_t f = smem_u32(&bar_qdo_full[s]);
+                const int h = tile_head(hs >> 1), q0 = hs_q0(hs);
+                mbar_arrive_expect_tx(f, 2 * C::H_BYTES);
+                tma_load_4d(smem_u32(stage_q(s)), &tm_q, f, 0, h, q0, b);
+                tma_load_4d(smem_u32(stage_do(s)), &tm_do, f, 0, h, q0, b);
+            }
+            ++issued;
+            return true;
+        };
+        bool ok = true;
+        for (int hs = 0; ok && hs < C::NQS && hs < n_hs; ++hs) ok = load(hs);
+        constexpr uint32_t id_dq = idesc_make(FMT_F16, 128, D, true, true);   // A, B MN-major
+        const uint64_t dKmn = mndesc(sK, C::BKV * 128);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV);
+        for (int tau = 0; ok && tau < n_tiles; ++tau) {
+            const int tb = tau & 1;
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_ds_tile[tb]), (tau >> 1) & 1, w, SITE_BWD_DS_READY))) break;
+            // The drain warps have taken the previous tile's dQ' out of TMEM.
+            if (tau >= 1 && !(ok = mbar_wait_warp(smem_u32(&bar_dq_free), (tau - 1) & 1, w, SITE_BWD_DQ_FREE)))
+                break;
+            tc_fence_after();
+            const uint64_t dSmn = mndesc(ds_tile(tb), C::DS_CHUNK);
+#pragma unroll
+            for (int ks = 0; ks < C::BKV / 16; ++ks)        // dQ' = dS K', K = key rows
+                umma_ss_e<false>(tm + C::DQ_COL, sdesc_add(dSmn, ks * 16 * 128), sdesc_add(dKmn, ks * 16 * 128),
+                                 id_dq, ks > 0);
+            umma_commit_e(smem_u32(&bar_dq_full));
+            umma_commit_e(smem_u32(&bar_ds_free[tb]));
+            for (int hs = 2 * tau + C::NQS; ok && hs < 2 * tau + C::NQS + 2 && hs < n_hs; ++hs) ok = load(hs);
+        }
+        umma_commit_e(smem_u32(&bar_final));
+        // Teardown: every copy this CTA started must have landed before exit.
+        if (lane == 0) {
+            mbar_wait_drain(kvf, 0, w, SITE_BWD_DRAIN);
+            for (int hs = max(0, issued - C::NQS); hs < issued; ++hs)
+                mbar_wait_drain(smem_u32(&bar_qdo_full[hs % C::NQS]), (hs / C::NQS) & 1, w, SITE_BWD_DRAIN);
+        }
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ S^T (warp 1) / dP^T (warp 2)
+        const bool is_s = warp == 1;
+        // S^T = K'Q'^T on fp16 operands with A (K') from TMEM; dP^T = V dO^T on bf16.
+        const uint32_t id = is_s ? idesc_make(FMT_F16, 128, C::BH, false, false)
+                                 : idesc_make(FMT_BF16, 128, C::BH, false, false);
+        const uint64_t dV = kdesc(sV);
+        const uint64_t dB0 = kdesc(is_s ? stage_q(0) : stage_do(0));
+        uint64_t* full = is_s ? bar_s_full : bar_dp_full;
+        // S^T waits for the rotated K' (in TMEM) and Q'; dP^T only for the copies of V and dO.
+        uint64_t* ready = is_s ? bar_q_ready : bar_qdo_full;
+        bool ok = is_s ? mbar_wait_warp(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV)
+                       : mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
+        for (int hs = 0; ok && hs < n_hs; ++hs) {
+            const int s = hs % C::NQS, bf = hs & 1;
+            if (!(ok = mbar_wait_warp(smem_u32(&ready[s]), (hs / C::NQS) & 1, w, SITE_BWD_Q_READY))) break;
+            // Buffer bf is free once the softmax-gradient warps hold half-step hs-2's S^T and
+            // dP^T in registers.
+            if (hs >= 2 &&
+                !(ok = mbar_wait_warp(smem_u32(&bar_sp_read[bf]), ((hs - 2) >> 1) & 1, w, SITE_BWD_DS_READY)))
+                break;
+            tc_fence_after();
+            const uint64_t dB = sdesc_add(dB0, s * C::STAGE_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {          // K = head_dim: 16 per step (32 bytes, 8 columns)
+                if (is_s) umma_ts_e<false>(tm + s_col(bf), tm + C::KA_COL + 8 * ks, sdesc_add(dB, ks * 32), id, ks > 0);
+                else umma_ss_e<false>(tm + dp_col(bf), sdesc_add(dV, ks * 32), sdesc_add(dB, ks * 32), id, ks > 0);
+            }
+            umma_commit_e(smem_u32(&full[bf]));
+        }
+        umma_commit_e(smem_u32(&bar_final));
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ dV, dK' issuer
+        constexpr uint32_t id_dv = idesc_make(FMT_BF16, 128, D, false, true);   // B (dO) MN-major
+        constexpr uint32_t id_dk = idesc_make(FMT_F16, 128, D, false, true);    // B (Q') MN-major
+        const uint64_t dQmn0 = mndesc(stage_q(0), C::H_BYTES), dOmn0 = mndesc(stage_do(0), C::H_BYTES);
+        bool ok = true;
+        for (int hs = 0; ok && hs < n_hs; ++hs) {
+            const int s = hs % C::NQS, half = hs & 1, tau = hs >> 1, tb = tau & 1;
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_ds_half[half]), tau & 1, w, SITE_BWD_DS_READY))) break;
+            tc_fence_after();
+            const uint64_t dOmn = sdesc_add(dOmn0, s * C::STAGE_BYTES), dQmn = sdesc_add(dQmn0, s * C::STAGE_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < C::BH / 16; ++ks)         // dV += P^T dO (P^T from TMEM), K = queries
+                umma_ts_e<false>(tm + C::DV_COL, tm + C::PT_COL + 8 * ks, sdesc_add(dOmn, ks * 16 * 128), id_dv,
+                                 (hs > 0 || ks > 0) ? 1u : 0u);
+            umma_commit_e(smem_u32(&bar_p_free));
+            const uint64_t dDS = kdesc(ds_tile(tb) + half * C::DS_CHUNK);
+#pragma unroll
+            for (int ks = 0; ks < C::BH / 16; ++ks)         // dK' += dS^T Q', K = queries
+                umma_ss_e<false>(tm + C::DK_COL, sdesc_add(dDS, ks * 32), sdesc_add(dQmn, ks * 16 * 128), id_dk,
+                                 (hs > 0 || ks > 0) ? 1u : 0u);
+            umma_commit_e(smem_u32(&bar_qdo_empty[s]));
+            if (half == 1) umma_commit_e(smem_u32(&bar_ds_free[tb]));
+        }
+        umma_commit_e(smem_u32(&bar_dkv_full));
+        umma_commit_e(smem_u32(&bar_final));
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ RoPE on K and Q; dQ' drain
+        const int r = tid - 128;
+        const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
+        bool ovf = false;
+        bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
+        if (ok) {
+            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_F16, true>(sK, nullptr, kv0, T, r, a.rope);
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_k_rot));
+            ok = mbar_wait_warp(smem_u32(&bar_k_rot), 0, w, SITE_BWD_KV);
+        }
+        if (ok) {
+            // Key row r of K' into TMEM lane r as a packed A operand (64 values = 32 columns,
+            // in the order of the 16-byte units of the swizzled row).
+            uint32_t kr[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint4 kk = *reinterpret_cast<const uint4*>(sK + sw128_offset(r, u));
+                kr[4 * u] = kk.x; kr[4 * u + 1] = kk.y; kr[4 * u + 2] = kk.z; kr[4 * u + 3] = kk.w;
+            }
+            tmem_st32(lt + C::KA_COL, kr);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_k_ready));
+        }
+        int rot = 0;   // next half-step whose Q tile is rotated
+        auto rotate_upto = [&](int lim) -> bool {
+            for (; rot < lim && rot < n_hs; ++rot) {
+                const int s = rot % C::NQS;
+                if (!mbar_wait_warp(smem_u32(&bar_qdo_full[s]), (rot / C::NQS) & 1, w, SITE_BWD_QDO_FULL)) return false;
+                ovf |= rope_tile_smem<D, C::BH, 128, ROPE_F16, true>(stage_q(s), nullptr, hs_q0(rot), T, r, a.rope);
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bar_q_ready[s]));
+            }
+            return true;
+        };
+        if (r == 0) tma_prefetch_desc(&tm_dq);
+        if (ok) ok = rotate_upto(C::LOOKAHEAD);
+        for (int tau = 0; ok && tau < n_tiles; ++tau) {
+            if (!(ok = rotate_upto(2 * tau + 2 + C::LOOKAHEAD))) break;
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_dq_full), tau & 1, w, SITE_BWD_DQ_FULL))) break;
+            tc_fence_after();
+            uint32_t v[64];
+            tmem_ld_cols<2>(lt + C::DQ_COL, v);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_dq_free));
+            // The staging tile is free once the previous tile's reduce has read it.
+            if (tau > 0) {
+                if (r == 0) {
+                    bulk_wait_group_read0();
+                    mbar_arrive(smem_u32(&bar_stage_free));
+                }
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_stage_free), (tau - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4*>(sDQ + c * (C::BT * 128) + sw128_offset(r, u)) =
+                        make_uint4(v[32 * c + 4 * u], v[32 * c + 4 * u + 1], v[32 * c + 4 * u + 2], v[32 * c + 4 * u + 3]);
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_staged));
+            if (r == 0) {
+                if (!(ok = mbar_wait(smem_u32(&bar_staged), tau & 1, w, SITE_BWD_DQ_FULL))) break;
+                // Rows at or beyond T lie outside the tensor map and are skipped.
+                const int h = tile_head(tau), q0 = tile_q0(tau);
+                tma_reduce_add_4d(&tm_dq, smem_u32(sDQ), 0, h, q0, b);
+                tma_reduce_add_4d(&tm_dq, smem_u32(sDQ + C::BT * 128), 32, h, q0, b);
+                bulk_commit_group();
+            }
+        }
+        if (r == 0) bulk_wait_group0();   // the last reduces have completed before the CTA exits
+        if (ovf) atomicCAS(a.err, 0, SITE_RANGE);
+    } else {
+        // ------------------------------------------------------------ P^T, dS^T; dK, dV epilogue
+        const int g = (warp - 8) >> 2;
+        const int r = (warp & 3) * 32 + lane;            // key row = TMEM lane
+        const int kvpos = kv0 + r;
+        const int cb = 32 * g;                           // this group's query columns of a half-step
+        const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sl2 = a.scale_log2;
+        float amax = 0.f;
+        bool ok = true;
+        // LSE / Delta of this group's 32 query columns: lane l fetches column l of the next
+        // half-step while the current one runs, and the warp stages them in its own
+        // double-buffered slot (read back as broadcasts; __syncwarp orders the warp's own
+        // writes and reads, so no cross-warp barrier is needed).
+        const int sw = warp - 8;
+        auto row_vals = [&](int hs, float& lv, float& dv) {
+            const int qpos = hs_q0(hs) + cb + lane;
+            const size_t rix = ((size_t)b * a.Hq + tile_head(hs >> 1)) * T + qpos;
+            lv = qpos < T ? a.lse[rix] * 1.4426950408889634f : 0.f;
+            dv = qpos < T ? a.delta[rix] : 0.f;
+        };
+        auto publish = [&](int hs, float lv, float dv) {
+            s_lse[sw][hs & 1][lane] = lv;
+            s_delta[sw][hs & 1][lane] = dv;
+            __syncwarp();
+        };
+        if (n_hs > 0) {
+            float lv, dv;
+            row_vals(0, lv, dv);
+            publish(0, lv, dv);
+        }
+        for (int hs = 0; hs < n_hs; ++hs) {
+            const int bf = hs & 1, half = hs & 1, tau = hs >> 1, tb = tau & 1;
+            const int q0 = hs_q0(hs) + cb;
+            float lv_n = 0.f, dv_n = 0.f;
+            if (hs + 1 < n_hs) row_vals(hs + 1, lv_n, dv_n);   // in flight during this half-step
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[bf]), (hs >> 1) & 1, w, SITE_BWD_S_FULL))) break;
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_dp_full[bf]), (hs >> 1) & 1, w, SITE_BWD_DP_FULL))) break;
+            tc_fence_after();
+            uint32_t sr[32], dr[32];
+            tmem_ld32(lt + s_col(bf) + cb, sr);
+            tmem_ld32(lt + dp_col(bf) + cb, dr);
+            tmem_wait_ld();
+            reg_fence32(sr);
+            reg_fence32(dr);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_sp_read[bf]));      // the buffer may take half-step hs+2
+            const bool diag = kvpos > q0;                // some of this row's queries precede the key
+            uint32_t pk[16], dk[16];
+            const float4* l4 = reinterpret_cast<const float4*>(&s_lse[sw][bf][0]);
+            const float4* d4 = reinterpret_cast<const float4*>(&s_delta[sw][bf][0]);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 lq4 = l4[e >> 2], dq4 = d4[e >> 2];   // broadcast reads
+                const float lq[4] = {lq4.x, lq4.y, lq4.z, lq4.w}, dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w};
+                float p[4], ds[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
+                    if (diag && kvpos > q0 + e + k) p[k] = 0.f;
+                    ds[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
+                    amax = fmaxf(amax, fabsf(ds[k]));
+                }
+                pk[e >> 1] = pack_bf162(p[0], p[1]);
+                pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
+                dk[e >> 1] = pack_half2(ds[0], ds[1]);
+                dk[(e >> 1) + 1] = pack_half2(ds[2], ds[3]);
+            }
+            // P^T's columns are free once dV of the previous half-step has read them.
+            if (hs >= 1 && !(ok = mbar_wait_warp(smem_u32(&bar_p_free), (hs - 1) & 1, w, SITE_BWD_DS_READY))) break;
+            tc_fence_after();
+            tmem_st16(lt + C::PT_COL + 16 * g, pk);
+            // The dS^T tile buffer is reused every second tile: dK' and dQ' of tile tau-2
+            // must be done with it.
+            if (half == 0 && tau >= 2 &&
+                !(ok = mbar_wait_warp(smem_u32(&bar_ds_free[tb]), ((tau - 2) >> 1) & 1, w, SITE_BWD_DS_FREE)))
+                break;
+            uint8_t* base = ds_tile(tb) + half * C::DS_CHUNK;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4*>(base + sw128_offset(r, 4 * g + k)) =
+                    make_uint4(dk[4 * k], dk[4 * k + 1], dk[4 * k + 2], dk[4 * k + 3]);
+            fence_proxy_async_smem();
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_ds_half[half]));
+            if (half == 1) mbar_arrive(smem_u32(&bar_ds_tile[tb]));
+            if (hs + 1 < n_hs) publish(hs + 1, lv_n, dv_n);
+        }
+        if (amax > 65504.f) atomicCAS(a.err, 0, SITE_RANGE);   // a dS beyond the fp16 range
+        // Epilogue, key row r of this CTA's tile: group 0 writes dK = s R^T dK', group 1 dV.
+        if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
+            tc_fence_after();
+            const bool valid = kvpos < T;
+            const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t x[32];
+                tmem_ld32(lt + (g == 0 ? C::DK_COL : C::DV_COL) + c, x);
+                tmem_wait_ld();
+                reg_fence32(x);
+                if (!valid) continue;
+                uint32_t pk[16];
+                if (g == 0) {
+                    const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)kvpos * (D / 2) + c / 2);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 cs = __ldg(tab + e / 4);
+                        const float g0 = __uint_as_float(x[e]) * a.scale, g1 = __uint_as_float(x[e + 1]) * a.scale;
+                        const float g2 = __uint_as_float(x[e + 2]) * a.scale, g3 = __uint_as_float(x[e + 3]) * a.scale;
+                        pk[e >> 1] = pack_bf162(g0 * cs.x + g1 * cs.y, -g0 * cs.y + g1 * cs.x);
+                        pk[(e >> 1) + 1] = pack_bf162(g2 * cs.z + g3 * cs.w, -g2 * cs.w + g3 * cs.z);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf162(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+                }
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g == 0 ? a.dk : a.dv) + orow + c);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        mbar_wait_drain(smem_u32(&bar_final), 0, w, SITE_BWD_DRAIN);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tm, 512);
+    }
+}
+
+}  // namespace
+
+int bwd_d64_q_box_rows() { return Bwd64::BH; }
+
+cudaError_t launch_bwd_d64(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t st) {
+    auto kfn = attn_bwd_d64_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Bwd64::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.Hkv, B, a.n_kvt);
+    return launch_k(kfn, grid, dim3(Bwd64::THREADS), Bwd64::SMEM, st, tq, tk, tv, tdo, tdq, a);
+}
+
+}  // namespace ne

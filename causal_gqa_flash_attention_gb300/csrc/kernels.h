@@ -101,10 +101,18 @@ cudaError_t launch_rope_table(float* cos_out, float* sin_out, float2* interleave
 cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st);
+// `tdq` maps the fp32 dQ accumulator (used by the head_dim-64 kernel).
 cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& a,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
                        cudaStream_t st);
 cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st);
+// head_dim 64, bf16: the half-step kernel; its Q and dO tensor maps use bwd_d64_q_box_rows() rows,
+// and it adds dQ' into the accumulator through `tdq` (fp32 [B,T,Hq,D], 128-row boxes).
+int bwd_d64_q_box_rows();
+cudaError_t launch_bwd_d64(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t st);
+// Rows of the Q / dO tensor-map boxes the backward main kernel for (dtype, D) expects.
+int bwd_q_box_rows(bool tf32, int D);
 // fp32 tensors on TF32 tensor cores; its Q and dO tensor maps use bwd_tf32_q_box_rows() rows.
 int bwd_tf32_q_box_rows();
 cudaError_t launch_bwd_tf32(int D, int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
