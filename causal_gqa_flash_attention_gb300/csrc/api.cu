@@ -178,7 +178,8 @@ ne_status encode_fn(EncodeTiledFn* out) {
 
 // Tiled map over a [B, T, H, D] tensor: box = (128 bytes of D, 1 head, rows, 1 batch),
 // 128-byte swizzle, zero fill out of bounds (ragged T tails).
-ne_status map_bthd(CUtensorMap* m, const void* ptr, bool f32, int B, int T, int H, int D, int rows) {
+ne_status map_bthd(CUtensorMap* m, const void* ptr, bool f32, int B, int T, int H, int D, int rows,
+                   bool f16 = false) {
     EncodeTiledFn enc;
     ne_status s = encode_fn(&enc);
     if (s != NE_OK) return s;
@@ -187,7 +188,9 @@ ne_status map_bthd(CUtensorMap* m, const void* ptr, bool f32, int B, int T, int 
     cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es, (cuuint64_t)T * H * D * es};
     cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+    const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : (f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    CUresult r = enc(m, dt, 4,
                      const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -222,9 +225,22 @@ ne_status check_ptrs(std::initializer_list<const void*> ps) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t bwd_ws_bytes(int B, int T, int Hq, int D) {
-    return round_up((size_t)B * Hq * T * sizeof(float), 256) + (size_t)B * T * Hq * D * sizeof(float);
+// Backward workspace: Delta fp32 [B,Hq,T] | dQ accumulator fp32 [B,T,Hq,D] | rotated fp16
+// Q' [B,T,Hq,D] (written by the preprocess kernel for the bf16 head_dim-64 kernel).
+struct BwdWs {
+    size_t delta, acc, q16, total;
+};
+BwdWs bwd_ws_layout(int B, int T, int Hq, int D) {
+    BwdWs l;
+    l.delta = 0;
+    l.acc = round_up((size_t)B * Hq * T * sizeof(float), 256);
+    l.q16 = l.acc + round_up((size_t)B * T * Hq * D * sizeof(float), 256);
+    l.total = l.q16 + (size_t)B * T * Hq * D * 2;
+    return l;
 }
+size_t bwd_ws_bytes(int B, int T, int Hq, int D) { return bwd_ws_layout(B, T, Hq, D).total; }
+// The bf16 head_dim-64 kernel reads Q rotated ahead of time by the preprocess kernel.
+bool bwd_uses_q16(bool f32, int D) { return !f32 && D == 64; }
 
 // ------------------------------------------------------------------ forward / backward
 ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
@@ -281,17 +297,19 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     if ((s = error_word(dev, &err)) != NE_OK) return s;
     const float2* rope;
     if ((s = rope_cache(dev, T, D, theta, st, &rope)) != NE_OK) return s;
+    const BwdWs wl = bwd_ws_layout(B, T, Hq, D);
     float* delta = static_cast<float*>(ws);
-    float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up((size_t)B * Hq * T * sizeof(float), 256));
+    float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.acc);
+    void* q16 = bwd_uses_q16(f32, D) ? static_cast<char*>(ws) + wl.q16 : nullptr;
     const long long rows = (long long)B * T * Hq;
 
-    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D};
+    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, err};
     cudaError_t e = timed(1, st, [&] { return ne::launch_bwd_pre(f32, pa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
 
     CUtensorMap tq, tk, tv, tdo, tdq;
     const int q_rows = ne::bwd_q_box_rows(f32, D);
-    if ((s = map_bthd(&tq, q, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
+    if ((s = map_bthd(&tq, q16 ? q16 : q, f32, B, T, Hq, D, q_rows, q16 != nullptr)) != NE_OK) return s;
     if ((s = map_bthd(&tk, k, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tv, v, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tdo, dO, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
@@ -330,7 +348,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
 // library holds it until the process exits).  Layout per call: RoPE table
 // [T, D/2] float2 | Delta [B, Hq, T] fp32 | dQ accumulator [B, T, Hq, D] fp32, each
 // part starting on a 256-byte boundary.
-constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch per device ordinal.  In host code the array's
@@ -516,12 +534,13 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     if ((s = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv})) != NE_OK) return s;
     const size_t rope_bytes = round_up((size_t)ne::rope_table_rows(T) * (D / 2) * sizeof(float2), 256);
     const size_t delta_bytes = round_up((size_t)B * Hq * T * sizeof(float), 256);
-    const size_t acc_bytes = (size_t)B * T * Hq * D * sizeof(float);
-    if (rope_bytes + delta_bytes + acc_bytes > kNoAllocScratchBytes)
+    const size_t acc_bytes = round_up((size_t)B * T * Hq * D * sizeof(float), 256);
+    const size_t q16_bytes = bwd_uses_q16(false, D) ? (size_t)B * T * Hq * D * 2 : 0;
+    if (rope_bytes + delta_bytes + acc_bytes + q16_bytes > kNoAllocScratchBytes)
         return fail(NE_ERR_INVALID_ARG,
                     "ne_attn_bwd_noalloc: this shape needs %zu bytes of scratch, above its fixed maximum of %zu "
                     "(%zu MiB); use ne_attn_bwd with a caller-allocated workspace",
-                    rope_bytes + delta_bytes + acc_bytes, kNoAllocScratchBytes, kNoAllocScratchBytes >> 20);
+                    rope_bytes + delta_bytes + acc_bytes + q16_bytes, kNoAllocScratchBytes, kNoAllocScratchBytes >> 20);
     int dev;
     if ((s = current_device(&dev)) != NE_OK) return s;
     void* base;
@@ -529,17 +548,18 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     float2* rope = static_cast<float2*>(base);
     float* delta = reinterpret_cast<float*>(static_cast<char*>(base) + rope_bytes);
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(base) + rope_bytes + delta_bytes);
+    void* q16 = q16_bytes ? static_cast<char*>(base) + rope_bytes + delta_bytes + acc_bytes : nullptr;
     const long long rows = (long long)B * T * Hq;
 
     // The table is rebuilt on every call: the scratch keeps whatever the last call left.
     cudaError_t e = ne::launch_rope_table(nullptr, nullptr, rope, ne::rope_table_rows(T), D, rope_theta, st);
     if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
-    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D};   // also zeroes dq_acc
+    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, nullptr};   // also zeroes dq_acc
     e = ne::launch_bwd_pre(false, pa, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
     CUtensorMap tq, tk, tv, tdo, tdq;
     const int q_rows = ne::bwd_q_box_rows(false, D);
-    if ((s = map_bthd(&tq, q, false, B, T, Hq, D, q_rows)) != NE_OK) return s;
+    if ((s = map_bthd(&tq, q16 ? q16 : q, false, B, T, Hq, D, q_rows, q16 != nullptr)) != NE_OK) return s;
     if ((s = map_bthd(&tk, k, false, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tv, v, false, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tdo, dO, false, B, T, Hq, D, q_rows)) != NE_OK) return s;

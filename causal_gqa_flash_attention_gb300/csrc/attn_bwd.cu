@@ -26,6 +26,7 @@
 //               and dS^T from S^T, dP^T, LSE, Delta; P^T to TMEM, dS^T (bf16) to shared
 //               memory; at the end group 0 writes dK (inverse rotation), group 1 dV.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include "kernels.h"
 #include "ptx.cuh"
 #include "rope_smem.cuh"
@@ -35,11 +36,13 @@ namespace ne {
 namespace {
 
 // ------------------------------------------------------------------------ pre
-// Delta[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]; also zeroes dq_acc.  A group of LPR
-// lanes takes one row (D elements); rows are [B,T,Hq] in memory order.  Each warp keeps
-// U row units (RPW rows each) in flight per pass and zeroes the accumulator rows of the
-// units it reads: interleaving the zero stores with the loads row by row kept HBM busier
-// than a zeroing sweep followed by the loads.
+// Delta[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]; also zeroes dq_acc and, when q16 is set
+// (bf16 tensors), writes Q' = R_t Q rounded to fp16 (the logit and dK' operand of the
+// head_dim-64 main kernel, so each query row is rotated once instead of once per key
+// tile).  A group of LPR lanes takes one row (D elements); rows are [B,T,Hq] in memory
+// order.  Each warp keeps U row units (RPW rows each) in flight per pass and zeroes the
+// accumulator rows of the units it reads: interleaving the zero stores with the loads row
+// by row kept HBM busier than a zeroing sweep followed by the loads.
 template <typename Tin, int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
     constexpr int EPV = 16 / sizeof(Tin);        // elements per 16-byte vector
@@ -55,16 +58,45 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
     const uint4* o4 = static_cast<const uint4*>(a.o);
     const uint4* g4 = static_cast<const uint4*>(a.dO);
+    const bool rot = sizeof(Tin) == 2 && a.q16 != nullptr;
+    bool ovf = false;
     for (long long r0 = wg * RPW + sub; r0 - sub < a.rows; r0 += nw * RPW * U) {
-        uint4 ov[U], gv[U];
+        uint4 ov[U], gv[U], qv[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const long long row = r0 + k * nw * RPW;
             if (row < a.rows) {
                 ov[k] = o4[row * LPR + li];
                 gv[k] = g4[row * LPR + li];
+                if (rot) qv[k] = static_cast<const uint4*>(a.q)[row * LPR + li];
             } else {
-                ov[k] = gv[k] = make_uint4(0u, 0u, 0u, 0u);
+                ov[k] = gv[k] = qv[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if constexpr (sizeof(Tin) == 2) {
+            if (rot) {
+                // Lane li holds elements 8li .. 8li+7 of the row: pairs 4li .. 4li+3.
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const long long row = r0 + k * nw * RPW;
+                    if (row >= a.rows) continue;
+                    const int t = (int)((row / a.Hq) % a.T);
+                    const float4* cs4 = reinterpret_cast<const float4*>(a.rope + (size_t)t * (D / 2) + 4 * li);
+                    const float4 c01 = __ldg(cs4), c23 = __ldg(cs4 + 1);
+                    const float cs[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
+                    const uint32_t wq[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+                    uint32_t o16[4];
+#pragma unroll
+                    for (int pr = 0; pr < 4; ++pr) {
+                        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[pr]));
+                        const float c = cs[2 * pr], sn = cs[2 * pr + 1];
+                        const float y0 = x.x * c - x.y * sn, y1 = x.x * sn + x.y * c;
+                        ovf |= fmaxf(fabsf(y0), fabsf(y1)) > 65504.f;
+                        const __half2 h = __floats2half2_rn(y0, y1);
+                        o16[pr] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    static_cast<uint4*>(a.q16)[row * LPR + li] = make_uint4(o16[0], o16[1], o16[2], o16[3]);
+                }
             }
         }
 #pragma unroll
@@ -103,6 +135,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
             }
         }
     }
+    if (ovf && a.err) atomicCAS(a.err, 0, SITE_RANGE);   // a rotated query beyond the fp16 range
 }
 
 // ------------------------------------------------------------------------ post

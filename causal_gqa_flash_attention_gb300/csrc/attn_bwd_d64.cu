@@ -8,26 +8,23 @@
 //
 // One CTA per (batch, kv head, 128-key tile) loops over the G query heads of its group
 // and every 128-query tile on or after the diagonal; dK and dV stay in TMEM for the whole
-// group (no atomics).  Each query tile is taken as two 64-query half-steps: while the
-// softmax-gradient warps work on half-step i, the tensor core computes S^T and dP^T of
-// i+1 and dV / dK of i-1.  dQ' of a whole 128-query tile is one M = 128 MMA over the two
-// halves' dS; the drain warps stage it in shared memory and one TMA bulk reduce-add per
-// tile adds it into the fp32 accumulator.
+// group (no atomics).  Each query tile is taken as two 64-query half-steps, and the two
+// softmax-gradient warp groups take alternate half-steps (group h the half h of every
+// tile): while one group waits on its barriers, the other keeps the special-function unit
+// busy with its exponentials.  dQ' of a whole 128-query tile is one M = 128 MMA over the
+// two halves' dS; the drain warps stage it in shared memory and one TMA bulk reduce-add
+// per tile adds it into the fp32 accumulator.
 //
-// Two limits shape the pipeline.  (1) A chain of K-step MMAs into one accumulator, plus
-// its commit and the waiter's wake-up, takes ~600 cycles on an idle tensor pipe and more
-// under load, so S^T and dP^T are double-buffered in TMEM: those of half-step i+2 are
-// issued as soon as the softmax-gradient warps hold half-step i's in registers.  (2) An
-// MMA with both operands in shared memory (M = 128, N = 64) reads 6 KB per 32 cycles of
-// math, more than the SM's 128 bytes per clock, and every other warp's shared-memory
-// access then queues behind it; so K' (constant per CTA) is copied into TMEM once and
-// S^T reads only Q' from shared memory, and dV takes P^T from TMEM.  The rest of TMEM
-// holds the accumulators, so V, dS^T (for dK') and dS, K' (for dQ') are read from shared
-// memory.
+// A chain of K-step MMAs into one accumulator, plus its commit and the waiter's wake-up,
+// takes ~600 cycles on an idle tensor pipe and more under load, so S^T, dP^T and P^T are
+// double-buffered in TMEM (one buffer per warp group): those of half-step i+2 are issued
+// as soon as its group holds half-step i's in registers.
 //
 // Operand precision: Q', K' and dS are fp16 (logits and dS keep 3 more mantissa bits
 // than bf16; a rotated value or a dS beyond the fp16 range is reported as an error, never
-// silently saturated); P^T, V and dO are bf16.  Every MMA has one operand type.
+// silently saturated); P^T, V and dO are bf16.  Every MMA has one operand type.  Q' comes
+// rotated and rounded to fp16 from the preprocess kernel (each query row is rotated once,
+// not once per key tile); K' is rotated here.
 //
 // Warp roles (512 threads, one CTA per SM):
 //   warp 0      TMA producer (K, V once; Q, dO half tiles into an NQS ring) and the dQ'
@@ -35,14 +32,13 @@
 //   warp 1      TMEM allocator; S^T issuer.
 //   warp 2      dP^T issuer.
 //   warp 3      dV and dK' issuer.
-//   warps 4-7   RoPE of K once (then the K' rows copied into TMEM) and of every Q half
-//               tile (in place, to fp16), and the dQ' drain (thread = query row of the
-//               tile = TMEM lane) through the staging tile.
-//   warps 8-15  two groups of 128 threads (thread = key row = TMEM lane), each on 32 of
-//               the 64 query columns of a half-step; at the end group 0 writes dK (inverse
-//               rotation, scale), group 1 writes dV.
-// TMEM: S^T of buffer b at 128b and dP^T at 128b + 64 (64 cols each), K' (fp16) at 256
-// as a packed A operand, packed bf16 P^T at 288, dV at 320, dK' at 384, dQ' at 448.
+//   warps 4-7   RoPE of K once (in place, to fp16), and the dQ' drain (thread = query row
+//               of the tile = TMEM lane) through the staging tile.
+//   warps 8-15  two groups of 128 threads (thread = key row = TMEM lane); group h takes
+//               the half-steps h, h+2, ... (all 64 query columns, in two 32-column
+//               chunks); at the end group 0 writes dK (inverse rotation, scale), group 1 dV.
+// TMEM: S^T of buffer b (= warp group) at 128b and dP^T at 128b + 64 (64 cols each),
+// packed bf16 P^T of buffer b at 256 + 32b, dV at 320, dK' at 384, dQ' at 448.
 // Shared memory: K' (fp16), V, NQS x (Q' half | dO half), two dS^T tiles [key][query], the
 // fp32 dQ' staging tile (two 128-byte-swizzled column chunks, as the reduce's box expects).
 // Every wait is bounded; a CTA that gives up records an error code, drains its own copies
@@ -69,16 +65,15 @@ struct Bwd64 {
     static constexpr int DS_CHUNK = BKV * 128;
     static constexpr int DQ_STAGE = BT * D * 4;      // fp32 dQ' of a tile: two 32-column chunks
     static constexpr int SMEM = 1024 + 2 * KV_BYTES + NQS * STAGE_BYTES + 2 * DS_TILE + DQ_STAGE;
-    static constexpr int KA_COL = 256, PT_COL = 288, DV_COL = 320, DK_COL = 384, DQ_COL = 448;
+    static constexpr int PT_COL = 256, DV_COL = 320, DK_COL = 384, DQ_COL = 448;
     static constexpr int THREADS = 512;
-    static constexpr int LOOKAHEAD = 4;              // Q half tiles rotated ahead of the drain
     static_assert(SMEM <= 227 * 1024, "shared memory");
-    static_assert(LOOKAHEAD <= NQS + 2, "rotation lookahead must not outrun the TMA ring");
 };
 
 __device__ __forceinline__ uint32_t s_col(int b) { return (uint32_t)(128 * b); }
 __device__ __forceinline__ uint32_t dp_col(int b) { return (uint32_t)(128 * b + 64); }
-// Packed P^T: 64 queries in 32 columns, group g's 32 queries at +16g.
+// Packed P^T of buffer b: 64 queries in 32 columns.
+__device__ __forceinline__ uint32_t pt_col(int b) { return (uint32_t)(Bwd64::PT_COL + 32 * b); }
 
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -97,18 +92,18 @@ __global__ void __launch_bounds__(512, 1)
     auto stage_do = [&](int s) { return sStage + s * C::STAGE_BYTES + C::H_BYTES; };
     auto ds_tile = [&](int tb) { return sDS + tb * C::DS_TILE; };
 
-    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_rot, bar_k_ready, bar_dkv_full, bar_final;
-    __shared__ __align__(8) uint64_t bar_qdo_full[C::NQS], bar_q_ready[C::NQS], bar_qdo_empty[C::NQS];
+    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_dkv_full, bar_final;
+    __shared__ __align__(8) uint64_t bar_qdo_full[C::NQS], bar_qdo_empty[C::NQS];
     __shared__ __align__(8) uint64_t bar_s_full[2], bar_dp_full[2];   // [S^T/dP^T buffer]: MMA done
     __shared__ __align__(8) uint64_t bar_sp_read[2];                  // ... read into registers
-    __shared__ __align__(8) uint64_t bar_p_free;                      // P^T read by dV
+    __shared__ __align__(8) uint64_t bar_p_free[2];                   // [P^T buffer]: read by dV
     __shared__ __align__(8) uint64_t bar_ds_half[2];   // [half]: P^T and the dS^T half of a half-step written
     __shared__ __align__(8) uint64_t bar_ds_tile[2];   // [dS^T tile buffer]: both halves written
     __shared__ __align__(8) uint64_t bar_ds_free[2];   // [dS^T tile buffer]: dK' and dQ' done with it
     __shared__ __align__(8) uint64_t bar_dq_full, bar_dq_free;          // dQ' TMEM accumulator
     __shared__ __align__(8) uint64_t bar_stage_free, bar_staged;   // dQ' staging tile
-    __shared__ __align__(16) float s_lse[8][2][32];    // [softmax warp][buffer][query column of its group]
-    __shared__ __align__(16) float s_delta[8][2][32];
+    __shared__ __align__(16) float s_lse[8][2][64];    // [softmax warp][buffer][query column]
+    __shared__ __align__(16) float s_delta[8][2][64];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -126,21 +121,20 @@ __global__ void __launch_bounds__(512, 1)
 
     if (tid == 0) {
         mbar_init(smem_u32(&bar_kv_full), 1);
-        mbar_init(smem_u32(&bar_k_rot), 128);
         mbar_init(smem_u32(&bar_k_ready), 128);
-        mbar_init(smem_u32(&bar_p_free), 1);
+
         mbar_init(smem_u32(&bar_dkv_full), 1);
         mbar_init(smem_u32(&bar_final), 4);          // one commit per UMMA issuer
         for (int s = 0; s < C::NQS; ++s) {
             mbar_init(smem_u32(&bar_qdo_full[s]), 1);
-            mbar_init(smem_u32(&bar_q_ready[s]), 128);
             mbar_init(smem_u32(&bar_qdo_empty[s]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bar_s_full[i]), 1);
             mbar_init(smem_u32(&bar_dp_full[i]), 1);
-            mbar_init(smem_u32(&bar_sp_read[i]), 256);
-            mbar_init(smem_u32(&bar_ds_half[i]), 256);
+            mbar_init(smem_u32(&bar_sp_read[i]), 128);   // the warp group of buffer i
+            mbar_init(smem_u32(&bar_p_free[i]), 1);
+            mbar_init(smem_u32(&bar_ds_half[i]), 128);   // the warp group of half i
             mbar_init(smem_u32(&bar_ds_tile[i]), 256);
             mbar_init(smem_u32(&bar_ds_free[i]), 2);  // dK' issuer (after the odd half) and dQ' issuer
         }
@@ -229,31 +223,29 @@ __global__ void __launch_bounds__(512, 1)
     } else if (warp == 1 || warp == 2) {
         // ------------------------------------------------------------ S^T (warp 1) / dP^T (warp 2)
         const bool is_s = warp == 1;
-        // S^T = K'Q'^T on fp16 operands with A (K') from TMEM; dP^T = V dO^T on bf16.
+        // S^T = K'Q'^T on fp16 operands, dP^T = V dO^T on bf16.
         const uint32_t id = is_s ? idesc_make(FMT_F16, 128, C::BH, false, false)
                                  : idesc_make(FMT_BF16, 128, C::BH, false, false);
-        const uint64_t dV = kdesc(sV);
+        const uint64_t dA = kdesc(is_s ? sK : sV);
         const uint64_t dB0 = kdesc(is_s ? stage_q(0) : stage_do(0));
         uint64_t* full = is_s ? bar_s_full : bar_dp_full;
-        // S^T waits for the rotated K' (in TMEM) and Q'; dP^T only for the copies of V and dO.
-        uint64_t* ready = is_s ? bar_q_ready : bar_qdo_full;
+        // S^T waits for the rotated K' (once), both for the copies of Q' / dO.
         bool ok = is_s ? mbar_wait_warp(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV)
                        : mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
         for (int hs = 0; ok && hs < n_hs; ++hs) {
             const int s = hs % C::NQS, bf = hs & 1;
-            if (!(ok = mbar_wait_warp(smem_u32(&ready[s]), (hs / C::NQS) & 1, w, SITE_BWD_Q_READY))) break;
-            // Buffer bf is free once the softmax-gradient warps hold half-step hs-2's S^T and
-            // dP^T in registers.
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_qdo_full[s]), (hs / C::NQS) & 1, w, SITE_BWD_QDO_FULL))) break;
+            // Buffer bf is free once its warp group holds half-step hs-2's S^T and dP^T in
+            // registers.
             if (hs >= 2 &&
                 !(ok = mbar_wait_warp(smem_u32(&bar_sp_read[bf]), ((hs - 2) >> 1) & 1, w, SITE_BWD_DS_READY)))
                 break;
             tc_fence_after();
             const uint64_t dB = sdesc_add(dB0, s * C::STAGE_BYTES);
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {          // K = head_dim: 16 per step (32 bytes, 8 columns)
-                if (is_s) umma_ts_e<false>(tm + s_col(bf), tm + C::KA_COL + 8 * ks, sdesc_add(dB, ks * 32), id, ks > 0);
-                else umma_ss_e<false>(tm + dp_col(bf), sdesc_add(dV, ks * 32), sdesc_add(dB, ks * 32), id, ks > 0);
-            }
+            for (int ks = 0; ks < D / 16; ++ks)            // K = head_dim: 16 per step (32 bytes)
+                umma_ss_e<false>(tm + (is_s ? s_col(bf) : dp_col(bf)), sdesc_add(dA, ks * 32), sdesc_add(dB, ks * 32),
+                                 id, ks > 0);
             umma_commit_e(smem_u32(&full[bf]));
         }
         umma_commit_e(smem_u32(&bar_final));
@@ -270,9 +262,9 @@ __global__ void __launch_bounds__(512, 1)
             const uint64_t dOmn = sdesc_add(dOmn0, s * C::STAGE_BYTES), dQmn = sdesc_add(dQmn0, s * C::STAGE_BYTES);
 #pragma unroll
             for (int ks = 0; ks < C::BH / 16; ++ks)         // dV += P^T dO (P^T from TMEM), K = queries
-                umma_ts_e<false>(tm + C::DV_COL, tm + C::PT_COL + 8 * ks, sdesc_add(dOmn, ks * 16 * 128), id_dv,
+                umma_ts_e<false>(tm + C::DV_COL, tm + pt_col(half) + 8 * ks, sdesc_add(dOmn, ks * 16 * 128), id_dv,
                                  (hs > 0 || ks > 0) ? 1u : 0u);
-            umma_commit_e(smem_u32(&bar_p_free));
+            umma_commit_e(smem_u32(&bar_p_free[half]));
             const uint64_t dDS = kdesc(ds_tile(tb) + half * C::DS_CHUNK);
 #pragma unroll
             for (int ks = 0; ks < C::BH / 16; ++ks)         // dK' += dS^T Q', K = queries
@@ -292,38 +284,10 @@ __global__ void __launch_bounds__(512, 1)
         if (ok) {
             ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_F16, true>(sK, nullptr, kv0, T, r, a.rope);
             fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bar_k_rot));
-            ok = mbar_wait_warp(smem_u32(&bar_k_rot), 0, w, SITE_BWD_KV);
-        }
-        if (ok) {
-            // Key row r of K' into TMEM lane r as a packed A operand (64 values = 32 columns,
-            // in the order of the 16-byte units of the swizzled row).
-            uint32_t kr[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint4 kk = *reinterpret_cast<const uint4*>(sK + sw128_offset(r, u));
-                kr[4 * u] = kk.x; kr[4 * u + 1] = kk.y; kr[4 * u + 2] = kk.z; kr[4 * u + 3] = kk.w;
-            }
-            tmem_st32(lt + C::KA_COL, kr);
-            tmem_wait_st();
-            tc_fence_before();
             mbar_arrive(smem_u32(&bar_k_ready));
         }
-        int rot = 0;   // next half-step whose Q tile is rotated
-        auto rotate_upto = [&](int lim) -> bool {
-            for (; rot < lim && rot < n_hs; ++rot) {
-                const int s = rot % C::NQS;
-                if (!mbar_wait_warp(smem_u32(&bar_qdo_full[s]), (rot / C::NQS) & 1, w, SITE_BWD_QDO_FULL)) return false;
-                ovf |= rope_tile_smem<D, C::BH, 128, ROPE_F16, true>(stage_q(s), nullptr, hs_q0(rot), T, r, a.rope);
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&bar_q_ready[s]));
-            }
-            return true;
-        };
         if (r == 0) tma_prefetch_desc(&tm_dq);
-        if (ok) ok = rotate_upto(C::LOOKAHEAD);
         for (int tau = 0; ok && tau < n_tiles; ++tau) {
-            if (!(ok = rotate_upto(2 * tau + 2 + C::LOOKAHEAD))) break;
             if (!(ok = mbar_wait_warp(smem_u32(&bar_dq_full), tau & 1, w, SITE_BWD_DQ_FULL))) break;
             tc_fence_after();
             uint32_t v[64];
@@ -359,92 +323,112 @@ __global__ void __launch_bounds__(512, 1)
         if (ovf) atomicCAS(a.err, 0, SITE_RANGE);
     } else {
         // ------------------------------------------------------------ P^T, dS^T; dK, dV epilogue
-        const int g = (warp - 8) >> 2;
+        const int g = (warp - 8) >> 2;                   // warp group = half index = TMEM buffer
         const int r = (warp & 3) * 32 + lane;            // key row = TMEM lane
         const int kvpos = kv0 + r;
-        const int cb = 32 * g;                           // this group's query columns of a half-step
         const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
         const float sl2 = a.scale_log2;
         float amax = 0.f;
         bool ok = true;
-        // LSE / Delta of this group's 32 query columns: lane l fetches column l of the next
-        // half-step while the current one runs, and the warp stages them in its own
-        // double-buffered slot (read back as broadcasts; __syncwarp orders the warp's own
-        // writes and reads, so no cross-warp barrier is needed).
+        // LSE / Delta of the 64 query columns: lanes l and l+32 fetch columns l and l+32 of
+        // the group's next half-step while the current one runs, and the warp stages them in
+        // its own double-buffered slot (read back as broadcasts; __syncwarp orders the warp's
+        // own writes and reads, so no cross-warp barrier is needed).  The loaded values are
+        // not touched until they are staged (a use right after the load would stall).
         const int sw = warp - 8;
-        auto row_vals = [&](int hs, float& lv, float& dv) {
-            const int qpos = hs_q0(hs) + cb + lane;
-            const size_t rix = ((size_t)b * a.Hq + tile_head(hs >> 1)) * T + qpos;
-            lv = qpos < T ? a.lse[rix] * 1.4426950408889634f : 0.f;
-            dv = qpos < T ? a.delta[rix] : 0.f;
+        auto row_vals = [&](int hs, float (&lv)[2], float (&dv)[2]) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int qpos = hs_q0(hs) + lane + 32 * k;
+                const size_t rix = ((size_t)b * a.Hq + tile_head(hs >> 1)) * T + qpos;
+                lv[k] = 0.f;
+                dv[k] = 0.f;
+                if (qpos < T) {
+                    lv[k] = __ldg(a.lse + rix);
+                    dv[k] = __ldg(a.delta + rix);
+                }
+            }
         };
-        auto publish = [&](int hs, float lv, float dv) {
-            s_lse[sw][hs & 1][lane] = lv;
-            s_delta[sw][hs & 1][lane] = dv;
+        auto publish = [&](int hs, const float (&lv)[2], const float (&dv)[2]) {
+            const int buf = (hs >> 1) & 1;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                s_lse[sw][buf][lane + 32 * k] = lv[k] * 1.4426950408889634f;
+                s_delta[sw][buf][lane + 32 * k] = dv[k];
+            }
             __syncwarp();
         };
-        if (n_hs > 0) {
-            float lv, dv;
-            row_vals(0, lv, dv);
-            publish(0, lv, dv);
+        if (g < n_hs) {
+            float lv[2], dv[2];
+            row_vals(g, lv, dv);
+            publish(g, lv, dv);
         }
-        for (int hs = 0; hs < n_hs; ++hs) {
-            const int bf = hs & 1, half = hs & 1, tau = hs >> 1, tb = tau & 1;
-            const int q0 = hs_q0(hs) + cb;
-            float lv_n = 0.f, dv_n = 0.f;
-            if (hs + 1 < n_hs) row_vals(hs + 1, lv_n, dv_n);   // in flight during this half-step
-            if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[bf]), (hs >> 1) & 1, w, SITE_BWD_S_FULL))) break;
-            if (!(ok = mbar_wait_warp(smem_u32(&bar_dp_full[bf]), (hs >> 1) & 1, w, SITE_BWD_DP_FULL))) break;
+        for (int hs = g; hs < n_hs; hs += 2) {
+            const int tau = hs >> 1, tb = tau & 1, buf = (hs >> 1) & 1;
+            const int q0 = hs_q0(hs);
+            float lv_n[2] = {0.f, 0.f}, dv_n[2] = {0.f, 0.f};
+            if (hs + 2 < n_hs) row_vals(hs + 2, lv_n, dv_n);   // in flight during this half-step
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[g]), (hs >> 1) & 1, w, SITE_BWD_S_FULL))) break;
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_dp_full[g]), (hs >> 1) & 1, w, SITE_BWD_DP_FULL))) break;
             tc_fence_after();
-            uint32_t sr[32], dr[32];
-            tmem_ld32(lt + s_col(bf) + cb, sr);
-            tmem_ld32(lt + dp_col(bf) + cb, dr);
-            tmem_wait_ld();
-            reg_fence32(sr);
-            reg_fence32(dr);
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_sp_read[bf]));      // the buffer may take half-step hs+2
             const bool diag = kvpos > q0;                // some of this row's queries precede the key
-            uint32_t pk[16], dk[16];
-            const float4* l4 = reinterpret_cast<const float4*>(&s_lse[sw][bf][0]);
-            const float4* d4 = reinterpret_cast<const float4*>(&s_delta[sw][bf][0]);
+            uint8_t* dsbase = ds_tile(tb) + g * C::DS_CHUNK;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-                const float4 lq4 = l4[e >> 2], dq4 = d4[e >> 2];   // broadcast reads
-                const float lq[4] = {lq4.x, lq4.y, lq4.z, lq4.w}, dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w};
-                float p[4], ds[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
-                    if (diag && kvpos > q0 + e + k) p[k] = 0.f;
-                    ds[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
-                    amax = fmaxf(amax, fabsf(ds[k]));
+            for (int c = 0; c < 2; ++c) {                // two 32-query chunks
+                uint32_t sr[32], dr[32];
+                tmem_ld32(lt + s_col(g) + 32 * c, sr);
+                tmem_ld32(lt + dp_col(g) + 32 * c, dr);
+                tmem_wait_ld();
+                reg_fence32(sr);
+                reg_fence32(dr);
+                if (c == 1) {                            // the buffer may take half-step hs+2
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bar_sp_read[g]));
                 }
-                pk[e >> 1] = pack_bf162(p[0], p[1]);
-                pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
-                dk[e >> 1] = pack_half2(ds[0], ds[1]);
-                dk[(e >> 1) + 1] = pack_half2(ds[2], ds[3]);
-            }
-            // P^T's columns are free once dV of the previous half-step has read them.
-            if (hs >= 1 && !(ok = mbar_wait_warp(smem_u32(&bar_p_free), (hs - 1) & 1, w, SITE_BWD_DS_READY))) break;
-            tc_fence_after();
-            tmem_st16(lt + C::PT_COL + 16 * g, pk);
-            // The dS^T tile buffer is reused every second tile: dK' and dQ' of tile tau-2
-            // must be done with it.
-            if (half == 0 && tau >= 2 &&
-                !(ok = mbar_wait_warp(smem_u32(&bar_ds_free[tb]), ((tau - 2) >> 1) & 1, w, SITE_BWD_DS_FREE)))
-                break;
-            uint8_t* base = ds_tile(tb) + half * C::DS_CHUNK;
+                uint32_t pk[16], dk[16];
+                const float4* l4 = reinterpret_cast<const float4*>(&s_lse[sw][buf][32 * c]);
+                const float4* d4 = reinterpret_cast<const float4*>(&s_delta[sw][buf][32 * c]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4*>(base + sw128_offset(r, 4 * g + k)) =
-                    make_uint4(dk[4 * k], dk[4 * k + 1], dk[4 * k + 2], dk[4 * k + 3]);
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 lq4 = l4[e >> 2], dq4 = d4[e >> 2];   // broadcast reads
+                    const float lq[4] = {lq4.x, lq4.y, lq4.z, lq4.w}, dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w};
+                    float p[4], ds[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
+                        if (diag && kvpos > q0 + 32 * c + e + k) p[k] = 0.f;
+                        ds[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
+                        amax = fmaxf(amax, fabsf(ds[k]));
+                    }
+                    pk[e >> 1] = pack_bf162(p[0], p[1]);
+                    pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
+                    dk[e >> 1] = pack_half2(ds[0], ds[1]);
+                    dk[(e >> 1) + 1] = pack_half2(ds[2], ds[3]);
+                }
+                if (c == 0) {
+                    // P^T buffer g is free once dV of half-step hs-2 has read it; the dS^T
+                    // tile buffer once dK' and dQ' of tile tau-2 have.
+                    if (hs >= 2 &&
+                        !(ok = mbar_wait_warp(smem_u32(&bar_p_free[g]), ((hs - 2) >> 1) & 1, w, SITE_BWD_DS_READY)))
+                        break;
+                    if (tau >= 2 &&
+                        !(ok = mbar_wait_warp(smem_u32(&bar_ds_free[tb]), ((tau - 2) >> 1) & 1, w, SITE_BWD_DS_FREE)))
+                        break;
+                    tc_fence_after();
+                }
+                tmem_st16(lt + pt_col(g) + 16 * c, pk);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4*>(dsbase + sw128_offset(r, 4 * c + k)) =
+                        make_uint4(dk[4 * k], dk[4 * k + 1], dk[4 * k + 2], dk[4 * k + 3]);
+            }
+            if (!ok) break;
             fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_ds_half[half]));
-            if (half == 1) mbar_arrive(smem_u32(&bar_ds_tile[tb]));
-            if (hs + 1 < n_hs) publish(hs + 1, lv_n, dv_n);
+            mbar_arrive(smem_u32(&bar_ds_half[g]));
+            mbar_arrive(smem_u32(&bar_ds_tile[tb]));
+            if (hs + 2 < n_hs) publish(hs + 2, lv_n, dv_n);
         }
         if (amax > 65504.f) atomicCAS(a.err, 0, SITE_RANGE);   // a dS beyond the fp16 range
         // Epilogue, key row r of this CTA's tile: group 0 writes dK = s R^T dK', group 1 dV.

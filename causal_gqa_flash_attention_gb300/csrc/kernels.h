@@ -44,6 +44,10 @@ struct BwdPreArgs {
     float* dq_acc;           // [B,T,Hq,D] fp32, zeroed here
     long long rows;          // B*T*Hq
     int T, Hq, D;
+    const void* q;           // [B,T,Hq,D] bf16: rotated into q16 when q16 is set
+    void* q16;               // [B,T,Hq,D] fp16 R Q, or nullptr
+    const float2* rope;      // [T, D/2] (cos, sin), when q16 is set
+    int* err;                // device error word (an fp16 overflow of R Q), may be null
 };
 
 struct BwdArgs {

@@ -84,7 +84,8 @@ ne_status ne_attn_fwd_f32(const float* q, const float* k, const float* v, float*
 
 /* Bytes of device workspace ne_attn_bwd needs for this shape (0 on a bad shape).
  * Layout: Delta fp32 [B,Hq,T] at offset 0, then (256-byte aligned) the fp32 dQ
- * accumulator [B,T,Hq,D].  Both are rewritten by every call. */
+ * accumulator [B,T,Hq,D], then (256-byte aligned) the rotated queries R Q as fp16
+ * [B,T,Hq,D] (used by the bf16 head_dim-64 kernel).  All are rewritten by every call. */
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D);
 
 /* Backward (검증 및 안정성: the hand-written backward), the vector-Jacobian product of
@@ -104,15 +105,16 @@ ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const 
 /* Backward that allocates nothing (there is no counterpart of this call on the
  * pages: it is a deployment convenience).  Same computation, arguments and outputs
  * as ne_attn_bwd for bf16 tensors, but without a workspace argument: its scratch
- * (RoPE table, Delta, fp32 dQ accumulator) lives in one file-scope device array of
- * 32 MiB that every GPU loading the library keeps until the process exits.  It is for
+ * (RoPE table, Delta, fp32 dQ accumulator, rotated queries) lives in one file-scope
+ * device array of 48 MiB that every GPU loading the library keeps until the process exits.  It is for
  * callers that cannot call cudaMalloc at this point: code that runs while a stream
  * is being captured into a CUDA graph (allocation is not allowed there), runtimes
  * whose own allocator already owns the device's free memory, or real-time loops that
  * forbid allocation after start-up.  It calls no cudaMalloc, cudaFree or allocating
  * library routine.
- *  - Limit: round256(T*(D/2)*8) + round256(B*Hq*T*4) + B*T*Hq*D*4 <= 33554432 bytes
- *    (the GPU-pipeline shape B=16 T=512 Hq=12 D=64 uses 25.7 MB); larger shapes
+ *  - Limit: round256(T*(D/2)*8) + round256(B*Hq*T*4) + round256(B*T*Hq*D*4)
+ *    + (D == 64 ? B*T*Hq*D*2 : 0) <= 50331648 bytes (the GPU-pipeline shape B=16 T=512
+ *    Hq=12 D=64 uses 38.3 MB); larger shapes
  *    return NE_ERR_INVALID_ARG before anything is enqueued.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any stream

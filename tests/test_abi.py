@@ -41,9 +41,10 @@ def test_status_strings(lib):
 
 def test_workspace_size_formula(lib):
     B, T, Hq, Hkv, D = 16, 512, 12, 4, 64
-    delta = B * Hq * T * 4
-    delta_al = (delta + 255) // 256 * 256
-    assert lib.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D) == delta_al + B * T * Hq * D * 4
+    r256 = lambda x: (x + 255) // 256 * 256
+    # Delta fp32 [B,Hq,T] | dQ accumulator fp32 [B,T,Hq,D] | rotated fp16 Q [B,T,Hq,D]
+    want = r256(B * Hq * T * 4) + r256(B * T * Hq * D * 4) + B * T * Hq * D * 2
+    assert lib.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D) == want
     assert lib.ne_attn_bwd_workspace_size(1, 8, 3, 2, 64) == 0   # Hq % Hkv != 0
 
 
