@@ -40,15 +40,15 @@ namespace {
 // (bf16 tensors), writes Q' = R_t Q rounded to fp16 (the logit and dK' operand of the
 // head_dim-64 main kernel, so each query row is rotated once instead of once per key
 // tile).  A group of LPR lanes takes one row (D elements); rows are [B,T,Hq] in memory
-// order.  Each warp keeps U row units (RPW rows each) in flight per pass and zeroes the
-// accumulator rows of the units it reads: interleaving the zero stores with the loads row
-// by row kept HBM busier than a zeroing sweep followed by the loads.
+// order.  Each warp zeroes the accumulator rows of the units it reads: interleaving the
+// zero stores with the loads row by row kept HBM busier than a zeroing sweep followed by
+// the loads.
 template <typename Tin, int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
     constexpr int EPV = 16 / sizeof(Tin);        // elements per 16-byte vector
     constexpr int LPR = D / EPV;                 // lanes per row (8 or 16)
     constexpr int RPW = 32 / LPR;                // rows per warp unit
-    constexpr int U = 2;                         // units in flight per pass
+    constexpr int U = 1;                         // units per pass (more were slower when measured)
     constexpr int ZPL = D / 4 / LPR;             // 16-byte zero stores per lane per row
     griddep_launch_dependents();
     griddep_wait();

@@ -7,14 +7,15 @@
 //
 // One CTA owns two consecutive 128-row query subtiles (u = 0, 1) of one (batch, query
 // head) and walks 64-key tiles up to the diagonal; every K/V tile is loaded and
-// rotated once for both subtiles.  Warp roles (416 threads, one CTA per SM):
+// rotated once for both subtiles.  Warp roles (480 threads, one CTA per SM):
 //   warp 0       TMA producer: Q0, Q1 once, then K/V tiles into an NS-stage ring.
-//   warp 1, 2    UMMA issuer of subtile 0 / 1 (warp 1 also owns the 512 TMEM columns).
-//                One thread issues a tcgen05.mma only every ~100 cycles, so each subtile
-//                gets its own issuer: S_u(j+2) = Q'_u K'_j+2^T into S buffer j % 2 right
-//                after PV_u(j) = P_u(j) V_j, two tiles ahead of the softmax.
-//   warps 3, 12  RoPE on every K tile in place (fp16 logit operand; TF32: rounded fp32)
-//                and, for TF32, V transposed (TF32 UMMA reads K-major operands only).
+//   warp 1, 2    UMMA issuer of subtile 0 / 1 (warp 1 also owns the 512 TMEM columns);
+//                each subtile has its own issuing warp (the whole warp runs the loop,
+//                one elected lane issues): S_u(j+2) = Q'_u K'_j+2^T into S buffer j % 2
+//                right after PV_u(j) = P_u(j) V_j, two tiles ahead of the softmax.
+//   warps 3, 12-14  RoPE on every K tile in place (fp16 logit operand; TF32: rounded
+//                fp32) and, for TF32, V transposed (TF32 UMMA reads K-major operands
+//                only).  Four warps: with two, the rotation paced the whole pipeline.
 //   warps 4-7    softmax of subtile 0; warps 8-11 softmax of subtile 1.  Thread r owns
 //                query row r (TMEM lane r): it rotates its Q row block once, then per
 //                tile reads the S row from TMEM, updates the running max m and sum l,
@@ -57,7 +58,8 @@ struct FwdCfg {
     static constexpr uint32_t FMT_S = TF32 ? FMT_TF32 : FMT_F16;
     static constexpr uint32_t FMT_PV = TF32 ? FMT_TF32 : FMT_BF16;
     static constexpr int MODE = TF32 ? ROPE_TF32 : ROPE_F16;
-    static constexpr int THREADS = 416;             // 13 warps
+    static constexpr int THREADS = 480;             // 15 warps
+    static constexpr int ROPE_THREADS = 128;        // warps 3, 12, 13, 14
     static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
     static_assert(D <= 128, "O subtiles must fit next to four S buffers in 512 TMEM columns");
     static_assert(NS >= 3, "need at least three K/V stages (S runs two tiles ahead)");
@@ -179,7 +181,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int u, i
 }
 
 template <bool TF32, int D>
-__global__ void __launch_bounds__(416, 1)
+__global__ void __launch_bounds__(480, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FwdArgs a) {
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(416, 1)
         }
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(smem_u32(&bar_kv_full[s]), 1);
-            mbar_init(smem_u32(&bar_k_ready[s]), 64);
+            mbar_init(smem_u32(&bar_k_ready[s]), C::ROPE_THREADS);
             mbar_init(smem_u32(&bar_kv_empty[s]), 2);    // one commit per UMMA issuer
         }
         abort_flag = 0;
@@ -280,13 +282,13 @@ __global__ void __launch_bounds__(416, 1)
         }
     } else if (warp == 1 || warp == 2) {
         // ------------------------------------------------------------ UMMA issuers
-        // A single thread issues a tcgen05.mma only every ~100 cycles, so each subtile
-        // has its own issuer (lane 0 of warp 1 + u).  S_u(j) goes to S buffer j % 2,
-        // two tiles ahead of the softmax, and overwrites P_u(j-2), whose PV the same
-        // thread issued earlier (one thread's UMMAs execute in order).
+        // Each subtile has its own issuing warp (1 + u); the whole warp runs the loop and
+        // one elected lane issues.  S_u(j) goes to S buffer j % 2, two tiles ahead of the
+        // softmax, and overwrites P_u(j-2), whose PV the same lane issued earlier (one
+        // thread's UMMAs execute in order).
         const int u = warp - 1;
         const int n = n_u[u];
-        if (lane == 0) {
+        {
             constexpr uint32_t id_s = idesc_make(C::FMT_S, 128, C::BN, false, false);
             constexpr uint32_t id_o = idesc_make(C::FMT_PV, 128, D, false, !TF32);
             // Descriptors are built once; a K-step or a stage only moves the start address.
@@ -301,13 +303,13 @@ __global__ void __launch_bounds__(416, 1)
 #pragma unroll
                 for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
                     const uint32_t byte = ks * 32;
-                    umma_ss<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
+                    umma_ss_e<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
                                   sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
                 }
-                umma_commit(smem_u32(&bar_s_full[u * 2 + (j & 1)]));
+                umma_commit_e(smem_u32(&bar_s_full[u * 2 + (j & 1)]));
             };
             auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait(smem_u32(&bar_p_ready[u * 2 + (j & 1)]), (j >> 1) & 1, w, SITE_FWD_P_READY))
+                if (!mbar_wait_warp(smem_u32(&bar_p_ready[u * 2 + (j & 1)]), (j >> 1) & 1, w, SITE_FWD_P_READY))
                     return false;
                 tc_fence_after();
                 const uint64_t dv = sdesc_add(dv0, (j % C::NS) * C::STAGE_BYTES);
@@ -317,18 +319,18 @@ __global__ void __launch_bounds__(416, 1)
                     // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
                     // MN-major, PV_ROWS keys per K-step.
                     const uint32_t off = TF32 ? ((ks * 32) >> 7) * D * 128 + ((ks * 32) & 127) : ks * C::PV_ROWS * 128;
-                    umma_ts<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+                    umma_ts_e<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
                 }
-                umma_commit(smem_u32(&bar_o_done[u]));
+                umma_commit_e(smem_u32(&bar_o_done[u]));
                 return true;
             };
             auto k_ready = [&](int j) {
-                const bool r = mbar_wait(smem_u32(&bar_k_ready[j % C::NS]), (j / C::NS) & 1, w, SITE_FWD_K_READY);
+                const bool r = mbar_wait_warp(smem_u32(&bar_k_ready[j % C::NS]), (j / C::NS) & 1, w, SITE_FWD_K_READY);
                 tc_fence_after();
                 return r;
             };
             // A subtile beyond T (n == 0) issues nothing but still releases every stage.
-            bool ok = n == 0 || mbar_wait(smem_u32(&bar_q_ready[u]), 0, w, SITE_FWD_Q);
+            bool ok = n == 0 || mbar_wait_warp(smem_u32(&bar_q_ready[u]), 0, w, SITE_FWD_Q);
             for (int j = 0; ok && j < 2 && j < n; ++j) {
                 if (!(ok = k_ready(j))) break;
                 issue_s(j);
@@ -346,14 +348,14 @@ __global__ void __launch_bounds__(416, 1)
                 } else if (!(ok = k_ready(j))) {
                     break;
                 }
-                umma_commit(smem_u32(&bar_kv_empty[j % C::NS]));
+                umma_commit_e(smem_u32(&bar_kv_empty[j % C::NS]));
             }
-            umma_commit(smem_u32(&bar_final));
+            umma_commit_e(smem_u32(&bar_final));
         }
-    } else if (warp == 3 || warp == 12) {
+    } else if (warp == 3 || warp >= 12) {
         // ------------------------------------------------------------ RoPE on K (+ V^T)
-        const int rt = lane + (warp == 12 ? 32 : 0);
-        using Rope = RopeTile<D, C::BN, 64, C::MODE>;
+        const int rt = lane + (warp == 3 ? 0 : 32 * (warp - 11));
+        using Rope = RopeTile<D, C::BN, C::ROPE_THREADS, C::MODE>;
         Rope rope;
         rope.init(rt, a.rope);
         float4 next[Rope::F4];
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(416, 1)
             for (int e = 0; e < Rope::F4; ++e) cur[e] = next[e];
             if (j + 1 < n_kv) rope.load_base(next, (j + 1) * C::BN, T, a.rope);   // one tile early
             if (!mbar_wait_warp(smem_u32(&bar_kv_full[s]), (j / C::NS) & 1, w, SITE_FWD_KV_FULL)) break;
-            if constexpr (TF32) transpose_v_tf32<D, C::BN, 64>(stage_v(s), stage_vt(s), rt);
+            if constexpr (TF32) transpose_v_tf32<D, C::BN, C::ROPE_THREADS>(stage_v(s), stage_vt(s), rt);
             rope.template apply<false>(stage_k(s), nullptr, cur);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready[s]));
