@@ -70,6 +70,25 @@ struct Bwd64 {
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
+// (query head, first query row) of tile tau, advanced one tile at a time: the tiles of a
+// CTA run over the G heads of its kv group and, per head, the 128-query tiles j .. n_qt-1.
+// (Dividing tau by the per-head count in the loops would go through the special-function
+// unit, which the exponentials keep busy.)
+struct TileWalk {
+    int h, qt;
+    __device__ __forceinline__ void init(int hkv, int G, int j) {
+        h = hkv * G;
+        qt = j;
+    }
+    __device__ __forceinline__ void next(int j, int n_qt) {
+        if (++qt == n_qt) {
+            qt = j;
+            ++h;
+        }
+    }
+    __device__ __forceinline__ int q0() const { return qt * Bwd64::BT; }
+};
+
 __device__ __forceinline__ uint32_t s_col(int b) { return (uint32_t)(128 * b); }
 __device__ __forceinline__ uint32_t dp_col(int b) { return (uint32_t)(128 * b + 64); }
 // Packed P^T of buffer b: 64 queries in 32 columns.
@@ -115,9 +134,6 @@ __global__ void __launch_bounds__(512, 1)
     const int per_head = n_qt - j;                   // 128-query tiles on or after the diagonal
     const int n_tiles = G * per_head;
     const int n_hs = 2 * n_tiles;
-    auto tile_head = [&](int tau) { return hkv * G + tau / per_head; };
-    auto tile_q0 = [&](int tau) { return (j + tau % per_head) * C::BT; };
-    auto hs_q0 = [&](int hs) { return tile_q0(hs >> 1) + (hs & 1) * C::BH; };
 
     if (tid == 0) {
         mbar_init(smem_u32(&bar_kv_full), 1);
@@ -177,6 +193,8 @@ __global__ void __launch_bounds__(512, 1)
             tma_load_4d(smem_u32(sV), &tm_v, kvf, 0, hkv, kv0, b);
         }
         int issued = 0;
+        TileWalk lw;                                 // tile of the next half-step to load
+        lw.init(hkv, G, j);
         auto load = [&](int hs) -> bool {
             const int s = hs % C::NQS;
             if (hs >= C::NQS &&
@@ -184,11 +202,12 @@ __global__ void __launch_bounds__(512, 1)
                 return false;
             if (lane == 0) {
                 const uint32_t f = smem_u32(&bar_qdo_full[s]);
-                const int h = tile_head(hs >> 1), q0 = hs_q0(hs);
+                const int h = lw.h, q0 = lw.q0() + (hs & 1) * C::BH;
                 mbar_arrive_expect_tx(f, 2 * C::H_BYTES);
                 tma_load_4d(smem_u32(stage_q(s)), &tm_q, f, 0, h, q0, b);
                 tma_load_4d(smem_u32(stage_do(s)), &tm_do, f, 0, h, q0, b);
             }
+            if (hs & 1) lw.next(j, n_qt);
             ++issued;
             return true;
         };
@@ -287,7 +306,9 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive(smem_u32(&bar_k_ready));
         }
         if (r == 0) tma_prefetch_desc(&tm_dq);
-        for (int tau = 0; ok && tau < n_tiles; ++tau) {
+        TileWalk dw;
+        dw.init(hkv, G, j);
+        for (int tau = 0; ok && tau < n_tiles; ++tau, dw.next(j, n_qt)) {
             if (!(ok = mbar_wait_warp(smem_u32(&bar_dq_full), tau & 1, w, SITE_BWD_DQ_FULL))) break;
             tc_fence_after();
             uint32_t v[64];
@@ -313,7 +334,7 @@ __global__ void __launch_bounds__(512, 1)
             if (r == 0) {
                 if (!(ok = mbar_wait(smem_u32(&bar_staged), tau & 1, w, SITE_BWD_DQ_FULL))) break;
                 // Rows at or beyond T lie outside the tensor map and are skipped.
-                const int h = tile_head(tau), q0 = tile_q0(tau);
+                const int h = dw.h, q0 = dw.q0();
                 tma_reduce_add_4d(&tm_dq, smem_u32(sDQ), 0, h, q0, b);
                 tma_reduce_add_4d(&tm_dq, smem_u32(sDQ + C::BT * 128), 32, h, q0, b);
                 bulk_commit_group();
@@ -336,11 +357,17 @@ __global__ void __launch_bounds__(512, 1)
         // own writes and reads, so no cross-warp barrier is needed).  The loaded values are
         // not touched until they are staged (a use right after the load would stall).
         const int sw = warp - 8;
-        auto row_vals = [&](int hs, float (&lv)[2], float (&dv)[2]) {
+        // Half-step hs = 2 tau + g lies in tile tau; `cur` walks the group's current tile,
+        // `nxt` the one after it.
+        TileWalk cur, nxt;
+        cur.init(hkv, G, j);
+        nxt = cur;
+        nxt.next(j, n_qt);
+        auto row_vals = [&](const TileWalk& tw, float (&lv)[2], float (&dv)[2]) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                const int qpos = hs_q0(hs) + lane + 32 * k;
-                const size_t rix = ((size_t)b * a.Hq + tile_head(hs >> 1)) * T + qpos;
+                const int qpos = tw.q0() + g * C::BH + lane + 32 * k;
+                const size_t rix = ((size_t)b * a.Hq + tw.h) * T + qpos;
                 lv[k] = 0.f;
                 dv[k] = 0.f;
                 if (qpos < T) {
@@ -360,14 +387,14 @@ __global__ void __launch_bounds__(512, 1)
         };
         if (g < n_hs) {
             float lv[2], dv[2];
-            row_vals(g, lv, dv);
+            row_vals(cur, lv, dv);
             publish(g, lv, dv);
         }
-        for (int hs = g; hs < n_hs; hs += 2) {
+        for (int hs = g; hs < n_hs; hs += 2, cur = nxt, nxt.next(j, n_qt)) {
             const int tau = hs >> 1, tb = tau & 1, buf = (hs >> 1) & 1;
-            const int q0 = hs_q0(hs);
+            const int q0 = cur.q0() + g * C::BH;
             float lv_n[2] = {0.f, 0.f}, dv_n[2] = {0.f, 0.f};
-            if (hs + 2 < n_hs) row_vals(hs + 2, lv_n, dv_n);   // in flight during this half-step
+            if (hs + 2 < n_hs) row_vals(nxt, lv_n, dv_n);   // in flight during this half-step
             if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[g]), (hs >> 1) & 1, w, SITE_BWD_S_FULL))) break;
             if (!(ok = mbar_wait_warp(smem_u32(&bar_dp_full[g]), (hs >> 1) & 1, w, SITE_BWD_DP_FULL))) break;
             tc_fence_after();
