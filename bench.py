@@ -397,7 +397,9 @@ def run_ours(args, w):
     dom = max(kernels, key=lambda k: kernels[k]["share"])
     dk = kernels[dom]
     dom_peak = peak if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
-    src = {"attn_fwd": "attn_fwd.cu", "attn_bwd": "attn_bwd.cu", "bwd_pre": "attn_bwd.cu", "bwd_post": "attn_bwd.cu"}[dom]
+    bwd_main_src = "attn_bwd_d64.cu" if (w.dtype == "bf16" and w.D == 64) else \
+        ("attn_bwd_tf32.cu" if w.dtype == "f32" else "attn_bwd.cu")
+    src = {"attn_fwd": "attn_fwd.cu", "attn_bwd": bwd_main_src, "bwd_pre": "attn_bwd.cu", "bwd_post": "attn_bwd.cu"}[dom]
     traffic = profiled_traffic(os.path.join(ROOT, "causal_gqa_flash_attention_gb300", "csrc", src), f"{dom}:{w.name}")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": hz.world, "steps": args.steps,
