@@ -60,8 +60,15 @@ def _load():
                                             ctypes.c_double]
             lib.ne_ref_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, ctypes.c_void_p, i, i, i, i,
                                             i, ctypes.c_double]
+            ip = ctypes.POINTER(ctypes.c_int)
+            vp = ctypes.c_void_p
+            lib.ne_ref_attn_qrows.argtypes = [dp, dp, dp, vp, i, i, ip, i, dp, dp, vp, vp, i, i, i, i, i,
+                                              ctypes.c_double]
+            lib.ne_ref_attn_krows.argtypes = [dp, dp, dp, dp, i, i, ip, i, dp, dp, i, i, i, i, i,
+                                              ctypes.c_double]
             for f in (lib.ne_ref_rope_table, lib.ne_ref_rope_apply, lib.ne_ref_attn_fwd,
-                      lib.ne_ref_attn_bwd, lib.ne_ref_num_threads):
+                      lib.ne_ref_attn_bwd, lib.ne_ref_attn_qrows, lib.ne_ref_attn_krows,
+                      lib.ne_ref_num_threads):
                 f.restype = ctypes.c_int
             lib.ne_ref_num_threads.argtypes = []
             _lib = lib
@@ -136,3 +143,55 @@ def attn_bwd(q, k, v, dO, theta: float = 10000.0, return_delta: bool = False):
     if rc != 0:
         raise ValueError("bad attention shape")
     return (dq, dk, dv, delta) if return_delta else (dq, dk, dv)
+
+
+def _batch(x, b):
+    """Batch row b of x (a NumPy array or a CPU tensor of any float dtype) as a
+    C-contiguous fp64 array of shape [1, T, H, D]."""
+    xb = x[b:b + 1]
+    if hasattr(xb, "detach"):          # a tensor: bf16 has no NumPy dtype, widen first
+        xb = xb.detach().double().cpu().numpy()
+    return np.ascontiguousarray(_f64(xb))
+
+
+def attn_qrows(q, k, v, dO, b: int, h: int, rows, theta: float = 10000.0):
+    """Query rows `rows` of (batch b, query head h), each computed on its own from the
+    definitions: O rows [n, D], LSE [n], and with dO also dQ rows [n, D] and Delta [n]
+    (None otherwise).  For checks at sizes where the full oracle does not fit."""
+    qb, kb, vb = _batch(q, b), _batch(k, b), _batch(v, b)
+    _, T, Hq, D = qb.shape
+    Hkv = kb.shape[2]
+    r = np.ascontiguousarray(np.asarray(rows, np.int32))
+    n = r.size
+    o = np.zeros((n, D), np.float64)
+    lse = np.zeros(n, np.float64)
+    dob = _batch(dO, b) if dO is not None else None
+    dq = np.zeros((n, D), np.float64) if dO is not None else None
+    delta = np.zeros(n, np.float64) if dO is not None else None
+    rc = _load().ne_ref_attn_qrows(_ptr(qb), _ptr(kb), _ptr(vb), dob.ctypes.data if dob is not None else None,
+                                   0, h, r.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n, _ptr(o), _ptr(lse),
+                                   dq.ctypes.data if dq is not None else None,
+                                   delta.ctypes.data if delta is not None else None,
+                                   1, T, Hq, Hkv, D, float(theta))
+    if rc != 0:
+        raise ValueError("bad attn_qrows arguments")
+    return o, lse, dq, delta
+
+
+def attn_krows(q, k, v, dO, b: int, g: int, rows, theta: float = 10000.0):
+    """dK and dV rows [n, D] of key rows `rows` of (batch b, kv head g), summed over the
+    group's query heads, from the definitions; cheap for rows near the end of the
+    sequence (every query row at or after the first requested key is visited)."""
+    qb, kb, vb, dob = _batch(q, b), _batch(k, b), _batch(v, b), _batch(dO, b)
+    _, T, Hq, D = qb.shape
+    Hkv = kb.shape[2]
+    r = np.ascontiguousarray(np.asarray(rows, np.int32))
+    n = r.size
+    dk = np.zeros((n, D), np.float64)
+    dv = np.zeros((n, D), np.float64)
+    rc = _load().ne_ref_attn_krows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(dob), 0, g,
+                                   r.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n, _ptr(dk), _ptr(dv),
+                                   1, T, Hq, Hkv, D, float(theta))
+    if rc != 0:
+        raise ValueError("bad attn_krows arguments")
+    return dk, dv

@@ -231,6 +231,140 @@ int ne_ref_attn_bwd(const double* q, const double* k, const double* v, const dou
     return 0;
 }
 
+/* Selected query rows of one (b, q head h), for checks at sizes where the full matrices
+ * do not fit: for each row i in rows[0..n) the same definitions as above restricted to
+ * that row -- S_ij = s q'_i . k'_j (j <= i), P_ij = exp(S_ij - LSE_i), O_i = sum_j P_ij v_j,
+ * and, when dO is given, dP_ij = dO_i . v_j, Delta_i = sum_j P_ij dP_ij,
+ * dq_i = R_i^T s sum_j P_ij (dP_ij - Delta_i) k'_j.  Outputs are [n, D] (o, dq) and [n]
+ * (lse, delta); dO, dq and delta may be NULL. */
+int ne_ref_attn_qrows(const double* q, const double* k, const double* v, const double* dO, int b, int h,
+                      const int* rows, int n, double* o, double* lse, double* dq, double* delta, int B,
+                      int T, int Hq, int Hkv, int D, double theta) {
+    if (bad_shape(B, T, Hq, Hkv, D) || b < 0 || b >= B || h < 0 || h >= Hq) return 1;
+    for (int r = 0; r < n; ++r)
+        if (rows[r] < 0 || rows[r] >= T) return 1;
+    const int g = h / (Hq / Hkv);
+    const double s = 1.0 / std::sqrt((double)D);
+    std::vector<double> kr;
+    rotated_head(k, b, g, T, Hkv, D, theta, kr);
+#pragma omp parallel for schedule(dynamic)
+    for (int r = 0; r < n; ++r) {
+        const int i = rows[r];
+        std::vector<double> qi((size_t)D), S((size_t)i + 1), P((size_t)i + 1), dP((size_t)i + 1);
+        rotate_row(&q[idx4(b, i, h, 0, T, Hq, D)], qi.data(), i, D, theta);
+        double m = -INFINITY;
+        for (int j = 0; j <= i; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += qi[d] * kr[(size_t)j * D + d];
+            S[j] = s * dot;
+            if (S[j] > m) m = S[j];
+        }
+        double sum = 0.0;
+        for (int j = 0; j <= i; ++j) sum += std::exp(S[j] - m);
+        const double l = m + std::log(sum);
+        for (int j = 0; j <= i; ++j) P[j] = std::exp(S[j] - l);
+        lse[r] = l;
+        for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int j = 0; j <= i; ++j) acc += P[j] * v[idx4(b, j, g, d, T, Hkv, D)];
+            o[(size_t)r * D + d] = acc;
+        }
+        if (!dO) continue;
+        double dl = 0.0;
+        for (int j = 0; j <= i; ++j) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += dO[idx4(b, i, h, d, T, Hq, D)] * v[idx4(b, j, g, d, T, Hkv, D)];
+            dP[j] = acc;
+            dl += P[j] * acc;
+        }
+        if (delta) delta[r] = dl;
+        if (dq) {
+            std::vector<double> dqr((size_t)D, 0.0);
+            for (int j = 0; j <= i; ++j) {
+                const double ds = P[j] * (dP[j] - dl);
+                for (int d = 0; d < D; ++d) dqr[d] += s * ds * kr[(size_t)j * D + d];
+            }
+            rotate_row_transpose(dqr.data(), &dq[(size_t)r * D], i, D, theta);
+        }
+    }
+    return 0;
+}
+
+/* Selected key rows of one (b, kv head g): dV_j = sum_h sum_{i >= j} P_ij dO_i and
+ * dk_j = R_j^T s sum_h sum_{i >= j} dS_ij q'_i over the G query heads h of g, with P and
+ * dS as above.  Every query row i >= min(rows) is needed, each for its LSE_i and Delta_i,
+ * so rows near the end of the sequence are cheap.  Outputs dk, dv are [n, D]. */
+int ne_ref_attn_krows(const double* q, const double* k, const double* v, const double* dO, int b, int g,
+                      const int* rows, int n, double* dk, double* dv, int B, int T, int Hq, int Hkv,
+                      int D, double theta) {
+    if (bad_shape(B, T, Hq, Hkv, D) || b < 0 || b >= B || g < 0 || g >= Hkv) return 1;
+    int jmin = T;
+    for (int r = 0; r < n; ++r) {
+        if (rows[r] < 0 || rows[r] >= T) return 1;
+        if (rows[r] < jmin) jmin = rows[r];
+    }
+    if (n == 0) return 0;
+    const int G = Hq / Hkv;
+    const double s = 1.0 / std::sqrt((double)D);
+    std::vector<double> kr;
+    rotated_head(k, b, g, T, Hkv, D, theta, kr);
+    std::vector<double> acck((size_t)n * D, 0.0), accv((size_t)n * D, 0.0);
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+        // LSE_i and Delta_i of every query row that can see one of the requested keys.
+        const int nq = T - jmin;
+        std::vector<double> L((size_t)nq), Dl((size_t)nq), qr((size_t)nq * D);
+#pragma omp parallel for schedule(dynamic)
+        for (int ii = 0; ii < nq; ++ii) {
+            const int i = jmin + ii;
+            double* qi = &qr[(size_t)ii * D];
+            rotate_row(&q[idx4(b, i, h, 0, T, Hq, D)], qi, i, D, theta);
+            std::vector<double> S((size_t)i + 1);
+            double m = -INFINITY;
+            for (int j = 0; j <= i; ++j) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += qi[d] * kr[(size_t)j * D + d];
+                S[j] = s * dot;
+                if (S[j] > m) m = S[j];
+            }
+            double sum = 0.0;
+            for (int j = 0; j <= i; ++j) sum += std::exp(S[j] - m);
+            const double l = m + std::log(sum);
+            double dl = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                double dp = 0.0;
+                for (int d = 0; d < D; ++d) dp += dO[idx4(b, i, h, d, T, Hq, D)] * v[idx4(b, j, g, d, T, Hkv, D)];
+                dl += std::exp(S[j] - l) * dp;
+            }
+            L[ii] = l;
+            Dl[ii] = dl;
+        }
+#pragma omp parallel for schedule(dynamic)
+        for (int r = 0; r < n; ++r) {
+            const int j = rows[r];
+            for (int i = j; i < T; ++i) {
+                const int ii = i - jmin;
+                const double* qi = &qr[(size_t)ii * D];
+                double dot = 0.0, dp = 0.0;
+                for (int d = 0; d < D; ++d) {
+                    dot += qi[d] * kr[(size_t)j * D + d];
+                    dp += dO[idx4(b, i, h, d, T, Hq, D)] * v[idx4(b, j, g, d, T, Hkv, D)];
+                }
+                const double p = std::exp(s * dot - L[ii]);
+                const double ds = p * (dp - Dl[ii]);
+                for (int d = 0; d < D; ++d) {
+                    acck[(size_t)r * D + d] += s * ds * qi[d];
+                    accv[(size_t)r * D + d] += p * dO[idx4(b, i, h, d, T, Hq, D)];
+                }
+            }
+        }
+    }
+    for (int r = 0; r < n; ++r) {
+        rotate_row_transpose(&acck[(size_t)r * D], &dk[(size_t)r * D], rows[r], D, theta);
+        for (int d = 0; d < D; ++d) dv[(size_t)r * D + d] = accv[(size_t)r * D + d];
+    }
+    return 0;
+}
+
 int ne_ref_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

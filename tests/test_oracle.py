@@ -262,3 +262,43 @@ def test_synthetic_inputs_are_seeded_and_rounded():
     q, k, v, dO = synthetic.make_inputs(small)
     assert q.dtype == torch.bfloat16 and w4.qk_sigma == 3.0
     assert 2.0 < float(q.float().std()) < 4.0 and 0.5 < float(v.float().std()) < 1.5
+
+
+@pytest.mark.parametrize("shape", [(2, 37, 6, 2, 8), (1, 70, 4, 4, 64), (1, 130, 3, 1, 32)])
+def test_row_sampled_oracle_matches_full_oracle(oracle_mod, shape):
+    """The row-by-row forms (used where the full matrices do not fit) give the full
+    oracle's values: O, LSE, dQ, Delta for query rows, dK, dV for key rows."""
+    B, T, Hq, Hkv, D = shape
+    rng = np.random.default_rng(sum(shape))
+    q, dO = rng.standard_normal((B, T, Hq, D)), rng.standard_normal((B, T, Hq, D))
+    k, v = rng.standard_normal((B, T, Hkv, D)), rng.standard_normal((B, T, Hkv, D))
+    o, lse = oracle_mod.attn_fwd(q, k, v)
+    dq, dk, dv, delta = oracle_mod.attn_bwd(q, k, v, dO, return_delta=True)
+    qrows = [0, T - 1, T // 2, 1]
+    krows = [T - 1, 0, T // 3]
+    for b in range(B):
+        for h in range(Hq):
+            o2, l2, dq2, d2 = oracle_mod.attn_qrows(q, k, v, dO, b, h, qrows)
+            np.testing.assert_allclose(o2, o[b, qrows, h], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(l2, lse[b, h, qrows], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(dq2, dq[b, qrows, h], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(d2, delta[b, h, qrows], rtol=0, atol=1e-12)
+            o3, l3, dq3, d3 = oracle_mod.attn_qrows(q, k, v, None, b, h, qrows)
+            assert dq3 is None and d3 is None and np.array_equal(o3, o2)
+        for g in range(Hkv):
+            dk2, dv2 = oracle_mod.attn_krows(q, k, v, dO, b, g, krows)
+            np.testing.assert_allclose(dk2, dk[b, krows, g], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(dv2, dv[b, krows, g], rtol=0, atol=1e-12)
+
+
+def test_row_sampled_oracle_zero_queries_closed_form(oracle_mod):
+    """With Q = 0 each query row averages the values at and before it: O_i is the causal
+    running mean of V and LSE_i = ln(i + 1), independently of the full oracle."""
+    T, D = 300, 16
+    rng = np.random.default_rng(3)
+    q = np.zeros((1, T, 2, D)); k = rng.standard_normal((1, T, 1, D)); v = rng.standard_normal((1, T, 1, D))
+    rows = [0, 1, 149, 299]
+    o, lse, _, _ = oracle_mod.attn_qrows(q, k, v, None, 0, 1, rows)
+    running = np.cumsum(v[0, :, 0], axis=0) / np.arange(1, T + 1)[:, None]
+    np.testing.assert_allclose(o, running[rows], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, np.log(np.asarray(rows) + 1.0), rtol=0, atol=1e-13)
