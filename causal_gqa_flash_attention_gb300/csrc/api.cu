@@ -266,10 +266,12 @@ ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, v
     a.o = o;
     a.lse = lse;
     a.rope = rope;
+    a.B = B;
     a.T = T;
     a.Hq = Hq;
     a.G = Hq / Hkv;
     a.n_qt = (T + 255) / 256;
+    a.n_units = B * Hq * a.n_qt;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     a.err = err;
     a.timeout_ns = timeout_ns();

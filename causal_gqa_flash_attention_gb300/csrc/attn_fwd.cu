@@ -5,24 +5,32 @@
 // RoPE on queries and keys and grouped-query heads (same page, 기술 사양); causal mask
 // j <= i ("Tiny hackable CUDA language model implementation", Core Mechanics).
 //
-// One CTA owns two consecutive 128-row query subtiles (u = 0, 1) of one (batch, query
-// head) and walks 64-key tiles up to the diagonal; every K/V tile is loaded and
-// rotated once for both subtiles.  Warp roles (480 threads, one CTA per SM):
-//   warp 0       TMA producer: Q0, Q1 once, then K/V tiles into an NS-stage ring.
+// Persistent kernel: one CTA per SM walks a static list of work units.  A unit is two
+// consecutive 128-row query subtiles (u = 0, 1) of one (batch, query head); the units are
+// numbered heaviest first (latest query rows) and dealt to the CTAs in snake order
+// (round r goes left to right when r is even, right to left when odd), which balances
+// the causal work about as well as greedy longest-first.  Inside a unit the CTA walks
+// 64-key tiles up to the diagonal; every K/V tile is loaded and rotated once for both
+// subtiles.  The pipeline does not drain between units: the next unit's Q is loaded and
+// rotated, and its first S tiles are computed, while the softmax warps finish the
+// current one, so a CTA pays its set-up (TMEM allocation, barrier set-up, first loads)
+// once instead of once per unit.  Warp roles (480 threads):
+//   warp 0       TMA producer: Q pairs into NQB buffers, K/V tiles into an NS-stage ring.
 //   warp 1, 2    UMMA issuer of subtile 0 / 1 (warp 1 also owns the 512 TMEM columns);
-//                each subtile has its own issuing warp (the whole warp runs the loop,
-//                one elected lane issues): S_u(j+2) = Q'_u K'_j+2^T into S buffer j % 2
-//                right after PV_u(j) = P_u(j) V_j, two tiles ahead of the softmax.
-//   warps 3, 12-14  RoPE on every K tile in place (fp16 logit operand; TF32: rounded
-//                fp32) and, for TF32, V transposed (TF32 UMMA reads K-major operands
-//                only).  Four warps: with two, the rotation paced the whole pipeline.
+//                the whole warp runs the loop, one elected lane issues.  Over the
+//                subtile's tiles in order (across units), S(t+2) = Q'K'^T goes into S
+//                buffer t % 2 right after PV(t) = P(t) V, two tiles ahead of the softmax.
+//   warps 3, 12-14  RoPE: each unit's Q pair, then every K tile, in place (fp16 logit
+//                operand; TF32: rounded fp32) and, for TF32, V transposed (TF32 UMMA reads
+//                K-major operands only).
 //   warps 4-7    softmax of subtile 0; warps 8-11 softmax of subtile 1.  Thread r owns
-//                query row r (TMEM lane r): it rotates its Q row block once, then per
-//                tile reads the S row from TMEM, updates the running max m and sum l,
-//                writes P (bf16, or TF32 fp32) back over S, rescales its O row when m
-//                grew by more than 2^8, and at the end writes O / l (staged in shared
-//                memory, stored by TMA) and LSE.
-// TMEM: S buffers (u, b) at 64 * (2u + b), b = 0, 1; O_u at 256 + u * D.
+//                query row r (TMEM lane r): per tile it reads the S row from TMEM, updates
+//                the running max m and sum l, writes P (bf16, or TF32 fp32) back over S,
+//                rescales its O row when m grew by more than 2^8; at the end of a unit it
+//                writes O / l (staged in the unit's Q buffer, stored by TMA) and LSE.
+// TMEM: S buffers (u, b) at 64 * (2u + b), b = 0, 1; O_u at 256 + u * D.  A unit's first
+// PV overwrites O_u; it needs P of the unit's first tile, which the softmax threads write
+// only after their epilogue has read the previous unit's O_u.
 // Every wait is bounded (WaitCtx); a CTA that gives up records an error code, drains
 // its own copies and MMAs, frees its TMEM and exits.
 #include <cuda_bf16.h>
@@ -48,9 +56,13 @@ struct FwdCfg {
     static constexpr int KV_BYTES = BN * ROWB;
     static constexpr int VT_BYTES = TF32 ? BN * ROWB : 0;
     static constexpr int STAGE_BYTES = 2 * KV_BYTES + VT_BYTES;
-    static constexpr int NS_FIT = (220 * 1024 - 2 * Q_BYTES) / STAGE_BYTES;
+    static constexpr int QBUF = 2 * Q_BYTES;           // one Q buffer: both subtiles
+    // Two Q buffers (the next unit's Q lands while this one runs) where that leaves at
+    // least four K/V stages; otherwise one.
+    static constexpr int NQB = (220 * 1024 - 2 * QBUF) / STAGE_BYTES >= 4 ? 2 : 1;
+    static constexpr int NS_FIT = (220 * 1024 - NQB * QBUF) / STAGE_BYTES;
     static constexpr int NS = NS_FIT > 6 ? 6 : NS_FIT; // K/V pipeline stages
-    static constexpr int SMEM = 1024 + 2 * Q_BYTES + NS * STAGE_BYTES;
+    static constexpr int SMEM = 1024 + NQB * QBUF + NS * STAGE_BYTES;
     static constexpr int O_COL = 256;                  // O_u at O_COL + u*D
     static constexpr int S_KSTEPS = ROWB / 32;         // 32-byte K-steps of S = Q K^T
     static constexpr int PV_KSTEPS = BN * ES / 32;     // K-steps of O += P V
@@ -63,6 +75,7 @@ struct FwdCfg {
     static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
     static_assert(D <= 128, "O subtiles must fit next to four S buffers in 512 TMEM columns");
     static_assert(NS >= 3, "need at least three K/V stages (S runs two tiles ahead)");
+    static_assert(NQB == 1 || NS >= 4, "S of the next unit may wait inside a unit's loop: four stages");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -97,10 +110,11 @@ struct RowState {
 };
 
 // One key tile of one softmax thread: mask, max, rescale decision (and O rescale),
-// exp2, P written back over this tile's S buffer, p_ready arrival.  Returns false
-// when a wait ran out.
+// exp2, P written back over this tile's S buffer, p_ready arrival.  j is the tile's
+// index within the unit, t its index in the subtile's sequence of tiles over all units
+// (S buffer t % 2; barrier phases).  Returns false when a wait ran out.
 template <bool TF32, int D>
-__device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int u, int qsub0, int qpos, uint32_t lt,
+__device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, int u, int qsub0, int qpos, uint32_t lt,
                                              float sl2, RowState& st, uint64_t* bar_o_done, uint64_t* bar_p_ready,
                                              const WaitCtx& w) {
     using C = FwdCfg<TF32, D>;
@@ -126,14 +140,15 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int u, i
     // A row whose max grew by more than 2^8 rescales l and its O row; the others keep
     // their max (p <= 2^8 stays exact).  TMEM access is warp-collective, so a warp
     // rescales when any lane needs it (alpha = 1 elsewhere).  O is idle once the PV of
-    // tile j-1 is done (it is issued before P of tile j can be consumed).
+    // tile t-1 is done (PV(t) needs this thread's P(t)).  The per-PV barrier is then at
+    // most one phase short of it: PV(t-2) completed before S(t), issued after it, did.
     const bool need = j > 0 && m_tile > st.m_used + 8.f;
     if (j == 0) st.m_used = m_tile;
     if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2(st.m_used - m_tile) : 1.f;
         st.l *= alpha;
         if (need) st.m_used = m_tile;
-        if (!mbar_wait_warp(smem_u32(&bar_o_done[u]), (j - 1) & 1, w, SITE_FWD_O_DONE)) return false;
+        if (!mbar_wait_warp(smem_u32(&bar_o_done[u]), (t - 1) & 1, w, SITE_FWD_O_DONE)) return false;
         tc_fence_after();
         const uint32_t oc = C::O_COL + u * D;
 #pragma unroll 1
@@ -148,7 +163,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int u, i
     }
     float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const float neg_m = -st.m_used;
-    const uint32_t sc = lt + s_col(u, j & 1);
+    const uint32_t sc = lt + s_col(u, t & 1);
 #pragma unroll
     for (int c = 0; c < C::BN; c += 32) {
         if constexpr (TF32) {
@@ -176,9 +191,81 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int u, i
     st.l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(smem_u32(&bar_p_ready[u * 2 + (j & 1)]));
+    mbar_arrive(smem_u32(&bar_p_ready[u * 2 + (t & 1)]));
     return true;
 }
+
+// Work unit U of the persistent schedule: (batch, query head, pair of 128-row query
+// subtiles), numbered heaviest first (the pair holding the latest query rows).
+struct FwdUnit {
+    int b, h, q0;
+    int n_u[2];    // key tiles of subtile u (0: subtile beyond T)
+    int n_kv;      // key tiles the unit loads: max(n_u)
+    int n_qsub;    // subtiles inside T
+};
+
+template <int BM, int BN>
+__device__ __forceinline__ FwdUnit fwd_unit(int U, const FwdArgs& a) {
+    FwdUnit f;
+    const int n_bh = a.B * a.Hq;
+    const int rank = U / n_bh, rem = U - rank * n_bh;
+    f.h = rem % a.Hq;
+    f.b = rem / a.Hq;
+    f.q0 = (a.n_qt - 1 - rank) * 2 * BM;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int qu = f.q0 + u * BM;
+        f.n_u[u] = qu < a.T ? min(qu + BM - 1, a.T - 1) / BN + 1 : 0;
+    }
+    f.n_kv = max(f.n_u[0], f.n_u[1]);
+    f.n_qsub = f.n_u[1] > 0 ? 2 : 1;
+    return f;
+}
+
+// The k-th unit of this CTA, or -1 past the end: round k takes units k*G .. k*G+G-1
+// (G CTAs), left to right for even k and right to left for odd k.
+__device__ __forceinline__ int fwd_unit_index(int k, int n_units) {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const long long U = (long long)k * G + ((k & 1) ? G - 1 - c : c);
+    return U < n_units ? (int)U : -1;
+}
+
+// Walks one subtile's tiles over the CTA's units in order, skipping units where the
+// subtile lies beyond T: unit iteration k (-1 at the end), tile j of n, and kvb, the
+// index of the unit's first K/V tile in the CTA's K/V sequence.
+template <int BM, int BN>
+struct FwdWalk {
+    int k, j, n, n_kv, kvb;
+    __device__ __forceinline__ void load(int kk, int u, const FwdArgs& a) {
+        const int U = fwd_unit_index(kk, a.n_units);
+        k = U < 0 ? -1 : kk;
+        if (U >= 0) {
+            const FwdUnit f = fwd_unit<BM, BN>(U, a);
+            n = u == 0 ? f.n_u[0] : f.n_u[1];   // (a select: no local-memory array)
+            n_kv = f.n_kv;
+        }
+    }
+    __device__ __forceinline__ void skip_empty(int u, const FwdArgs& a) {
+        while (k >= 0 && n == 0) {
+            kvb += n_kv;
+            load(k + 1, u, a);
+        }
+    }
+    __device__ __forceinline__ void init(int u, const FwdArgs& a) {
+        j = 0;
+        kvb = 0;
+        load(0, u, a);
+        skip_empty(u, a);
+    }
+    __device__ __forceinline__ void advance(int u, const FwdArgs& a) {
+        if (++j == n) {
+            j = 0;
+            kvb += n_kv;
+            load(k + 1, u, a);
+            skip_empty(u, a);
+        }
+    }
+};
 
 template <bool TF32, int D>
 __global__ void __launch_bounds__(480, 1)
@@ -188,38 +275,29 @@ __global__ void __launch_bounds__(480, 1)
     using C = FwdCfg<TF32, D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;                               // Q0 | Q1 (later: O staging)
-    uint8_t* sStage = sQ + 2 * C::Q_BYTES;            // NS x (K | V | Vt)
+    uint8_t* sQ = smem;                               // NQB x (Q0 | Q1), later O staging
+    uint8_t* sStage = sQ + C::NQB * C::QBUF;          // NS x (K | V | Vt)
 
-    __shared__ __align__(8) uint64_t bar_q_full, bar_final;
-    __shared__ __align__(8) uint64_t bar_q_ready[2], bar_o_done[2], bar_o_staged[2];
+    __shared__ __align__(8) uint64_t bar_final;
+    __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_ready[2], bar_q_empty[2];   // [Q buffer]
+    __shared__ __align__(8) uint64_t bar_o_done[2], bar_o_final[2], bar_o_staged[2];  // [subtile]
     __shared__ __align__(8) uint64_t bar_s_full[4], bar_p_ready[4];     // [u * 2 + buffer]
     __shared__ __align__(8) uint64_t bar_kv_full[C::NS], bar_k_ready[C::NS], bar_kv_empty[C::NS];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, b = blockIdx.y;
-    const int pair = a.n_qt - 1 - (int)blockIdx.z;    // heaviest query tiles launch first
-    const int hkv = h / a.G;
     const int T = a.T;
-    const int q0 = pair * 2 * C::BM;
-    int n_u[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int qu = q0 + u * C::BM;
-        n_u[u] = qu < T ? min(qu + C::BM - 1, T - 1) / C::BN + 1 : 0;
-    }
-    const int n_kv = max(n_u[0], n_u[1]);
-    const int n_qsub = n_u[1] > 0 ? 2 : 1;
 
     if (tid == 0) {
-        mbar_init(smem_u32(&bar_q_full), 1);
         mbar_init(smem_u32(&bar_final), 2);              // one commit per UMMA issuer
-        for (int u = 0; u < 2; ++u) {
-            mbar_init(smem_u32(&bar_q_ready[u]), 128);
-            mbar_init(smem_u32(&bar_o_done[u]), 1);
-            mbar_init(smem_u32(&bar_o_staged[u]), 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bar_q_full[i]), 1);
+            mbar_init(smem_u32(&bar_q_ready[i]), C::ROPE_THREADS);
+            mbar_init(smem_u32(&bar_q_empty[i]), 2);     // one arrival per subtile epilogue
+            mbar_init(smem_u32(&bar_o_done[i]), 1);      // every PV
+            mbar_init(smem_u32(&bar_o_final[i]), 1);     // the last PV of a unit
+            mbar_init(smem_u32(&bar_o_staged[i]), 128);
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(smem_u32(&bar_s_full[i]), 1);
@@ -245,76 +323,154 @@ __global__ void __launch_bounds__(480, 1)
     griddep_wait();                // inputs of earlier kernels on the stream are visible
     const uint32_t tm = tmem_slot;
     const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
+    auto q_buf = [&](int k) { return sQ + (k % C::NQB) * C::QBUF; };
     auto stage_k = [&](int s) { return sStage + s * C::STAGE_BYTES; };
     auto stage_v = [&](int s) { return sStage + s * C::STAGE_BYTES + C::KV_BYTES; };
     auto stage_vt = [&](int s) { return sStage + s * C::STAGE_BYTES + 2 * C::KV_BYTES; };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            const uint32_t qf = smem_u32(&bar_q_full);
-            mbar_arrive_expect_tx(qf, n_qsub * C::Q_BYTES);
-            for (int u = 0; u < n_qsub; ++u)
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_load_4d(smem_u32(sQ + u * C::Q_BYTES + c * C::BM * 128), &tm_q, qf, c * C::EPC, h,
-                                q0 + u * C::BM, b);
-            int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % C::NS;
-                if (j >= C::NS &&
-                    !mbar_wait(smem_u32(&bar_kv_empty[s]), ((j / C::NS) - 1) & 1, w, SITE_FWD_KV_EMPTY))
-                    break;
-                const uint32_t full = smem_u32(&bar_kv_full[s]);
-                mbar_arrive_expect_tx(full, 2 * C::KV_BYTES);
-                for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_4d(smem_u32(stage_k(s) + c * C::BN * 128), &tm_k, full, c * C::EPC, hkv, j * C::BN, b);
-                    tma_load_4d(smem_u32(stage_v(s) + c * C::BN * 128), &tm_v, full, c * C::EPC, hkv, j * C::BN, b);
-                }
-                ++issued;
+    // RoPE role, thread rt of the ROPE_THREADS (warp 3 and warps 12-14).
+    auto rope_role = [&](const int rt) {
+        // ------------------------------------------------------------ RoPE on Q and K (+ V^T)
+        using RopeK = RopeTile<D, C::BN, C::ROPE_THREADS, C::MODE>;
+        using RopeQ = RopeTile<D, C::BM, C::ROPE_THREADS, C::MODE>;
+        RopeK rk;
+        rk.init(rt, a.rope);
+        RopeQ rq;
+        rq.init(rt, a.rope);
+        int g = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int U = fwd_unit_index(k, a.n_units);
+            if (U < 0) break;
+            const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+            uint8_t* qbuf = q_buf(k);
+            // The table rows are fetched before the wait, so their latency overlaps it.
+            float4 qa[RopeQ::F4], qc[RopeQ::F4], kn[RopeK::F4];
+            rq.load_base(qa, f.q0, T, a.rope);
+            rq.load_base(qc, f.q0 + C::BM, T, a.rope);
+            rk.load_base(kn, 0, T, a.rope);
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_q_full[k % C::NQB]), (k / C::NQB) & 1, w, SITE_FWD_Q))) break;
+            rq.template apply<false>(qbuf, nullptr, qa);
+            if (f.n_qsub == 2) rq.template apply<false>(qbuf + C::Q_BYTES, nullptr, qc);
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_q_ready[k % C::NQB]));
+            for (int j = 0; j < f.n_kv; ++j, ++g) {
+                const int s = g % C::NS;
+                float4 cur[RopeK::F4];
+#pragma unroll
+                for (int e = 0; e < RopeK::F4; ++e) cur[e] = kn[e];
+                if (j + 1 < f.n_kv) rk.load_base(kn, (j + 1) * C::BN, T, a.rope);   // one tile early
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_kv_full[s]), (g / C::NS) & 1, w, SITE_FWD_KV_FULL))) break;
+                if constexpr (TF32) transpose_v_tf32<D, C::BN, C::ROPE_THREADS>(stage_v(s), stage_vt(s), rt);
+                rk.template apply<false>(stage_k(s), nullptr, cur);
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bar_k_ready[s]));
             }
-            // Teardown: every copy this CTA started must have landed before exit.
-            mbar_wait_drain(qf, 0, w, SITE_FWD_DRAIN);
-            for (int j = max(0, issued - C::NS); j < issued; ++j)
-                mbar_wait_drain(smem_u32(&bar_kv_full[j % C::NS]), (j / C::NS) & 1, w, SITE_FWD_DRAIN);
         }
-    } else if (warp == 1 || warp == 2) {
-        // ------------------------------------------------------------ UMMA issuers
-        // Each subtile has its own issuing warp (1 + u); the whole warp runs the loop and
-        // one elected lane issues.  S_u(j) goes to S buffer j % 2, two tiles ahead of the
-        // softmax, and overwrites P_u(j-2), whose PV the same lane issued earlier (one
-        // thread's UMMAs execute in order).
-        const int u = warp - 1;
-        const int n = n_u[u];
-        {
+    };
+
+    if (warp < 4) {
+        if (warp == 0) {
+            // ------------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+                int issued = 0;                           // K/V tiles loaded so far
+                int last_k0 = -1, last_k1 = -1;           // last unit loaded into Q buffer 0 / 1
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int U = fwd_unit_index(k, a.n_units);
+                    if (U < 0) break;
+                    const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+                    const int qb = k % C::NQB;
+                    // The Q buffer is free once both epilogues of unit k - NQB stored their O.
+                    if (k >= C::NQB &&
+                        !(ok = mbar_wait(smem_u32(&bar_q_empty[qb]), ((k / C::NQB) - 1) & 1, w, SITE_FWD_Q)))
+                        break;
+                    const uint32_t qf = smem_u32(&bar_q_full[qb]);
+                    mbar_arrive_expect_tx(qf, f.n_qsub * C::Q_BYTES);
+                    for (int u = 0; u < f.n_qsub; ++u)
+                        for (int c = 0; c < C::NCH; ++c)
+                            tma_load_4d(smem_u32(q_buf(k) + u * C::Q_BYTES + c * C::BM * 128), &tm_q, qf, c * C::EPC,
+                                        f.h, f.q0 + u * C::BM, f.b);
+                    if (qb == 0) last_k0 = k;
+                    else last_k1 = k;
+                    const int hkv = f.h / a.G;
+                    for (int j = 0; j < f.n_kv; ++j) {
+                        const int g = issued, s = g % C::NS;
+                        if (g >= C::NS &&
+                            !(ok = mbar_wait(smem_u32(&bar_kv_empty[s]), ((g / C::NS) - 1) & 1, w, SITE_FWD_KV_EMPTY)))
+                            break;
+                        const uint32_t full = smem_u32(&bar_kv_full[s]);
+                        mbar_arrive_expect_tx(full, 2 * C::KV_BYTES);
+                        for (int c = 0; c < C::NCH; ++c) {
+                            tma_load_4d(smem_u32(stage_k(s) + c * C::BN * 128), &tm_k, full, c * C::EPC, hkv, j * C::BN,
+                                        f.b);
+                            tma_load_4d(smem_u32(stage_v(s) + c * C::BN * 128), &tm_v, full, c * C::EPC, hkv, j * C::BN,
+                                        f.b);
+                        }
+                        ++issued;
+                    }
+                }
+                // Teardown: every copy this CTA started must have landed before exit.
+                if (last_k0 >= 0) mbar_wait_drain(smem_u32(&bar_q_full[0]), (last_k0 / C::NQB) & 1, w, SITE_FWD_DRAIN);
+                if (last_k1 >= 0) mbar_wait_drain(smem_u32(&bar_q_full[1]), (last_k1 / C::NQB) & 1, w, SITE_FWD_DRAIN);
+                for (int g = max(0, issued - C::NS); g < issued; ++g)
+                    mbar_wait_drain(smem_u32(&bar_kv_full[g % C::NS]), (g / C::NS) & 1, w, SITE_FWD_DRAIN);
+            }
+        } else if (warp < 3) {
+            // ------------------------------------------------------------ UMMA issuers
+            // Each subtile has its own issuing warp (1 + u); the whole warp runs the loop and
+            // one elected lane issues.  Tiles are numbered t = 0, 1, ... over all units of the
+            // CTA; S(t) goes to S buffer t % 2, two tiles ahead of the softmax, and overwrites
+            // P(t-2), whose PV the same lane issued earlier (one thread's UMMAs execute in
+            // order).
+            const int u = warp - 1;
             constexpr uint32_t id_s = idesc_make(C::FMT_S, 128, C::BN, false, false);
             constexpr uint32_t id_o = idesc_make(C::FMT_PV, 128, D, false, !TF32);
-            // Descriptors are built once; a K-step or a stage only moves the start address.
-            const uint64_t dq = sdesc(smem_u32(sQ + u * C::Q_BYTES), 16, 1024);
+            // Descriptors are built once; a K-step, a stage or a Q buffer only moves the start
+            // address.
+            const uint64_t dq0 = sdesc(smem_u32(sQ + u * C::Q_BYTES), 16, 1024);
             const uint64_t dk0 = sdesc(smem_u32(stage_k(0)), 16, 1024);
             const uint64_t dv0 = TF32 ? sdesc(smem_u32(stage_vt(0)), 16, 1024)
                                       : sdesc(smem_u32(stage_v(0)), C::BN * 128, 1024);
             const uint32_t ocol = tm + C::O_COL + u * D;
-            auto issue_s = [&](int j) {
-                const uint64_t dk = sdesc_add(dk0, (j % C::NS) * C::STAGE_BYTES);
-                const uint32_t dcol = tm + s_col(u, j & 1);
-#pragma unroll
+            auto k_ready = [&](int g) {
+                const bool r = mbar_wait_warp(smem_u32(&bar_k_ready[g % C::NS]), (g / C::NS) & 1, w, SITE_FWD_K_READY);
+                tc_fence_after();
+                return r;
+            };
+            int t_s = 0;                                  // S tiles issued
+            int qr_next = 0;                              // first unit whose Q' this issuer has not waited for
+            auto issue_s = [&](const FwdWalk<C::BM, C::BN>& c) -> bool {
+                // Q' of the unit (and of any unit skipped since the last one: every phase of
+                // the Q-ready barriers is waited for in order, so a parity never aliases).
+                for (; c.j == 0 && qr_next <= c.k; ++qr_next)
+                    if (!mbar_wait_warp(smem_u32(&bar_q_ready[qr_next % C::NQB]), (qr_next / C::NQB) & 1, w, SITE_FWD_Q))
+                        return false;
+                const int g = c.kvb + c.j;
+                if (!k_ready(g)) return false;
+                const uint64_t dq = sdesc_add(dq0, (c.k % C::NQB) * C::QBUF);
+                const uint64_t dk = sdesc_add(dk0, (g % C::NS) * C::STAGE_BYTES);
+                const uint32_t dcol = tm + s_col(u, t_s & 1);
+    #pragma unroll
                 for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
                     const uint32_t byte = ks * 32;
                     umma_ss_e<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
-                                  sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
+                                    sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
                 }
-                umma_commit_e(smem_u32(&bar_s_full[u * 2 + (j & 1)]));
+                umma_commit_e(smem_u32(&bar_s_full[u * 2 + (t_s & 1)]));
+                ++t_s;
+                return true;
             };
-            auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait_warp(smem_u32(&bar_p_ready[u * 2 + (j & 1)]), (j >> 1) & 1, w, SITE_FWD_P_READY))
+            auto issue_pv = [&](int t, int j, int g, bool last) -> bool {
+                if (!mbar_wait_warp(smem_u32(&bar_p_ready[u * 2 + (t & 1)]), (t >> 1) & 1, w, SITE_FWD_P_READY))
                     return false;
                 tc_fence_after();
-                const uint64_t dv = sdesc_add(dv0, (j % C::NS) * C::STAGE_BYTES);
-                const uint32_t pcol = tm + s_col(u, j & 1);
-#pragma unroll
+                const uint64_t dv = sdesc_add(dv0, (g % C::NS) * C::STAGE_BYTES);
+                const uint32_t pcol = tm + s_col(u, t & 1);
+    #pragma unroll
                 for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
                     // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
                     // MN-major, PV_ROWS keys per K-step.
@@ -322,90 +478,111 @@ __global__ void __launch_bounds__(480, 1)
                     umma_ts_e<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 umma_commit_e(smem_u32(&bar_o_done[u]));
+                if (last) umma_commit_e(smem_u32(&bar_o_final[u]));
                 return true;
             };
-            auto k_ready = [&](int j) {
-                const bool r = mbar_wait_warp(smem_u32(&bar_k_ready[j % C::NS]), (j / C::NS) & 1, w, SITE_FWD_K_READY);
-                tc_fence_after();
-                return r;
-            };
-            // A subtile beyond T (n == 0) issues nothing but still releases every stage.
-            bool ok = n == 0 || mbar_wait_warp(smem_u32(&bar_q_ready[u]), 0, w, SITE_FWD_Q);
-            for (int j = 0; ok && j < 2 && j < n; ++j) {
-                if (!(ok = k_ready(j))) break;
-                issue_s(j);
+            FwdWalk<C::BM, C::BN> sw;                     // the next tile to issue S for
+            sw.init(u, a);
+            int t = 0, g = 0;                             // PV tiles issued; K/V tiles passed
+            // S runs at most two tiles ahead of PV.  With one Q buffer the next unit's Q can
+            // only land after this unit's epilogues, which wait for this unit's last PVs, so
+            // S of the next unit waits until the current unit's loop is done.  With two, the
+            // next unit's Q depends only on the unit before this one; its S may then wait
+            // inside the loop, where this issuer has released all but the last
+            // n_kv - n_u + 1 <= 3 stages of the unit, and NS >= 4 lets the next unit's first
+            // K/V tile load regardless.
+            auto may_issue = [&](int k_cur) { return sw.k >= 0 && t_s < t + 2 && (C::NQB == 2 || sw.k <= k_cur); };
+            bool ok = true;
+            while (ok && may_issue(0)) {
+                ok = issue_s(sw);
+                sw.advance(u, a);
             }
-            // Every stage of the CTA's key range is released by both issuers.  The
-            // subtile with fewer tiles releases its tail without using it, but only once
-            // the stage really holds that tile (k_ready), so it never runs a phase ahead.
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j < n) {
-                    if (!(ok = issue_pv(j))) break;
-                    if (j + 2 < n) {
-                        if (!(ok = k_ready(j + 2))) break;
-                        issue_s(j + 2);
+            // Every K/V stage is released by both issuers, in order.  A tile beyond the
+            // subtile's diagonal is released without use, but only once the stage really
+            // holds it (k_ready), so the release never runs a phase ahead.
+            for (int k = 0; ok; ++k) {
+                const int U = fwd_unit_index(k, a.n_units);
+                if (U < 0) break;
+                const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+                for (int j = 0; ok && j < f.n_kv; ++j, ++g) {
+                    const int n = u == 0 ? f.n_u[0] : f.n_u[1];
+                    if (j < n) {
+                        if (!(ok = issue_pv(t, j, g, j == n - 1))) break;
+                        ++t;
+                        umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
+                        while (ok && may_issue(k)) {
+                            ok = issue_s(sw);
+                            sw.advance(u, a);
+                        }
+                    } else {
+                        if (!(ok = k_ready(g))) break;
+                        umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
                     }
-                } else if (!(ok = k_ready(j))) {
-                    break;
                 }
-                umma_commit_e(smem_u32(&bar_kv_empty[j % C::NS]));
+                while (ok && may_issue(k + 1)) {
+                    ok = issue_s(sw);
+                    sw.advance(u, a);
+                }
             }
             umma_commit_e(smem_u32(&bar_final));
-        }
-    } else if (warp == 3 || warp >= 12) {
-        // ------------------------------------------------------------ RoPE on K (+ V^T)
-        const int rt = lane + (warp == 3 ? 0 : 32 * (warp - 11));
-        using Rope = RopeTile<D, C::BN, C::ROPE_THREADS, C::MODE>;
-        Rope rope;
-        rope.init(rt, a.rope);
-        float4 next[Rope::F4];
-        rope.load_base(next, 0, T, a.rope);
-        for (int j = 0; j < n_kv; ++j) {
-            const int s = j % C::NS;
-            float4 cur[Rope::F4];
-#pragma unroll
-            for (int e = 0; e < Rope::F4; ++e) cur[e] = next[e];
-            if (j + 1 < n_kv) rope.load_base(next, (j + 1) * C::BN, T, a.rope);   // one tile early
-            if (!mbar_wait_warp(smem_u32(&bar_kv_full[s]), (j / C::NS) & 1, w, SITE_FWD_KV_FULL)) break;
-            if constexpr (TF32) transpose_v_tf32<D, C::BN, C::ROPE_THREADS>(stage_v(s), stage_vt(s), rt);
-            rope.template apply<false>(stage_k(s), nullptr, cur);
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bar_k_ready[s]));
+        } else {
+            rope_role(lane);
         }
     } else if (warp < 12) {
         // ------------------------------------------------------------ softmax (subtile u)
         const int u = (warp - 4) >> 2;
         const int r = tid - 128 - 128 * u;            // query row = TMEM lane
-        const int qsub0 = q0 + u * C::BM;
-        const int qpos = qsub0 + r;
-        const int n = n_u[u];
         const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t o_col = C::O_COL + u * D;
-        uint8_t* sQu = sQ + u * C::Q_BYTES;
         const float sl2 = a.scale_log2;
-        RowState st{kNegInf, 0.f};
-        bool ok = n > 0;
-        if (ok && mbar_wait_warp(smem_u32(&bar_q_full), 0, w, SITE_FWD_Q)) {
-            rope_tile_smem<D, C::BM, 128, C::MODE, false>(sQu, nullptr, qsub0, T, r, a.rope);
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bar_q_ready[u]));
-        } else {
-            ok = false;
-        }
-        for (int j = 0; ok && j < n; ++j) {
-            if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[u * 2 + (j & 1)]), (j >> 1) & 1, w, SITE_FWD_S_FULL)))
-                break;
+        int t = 0, n_epi = 0;                         // tiles and epilogues of this subtile so far
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            // Only what the tiles need stays live through the tile loop (the softmax
+            // holds a 64-register S row); the epilogue decodes the unit again.
+            int n, qsub0;
+            {
+                const int U = fwd_unit_index(k, a.n_units);
+                if (U < 0) break;
+                const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+                n = u == 0 ? f.n_u[0] : f.n_u[1];
+                qsub0 = f.q0 + u * C::BM;
+            }
+            const int qb = k % C::NQB;
+            if (n == 0) {                             // subtile beyond T: nothing to store
+                // Its release of the Q buffer must count toward this unit's phase, so it
+                // waits until the unit's Q has landed (the buffer's previous phase is
+                // then complete).
+                bool rel = true;
+                if (r == 0) {
+                    rel = mbar_wait(smem_u32(&bar_q_full[qb]), (k / C::NQB) & 1, w, SITE_FWD_Q);
+                    if (rel) mbar_arrive(smem_u32(&bar_q_empty[qb]));
+                }
+                if (!(ok = __all_sync(0xffffffffu, rel))) break;
+                continue;
+            }
+            const int qpos = qsub0 + r;
+            RowState st{kNegInf, 0.f};
+            for (int j = 0; j < n; ++j, ++t) {
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[u * 2 + (t & 1)]), (t >> 1) & 1, w, SITE_FWD_S_FULL)))
+                    break;
+                tc_fence_after();
+                uint32_t sr[64];
+                tmem_ld_cols<2>(lt + s_col(u, t & 1), sr);
+                if (!(ok = softmax_tile<TF32, D>(sr, j, t, u, qsub0, qpos, lt, sl2, st, bar_o_done, bar_p_ready, w)))
+                    break;
+            }
+            if (!ok) break;
+            // Epilogue: O / l staged (swizzled) in this subtile's half of the unit's Q
+            // buffer (its S MMAs completed before its last PV did), stored by TMA; LSE =
+            // natural log of the partition sum of the scaled logits.  The unit's last PV
+            // has its own barrier, one phase per unit: on the per-PV barrier both of the
+            // last two PVs may have completed before this wait starts, and the parity of
+            // the older one would then name a phase that is still to come.
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_o_final[u]), n_epi & 1, w, SITE_FWD_O_DONE))) break;
             tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld_cols<2>(lt + s_col(u, j & 1), sr);
-            if (!(ok = softmax_tile<TF32, D>(sr, j, u, qsub0, qpos, lt, sl2, st, bar_o_done, bar_p_ready, w))) break;
-        }
-        // Epilogue: O / l staged (swizzled) in this subtile's Q buffer, stored by TMA;
-        // LSE = natural log of the partition sum of the scaled logits.  The last two
-        // PVs may both be in flight: wait for them in order (parity would alias).
-        if (ok && n >= 2) ok = mbar_wait_warp(smem_u32(&bar_o_done[u]), (n - 2) & 1, w, SITE_FWD_O_DONE);
-        if (ok && mbar_wait_warp(smem_u32(&bar_o_done[u]), (n - 1) & 1, w, SITE_FWD_O_DONE)) {
-            tc_fence_after();
+            const FwdUnit f = fwd_unit<C::BM, C::BN>(fwd_unit_index(k, a.n_units), a);
+            uint8_t* sQu = q_buf(k) + u * C::Q_BYTES;
             const float inv_l = 1.f / st.l;
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
@@ -414,11 +591,11 @@ __global__ void __launch_bounds__(480, 1)
                 if constexpr (TF32) {
                     uint8_t* dst = sQu + (c >> 5) * C::BM * 128;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<float4*>(dst + sw128_offset(r, k)) =
-                            make_float4(__uint_as_float(orow[4 * k]) * inv_l, __uint_as_float(orow[4 * k + 1]) * inv_l,
-                                        __uint_as_float(orow[4 * k + 2]) * inv_l,
-                                        __uint_as_float(orow[4 * k + 3]) * inv_l);
+                    for (int kk = 0; kk < 8; ++kk)
+                        *reinterpret_cast<float4*>(dst + sw128_offset(r, kk)) =
+                            make_float4(__uint_as_float(orow[4 * kk]) * inv_l, __uint_as_float(orow[4 * kk + 1]) * inv_l,
+                                        __uint_as_float(orow[4 * kk + 2]) * inv_l,
+                                        __uint_as_float(orow[4 * kk + 3]) * inv_l);
                 } else {
                     uint32_t pk[16];
 #pragma unroll
@@ -427,21 +604,32 @@ __global__ void __launch_bounds__(480, 1)
                     uint8_t* dst = sQu + (c >> 6) * C::BM * 128;
                     const int u0 = (c & 63) >> 3;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        *reinterpret_cast<uint4*>(dst + sw128_offset(r, u0 + k)) =
-                            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    for (int kk = 0; kk < 4; ++kk)
+                        *reinterpret_cast<uint4*>(dst + sw128_offset(r, u0 + kk)) =
+                            make_uint4(pk[4 * kk], pk[4 * kk + 1], pk[4 * kk + 2], pk[4 * kk + 3]);
                 }
             }
+            tc_fence_before();
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_o_staged[u]));
-            if (qpos < T) a.lse[((size_t)b * a.Hq + h) * T + qpos] = (st.m_used + log2f(st.l)) * 0.6931471805599453f;
-            if (r == 0 && mbar_wait(smem_u32(&bar_o_staged[u]), 0, w, SITE_FWD_O_DONE)) {
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_store_4d(&tm_o, smem_u32(sQu + c * C::BM * 128), c * C::EPC, h, qsub0, b);
-                bulk_commit_group();
-                bulk_wait_group_read0();
+            if (qpos < T) a.lse[((size_t)f.b * a.Hq + f.h) * T + qpos] = (st.m_used + log2f(st.l)) * 0.6931471805599453f;
+            bool stored = true;
+            if (r == 0) {
+                stored = mbar_wait(smem_u32(&bar_o_staged[u]), n_epi & 1, w, SITE_FWD_O_DONE);
+                if (stored) {
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_store_4d(&tm_o, smem_u32(sQu + c * C::BM * 128), c * C::EPC, f.h, qsub0, f.b);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();          // the buffer may take the next Q
+                    mbar_arrive(smem_u32(&bar_q_empty[qb]));
+                }
             }
+            if (!(ok = __all_sync(0xffffffffu, stored))) break;   // the warp leaves the loop together
+            ++n_epi;
         }
+        if (r == 0) bulk_wait_group0();               // the last O store has completed
+    } else {
+        rope_role(lane + 32 * (warp - 11));
     }
 
     // ---------------------------------------------------------------- teardown
@@ -462,7 +650,11 @@ cudaError_t launch_fwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, co
     auto kfn = attn_fwd_kernel<TF32, D>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.Hq, B, a.n_qt);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // One CTA per SM (the shared memory allows no second), each walking its units.
+    dim3 grid(a.n_units < sms ? a.n_units : sms);
     return launch_k(kfn, grid, dim3(C::THREADS), C::SMEM, st, tq, tk, tv, to, a);
 }
 

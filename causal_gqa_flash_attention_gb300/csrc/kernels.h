@@ -31,7 +31,8 @@ struct FwdArgs {
     void* o;                 // [B,T,Hq,D], input dtype
     float* lse;              // [B,Hq,T]
     const float2* rope;      // [T, D/2] (cos, sin)
-    int T, Hq, G, n_qt;      // n_qt = ceil(T / 256): pairs of 128-row query tiles
+    int B, T, Hq, G, n_qt;   // n_qt = ceil(T / 256): pairs of 128-row query tiles
+    int n_units;             // B * Hq * n_qt work units of the persistent kernel
     float scale_log2;        // log2(e) / sqrt(D)
     int* err;
     unsigned long long timeout_ns;
