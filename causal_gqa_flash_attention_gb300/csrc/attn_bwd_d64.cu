@@ -44,6 +44,7 @@
 // Every wait is bounded; a CTA that gives up records an error code, drains its own copies
 // and MMAs and frees its TMEM.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include "kernels.h"
 #include "ptx.cuh"
 #include "rope_smem.cuh"
@@ -89,6 +90,39 @@ struct TileWalk {
     __device__ __forceinline__ int q0() const { return qt * Bwd64::BT; }
 };
 
+// One 32-query chunk of one key row: P^T = exp2(S^T s log2e - LSE log2e) and
+// dS^T = P^T o (dP^T - Delta), packed to bf16 (P^T) and fp16 (dS^T).  With MASK, query i
+// of the chunk is masked (P = 0) when i < kl: kl is the key's lane when the warp's 32
+// keys and the chunk's queries start at the same position, and 32 when every key
+// follows every query (the chunk is all zero).
+// amax2 keeps the largest |dS| as packed fp16, so a value past the fp16 range shows up
+// as infinity.
+template <bool MASK>
+__device__ __forceinline__ void grad_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* lse2,
+                                           const float* delta, float sl2, int kl, uint32_t (&pk)[16],
+                                           uint32_t (&dk)[16], __half2& amax2) {
+    const float4* l4 = reinterpret_cast<const float4*>(lse2);
+    const float4* d4 = reinterpret_cast<const float4*>(delta);
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+        const float4 lq4 = l4[e >> 2], dq4 = d4[e >> 2];   // broadcast reads
+        const float lq[4] = {lq4.x, lq4.y, lq4.z, lq4.w}, dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w};
+        float p[4], ds[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
+            if (MASK && kl > e + k) p[k] = 0.f;
+            ds[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
+        }
+        pk[e >> 1] = pack_bf162(p[0], p[1]);
+        pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
+        dk[e >> 1] = pack_half2(ds[0], ds[1]);
+        dk[(e >> 1) + 1] = pack_half2(ds[2], ds[3]);
+        amax2 = __hmax2(amax2, __habs2(*reinterpret_cast<const __half2*>(&dk[e >> 1])));
+        amax2 = __hmax2(amax2, __habs2(*reinterpret_cast<const __half2*>(&dk[(e >> 1) + 1])));
+    }
+}
+
 __device__ __forceinline__ uint32_t s_col(int b) { return (uint32_t)(128 * b); }
 __device__ __forceinline__ uint32_t dp_col(int b) { return (uint32_t)(128 * b + 64); }
 // Packed P^T of buffer b: 64 queries in 32 columns.
@@ -113,9 +147,8 @@ __global__ void __launch_bounds__(512, 1)
 
     __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_dkv_full, bar_final;
     __shared__ __align__(8) uint64_t bar_qdo_full[C::NQS], bar_qdo_empty[C::NQS];
-    __shared__ __align__(8) uint64_t bar_s_full[2], bar_dp_full[2];   // [S^T/dP^T buffer]: MMA done
+    __shared__ __align__(8) uint64_t bar_sdp_full[2];                 // [S^T/dP^T buffer]: both MMAs done
     __shared__ __align__(8) uint64_t bar_sp_read[2];                  // ... read into registers
-    __shared__ __align__(8) uint64_t bar_p_free[2];                   // [P^T buffer]: read by dV
     __shared__ __align__(8) uint64_t bar_ds_half[2];   // [half]: P^T and the dS^T half of a half-step written
     __shared__ __align__(8) uint64_t bar_ds_tile[2];   // [dS^T tile buffer]: both halves written
     __shared__ __align__(8) uint64_t bar_ds_free[2];   // [dS^T tile buffer]: dK' and dQ' done with it
@@ -146,10 +179,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(smem_u32(&bar_qdo_empty[s]), 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bar_s_full[i]), 1);
-            mbar_init(smem_u32(&bar_dp_full[i]), 1);
+            mbar_init(smem_u32(&bar_sdp_full[i]), 2);   // the S^T and the dP^T issuer
             mbar_init(smem_u32(&bar_sp_read[i]), 128);   // the warp group of buffer i
-            mbar_init(smem_u32(&bar_p_free[i]), 1);
             mbar_init(smem_u32(&bar_ds_half[i]), 128);   // the warp group of half i
             mbar_init(smem_u32(&bar_ds_tile[i]), 256);
             mbar_init(smem_u32(&bar_ds_free[i]), 2);  // dK' issuer (after the odd half) and dQ' issuer
@@ -247,7 +278,6 @@ __global__ void __launch_bounds__(512, 1)
                                  : idesc_make(FMT_BF16, 128, C::BH, false, false);
         const uint64_t dA = kdesc(is_s ? sK : sV);
         const uint64_t dB0 = kdesc(is_s ? stage_q(0) : stage_do(0));
-        uint64_t* full = is_s ? bar_s_full : bar_dp_full;
         // S^T waits for the rotated K' (once), both for the copies of Q' / dO.
         bool ok = is_s ? mbar_wait_warp(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV)
                        : mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
@@ -265,7 +295,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int ks = 0; ks < D / 16; ++ks)            // K = head_dim: 16 per step (32 bytes)
                 umma_ss_e<false>(tm + (is_s ? s_col(bf) : dp_col(bf)), sdesc_add(dA, ks * 32), sdesc_add(dB, ks * 32),
                                  id, ks > 0);
-            umma_commit_e(smem_u32(&full[bf]));
+            umma_commit_e(smem_u32(&bar_sdp_full[bf]));
         }
         umma_commit_e(smem_u32(&bar_final));
     } else if (warp == 3) {
@@ -283,7 +313,6 @@ __global__ void __launch_bounds__(512, 1)
             for (int ks = 0; ks < C::BH / 16; ++ks)         // dV += P^T dO (P^T from TMEM), K = queries
                 umma_ts_e<false>(tm + C::DV_COL, tm + pt_col(half) + 8 * ks, sdesc_add(dOmn, ks * 16 * 128), id_dv,
                                  (hs > 0 || ks > 0) ? 1u : 0u);
-            umma_commit_e(smem_u32(&bar_p_free[half]));
             const uint64_t dDS = kdesc(ds_tile(tb) + half * C::DS_CHUNK);
 #pragma unroll
             for (int ks = 0; ks < C::BH / 16; ++ks)         // dK' += dS^T Q', K = queries
@@ -347,9 +376,10 @@ __global__ void __launch_bounds__(512, 1)
         const int g = (warp - 8) >> 2;                   // warp group = half index = TMEM buffer
         const int r = (warp & 3) * 32 + lane;            // key row = TMEM lane
         const int kvpos = kv0 + r;
+        const int kw = kv0 + (warp & 3) * 32;            // first key row of this warp
         const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
         const float sl2 = a.scale_log2;
-        float amax = 0.f;
+        __half2 amax2 = __floats2half2_rn(0.f, 0.f);
         bool ok = true;
         // LSE / Delta of the 64 query columns: lanes l and l+32 fetch columns l and l+32 of
         // the group's next half-step while the current one runs, and the warp stages them in
@@ -395,10 +425,8 @@ __global__ void __launch_bounds__(512, 1)
             const int q0 = cur.q0() + g * C::BH;
             float lv_n[2] = {0.f, 0.f}, dv_n[2] = {0.f, 0.f};
             if (hs + 2 < n_hs) row_vals(nxt, lv_n, dv_n);   // in flight during this half-step
-            if (!(ok = mbar_wait_warp(smem_u32(&bar_s_full[g]), (hs >> 1) & 1, w, SITE_BWD_S_FULL))) break;
-            if (!(ok = mbar_wait_warp(smem_u32(&bar_dp_full[g]), (hs >> 1) & 1, w, SITE_BWD_DP_FULL))) break;
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_sdp_full[g]), (hs >> 1) & 1, w, SITE_BWD_S_FULL))) break;
             tc_fence_after();
-            const bool diag = kvpos > q0;                // some of this row's queries precede the key
             uint8_t* dsbase = ds_tile(tb) + g * C::DS_CHUNK;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {                // two 32-query chunks
@@ -412,31 +440,23 @@ __global__ void __launch_bounds__(512, 1)
                     tc_fence_before();
                     mbar_arrive(smem_u32(&bar_sp_read[g]));
                 }
+                // The causal mask on the block of this warp's 32 keys and the chunk's 32
+                // queries (both start on 32-row boundaries) is warp-uniform: every key
+                // after every query, none, or the diagonal block (key lane masked for the
+                // queries before it).
                 uint32_t pk[16], dk[16];
-                const float4* l4 = reinterpret_cast<const float4*>(&s_lse[sw][buf][32 * c]);
-                const float4* d4 = reinterpret_cast<const float4*>(&s_delta[sw][buf][32 * c]);
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 lq4 = l4[e >> 2], dq4 = d4[e >> 2];   // broadcast reads
-                    const float lq[4] = {lq4.x, lq4.y, lq4.z, lq4.w}, dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w};
-                    float p[4], ds[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
-                        if (diag && kvpos > q0 + 32 * c + e + k) p[k] = 0.f;
-                        ds[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
-                        amax = fmaxf(amax, fabsf(ds[k]));
-                    }
-                    pk[e >> 1] = pack_bf162(p[0], p[1]);
-                    pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
-                    dk[e >> 1] = pack_half2(ds[0], ds[1]);
-                    dk[(e >> 1) + 1] = pack_half2(ds[2], ds[3]);
-                }
+                const int qc = q0 + 32 * c;
+                const float* lrow = &s_lse[sw][buf][32 * c];
+                const float* drow = &s_delta[sw][buf][32 * c];
+                if (kw < qc) grad_chunk<false>(sr, dr, lrow, drow, sl2, -1, pk, dk, amax2);
+                else grad_chunk<true>(sr, dr, lrow, drow, sl2, kw == qc ? lane : 32, pk, dk, amax2);
                 if (c == 0) {
-                    // P^T buffer g is free once dV of half-step hs-2 has read it; the dS^T
-                    // tile buffer once dK' and dQ' of tile tau-2 have.
-                    if (hs >= 2 &&
-                        !(ok = mbar_wait_warp(smem_u32(&bar_p_free[g]), ((hs - 2) >> 1) & 1, w, SITE_BWD_DS_READY)))
+                    // P^T buffer g is free once dV of half-step hs-2 has read it: that
+                    // half-step's stage release, committed after its dK' (issued after its
+                    // dV by the same thread), says so.  The dS^T tile buffer is free once
+                    // dK' and dQ' of tile tau-2 have read it.
+                    if (hs >= 2 && !(ok = mbar_wait_warp(smem_u32(&bar_qdo_empty[(hs - 2) % C::NQS]),
+                                                         ((hs - 2) / C::NQS) & 1, w, SITE_BWD_DS_READY)))
                         break;
                     if (tau >= 2 &&
                         !(ok = mbar_wait_warp(smem_u32(&bar_ds_free[tb]), ((tau - 2) >> 1) & 1, w, SITE_BWD_DS_FREE)))
@@ -457,7 +477,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive(smem_u32(&bar_ds_tile[tb]));
             if (hs + 2 < n_hs) publish(hs + 2, lv_n, dv_n);
         }
-        if (amax > 65504.f) atomicCAS(a.err, 0, SITE_RANGE);   // a dS beyond the fp16 range
+        // A dS beyond the fp16 range rounded to infinity.
+        if (fmaxf(__low2float(amax2), __high2float(amax2)) > 65504.f) atomicCAS(a.err, 0, SITE_RANGE);
         // Epilogue, key row r of this CTA's tile: group 0 writes dK = s R^T dK', group 1 dV.
         if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
             tc_fence_after();

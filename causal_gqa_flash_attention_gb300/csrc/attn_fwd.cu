@@ -112,11 +112,12 @@ struct RowState {
 // One key tile of one softmax thread: mask, max, rescale decision (and O rescale),
 // exp2, P written back over this tile's S buffer, p_ready arrival.  j is the tile's
 // index within the unit, t its index in the subtile's sequence of tiles over all units
-// (S buffer t % 2; barrier phases).  Returns false when a wait ran out.
+// (S buffer t % 2; barrier phases), g its index in the CTA's K/V sequence.  Returns
+// false when a wait ran out.
 template <bool TF32, int D>
-__device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, int u, int qsub0, int qpos, uint32_t lt,
-                                             float sl2, RowState& st, uint64_t* bar_o_done, uint64_t* bar_p_ready,
-                                             const WaitCtx& w) {
+__device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, int g, int u, int qsub0, int qpos,
+                                             uint32_t lt, float sl2, RowState& st, uint64_t* bar_kv_empty,
+                                             uint64_t* bar_p_ready, const WaitCtx& w) {
     using C = FwdCfg<TF32, D>;
     const int kv0 = j * C::BN;
     if (kv0 + C::BN - 1 > qsub0) {   // tile crosses the diagonal: mask keys after the row
@@ -140,15 +141,18 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
     // A row whose max grew by more than 2^8 rescales l and its O row; the others keep
     // their max (p <= 2^8 stays exact).  TMEM access is warp-collective, so a warp
     // rescales when any lane needs it (alpha = 1 elsewhere).  O is idle once the PV of
-    // tile t-1 is done (PV(t) needs this thread's P(t)).  The per-PV barrier is then at
-    // most one phase short of it: PV(t-2) completed before S(t), issued after it, did.
+    // the previous tile is done (PV(t) needs this thread's P(t)); that tile's stage
+    // release, which both issuers commit after their PV of it, says so.  (The release
+    // barrier cannot have run a phase further: the stage's next tile is not loaded
+    // before this release.)
     const bool need = j > 0 && m_tile > st.m_used + 8.f;
     if (j == 0) st.m_used = m_tile;
     if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2(st.m_used - m_tile) : 1.f;
         st.l *= alpha;
         if (need) st.m_used = m_tile;
-        if (!mbar_wait_warp(smem_u32(&bar_o_done[u]), (t - 1) & 1, w, SITE_FWD_O_DONE)) return false;
+        if (!mbar_wait_warp(smem_u32(&bar_kv_empty[(g - 1) % C::NS]), ((g - 1) / C::NS) & 1, w, SITE_FWD_O_DONE))
+            return false;
         tc_fence_after();
         const uint32_t oc = C::O_COL + u * D;
 #pragma unroll 1
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(480, 1)
 
     __shared__ __align__(8) uint64_t bar_final;
     __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_ready[2], bar_q_empty[2];   // [Q buffer]
-    __shared__ __align__(8) uint64_t bar_o_done[2], bar_o_final[2], bar_o_staged[2];  // [subtile]
+    __shared__ __align__(8) uint64_t bar_o_final[2], bar_o_staged[2];  // [subtile]
     __shared__ __align__(8) uint64_t bar_s_full[4], bar_p_ready[4];     // [u * 2 + buffer]
     __shared__ __align__(8) uint64_t bar_kv_full[C::NS], bar_k_ready[C::NS], bar_kv_empty[C::NS];
     __shared__ uint32_t tmem_slot;
@@ -295,7 +299,6 @@ __global__ void __launch_bounds__(480, 1)
             mbar_init(smem_u32(&bar_q_full[i]), 1);
             mbar_init(smem_u32(&bar_q_ready[i]), C::ROPE_THREADS);
             mbar_init(smem_u32(&bar_q_empty[i]), 2);     // one arrival per subtile epilogue
-            mbar_init(smem_u32(&bar_o_done[i]), 1);      // every PV
             mbar_init(smem_u32(&bar_o_final[i]), 1);     // the last PV of a unit
             mbar_init(smem_u32(&bar_o_staged[i]), 128);
         }
@@ -328,9 +331,165 @@ __global__ void __launch_bounds__(480, 1)
     auto stage_v = [&](int s) { return sStage + s * C::STAGE_BYTES + C::KV_BYTES; };
     auto stage_vt = [&](int s) { return sStage + s * C::STAGE_BYTES + 2 * C::KV_BYTES; };
 
-    // RoPE role, thread rt of the ROPE_THREADS (warp 3 and warps 12-14).
-    auto rope_role = [&](const int rt) {
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            int issued = 0;                           // K/V tiles loaded so far
+            int last_k0 = -1, last_k1 = -1;           // last unit loaded into Q buffer 0 / 1
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int U = fwd_unit_index(k, a.n_units);
+                if (U < 0) break;
+                const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+                const int qb = k % C::NQB;
+                // The Q buffer is free once both epilogues of unit k - NQB stored their O.
+                if (k >= C::NQB &&
+                    !(ok = mbar_wait(smem_u32(&bar_q_empty[qb]), ((k / C::NQB) - 1) & 1, w, SITE_FWD_Q)))
+                    break;
+                const uint32_t qf = smem_u32(&bar_q_full[qb]);
+                mbar_arrive_expect_tx(qf, f.n_qsub * C::Q_BYTES);
+                for (int u = 0; u < f.n_qsub; ++u)
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_4d(smem_u32(q_buf(k) + u * C::Q_BYTES + c * C::BM * 128), &tm_q, qf, c * C::EPC,
+                                    f.h, f.q0 + u * C::BM, f.b);
+                if (qb == 0) last_k0 = k;
+                else last_k1 = k;
+                const int hkv = f.h / a.G;
+                for (int j = 0; j < f.n_kv; ++j) {
+                    const int g = issued, s = g % C::NS;
+                    if (g >= C::NS &&
+                        !(ok = mbar_wait(smem_u32(&bar_kv_empty[s]), ((g / C::NS) - 1) & 1, w, SITE_FWD_KV_EMPTY)))
+                        break;
+                    const uint32_t full = smem_u32(&bar_kv_full[s]);
+                    mbar_arrive_expect_tx(full, 2 * C::KV_BYTES);
+                    for (int c = 0; c < C::NCH; ++c) {
+                        tma_load_4d(smem_u32(stage_k(s) + c * C::BN * 128), &tm_k, full, c * C::EPC, hkv, j * C::BN,
+                                    f.b);
+                        tma_load_4d(smem_u32(stage_v(s) + c * C::BN * 128), &tm_v, full, c * C::EPC, hkv, j * C::BN,
+                                    f.b);
+                    }
+                    ++issued;
+                }
+            }
+            // Teardown: every copy this CTA started must have landed before exit.
+            if (last_k0 >= 0) mbar_wait_drain(smem_u32(&bar_q_full[0]), (last_k0 / C::NQB) & 1, w, SITE_FWD_DRAIN);
+            if (last_k1 >= 0) mbar_wait_drain(smem_u32(&bar_q_full[1]), (last_k1 / C::NQB) & 1, w, SITE_FWD_DRAIN);
+            for (int g = max(0, issued - C::NS); g < issued; ++g)
+                mbar_wait_drain(smem_u32(&bar_kv_full[g % C::NS]), (g / C::NS) & 1, w, SITE_FWD_DRAIN);
+        }
+    } else if (warp < 3) {
+        // ------------------------------------------------------------ UMMA issuers
+        // Each subtile has its own issuing warp (1 + u); the whole warp runs the loop and
+        // one elected lane issues.  Tiles are numbered t = 0, 1, ... over all units of the
+        // CTA; S(t) goes to S buffer t % 2, two tiles ahead of the softmax, and overwrites
+        // P(t-2), whose PV the same lane issued earlier (one thread's UMMAs execute in
+        // order).
+        const int u = warp - 1;
+        constexpr uint32_t id_s = idesc_make(C::FMT_S, 128, C::BN, false, false);
+        constexpr uint32_t id_o = idesc_make(C::FMT_PV, 128, D, false, !TF32);
+        // Descriptors are built once; a K-step, a stage or a Q buffer only moves the start
+        // address.
+        const uint64_t dq0 = sdesc(smem_u32(sQ + u * C::Q_BYTES), 16, 1024);
+        const uint64_t dk0 = sdesc(smem_u32(stage_k(0)), 16, 1024);
+        const uint64_t dv0 = TF32 ? sdesc(smem_u32(stage_vt(0)), 16, 1024)
+                                  : sdesc(smem_u32(stage_v(0)), C::BN * 128, 1024);
+        const uint32_t ocol = tm + C::O_COL + u * D;
+        auto k_ready = [&](int g) {
+            const bool r = mbar_wait_warp(smem_u32(&bar_k_ready[g % C::NS]), (g / C::NS) & 1, w, SITE_FWD_K_READY);
+            tc_fence_after();
+            return r;
+        };
+        int t_s = 0;                                  // S tiles issued
+        int qr_next = 0;                              // first unit whose Q' this issuer has not waited for
+        auto issue_s = [&](const FwdWalk<C::BM, C::BN>& c) -> bool {
+            // Q' of the unit (and of any unit skipped since the last one: every phase of
+            // the Q-ready barriers is waited for in order, so a parity never aliases).
+            for (; c.j == 0 && qr_next <= c.k; ++qr_next)
+                if (!mbar_wait_warp(smem_u32(&bar_q_ready[qr_next % C::NQB]), (qr_next / C::NQB) & 1, w, SITE_FWD_Q))
+                    return false;
+            const int g = c.kvb + c.j;
+            if (!k_ready(g)) return false;
+            const uint64_t dq = sdesc_add(dq0, (c.k % C::NQB) * C::QBUF);
+            const uint64_t dk = sdesc_add(dk0, (g % C::NS) * C::STAGE_BYTES);
+            const uint32_t dcol = tm + s_col(u, t_s & 1);
+#pragma unroll
+            for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
+                const uint32_t byte = ks * 32;
+                umma_ss_e<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
+                                sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
+            }
+            umma_commit_e(smem_u32(&bar_s_full[u * 2 + (t_s & 1)]));
+            ++t_s;
+            return true;
+        };
+        auto issue_pv = [&](int t, int j, int g, bool last) -> bool {
+            if (!mbar_wait_warp(smem_u32(&bar_p_ready[u * 2 + (t & 1)]), (t >> 1) & 1, w, SITE_FWD_P_READY))
+                return false;
+            tc_fence_after();
+            const uint64_t dv = sdesc_add(dv0, (g % C::NS) * C::STAGE_BYTES);
+            const uint32_t pcol = tm + s_col(u, t & 1);
+#pragma unroll
+            for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
+                // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
+                // MN-major, PV_ROWS keys per K-step.
+                const uint32_t off = TF32 ? ((ks * 32) >> 7) * D * 128 + ((ks * 32) & 127) : ks * C::PV_ROWS * 128;
+                umma_ts_e<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+            }
+            if (last) umma_commit_e(smem_u32(&bar_o_final[u]));
+            return true;
+        };
+        FwdWalk<C::BM, C::BN> sw;                     // the next tile to issue S for
+        sw.init(u, a);
+        int t = 0, g = 0;                             // PV tiles issued; K/V tiles passed
+        // S runs at most two tiles ahead of PV.  With one Q buffer the next unit's Q can
+        // only land after this unit's epilogues, which wait for this unit's last PVs, so
+        // S of the next unit waits until the current unit's loop is done.  With two, the
+        // next unit's Q depends only on the unit before this one; its S may then wait
+        // inside the loop, where this issuer has released all but the last
+        // n_kv - n_u + 1 <= 3 stages of the unit, and NS >= 4 lets the next unit's first
+        // K/V tile load regardless.
+        auto may_issue = [&](int k_cur) { return sw.k >= 0 && t_s < t + 2 && (C::NQB == 2 || sw.k <= k_cur); };
+        bool ok = true;
+        while (ok && may_issue(0)) {
+            ok = issue_s(sw);
+            sw.advance(u, a);
+        }
+        // Every K/V stage is released by both issuers, in order.  A tile beyond the
+        // subtile's diagonal is released without use, but only once the stage really
+        // holds it (k_ready), so the release never runs a phase ahead.
+        for (int k = 0; ok; ++k) {
+            const int U = fwd_unit_index(k, a.n_units);
+            if (U < 0) break;
+            const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+            for (int j = 0; ok && j < f.n_kv; ++j, ++g) {
+                const int n = u == 0 ? f.n_u[0] : f.n_u[1];
+                if (j < n) {
+                    if (!(ok = issue_pv(t, j, g, j == n - 1))) break;
+                    ++t;
+                    umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
+                    while (ok && may_issue(k)) {
+                        ok = issue_s(sw);
+                        sw.advance(u, a);
+                    }
+                } else {
+                    if (!(ok = k_ready(g))) break;
+                    umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
+                }
+            }
+            while (ok && may_issue(k + 1)) {
+                ok = issue_s(sw);
+                sw.advance(u, a);
+            }
+        }
+        umma_commit_e(smem_u32(&bar_final));
+    } else if (warp == 3 || warp >= 12) {
         // ------------------------------------------------------------ RoPE on Q and K (+ V^T)
+        // One branch for all four warps: a second inlined copy of this code measurably
+        // slowed the kernel (instruction fetch).
+        const int rt = lane + (warp == 3 ? 0 : 32 * (warp - 11));
         using RopeK = RopeTile<D, C::BN, C::ROPE_THREADS, C::MODE>;
         using RopeQ = RopeTile<D, C::BM, C::ROPE_THREADS, C::MODE>;
         RopeK rk;
@@ -367,167 +526,6 @@ __global__ void __launch_bounds__(480, 1)
                 mbar_arrive(smem_u32(&bar_k_ready[s]));
             }
         }
-    };
-
-    if (warp < 4) {
-        if (warp == 0) {
-            // ------------------------------------------------------------ TMA producer
-            if (lane == 0) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_k);
-                tma_prefetch_desc(&tm_v);
-                int issued = 0;                           // K/V tiles loaded so far
-                int last_k0 = -1, last_k1 = -1;           // last unit loaded into Q buffer 0 / 1
-                bool ok = true;
-                for (int k = 0; ok; ++k) {
-                    const int U = fwd_unit_index(k, a.n_units);
-                    if (U < 0) break;
-                    const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
-                    const int qb = k % C::NQB;
-                    // The Q buffer is free once both epilogues of unit k - NQB stored their O.
-                    if (k >= C::NQB &&
-                        !(ok = mbar_wait(smem_u32(&bar_q_empty[qb]), ((k / C::NQB) - 1) & 1, w, SITE_FWD_Q)))
-                        break;
-                    const uint32_t qf = smem_u32(&bar_q_full[qb]);
-                    mbar_arrive_expect_tx(qf, f.n_qsub * C::Q_BYTES);
-                    for (int u = 0; u < f.n_qsub; ++u)
-                        for (int c = 0; c < C::NCH; ++c)
-                            tma_load_4d(smem_u32(q_buf(k) + u * C::Q_BYTES + c * C::BM * 128), &tm_q, qf, c * C::EPC,
-                                        f.h, f.q0 + u * C::BM, f.b);
-                    if (qb == 0) last_k0 = k;
-                    else last_k1 = k;
-                    const int hkv = f.h / a.G;
-                    for (int j = 0; j < f.n_kv; ++j) {
-                        const int g = issued, s = g % C::NS;
-                        if (g >= C::NS &&
-                            !(ok = mbar_wait(smem_u32(&bar_kv_empty[s]), ((g / C::NS) - 1) & 1, w, SITE_FWD_KV_EMPTY)))
-                            break;
-                        const uint32_t full = smem_u32(&bar_kv_full[s]);
-                        mbar_arrive_expect_tx(full, 2 * C::KV_BYTES);
-                        for (int c = 0; c < C::NCH; ++c) {
-                            tma_load_4d(smem_u32(stage_k(s) + c * C::BN * 128), &tm_k, full, c * C::EPC, hkv, j * C::BN,
-                                        f.b);
-                            tma_load_4d(smem_u32(stage_v(s) + c * C::BN * 128), &tm_v, full, c * C::EPC, hkv, j * C::BN,
-                                        f.b);
-                        }
-                        ++issued;
-                    }
-                }
-                // Teardown: every copy this CTA started must have landed before exit.
-                if (last_k0 >= 0) mbar_wait_drain(smem_u32(&bar_q_full[0]), (last_k0 / C::NQB) & 1, w, SITE_FWD_DRAIN);
-                if (last_k1 >= 0) mbar_wait_drain(smem_u32(&bar_q_full[1]), (last_k1 / C::NQB) & 1, w, SITE_FWD_DRAIN);
-                for (int g = max(0, issued - C::NS); g < issued; ++g)
-                    mbar_wait_drain(smem_u32(&bar_kv_full[g % C::NS]), (g / C::NS) & 1, w, SITE_FWD_DRAIN);
-            }
-        } else if (warp < 3) {
-            // ------------------------------------------------------------ UMMA issuers
-            // Each subtile has its own issuing warp (1 + u); the whole warp runs the loop and
-            // one elected lane issues.  Tiles are numbered t = 0, 1, ... over all units of the
-            // CTA; S(t) goes to S buffer t % 2, two tiles ahead of the softmax, and overwrites
-            // P(t-2), whose PV the same lane issued earlier (one thread's UMMAs execute in
-            // order).
-            const int u = warp - 1;
-            constexpr uint32_t id_s = idesc_make(C::FMT_S, 128, C::BN, false, false);
-            constexpr uint32_t id_o = idesc_make(C::FMT_PV, 128, D, false, !TF32);
-            // Descriptors are built once; a K-step, a stage or a Q buffer only moves the start
-            // address.
-            const uint64_t dq0 = sdesc(smem_u32(sQ + u * C::Q_BYTES), 16, 1024);
-            const uint64_t dk0 = sdesc(smem_u32(stage_k(0)), 16, 1024);
-            const uint64_t dv0 = TF32 ? sdesc(smem_u32(stage_vt(0)), 16, 1024)
-                                      : sdesc(smem_u32(stage_v(0)), C::BN * 128, 1024);
-            const uint32_t ocol = tm + C::O_COL + u * D;
-            auto k_ready = [&](int g) {
-                const bool r = mbar_wait_warp(smem_u32(&bar_k_ready[g % C::NS]), (g / C::NS) & 1, w, SITE_FWD_K_READY);
-                tc_fence_after();
-                return r;
-            };
-            int t_s = 0;                                  // S tiles issued
-            int qr_next = 0;                              // first unit whose Q' this issuer has not waited for
-            auto issue_s = [&](const FwdWalk<C::BM, C::BN>& c) -> bool {
-                // Q' of the unit (and of any unit skipped since the last one: every phase of
-                // the Q-ready barriers is waited for in order, so a parity never aliases).
-                for (; c.j == 0 && qr_next <= c.k; ++qr_next)
-                    if (!mbar_wait_warp(smem_u32(&bar_q_ready[qr_next % C::NQB]), (qr_next / C::NQB) & 1, w, SITE_FWD_Q))
-                        return false;
-                const int g = c.kvb + c.j;
-                if (!k_ready(g)) return false;
-                const uint64_t dq = sdesc_add(dq0, (c.k % C::NQB) * C::QBUF);
-                const uint64_t dk = sdesc_add(dk0, (g % C::NS) * C::STAGE_BYTES);
-                const uint32_t dcol = tm + s_col(u, t_s & 1);
-    #pragma unroll
-                for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
-                    const uint32_t byte = ks * 32;
-                    umma_ss_e<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
-                                    sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
-                }
-                umma_commit_e(smem_u32(&bar_s_full[u * 2 + (t_s & 1)]));
-                ++t_s;
-                return true;
-            };
-            auto issue_pv = [&](int t, int j, int g, bool last) -> bool {
-                if (!mbar_wait_warp(smem_u32(&bar_p_ready[u * 2 + (t & 1)]), (t >> 1) & 1, w, SITE_FWD_P_READY))
-                    return false;
-                tc_fence_after();
-                const uint64_t dv = sdesc_add(dv0, (g % C::NS) * C::STAGE_BYTES);
-                const uint32_t pcol = tm + s_col(u, t & 1);
-    #pragma unroll
-                for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
-                    // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
-                    // MN-major, PV_ROWS keys per K-step.
-                    const uint32_t off = TF32 ? ((ks * 32) >> 7) * D * 128 + ((ks * 32) & 127) : ks * C::PV_ROWS * 128;
-                    umma_ts_e<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
-                }
-                umma_commit_e(smem_u32(&bar_o_done[u]));
-                if (last) umma_commit_e(smem_u32(&bar_o_final[u]));
-                return true;
-            };
-            FwdWalk<C::BM, C::BN> sw;                     // the next tile to issue S for
-            sw.init(u, a);
-            int t = 0, g = 0;                             // PV tiles issued; K/V tiles passed
-            // S runs at most two tiles ahead of PV.  With one Q buffer the next unit's Q can
-            // only land after this unit's epilogues, which wait for this unit's last PVs, so
-            // S of the next unit waits until the current unit's loop is done.  With two, the
-            // next unit's Q depends only on the unit before this one; its S may then wait
-            // inside the loop, where this issuer has released all but the last
-            // n_kv - n_u + 1 <= 3 stages of the unit, and NS >= 4 lets the next unit's first
-            // K/V tile load regardless.
-            auto may_issue = [&](int k_cur) { return sw.k >= 0 && t_s < t + 2 && (C::NQB == 2 || sw.k <= k_cur); };
-            bool ok = true;
-            while (ok && may_issue(0)) {
-                ok = issue_s(sw);
-                sw.advance(u, a);
-            }
-            // Every K/V stage is released by both issuers, in order.  A tile beyond the
-            // subtile's diagonal is released without use, but only once the stage really
-            // holds it (k_ready), so the release never runs a phase ahead.
-            for (int k = 0; ok; ++k) {
-                const int U = fwd_unit_index(k, a.n_units);
-                if (U < 0) break;
-                const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
-                for (int j = 0; ok && j < f.n_kv; ++j, ++g) {
-                    const int n = u == 0 ? f.n_u[0] : f.n_u[1];
-                    if (j < n) {
-                        if (!(ok = issue_pv(t, j, g, j == n - 1))) break;
-                        ++t;
-                        umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
-                        while (ok && may_issue(k)) {
-                            ok = issue_s(sw);
-                            sw.advance(u, a);
-                        }
-                    } else {
-                        if (!(ok = k_ready(g))) break;
-                        umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
-                    }
-                }
-                while (ok && may_issue(k + 1)) {
-                    ok = issue_s(sw);
-                    sw.advance(u, a);
-                }
-            }
-            umma_commit_e(smem_u32(&bar_final));
-        } else {
-            rope_role(lane);
-        }
     } else if (warp < 12) {
         // ------------------------------------------------------------ softmax (subtile u)
         const int u = (warp - 4) >> 2;
@@ -536,8 +534,9 @@ __global__ void __launch_bounds__(480, 1)
         const uint32_t o_col = C::O_COL + u * D;
         const float sl2 = a.scale_log2;
         int t = 0, n_epi = 0;                         // tiles and epilogues of this subtile so far
+        int kvb = 0, n_kv = 0;                        // first K/V tile of the unit, its K/V tiles
         bool ok = true;
-        for (int k = 0; ok; ++k) {
+        for (int k = 0; ok; ++k, kvb += n_kv) {
             // Only what the tiles need stays live through the tile loop (the softmax
             // holds a 64-register S row); the epilogue decodes the unit again.
             int n, qsub0;
@@ -547,6 +546,7 @@ __global__ void __launch_bounds__(480, 1)
                 const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
                 n = u == 0 ? f.n_u[0] : f.n_u[1];
                 qsub0 = f.q0 + u * C::BM;
+                n_kv = f.n_kv;
             }
             const int qb = k % C::NQB;
             if (n == 0) {                             // subtile beyond T: nothing to store
@@ -569,7 +569,8 @@ __global__ void __launch_bounds__(480, 1)
                 tc_fence_after();
                 uint32_t sr[64];
                 tmem_ld_cols<2>(lt + s_col(u, t & 1), sr);
-                if (!(ok = softmax_tile<TF32, D>(sr, j, t, u, qsub0, qpos, lt, sl2, st, bar_o_done, bar_p_ready, w)))
+                if (!(ok = softmax_tile<TF32, D>(sr, j, t, kvb + j, u, qsub0, qpos, lt, sl2, st, bar_kv_empty,
+                                                 bar_p_ready, w)))
                     break;
             }
             if (!ok) break;
@@ -628,8 +629,6 @@ __global__ void __launch_bounds__(480, 1)
             ++n_epi;
         }
         if (r == 0) bulk_wait_group0();               // the last O store has completed
-    } else {
-        rope_role(lane + 32 * (warp - 11));
     }
 
     // ---------------------------------------------------------------- teardown
