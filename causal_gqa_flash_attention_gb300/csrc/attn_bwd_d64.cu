@@ -360,14 +360,18 @@ __global__ void __launch_bounds__(512, 1)
                         make_uint4(v[32 * c + 4 * u], v[32 * c + 4 * u + 1], v[32 * c + 4 * u + 2], v[32 * c + 4 * u + 3]);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_staged));
+            bool issued = true;
             if (r == 0) {
-                if (!(ok = mbar_wait(smem_u32(&bar_staged), tau & 1, w, SITE_BWD_DQ_FULL))) break;
-                // Rows at or beyond T lie outside the tensor map and are skipped.
-                const int h = dw.h, q0 = dw.q0();
-                tma_reduce_add_4d(&tm_dq, smem_u32(sDQ), 0, h, q0, b);
-                tma_reduce_add_4d(&tm_dq, smem_u32(sDQ + C::BT * 128), 32, h, q0, b);
-                bulk_commit_group();
+                issued = mbar_wait(smem_u32(&bar_staged), tau & 1, w, SITE_BWD_DQ_FULL);
+                if (issued) {
+                    // Rows at or beyond T lie outside the tensor map and are skipped.
+                    const int h = dw.h, q0 = dw.q0();
+                    tma_reduce_add_4d(&tm_dq, smem_u32(sDQ), 0, h, q0, b);
+                    tma_reduce_add_4d(&tm_dq, smem_u32(sDQ + C::BT * 128), 32, h, q0, b);
+                    bulk_commit_group();
+                }
             }
+            if (!(ok = __all_sync(0xffffffffu, issued))) break;   // the warp leaves the loop together
         }
         if (r == 0) bulk_wait_group0();   // the last reduces have completed before the CTA exits
         if (ovf) atomicCAS(a.err, 0, SITE_RANGE);
