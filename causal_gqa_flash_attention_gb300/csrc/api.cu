@@ -305,7 +305,8 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     void* q16 = bwd_uses_q16(f32, D) ? static_cast<char*>(ws) + wl.q16 : nullptr;
     const long long rows = (long long)B * T * Hq;
 
-    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, err};
+    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, err,
+                      ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T)};
     cudaError_t e = timed(1, st, [&] { return ne::launch_bwd_pre(f32, pa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
 
@@ -339,7 +340,8 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
 
-    ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale};
+    ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale, ne::make_fastdiv((uint32_t)Hq),
+                          ne::make_fastdiv((uint32_t)T)};
     e = timed(3, st, [&] { return ne::launch_bwd_post(f32, qa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dq epilogue launch");
     return NE_OK;
@@ -556,7 +558,8 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     // The table is rebuilt on every call: the scratch keeps whatever the last call left.
     cudaError_t e = ne::launch_rope_table(nullptr, nullptr, rope, ne::rope_table_rows(T), D, rope_theta, st);
     if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
-    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, nullptr};   // also zeroes dq_acc
+    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, nullptr,   // also zeroes dq_acc
+                      ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T)};
     e = ne::launch_bwd_pre(false, pa, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
     CUtensorMap tq, tk, tv, tdo, tdq;
@@ -585,7 +588,8 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     a.timeout_ns = timeout_ns();
     e = ne::launch_bwd(false, D, B, tq, tk, tv, tdo, tdq, a, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
-    ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale};
+    ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale, ne::make_fastdiv((uint32_t)Hq),
+                          ne::make_fastdiv((uint32_t)T)};
     e = ne::launch_bwd_post(false, qa, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dq epilogue launch");
     return NE_OK;

@@ -52,20 +52,24 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
     constexpr int ZPL = D / 4 / LPR;             // 16-byte zero stores per lane per row
     griddep_launch_dependents();
     griddep_wait();
-    const int lane = threadIdx.x & 31;
-    const int sub = lane / LPR, li = lane % LPR;
-    const long long wg = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    // Index math in 32 bits (rows * D < 2^31 is checked at the API) with the divisions
+    // by Hq and T as multiply-shifts: the 64-bit divide sequences dominated this pass's
+    // instruction count.
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t sub = lane / LPR, li = lane % LPR;
+    const uint32_t wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nw = (gridDim.x * blockDim.x) >> 5;
+    const uint32_t rows = (uint32_t)a.rows;
     const uint4* o4 = static_cast<const uint4*>(a.o);
     const uint4* g4 = static_cast<const uint4*>(a.dO);
     const bool rot = sizeof(Tin) == 2 && a.q16 != nullptr;
     bool ovf = false;
-    for (long long r0 = wg * RPW + sub; r0 - sub < a.rows; r0 += nw * RPW * U) {
+    for (uint32_t r0 = wg * RPW + sub; r0 - sub < rows; r0 += nw * RPW * U) {
         uint4 ov[U], gv[U], qv[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            const long long row = r0 + k * nw * RPW;
-            if (row < a.rows) {
+            const uint32_t row = r0 + k * nw * RPW;
+            if (row < rows) {
                 ov[k] = o4[row * LPR + li];
                 gv[k] = g4[row * LPR + li];
                 if (rot) qv[k] = static_cast<const uint4*>(a.q)[row * LPR + li];
@@ -78,9 +82,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
                 // Lane li holds elements 8li .. 8li+7 of the row: pairs 4li .. 4li+3.
 #pragma unroll
                 for (int k = 0; k < U; ++k) {
-                    const long long row = r0 + k * nw * RPW;
-                    if (row >= a.rows) continue;
-                    const int t = (int)((row / a.Hq) % a.T);
+                    const uint32_t row = r0 + k * nw * RPW;
+                    if (row >= rows) continue;
+                    const uint32_t bt = fast_div(row, a.div_hq);
+                    const uint32_t t = bt - fast_div(bt, a.div_t) * (uint32_t)a.T;
                     const float4* cs4 = reinterpret_cast<const float4*>(a.rope + (size_t)t * (D / 2) + 4 * li);
                     const float4 c01 = __ldg(cs4), c23 = __ldg(cs4 + 1);
                     const float cs[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
@@ -101,9 +106,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
         }
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            const long long row = r0 + k * nw * RPW;
-            if (row < a.rows) {
-                float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D);
+            const uint32_t row = r0 + k * nw * RPW;
+            if (row < rows) {
+                float4* z = reinterpret_cast<float4*>(a.dq_acc + (size_t)row * D);
 #pragma unroll
                 for (int e = 0; e < ZPL; ++e) z[li + e * LPR] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -128,10 +133,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
             }
 #pragma unroll
             for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            const long long row = r0 + k * nw * RPW;
-            if (row < a.rows && li == 0) {
-                const long long t = (row / a.Hq) % a.T, bh = (row / ((long long)a.Hq * a.T)) * a.Hq + row % a.Hq;
-                a.delta[bh * a.T + t] = acc;
+            const uint32_t row = r0 + k * nw * RPW;
+            if (row < rows && li == 0) {
+                const uint32_t bt = fast_div(row, a.div_hq), b = fast_div(bt, a.div_t);
+                const uint32_t h = row - bt * (uint32_t)a.Hq, t = bt - b * (uint32_t)a.T;
+                a.delta[(b * (uint32_t)a.Hq + h) * (uint32_t)a.T + t] = acc;
             }
         }
     }
@@ -147,20 +153,22 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdPostArgs a) {
     constexpr int U = 2;
     griddep_launch_dependents();
     griddep_wait();
-    const long long n = a.rows * G8;
-    const long long tg = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-    const long long nt = (long long)gridDim.x * blockDim.x;
+    // 32-bit index math (rows * D < 2^31), divisions by Hq and T as multiply-shifts.
+    const uint32_t n = (uint32_t)a.rows * G8;
+    const uint32_t tg = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t nt = gridDim.x * blockDim.x;
     const float4* acc4 = reinterpret_cast<const float4*>(a.dq_acc);
     const float4* rope4 = reinterpret_cast<const float4*>(a.rope);
-    for (long long i0 = tg; i0 < n; i0 += nt * U) {
+    for (uint32_t i0 = tg; i0 < n; i0 += nt * U) {
         float4 g[U][2], cs[U][2];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            const long long idx = i0 + k * nt;
+            const uint32_t idx = i0 + k * nt;
             if (idx < n) {
-                const long long row = idx / G8;
-                const int c8 = (int)(idx % G8);
-                const int t = (int)((row / a.Hq) % a.T);
+                const uint32_t row = idx / G8;
+                const uint32_t c8 = idx % G8;
+                const uint32_t bt = fast_div(row, a.div_hq);
+                const uint32_t t = bt - fast_div(bt, a.div_t) * (uint32_t)a.T;
                 g[k][0] = acc4[idx * 2];
                 g[k][1] = acc4[idx * 2 + 1];
                 cs[k][0] = __ldg(rope4 + (size_t)t * (D / 4) + 2 * c8);
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdPostArgs a) {
         }
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            const long long idx = i0 + k * nt;
+            const uint32_t idx = i0 + k * nt;
             if (idx >= n) continue;
             float y[8];
 #pragma unroll

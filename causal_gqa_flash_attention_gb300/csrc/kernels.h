@@ -27,6 +27,23 @@ enum WaitSite : int {
 constexpr int kRopeTableMinRows = 64;
 inline int rope_table_rows(int T) { return T > kRopeTableMinRows ? T : kRopeTableMinRows; }
 
+// Division by a runtime divisor d >= 1 of dividends below 2^31, without the divide
+// sequence: q = (n * m) >> k with k = 31 + ceil(log2 d) and m = floor(2^k / d) + 1,
+// computed once on the host.  With m d = 2^k + e, 0 < e <= d, the error n e / (d 2^k)
+// stays below 1/d for n < 2^31 (n e < 2^31 d <= 2^k), so q = floor(n / d) exactly.
+struct FastDiv {
+    uint32_t m, k;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t s = 0;
+    while ((1ull << s) < d) ++s;
+    const uint32_t k = 31 + s;
+    return FastDiv{(uint32_t)((1ull << k) / d + 1), k};
+}
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+    return (uint32_t)(((uint64_t)n * f.m) >> f.k);
+}
+
 struct FwdArgs {
     void* o;                 // [B,T,Hq,D], input dtype
     float* lse;              // [B,Hq,T]
@@ -49,6 +66,7 @@ struct BwdPreArgs {
     void* q16;               // [B,T,Hq,D] fp16 R Q, or nullptr
     const float2* rope;      // [T, D/2] (cos, sin), when q16 is set
     int* err;                // device error word (an fp16 overflow of R Q), may be null
+    FastDiv div_hq, div_t;   // by Hq and by T (row = (b T + t) Hq + h)
 };
 
 struct BwdArgs {
@@ -72,6 +90,7 @@ struct BwdPostArgs {
     long long rows;          // B*T*Hq
     int T, Hq, D;
     float scale;
+    FastDiv div_hq, div_t;   // by Hq and by T
 };
 
 // Programmatic dependent launch: every kernel of the library is launched with
