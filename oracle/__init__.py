@@ -36,15 +36,21 @@ _lock = threading.Lock()
 _lib = None
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compile one C++ source of the oracle's form into the shared library `out` with
+    g++ -O2 -fopenmp (portable flags only)."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-fopenmp", "-fPIC", "-shared", src, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle shared library with g++ -O2 -fopenmp (portable flags only)."""
+    """Compile the oracle shared library (once; again when the source is newer)."""
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["g++", "-O2", "-std=c++17", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
 
 
 def _load():
