@@ -31,7 +31,8 @@ EXPORTS = (
     "ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd_workspace_size", "ne_attn_bwd",
     "ne_attn_bwd_f32", "ne_status_string", "ne_last_error", "ne_get_device_error",
     "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown", "ne_attn_bwd_noalloc",
-    "ne_profile_enable", "ne_profile_totals",
+    "ne_profile_enable", "ne_profile_totals", "ne_attn_decode_workspace_size", "ne_attn_decode",
+    "ne_attn_decode_f32",
 )
 
 
@@ -74,8 +75,13 @@ def load(path: str | None = None):
         lib.ne_profile_totals.restype = i
         lib.ne_shutdown.argtypes = []
         lib.ne_shutdown.restype = None
+        lib.ne_attn_decode_workspace_size.argtypes = [i] * 5
+        lib.ne_attn_decode_workspace_size.restype = sz
+        lib.ne_attn_decode.argtypes = [vp] * 6 + [i] * 5 + [d, vp, sz, vp]
+        lib.ne_attn_decode_f32.argtypes = lib.ne_attn_decode.argtypes
         for f in ("ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd", "ne_attn_bwd_f32",
-                  "ne_get_device_error", "ne_selftest_wait_timeout", "ne_attn_bwd_noalloc"):
+                  "ne_get_device_error", "ne_selftest_wait_timeout", "ne_attn_bwd_noalloc", "ne_attn_decode",
+                  "ne_attn_decode_f32"):
             getattr(lib, f).restype = i
         _lib = lib
     return _lib
@@ -160,6 +166,42 @@ def attn_bwd(q, k, v, o, lse, dO, theta: float = 10000.0, workspace=None, dq=Non
               B, T, Hq, Hkv, D, float(theta), _ptr(workspace), workspace.numel() * workspace.element_size(),
               _stream(q)))
     return dq, dk, dv
+
+
+def decode_workspace_size(B, T_max, Hq, Hkv, D) -> int:
+    return int(load().ne_attn_decode_workspace_size(B, T_max, Hq, Hkv, D))
+
+
+def attn_decode(q, k_cache, v_cache, seq_lens, theta: float = 10000.0, o=None, lse=None, workspace=None):
+    """Decode step: q [B, Hq, D] is the newest token of each sequence (unrotated),
+    k_cache / v_cache [B, T_max, Hkv, D] hold positions 0 .. seq_lens[b] - 1 (the newest
+    token's key and value included), seq_lens int32 [B] on the device.  Returns
+    (o [B, Hq, D], lse [B, Hq] fp32): row seq_lens[b] - 1 of the causal attention."""
+    lib = load()
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, D] and the caches [B, T_max, Hkv, D]")
+    B, Hq, D = q.shape
+    T_max, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, T_max, Hkv, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError(f"caches must be [B, T_max, Hkv, D]; got {tuple(k_cache.shape)}, {tuple(v_cache.shape)}")
+    for t in (q, k_cache, v_cache):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("q and the caches must be contiguous CUDA tensors of one dtype")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("dtype must be bfloat16 or float32")
+    if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,) or not seq_lens.is_cuda \
+            or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous int32 CUDA tensor [B]")
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    need = decode_workspace_size(B, T_max, Hq, Hkv, D)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    fn = lib.ne_attn_decode if q.dtype == torch.bfloat16 else lib.ne_attn_decode_f32
+    _check(fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(o), _ptr(lse), B, T_max, Hq, Hkv, D,
+              float(theta), _ptr(workspace), ws_bytes, _stream(q)))
+    return o, lse
 
 
 def get_device_error(device=None) -> int:

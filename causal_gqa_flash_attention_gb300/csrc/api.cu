@@ -347,6 +347,70 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     return NE_OK;
 }
 
+// ------------------------------------------------------------------ decode
+// Decode workspace (only when the positions are cut into more than one chunk):
+// unnormalised chunk outputs fp32 [B, Hq, n_split, D], then (256-byte aligned) the
+// per-chunk (max, sum) pairs [B, Hq, n_split] float2.
+size_t decode_part_o_bytes(int B, int Hq, int D, const ne::DecodePlan& p) {
+    return round_up((size_t)B * Hq * p.n_split * D * sizeof(float), 256);
+}
+size_t decode_ws_bytes(int B, int Tmax, int Hq, int Hkv, int D) {
+    const ne::DecodePlan p = ne::decode_plan(B, Tmax, Hq, Hkv);
+    if (p.n_split <= 1) return 0;
+    return decode_part_o_bytes(B, Hq, D, p) + (size_t)B * Hq * p.n_split * sizeof(float2);
+}
+
+ne_status attn_decode_impl(bool f32, const void* q, const void* k, const void* v, const int* seq_lens, void* o,
+                           float* lse, int B, int Tmax, int Hq, int Hkv, int D, double theta, void* ws,
+                           size_t ws_bytes, cudaStream_t st) {
+    g_last_error.clear();
+    // Head, head_dim and theta rules as for the forward; the cache is indexed in 64 bits.
+    ne_status s = check_shape(B, 1, Hq, Hkv, D, theta, f32);
+    if (s != NE_OK) return s;
+    if (B > 65535) return fail(NE_ERR_INVALID_ARG, "decode needs B <= 65535 (B=%d)", B);
+    if (B == 0) return NE_OK;
+    if (Tmax < 1)
+        return fail(NE_ERR_INVALID_ARG, "decode needs T_max >= 1: the cache holds the newest token (T_max=%d)", Tmax);
+    if ((s = check_ptrs({q, k, v, o, lse})) != NE_OK) return s;
+    if (!seq_lens || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0)
+        return fail(NE_ERR_INVALID_ARG, "seq_lens must be a non-null, 4-byte aligned device pointer");
+    const size_t need = decode_ws_bytes(B, Tmax, Hq, Hkv, D);
+    if (need > 0 && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0))
+        return fail(NE_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned (%zu bytes needed)", need);
+    if (ws_bytes < need)
+        return fail(NE_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", ws_bytes, need);
+    int dev;
+    if ((s = current_device(&dev)) != NE_OK) return s;
+    int* err;
+    if ((s = error_word(dev, &err)) != NE_OK) return s;
+    const float2* rope;
+    if ((s = rope_cache(dev, Tmax, D, theta, st, &rope)) != NE_OK) return s;
+    const ne::DecodePlan p = ne::decode_plan(B, Tmax, Hq, Hkv);
+    ne::DecodeArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.seq_lens = seq_lens;
+    a.o = o;
+    a.lse = lse;
+    a.part_o = need ? static_cast<float*>(ws) : nullptr;
+    a.part_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(ws) + decode_part_o_bytes(B, Hq, D, p)) : nullptr;
+    a.rope = rope;
+    a.B = B;
+    a.Tmax = Tmax;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.n_hgrp = p.n_hgrp;
+    a.n_split = p.n_split;
+    a.chunk = p.chunk;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    a.err = err;
+    cudaError_t e = ne::launch_decode(f32, D, p, a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
+    return NE_OK;
+}
+
 // ------------------------------------------------------------------ allocation-free backward
 // Scratch of ne_attn_bwd_noalloc: a file-scope device array (every GPU that loads the
 // library holds it until the process exits).  Layout per call: RoPE table
@@ -432,6 +496,25 @@ ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const 
                          workspace_bytes, (cudaStream_t)stream);
 }
 
+size_t ne_attn_decode_workspace_size(int B, int T_max, int Hq, int Hkv, int D) {
+    if (B <= 0 || T_max <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return 0;
+    return decode_ws_bytes(B, T_max, Hq, Hkv, D);
+}
+
+ne_status ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, const int* seq_lens, void* o,
+                         float* lse, int B, int T_max, int Hq, int Hkv, int D, double rope_theta, void* workspace,
+                         size_t workspace_bytes, ne_stream_t stream) {
+    return attn_decode_impl(false, q, k_cache, v_cache, seq_lens, o, lse, B, T_max, Hq, Hkv, D, rope_theta,
+                            workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* v_cache, const int* seq_lens,
+                             float* o, float* lse, int B, int T_max, int Hq, int Hkv, int D, double rope_theta,
+                             void* workspace, size_t workspace_bytes, ne_stream_t stream) {
+    return attn_decode_impl(true, q, k_cache, v_cache, seq_lens, o, lse, B, T_max, Hq, Hkv, D, rope_theta,
+                            workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
 const char* ne_status_string(ne_status s) {
     switch (s) {
         case NE_OK: return "NE_OK";
@@ -461,6 +544,10 @@ ne_status ne_get_device_error(ne_stream_t stream) {
     if (h != 0) {
         e = cudaMemset(err, 0, sizeof(int));
         if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+        if (h == ne::SITE_DECODE_LEN)
+            return fail(NE_ERR_INVALID_ARG,
+                        "a decode call got a seq_lens entry outside [1, T_max]; it was clamped and the outputs of "
+                        "that sequence are invalid");
         if (h == ne::SITE_RANGE)
             return fail(NE_ERR_INVALID_ARG,
                         "a rotated q or k value exceeded 65504, the fp16 range of the bf16 path's logit operand; "

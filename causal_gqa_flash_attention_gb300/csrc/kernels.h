@@ -19,6 +19,8 @@ enum WaitSite : int {
     SITE_SELFTEST = 0x301,
     // Not a wait: a rotated q/k value exceeded the fp16 range of the logit operand.
     SITE_RANGE = 0x401,
+    // Not a wait: a decode call got a sequence length outside [1, T_max].
+    SITE_DECODE_LEN = 0x402,
 };
 
 // Rows of the interleaved RoPE table the kernels read: at least this many (shorter
@@ -93,6 +95,29 @@ struct BwdPostArgs {
     FastDiv div_hq, div_t;   // by Hq and by T
 };
 
+struct DecodeArgs {
+    const void* q;           // [B, Hq, D]: query row of each sequence's newest token, unrotated
+    const void* k;           // [B, Tmax, Hkv, D] key cache, unrotated
+    const void* v;           // [B, Tmax, Hkv, D] value cache
+    const int* seq_lens;     // [B]: cached positions of each sequence, newest token included
+    void* o;                 // [B, Hq, D]
+    float* lse;              // [B, Hq]
+    float* part_o;           // [B, Hq, n_split, D] unnormalised chunk outputs (n_split > 1)
+    float2* part_ml;         // [B, Hq, n_split] (running max in log2 units, sum) per chunk
+    const float2* rope;      // [>= Tmax, D/2] (cos, sin)
+    int B, Tmax, Hq, Hkv, G;
+    int n_hgrp, n_split, chunk;   // from decode_plan()
+    float scale_log2;        // log2(e) / sqrt(D)
+    int* err;
+};
+
+// Work split of a decode call: hpc query heads per CTA (a divisor of G), n_hgrp = G / hpc
+// head groups per kv head, and the positions cut into n_split chunks of `chunk` rows.
+struct DecodePlan {
+    int hpc, n_hgrp, n_split, chunk;
+};
+DecodePlan decode_plan(int B, int Tmax, int Hq, int Hkv);
+
 // Programmatic dependent launch: every kernel of the library is launched with
 // programmatic stream serialization (unless NE_ATTN_PDL=0), so it can be scheduled while
 // the previous kernel on the stream drains.  Each kernel does its on-chip set-up first,
@@ -142,5 +167,7 @@ int bwd_tf32_q_box_rows();
 cudaError_t launch_bwd_tf32(int D, int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_selftest_wait(int* err, unsigned long long timeout_ns, cudaStream_t st);
+// Decode step: the chunk kernel and, when n_split > 1, the merge of the chunks.
+cudaError_t launch_decode(bool f32, int D, const DecodePlan& p, const DecodeArgs& a, cudaStream_t st);
 
 }  // namespace ne

@@ -119,3 +119,27 @@ def make_custom(B, T, Hq, Hkv, D, dtype=torch.bfloat16, seed=1, qk_sigma=1.0):
     v = randn((B, T, Hkv, D), seed * 16 + 2, 1.0, dtype)
     dO = randn((B, T, Hq, D), seed * 16 + 3, 1.0, dtype)
     return q, k, v, dO
+
+
+def make_decode(B, T_max, Hq, Hkv, D, dtype=torch.bfloat16, seed=1, lens=None, tail=None):
+    """Inputs of one decode step: q [B, Hq, D] (each sequence's newest token), key and
+    value caches [B, T_max, Hkv, D] and seq_lens int32 [B], all on the CPU.
+
+    Lengths are ``lens`` when given, else drawn uniformly from [1, T_max] with the
+    last sequence full.  Cache rows at or past a sequence's length hold N(0, 1) values
+    like the rest (a reused cache), or ``tail`` (e.g. NaN) when given, so that a step
+    which reads them shows it."""
+    q = randn((B, Hq, D), seed * 16 + 0, 1.0, dtype)
+    k = randn((B, T_max, Hkv, D), seed * 16 + 1, 1.0, dtype)
+    v = randn((B, T_max, Hkv, D), seed * 16 + 2, 1.0, dtype)
+    if lens is None:
+        g = torch.Generator(device="cpu")
+        g.manual_seed(seed * 16 + 3)
+        lens = torch.randint(1, T_max + 1, (B,), generator=g, dtype=torch.int32)
+        lens[-1] = T_max
+    lens = torch.as_tensor(lens, dtype=torch.int32)
+    if tail is not None:
+        for b in range(B):
+            k[b, int(lens[b]):] = tail
+            v[b, int(lens[b]):] = tail
+    return q, k, v, lens

@@ -130,6 +130,39 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
                               int B, int T, int Hq, int Hkv, int D, double rope_theta,
                               ne_stream_t stream);
 
+/* Decode step over a key/value cache: the newest token of every sequence attends to
+ * all cached positions of its sequence.  For sequence b with len = seq_lens[b] the
+ * newest token sits at position len - 1, and the result is row len - 1 of the causal
+ * attention above over positions 0 .. len - 1: the same RoPE, grouped heads, scale and
+ * LSE convention.  The CUDA engine of "NanoEuler: C와 CUDA로 밑바닥부터 구축한 GPT-2 규모의
+ * LLM" (CUDA 엔진 및 성능) runs inference as well as training, and its chat command
+ * generates token by token ("NanoEuler – 순수 C/CUDA로 처음부터 만든 GPT-2 규모 언어
+ * 모델", Code Example).
+ *   q        [B, Hq, D]        query rows of the newest tokens, unrotated (in)
+ *   k_cache  [B, T_max, Hkv, D] keys, unrotated, positions 0 .. len-1 valid; the newest
+ *                              token's key must already be written at len - 1 (in)
+ *   v_cache  [B, T_max, Hkv, D] values, same positions (in)
+ *   seq_lens [B] int32         1 <= len <= T_max (device memory, 4-byte aligned) (in)
+ *   o        [B, Hq, D]        output rows, input dtype (out)
+ *   lse      [B, Hq] fp32      natural log of the softmax denominator (out)
+ * Rows at positions >= len are never read.  `workspace` holds
+ * ne_attn_decode_workspace_size() bytes (256-byte aligned, caller-owned, rewritten by
+ * every call); it may be NULL when that size is 0.  A seq_lens entry outside
+ * [1, T_max] is clamped on the device and reported by ne_get_device_error() as
+ * NE_ERR_INVALID_ARG; that sequence's outputs are then invalid.
+ * Supported: D in {64, 128} (bf16) or {32, 64} (f32), Hq % Hkv == 0, 1 <= B <= 65535,
+ * T_max >= 1; B == 0 is a no-op.  Arithmetic is fp32 throughout (no tensor cores: one
+ * query row per head is a matrix-vector product, bound by the read of the cache). */
+size_t ne_attn_decode_workspace_size(int B, int T_max, int Hq, int Hkv, int D);
+ne_status ne_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                         const int* seq_lens, void* o, float* lse, int B, int T_max, int Hq,
+                         int Hkv, int D, double rope_theta, void* workspace,
+                         size_t workspace_bytes, ne_stream_t stream);
+ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* v_cache,
+                             const int* seq_lens, float* o, float* lse, int B, int T_max,
+                             int Hq, int Hkv, int D, double rope_theta, void* workspace,
+                             size_t workspace_bytes, ne_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* ne_status_string(ne_status s);
 /* Detail of the last error on the calling thread ("" if none). */

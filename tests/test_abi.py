@@ -78,3 +78,41 @@ def test_backward_rejects_small_workspace_and_misalignment(lib):
     q = vp(4096 + 8)
     st = lib.ne_attn_bwd(q, p, p, p, p, p, p, p, p, 1, 8, 4, 2, 64, 10000.0, vp(4096), 1 << 20, vp(0))
     assert st == ne.NE_ERR_INVALID_ARG and "aligned" in lib.ne_last_error().decode()
+
+
+# ---------------------------------------------------------------- decode step
+
+def test_decode_workspace_size(lib):
+    r256 = lambda x: (x + 255) // 256 * 256
+    # One (batch, kv head) and 512 positions: the positions are cut into 8 chunks of 64,
+    # so the workspace holds 8 partial rows [D] fp32 and 8 (max, sum) pairs per query head.
+    B, T, Hq, Hkv, D = 1, 512, 4, 1, 64
+    assert lib.ne_attn_decode_workspace_size(B, T, Hq, Hkv, D) == r256(B * Hq * 8 * D * 4) + B * Hq * 8 * 8
+    # 152 sequences x 4 kv heads already give 608 CTAs: one chunk, no workspace.
+    assert lib.ne_attn_decode_workspace_size(152, 512, 12, 4, 64) == 0
+    assert lib.ne_attn_decode_workspace_size(1, 8, 3, 2, 64) == 0   # Hq % Hkv != 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((1, 8, 3, 2, 64), ne.NE_ERR_INVALID_ARG),     # Hq % Hkv
+    ((1, 8, 4, 2, 96), ne.NE_ERR_UNSUPPORTED),     # head_dim
+    ((1, 0, 4, 2, 64), ne.NE_ERR_INVALID_ARG),     # empty cache: the newest token must be in it
+    ((70000, 8, 4, 2, 64), ne.NE_ERR_INVALID_ARG), # batch beyond the grid's z extent
+])
+def test_decode_rejects_bad_shapes_before_any_device_work(lib, args, expect):
+    p = ctypes.c_void_p(4096)
+    B, T, Hq, Hkv, D = args
+    st = lib.ne_attn_decode(p, p, p, p, p, p, B, T, Hq, Hkv, D, 10000.0, p, 1 << 20, ctypes.c_void_p(0))
+    assert st == expect and lib.ne_last_error().decode() != ""
+
+
+def test_decode_rejects_bad_pointers_and_workspace(lib):
+    vp = ctypes.c_void_p
+    p, null = vp(4096), vp(0)
+    assert lib.ne_attn_decode(null, null, null, null, null, null, 0, 8, 4, 2, 64, 10000.0, null, 0, null) == ne.NE_OK
+    st = lib.ne_attn_decode(p, p, p, null, p, p, 1, 512, 4, 1, 64, 10000.0, p, 1 << 20, null)
+    assert st == ne.NE_ERR_INVALID_ARG and "seq_lens" in lib.ne_last_error().decode()
+    st = lib.ne_attn_decode(p, p, p, p, p, p, 1, 512, 4, 1, 64, 10000.0, p, 16, null)
+    assert st == ne.NE_ERR_INVALID_ARG and "workspace" in lib.ne_last_error().decode()
+    st = lib.ne_attn_decode(vp(4104), p, p, p, p, p, 1, 512, 4, 1, 64, 10000.0, p, 1 << 20, null)
+    assert st == ne.NE_ERR_INVALID_ARG and "aligned" in lib.ne_last_error().decode()
