@@ -6,6 +6,7 @@ working set is far larger than L2 and every step reads from HBM).  FLOPs per lay
 count exact causal pairs: 14 * D * T(T+1)/2 * B * Hq (4 D forward, 10 D backward).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --decode     # the decode step over a KV cache instead: cache-read GB/s
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the
 attention of independent sequences needs no exchange); the timed region is bracketed
@@ -38,6 +39,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", type=int, default=2, help="workload id (see synthetic.WORKLOADS)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--decode", action="store_true",
+                   help="time the decode step over a KV cache instead (cache-read GB/s)")
     p.add_argument("--phase-timing", choices=["timed", "separate"], default="separate",
                    help="per-kernel CUDA events inside the timed region, or (default) in as many profiled "
                         "steps right after it: events between kernels cost ~20%% and disable the overlap of "
@@ -434,10 +437,121 @@ def run_ours(args, w):
     hz.close()
 
 
+# ------------------------------------------------------------------ decode step
+DECODE_METRIC = "decode over a KV cache: cache-read GB/s (B8 T16384 Hq12/Hkv4 D64 bf16, 4 layers)"
+
+
+def run_decode(args):
+    """--decode: one decode step per layer (each sequence's newest token attends to its
+    whole cache) over 4 layers with distinct caches of 134 MB each, so a step streams
+    537 MB from HBM (more than L2).  Algorithmic bytes: the cache rows each step must
+    read (sum of lengths x Hkv x D x 2 tensors) plus q, o and lse.  The kernel time is
+    that of the chunk kernel and the merge of the chunks together (the merge moves
+    under 2% of the bytes)."""
+    import torch
+
+    import causal_gqa_flash_attention_gb300 as ne
+    from causal_gqa_flash_attention_gb300 import _build
+
+    B, T, Hq, Hkv, D, L = 8, 16384, 12, 4, 64, 4
+    hz = Harness("nccl")
+    torch.cuda.set_device(hz.local_rank)
+    dev = torch.device("cuda", hz.local_rank)
+    if hz.local_rank == 0:
+        _build.build()
+    hz.barrier()
+    ne.load()
+    from causal_gqa_flash_attention_gb300 import synthetic
+    layers, host = [], []
+    for i in range(L):
+        q, k, v, lens = synthetic.make_decode(B, T, Hq, Hkv, D, torch.bfloat16, seed=100 + i, lens=[T] * B)
+        hq = q.pin_memory()
+        host.append((hq, lens.pin_memory(), torch.empty_like(q).pin_memory(),
+                     torch.empty((B, Hq), dtype=torch.float32).pin_memory()))
+        layers.append(dict(q=q.to(dev), k=k.to(dev), v=v.to(dev), lens=lens.to(dev), o=torch.empty_like(q, device=dev),
+                           lse=torch.empty((B, Hq), dtype=torch.float32, device=dev)))
+    ws = torch.empty(max(ne.decode_workspace_size(B, T, Hq, Hkv, D), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for b in layers:
+            ne.attn_decode(b["q"], b["k"], b["v"], b["lens"], o=b["o"], lse=b["lse"], workspace=ws)
+
+    def step_e2e():
+        for b, (hq, hl, ho, hlse) in zip(layers, host):
+            b["q"].copy_(hq, non_blocking=True)
+            b["lens"].copy_(hl, non_blocking=True)
+            ne.attn_decode(b["q"], b["k"], b["v"], b["lens"], o=b["o"], lse=b["lse"], workspace=ws)
+            ho.copy_(b["o"], non_blocking=True)
+            hlse.copy_(b["lse"], non_blocking=True)
+
+    clocks = ClockSampler(hz.local_rank)
+    clocks.start()
+    clocks.wait_first()
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if ne.get_device_error() != ne.NE_OK:
+        raise RuntimeError("device error during warm-up: " + ne.last_error())
+    hz.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    hz.barrier()
+    ms = hz.max(e0.elapsed_time(e1) / args.steps, dev)
+    for _ in range(2):
+        step_e2e()
+    torch.cuda.synchronize(dev)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        step_e2e()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    e2e_ms = hz.max(g0.elapsed_time(g1) / args.steps, dev)
+    if ne.get_device_error() != ne.NE_OK:
+        raise RuntimeError("device error during timing: " + ne.last_error())
+
+    es = 2
+    per_layer = B * T * Hkv * D * es * 2 + 2 * B * Hq * D * es + B * Hq * 4
+    byts = per_layer * L * hz.world
+    value = byts / (ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    plan_ws = ne.decode_workspace_size(B, T, Hq, Hkv, D)
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": hz.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, f32 arithmetic", "data": "synthetic (seeded N(0,1) caches, every sequence full)",
+        "config": {"workload": f"decode B{B} T_max{T} Hq{Hq} Hkv{Hkv} D{D} bf16 x{L} layers", "seq_lens": T,
+                   "l2": f"inputs larger than L2: {L} distinct caches of {per_layer / 1e6:.0f} MB",
+                   "workspace_bytes": plan_ws, "parallelism": f"replicas x{hz.world}"},
+        "roofline": {"kernel": "attn_decode (chunk kernel + merge)", "bound": "hbm",
+                     "achieved": per_layer / (ms / L * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": per_layer / (ms / L * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "peak_source": f"{peaks['source']} HBM copy", "traffic": None,
+                     "per_launch_ms": ms / L, "timing": "CUDA events around the timed steps (2 launches per layer)"},
+        "e2e": {"value": byts / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": L * (B * Hq * D * es + B * 4),
+                "d2h_bytes_per_step": L * (B * Hq * D * es + B * Hq * 4), "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * L * (2 if plan_ws else 1),
+        "clocks": clk,
+    }
+    if hz.rank == 0:
+        print(json.dumps(line), flush=True)
+    hz.close()
+
+
 def main():
     args = parse()
     from causal_gqa_flash_attention_gb300 import synthetic
     w = synthetic.WORKLOADS[args.workload]
+    if args.decode and args.impl == "ours":
+        run_decode(args)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -369,8 +369,9 @@ ne_status attn_decode_impl(bool f32, const void* q, const void* k, const void* v
     if (s != NE_OK) return s;
     if (B > 65535) return fail(NE_ERR_INVALID_ARG, "decode needs B <= 65535 (B=%d)", B);
     if (B == 0) return NE_OK;
-    if (Tmax < 1)
-        return fail(NE_ERR_INVALID_ARG, "decode needs T_max >= 1: the cache holds the newest token (T_max=%d)", Tmax);
+    if (Tmax < 1 || Tmax > (1 << 30))
+        return fail(NE_ERR_INVALID_ARG, "decode needs 1 <= T_max <= 2^30: the cache holds the newest token (T_max=%d)",
+                    Tmax);
     if ((s = check_ptrs({q, k, v, o, lse})) != NE_OK) return s;
     if (!seq_lens || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0)
         return fail(NE_ERR_INVALID_ARG, "seq_lens must be a non-null, 4-byte aligned device pointer");

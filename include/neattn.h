@@ -151,7 +151,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
  * [1, T_max] is clamped on the device and reported by ne_get_device_error() as
  * NE_ERR_INVALID_ARG; that sequence's outputs are then invalid.
  * Supported: D in {64, 128} (bf16) or {32, 64} (f32), Hq % Hkv == 0, 1 <= B <= 65535,
- * T_max >= 1; B == 0 is a no-op.  Arithmetic is fp32 throughout (no tensor cores: one
+ * 1 <= T_max <= 2^30; B == 0 is a no-op.  Arithmetic is fp32 throughout (no tensor cores: one
  * query row per head is a matrix-vector product, bound by the read of the cache). */
 size_t ne_attn_decode_workspace_size(int B, int T_max, int Hq, int Hkv, int D);
 ne_status ne_attn_decode(const void* q, const void* k_cache, const void* v_cache,

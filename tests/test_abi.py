@@ -97,6 +97,7 @@ def test_decode_workspace_size(lib):
     ((1, 8, 3, 2, 64), ne.NE_ERR_INVALID_ARG),     # Hq % Hkv
     ((1, 8, 4, 2, 96), ne.NE_ERR_UNSUPPORTED),     # head_dim
     ((1, 0, 4, 2, 64), ne.NE_ERR_INVALID_ARG),     # empty cache: the newest token must be in it
+    ((1, (1 << 30) + 1, 4, 2, 64), ne.NE_ERR_INVALID_ARG),  # positions beyond 2^30
     ((70000, 8, 4, 2, 64), ne.NE_ERR_INVALID_ARG), # batch beyond the grid's z extent
 ])
 def test_decode_rejects_bad_shapes_before_any_device_work(lib, args, expect):
