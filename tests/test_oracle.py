@@ -302,3 +302,22 @@ def test_row_sampled_oracle_zero_queries_closed_form(oracle_mod):
     running = np.cumsum(v[0, :, 0], axis=0) / np.arange(1, T + 1)[:, None]
     np.testing.assert_allclose(o, running[rows], rtol=0, atol=1e-13)
     np.testing.assert_allclose(lse, np.log(np.asarray(rows) + 1.0), rtol=0, atol=1e-13)
+
+
+def test_decode_reading_is_a_row_of_the_causal_attention(oracle_mod):
+    """The decode step's reference: for a sequence of length L, the newest token's output
+    is row L-1 of the causal attention.  The row-sampled oracle on the first L positions
+    gives the full oracle's row L-1.  Positions after L-1 do not change that row, so a
+    longer cache with arbitrary later rows gives the same result."""
+    B, T, Hq, Hkv, D = 1, 50, 6, 2, 16
+    rng = np.random.default_rng(31)
+    q = rng.standard_normal((B, T, Hq, D))
+    k, v = rng.standard_normal((B, T, Hkv, D)), rng.standard_normal((B, T, Hkv, D))
+    o_full, lse_full = oracle_mod.attn_fwd(q, k, v)
+    for L in (1, 2, 17, 50):
+        o_pre, lse_pre = oracle_mod.attn_fwd(q[:, :L], k[:, :L], v[:, :L])
+        for h in range(Hq):
+            o_row, l_row, _, _ = oracle_mod.attn_qrows(q[:, :L], k[:, :L], v[:, :L], None, 0, h, [L - 1])
+            np.testing.assert_allclose(o_row[0], o_pre[0, L - 1, h], rtol=0, atol=1e-13)
+            np.testing.assert_allclose(o_row[0], o_full[0, L - 1, h], rtol=0, atol=1e-13)
+            assert abs(l_row[0] - lse_full[0, h, L - 1]) < 1e-13 and abs(lse_pre[0, h, L - 1] - l_row[0]) < 1e-13
