@@ -117,3 +117,30 @@ def test_decode_rejects_bad_pointers_and_workspace(lib):
     assert st == ne.NE_ERR_INVALID_ARG and "workspace" in lib.ne_last_error().decode()
     st = lib.ne_attn_decode(vp(4104), p, p, p, p, p, 1, 512, 4, 1, 64, 10000.0, p, 1 << 20, null)
     assert st == ne.NE_ERR_INVALID_ARG and "aligned" in lib.ne_last_error().decode()
+
+
+# ---------------------------------------------------------------- binding checks (no device work)
+
+def test_binding_rejects_host_tensors_and_bad_shapes(lib):
+    import torch
+    q = torch.zeros(1, 8, 4, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        ne.attn_fwd(q, k, k)                                   # host tensors never reach the library
+    with pytest.raises(ValueError, match="Hkv"):
+        ne.attn_fwd(q, torch.zeros(1, 9, 2, 64, dtype=torch.bfloat16), k)
+    with pytest.raises(ValueError):
+        ne.attn_fwd(q[0], k, k)                                # not [B, T, H, D]
+
+
+def test_decode_binding_rejects_bad_inputs(lib):
+    import torch
+    q = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(2, 16, 2, 64, dtype=torch.bfloat16)
+    lens = torch.tensor([16, 3], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        ne.attn_decode(q, kc, kc, lens)
+    with pytest.raises(ValueError, match="T_max"):
+        ne.attn_decode(q, kc[:1], kc[:1], lens)                # caches of another batch
+    with pytest.raises(ValueError):
+        ne.attn_decode(q.unsqueeze(1), kc, kc, lens)           # q must be [B, Hq, D]
