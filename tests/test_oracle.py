@@ -206,6 +206,29 @@ def _rope_complex(x: torch.Tensor, theta: float) -> torch.Tensor:
     return torch.view_as_real(z * rot).reshape(B, T, H, D)
 
 
+def test_rope_theta_is_a_parameter(oracle_mod):
+    """theta = 16, D = 4: the pair frequencies are 1 and 16^(-1/2) = 1/4, so the angle
+    of pair 1 is exactly 1 rad at t = 4; and attention at theta = 500 matches PyTorch's
+    fp64 attention on inputs rotated independently at theta = 500."""
+    c, s = oracle_mod.rope_table(5, 4, 16.0)
+    assert abs(c[4, 1] - math.cos(1.0)) < 1e-15 and abs(s[4, 1] - math.sin(1.0)) < 1e-15
+    assert abs(c[3, 0] - math.cos(3.0)) < 1e-15
+    B, T, Hq, Hkv, D = 1, 21, 4, 2, 8
+    gen = torch.Generator().manual_seed(41)
+    q = torch.randn(B, T, Hq, D, generator=gen, dtype=torch.float64)
+    k = torch.randn(B, T, Hkv, D, generator=gen, dtype=torch.float64)
+    v = torch.randn(B, T, Hkv, D, generator=gen, dtype=torch.float64)
+    qr, kr = _rope_complex(q, 500.0), _rope_complex(k, 500.0)
+    to_bhtd = lambda t: t.permute(0, 2, 1, 3)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        to_bhtd(qr), to_bhtd(kr.repeat_interleave(2, 2)), to_bhtd(v.repeat_interleave(2, 2)),
+        is_causal=True).permute(0, 2, 1, 3)
+    o, _ = oracle_mod.attn_fwd(q.numpy(), k.numpy(), v.numpy(), 500.0)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-11, atol=1e-12)
+    o_default, _ = oracle_mod.attn_fwd(q.numpy(), k.numpy(), v.numpy())
+    assert np.max(np.abs(o_default - o)) > 1e-3      # theta changes the result
+
+
 @pytest.mark.parametrize("shape", [(2, 33, 6, 2, 16), (1, 64, 4, 4, 32), (1, 17, 12, 4, 64)])
 def test_matches_torch_sdpa_fp64_with_autograd(oracle_mod, shape):
     B, T, Hq, Hkv, D = shape

@@ -27,6 +27,7 @@ ORACLE_DIR = os.path.join(ROOT, "oracle")
 # Pins that hold the oracle to something outside itself.
 INDEPENDENT_PINS = (
     "test_rope_table_hand_values",
+    "test_rope_theta_is_a_parameter",
     "test_rope_pairs_are_adjacent_and_rotate_counterclockwise",
     "test_rope_preserves_norms_and_depends_only_on_offset",
     "test_hand_case_two_positions_two_dims",
@@ -53,6 +54,7 @@ MUTANTS = [
     ("rope_half_split_pairs", "full",
      [("double x0 = x[2 * i], x1 = x[2 * i + 1];", "double x0 = x[i], x1 = x[i + D / 2];", 0)]),
     ("rope_positions_start_at_one", "full", [("return (double)t * std::pow", "return (double)(t + 1) * std::pow", 0)]),
+    ("rope_theta_ignored", "full", [("std::pow(theta, ", "std::pow(10000.0, ", 0)]),
     ("gradients_rotated_forward_not_back", "full",
      [("out[2 * i] = g0 * c + g1 * s;", "out[2 * i] = g0 * c - g1 * s;", 0),
       ("out[2 * i + 1] = -g0 * s + g1 * c;", "out[2 * i + 1] = g0 * s + g1 * c;", 0)]),
