@@ -84,6 +84,17 @@ def test_decode_matches_oracle(dtype, B, T, Hq, Hkv, D, lens):
     check(q, k, v, ln, dtype)
 
 
+def test_decode_other_rope_theta():
+    q, k, v, ln = synthetic.make_decode(3, 300, 12, 4, 64, torch.bfloat16, seed=41, lens=[300, 17, 1])
+    o, lse = ne.attn_decode(q.cuda(), k.cuda(), v.cuda(), ln.cuda(), 500.0)
+    torch.cuda.synchronize()
+    assert ne.get_device_error() == ne.NE_OK, ne.last_error()
+    o_ref, lse_ref = oracle_decode(q, k, v, ln, theta=500.0)
+    o = o.double().cpu().numpy()
+    assert rel(o, o_ref) <= TOL_O[torch.bfloat16]
+    assert float(np.max(np.abs(lse.double().cpu().numpy() - lse_ref))) <= TOL_LSE
+
+
 def test_decode_single_chunk_wide_batch():
     """152 sequences x 4 kv heads fill the GPU with one chunk each: no merge kernel."""
     assert ne.decode_workspace_size(152, 64, 12, 4, 64) == 0

@@ -155,11 +155,20 @@ def test_f32_small_model_workload_full_size():
 
 def test_rope_table_matches_fp64():
     import oracle
-    for T, D in ((16384, 64), (300, 128), (5, 2)):
-        c, s = ne.rope_table(T, D, 10000.0)
-        cr, sr = oracle.rope_table(T, D, 10000.0)
+    for T, D, theta in ((16384, 64, 10000.0), (300, 128, 10000.0), (5, 2, 10000.0), (1000, 64, 500.0)):
+        c, s = ne.rope_table(T, D, theta)
+        cr, sr = oracle.rope_table(T, D, theta)
         assert np.max(np.abs(f64(c) - cr)) < 1e-7
         assert np.max(np.abs(f64(s) - sr)) < 1e-7
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_other_rope_theta_matches_oracle(dtype):
+    """theta is an argument of every call: at theta = 500 the forward and backward match
+    the oracle at theta = 500 (and differ from theta = 10000 by far more than the bars)."""
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    q, k, v, dO = synthetic.make_custom(2, 200, 6, 2, 64, dt, seed=37)
+    check(q, k, v, dO, dtype, theta=500.0)
 
 
 # ---------------------------------------------------------------- error paths
