@@ -32,7 +32,7 @@ EXPORTS = (
     "ne_attn_bwd_f32", "ne_status_string", "ne_last_error", "ne_get_device_error",
     "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown", "ne_attn_bwd_noalloc",
     "ne_profile_enable", "ne_profile_totals", "ne_attn_decode_workspace_size", "ne_attn_decode",
-    "ne_attn_decode_f32",
+    "ne_attn_decode_f32", "ne_noalloc_get_device_error",
 )
 
 
@@ -69,6 +69,7 @@ def load(path: str | None = None):
         lib.ne_set_wait_timeout_ms.restype = None
         lib.ne_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         lib.ne_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 5 + [d, vp]
+        lib.ne_noalloc_get_device_error.argtypes = [vp]
         lib.ne_profile_enable.argtypes = [i]
         lib.ne_profile_enable.restype = None
         lib.ne_profile_totals.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
@@ -81,6 +82,7 @@ def load(path: str | None = None):
         lib.ne_attn_decode_f32.argtypes = lib.ne_attn_decode.argtypes
         for f in ("ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd", "ne_attn_bwd_f32",
                   "ne_get_device_error", "ne_selftest_wait_timeout", "ne_attn_bwd_noalloc", "ne_attn_decode",
+                  "ne_noalloc_get_device_error",
                   "ne_attn_decode_f32"):
             getattr(lib, f).restype = i
         _lib = lib

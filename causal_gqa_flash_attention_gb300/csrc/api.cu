@@ -412,6 +412,26 @@ ne_status attn_decode_impl(bool f32, const void* q, const void* k, const void* v
     return NE_OK;
 }
 
+// Reads a device error word (the stream that wrote it is already synchronised), clears
+// it, and maps a nonzero code to its status.
+ne_status read_and_clear(int* err) {
+    int h = 0;
+    cudaError_t e = cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (h == 0) return NE_OK;
+    e = cudaMemset(err, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    if (h == ne::SITE_DECODE_LEN)
+        return fail(NE_ERR_INVALID_ARG,
+                    "a decode call got a seq_lens entry outside [1, T_max]; it was clamped and the outputs of "
+                    "that sequence are invalid");
+    if (h == ne::SITE_RANGE)
+        return fail(NE_ERR_INVALID_ARG,
+                    "a rotated q or k value or a dS value exceeded 65504, the fp16 range of an MMA operand of "
+                    "the bf16 path; the outputs of that call are invalid");
+    return fail(NE_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel ran out (site 0x%x)", h);
+}
+
 // ------------------------------------------------------------------ allocation-free backward
 // Scratch of ne_attn_bwd_noalloc: a file-scope device array (every GPU that loads the
 // library holds it until the process exits).  Layout per call: RoPE table
@@ -419,24 +439,34 @@ ne_status attn_decode_impl(bool f32, const void* q, const void* k, const void* v
 // part starting on a 256-byte boundary.
 constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// The error word of the allocation-free calls, beside their scratch (zero at load):
+// the kernels they launch record range errors and bounded-wait timeouts here, and
+// ne_noalloc_get_device_error() reads and clears it.
+__device__ int g_noalloc_err;
 
-// Device address of g_noalloc_scratch per device ordinal.  In host code the array's
-// name is only a host-side stand-in, so the address comes from cudaGetSymbolAddress,
-// taken once per device with that device current.
+// Device addresses of g_noalloc_scratch and g_noalloc_err per device ordinal.  In host
+// code the names are only host-side stand-ins, so the addresses come from
+// cudaGetSymbolAddress, taken once per device with that device current.
 constexpr int kMaxDevices = 64;
 void* g_noalloc_ptr[kMaxDevices] = {};
+int* g_noalloc_err_ptr[kMaxDevices] = {};
 std::mutex g_noalloc_mu;
 
-ne_status noalloc_scratch(int dev, void** out) {
+ne_status noalloc_scratch(int dev, void** out, int** err_out) {
     if (dev < 0 || dev >= kMaxDevices) return fail(NE_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
         void* p = nullptr;
+        void* pe = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+        e = cudaGetSymbolAddress(&pe, g_noalloc_err);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        g_noalloc_err_ptr[dev] = static_cast<int*>(pe);
         g_noalloc_ptr[dev] = p;
     }
     *out = g_noalloc_ptr[dev];
+    *err_out = g_noalloc_err_ptr[dev];
     return NE_OK;
 }
 
@@ -539,23 +569,20 @@ ne_status ne_get_device_error(ne_stream_t stream) {
     if ((s = error_word(dev, &err)) != NE_OK) return s;
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    int h = 0;
-    e = cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
-    if (h != 0) {
-        e = cudaMemset(err, 0, sizeof(int));
-        if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
-        if (h == ne::SITE_DECODE_LEN)
-            return fail(NE_ERR_INVALID_ARG,
-                        "a decode call got a seq_lens entry outside [1, T_max]; it was clamped and the outputs of "
-                        "that sequence are invalid");
-        if (h == ne::SITE_RANGE)
-            return fail(NE_ERR_INVALID_ARG,
-                        "a rotated q or k value exceeded 65504, the fp16 range of the bf16 path's logit operand; "
-                        "the outputs of that call are invalid");
-        return fail(NE_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel ran out (site 0x%x)", h);
-    }
-    return NE_OK;
+    return read_and_clear(err);
+}
+
+ne_status ne_noalloc_get_device_error(ne_stream_t stream) {
+    g_last_error.clear();
+    int dev;
+    ne_status s = current_device(&dev);
+    if (s != NE_OK) return s;
+    void* base;
+    int* err;
+    if ((s = noalloc_scratch(dev, &base, &err)) != NE_OK) return s;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return read_and_clear(err);
 }
 
 void ne_set_wait_timeout_ms(uint32_t ms) { g_timeout_ms = ms; }
@@ -636,7 +663,8 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     int dev;
     if ((s = current_device(&dev)) != NE_OK) return s;
     void* base;
-    if ((s = noalloc_scratch(dev, &base)) != NE_OK) return s;
+    int* err;
+    if ((s = noalloc_scratch(dev, &base, &err)) != NE_OK) return s;
     float2* rope = static_cast<float2*>(base);
     float* delta = reinterpret_cast<float*>(static_cast<char*>(base) + rope_bytes);
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(base) + rope_bytes + delta_bytes);
@@ -646,7 +674,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     // The table is rebuilt on every call: the scratch keeps whatever the last call left.
     cudaError_t e = ne::launch_rope_table(nullptr, nullptr, rope, ne::rope_table_rows(T), D, rope_theta, st);
     if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
-    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, nullptr,   // also zeroes dq_acc
+    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, err,   // also zeroes dq_acc
                       ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T)};
     e = ne::launch_bwd_pre(false, pa, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
@@ -672,7 +700,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     a.n_kvt = (T + 127) / 128;
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     a.scale = (float)(1.0 / std::sqrt((double)D));
-    a.err = nullptr;            // no error word: that would need an allocation
+    a.err = err;                // the static error word of the allocation-free calls
     a.timeout_ns = timeout_ns();
     e = ne::launch_bwd(false, D, B, tq, tk, tv, tdo, tdq, a, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
             }
         }
     }
-    if (ovf && a.err) atomicCAS(a.err, 0, SITE_RANGE);   // a rotated query beyond the fp16 range
+    if (ovf) report_error(a.err, SITE_RANGE);   // a rotated query beyond the fp16 range
 }
 
 // ------------------------------------------------------------------------ post
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (it > 0 && !(ok = drain(it - 1))) break;
         }
-        if (ovf) atomicCAS(a.err, 0, SITE_RANGE);
+        if (ovf) report_error(a.err, SITE_RANGE);
     } else {
         // ------------------------------------------------------------ P^T, dS^T; dK, dV epilogue
         // Two groups share every key row: group g (warps 8-11 / 12-15) takes query columns

@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(512, 1)
             if (!(ok = __all_sync(0xffffffffu, issued))) break;   // the warp leaves the loop together
         }
         if (r == 0) bulk_wait_group0();   // the last reduces have completed before the CTA exits
-        if (ovf) atomicCAS(a.err, 0, SITE_RANGE);
+        if (ovf) report_error(a.err, SITE_RANGE);
     } else {
         // ------------------------------------------------------------ P^T, dS^T; dK, dV epilogue
         const int g = (warp - 8) >> 2;                   // warp group = half index = TMEM buffer
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(512, 1)
             if (hs + 2 < n_hs) publish(hs + 2, lv_n, dv_n);
         }
         // A dS beyond the fp16 range rounded to infinity.
-        if (fmaxf(__low2float(amax2), __high2float(amax2)) > 65504.f) atomicCAS(a.err, 0, SITE_RANGE);
+        if (fmaxf(__low2float(amax2), __high2float(amax2)) > 65504.f) report_error(a.err, SITE_RANGE);
         // Epilogue, key row r of this CTA's tile: group 0 writes dK = s R^T dK', group 1 dV.
         if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
             tc_fence_after();

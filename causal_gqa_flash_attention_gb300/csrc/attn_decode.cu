@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
 
     int len = a.seq_lens[b];
     if (len < 1 || len > a.Tmax) {        // reported, then clamped so every read stays in bounds
-        if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicCAS(a.err, 0, SITE_DECODE_LEN);
+        if (split == 0 && blockIdx.y == 0 && threadIdx.x == 0) report_error(a.err, SITE_DECODE_LEN);
         len = len < 1 ? 1 : a.Tmax;
     }
     const int j0 = split * a.chunk;

@@ -137,7 +137,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
     const float m_tile = mx * sl2;
     // An fp16 operand that overflowed (|rotated q or k| > 65504) turns logits into inf or
     // NaN; a finite row max rules that out for the whole row (masked rows are -inf).
-    if (!(fabsf(mx) < __int_as_float(0x7f800000)) && !(mx == kNegInf)) { if (w.err) atomicCAS(w.err, 0, SITE_RANGE); }
+    if (!(fabsf(mx) < __int_as_float(0x7f800000)) && !(mx == kNegInf)) report_error(w.err, SITE_RANGE);
     // A row whose max grew by more than 2^8 rescales l and its O row; the others keep
     // their max (p <= 2^8 stays exact).  TMEM access is warp-collective, so a warp
     // rescales when any lane needs it (alpha = 1 elsewhere).  O is idle once the PV of

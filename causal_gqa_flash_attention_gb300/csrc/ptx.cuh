@@ -81,8 +81,15 @@ struct WaitCtx {
     uint64_t timeout_ns;
 };
 
+// Records `code` in the device error word (first writer wins).  Every report goes
+// through here: a call may run without an error word (null), and then nothing is
+// written.
+__device__ __forceinline__ void report_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
 __device__ __forceinline__ void raise_error(const WaitCtx& w, int code) {
-    if (w.err) atomicCAS(w.err, 0, code);
+    report_error(w.err, code);
     *w.abort_smem = 1;
 }
 

@@ -122,13 +122,22 @@ ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const 
  *  - All calls share the one array, which keeps the last call's contents; every call
  *    rewrites what it reads.  Calls whose kernels overlap on the GPU (two streams, or
  *    two threads) race on the scratch and produce wrong gradients: serialise them.
- *  - The kernels still bound every internal wait, but a wait that runs out is not
- *    recorded (recording needs the allocated error word): use ne_attn_bwd when that
- *    report is wanted. */
+ *  - Device-side errors (a bounded wait that ran out, or an MMA operand beyond the
+ *    fp16 range: a rotated q or k, or dS) are recorded in a second file-scope device
+ *    word beside the scratch, not in the allocated word ne_get_device_error() reads;
+ *    read them with ne_noalloc_get_device_error(). */
 ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
                               int B, int T, int Hq, int Hkv, int D, double rope_theta,
                               ne_stream_t stream);
+/* The error report of the allocation-free calls (no counterpart on the pages).
+ * Synchronises `stream`, then reads and clears the current device's static error word
+ * of ne_attn_bwd_noalloc; allocates nothing.  Returns NE_ERR_INVALID_ARG when an MMA
+ * operand left the fp16 range (the outputs of that call are invalid),
+ * NE_ERR_DEVICE_TIMEOUT when a bounded wait ran out, NE_ERR_CUDA when the
+ * synchronisation failed, else NE_OK.  Like the scratch, the word is shared by all
+ * calls on a device. */
+ne_status ne_noalloc_get_device_error(ne_stream_t stream);
 
 /* Decode step over a key/value cache: the newest token of every sequence attends to
  * all cached positions of its sequence.  For sequence b with len = seq_lens[b] the

@@ -6,8 +6,13 @@ T x T matrices, so it computes sampled rows one by one from the same definitions
 (oracle.attn_qrows / attn_krows, pinned against the full oracle in test_oracle.py):
   - query rows at tile boundaries, the first and the last positions, for the first and the
     last batch row and every query head: O, LSE, dQ;
-  - the last key rows (the ones whose gradients the oracle can afford) for the same batch
-    rows and every kv head: dK, dV.
+  - key rows of the first key tiles (0, 1, 63, 64, 127, 128), the middle and the last
+    tiles, for the same batch rows and every kv head: dK, dV.  The first key tile is the
+    heaviest: its backward loops over every query tile of every head in the group (128
+    tiles x 3 heads at T = 16384), so it carries the longest TMEM accumulation and the
+    most barrier phases.  At T = 16384 the oracle's pass over every query row costs
+    O(T^2 D G) per (batch row, kv head), so the heavy rows are checked for the first
+    (batch, kv head) and the last one; the other kv heads keep the tail rows.
 The bound is the tolerance of the whole-tensor parity tests applied to the sampled rows:
 relative Frobenius error over all sampled rows of an output, bf16 O <= 5e-3 and
 dQ/dK/dV <= 1e-2, fp32 (TF32) 1e-3 / 2e-3; LSE max absolute error 3e-2 / 3e-3.
@@ -46,9 +51,17 @@ def query_rows(T):
     return sorted(r for r in rows if 0 <= r < T)
 
 
-def key_rows(T):
+def key_rows(T, heavy=True):
     rows = {T - 1, T - 2, T - 64, T - 65, T - 128, T - 129}
+    if heavy:
+        rows |= {0, 1, 63, 64, 127, 128, T // 2}
     return sorted(r for r in rows if 0 <= r < T)
+
+
+def heavy_key_rows(T, B, Hkv, b, g):
+    """Whether (b, g) gets the first key tiles: always up to T = 8192, else only the first
+    and the last (batch row, kv head)."""
+    return T <= 8192 or (b, g) in ((0, 0), (B - 1, Hkv - 1))
 
 
 def check_workload(w):
@@ -60,7 +73,7 @@ def check_workload(w):
     torch.cuda.synchronize()
     assert ne.get_device_error() == ne.NE_OK, ne.last_error()
     B, T, Hq, Hkv, G = w.B, w.T, w.Hq, w.Hkv, w.Hq // w.Hkv
-    qr, kr = query_rows(T), key_rows(T)
+    qr = query_rows(T)
     got = {n: [] for n in ("o", "dq", "dk", "dv")}
     ref = {n: [] for n in ("o", "dq", "dk", "dv")}
     lse_err = 0.0
@@ -73,6 +86,7 @@ def check_workload(w):
             got["dq"].append(dq_b[qr, h]); ref["dq"].append(dq_r)
             lse_err = max(lse_err, float(np.max(np.abs(lse_b[h, qr] - l_r))))
         for g in range(Hkv):
+            kr = key_rows(T, heavy_key_rows(T, B, Hkv, b, g))
             dk_r, dv_r = oracle.attn_krows(q, k, v, dO, b, g, kr, w.theta)
             got["dk"].append(dk_b[kr, g]); ref["dk"].append(dk_r)
             got["dv"].append(dv_b[kr, g]); ref["dv"].append(dv_r)

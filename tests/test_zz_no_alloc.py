@@ -48,14 +48,24 @@ def call_noalloc(lib, q, k, v, o, lse, dO, dq, dk, dv, theta=10000.0):
                                    B, T, Hq, Hkv, D, theta, st)
 
 
+def noalloc_error(lib):
+    return lib.ne_noalloc_get_device_error(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
 @pytest.mark.parametrize("shape", [(2, 300, 6, 2, 64), (1, 256, 4, 1, 128)])
 def test_noalloc_backward_matches_workspace_backward_twice(lib, shape):
+    import oracle
     B, T, Hq, Hkv, D = shape
-    q, k, v, dO = (t.cuda() for t in synthetic.make_custom(B, T, Hq, Hkv, D, torch.bfloat16, seed=31 + D))
+    qc, kc, vc, dOc = synthetic.make_custom(B, T, Hq, Hkv, D, torch.bfloat16, seed=31 + D)
+    q, k, v, dO = (t.cuda() for t in (qc, kc, vc, dOc))
     o, lse = ne.attn_fwd(q, k, v)
     dq_ref, dk_ref, dv_ref = ne.attn_bwd(q, k, v, o, lse, dO)
     torch.cuda.synchronize()
     assert ne.get_device_error() == ne.NE_OK
+    # The fp64 oracle on the same inputs: a mistake shared by both GPU entry points
+    # (the RoPE table, the preprocess pass) shows up here, not in the comparison above.
+    f = lambda t: t.double().numpy()
+    ora = dict(zip(("dq", "dk", "dv"), oracle.attn_bwd(f(qc), f(kc), f(vc), f(dOc))))
     for call in range(2):
         dq, dk, dv = torch.full_like(q, float("nan")), torch.full_like(k, float("nan")), torch.full_like(v, float("nan"))
         torch.cuda.synchronize()
@@ -63,6 +73,7 @@ def test_noalloc_backward_matches_workspace_backward_twice(lib, shape):
         alloc_before = torch.cuda.memory_allocated()
         assert call_noalloc(lib, q, k, v, o, lse, dO, dq, dk, dv) == ne.NE_OK, lib.ne_last_error()
         torch.cuda.synchronize()
+        assert noalloc_error(lib) == ne.NE_OK, lib.ne_last_error()
         # Nothing may be allocated by the call (memory freed meanwhile by torch is fine).
         if call == 1:   # the first call may still load the module holding the scratch
             assert torch.cuda.mem_get_info()[0] >= free_before
@@ -71,6 +82,26 @@ def test_noalloc_backward_matches_workspace_backward_twice(lib, shape):
             assert torch.isfinite(got).all(), (call, name)
             e = rel(got, ref)
             assert e <= GRAD_TOL, (call, name, e)
+            e = rel(got, torch.from_numpy(ora[name]))
+            assert e <= GRAD_TOL, ("oracle", call, name, e)
+
+
+def test_noalloc_backward_reports_fp16_overflow_in_its_own_error_word(lib):
+    """An upstream gradient large enough to push dS past the fp16 range of its MMA
+    operand is recorded in the allocation-free calls' own device word (the call has no
+    allocated one) and read back, then cleared, by ne_noalloc_get_device_error."""
+    q, k, v, dO = (t.cuda() for t in synthetic.make_custom(1, 96, 2, 1, 64, torch.bfloat16, seed=13))
+    o, lse = ne.attn_fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert ne.get_device_error() == ne.NE_OK
+    assert noalloc_error(lib) == ne.NE_OK
+    big = (dO * 1.0e6).contiguous()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    assert call_noalloc(lib, q, k, v, o, lse, big, dq, dk, dv) == ne.NE_OK, lib.ne_last_error()
+    assert noalloc_error(lib) == ne.NE_ERR_INVALID_ARG
+    assert "fp16" in lib.ne_last_error().decode()
+    assert noalloc_error(lib) == ne.NE_OK          # read and cleared
+    assert ne.get_device_error() == ne.NE_OK       # the allocated word was not touched
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
