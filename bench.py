@@ -34,11 +34,16 @@ METRIC = "causal GQA+RoPE attn fwd+bwd TFLOP/s (B16 T512 Hq12/Hkv4 D64 bf16), % 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", type=int, default=2, help="workload id (see synthetic.WORKLOADS)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="leave out the long-sequence sweep points and the TF32 peak measurement")
+    p.add_argument("--bare", action="store_true",
+                   help="only the warm-up and the K timed steps of one workload (layer 0 only), then a short "
+                        "line: the command profilers run")
     p.add_argument("--decode", action="store_true",
                    help="time the decode step over a KV cache instead (cache-read GB/s)")
     p.add_argument("--phase-timing", choices=["timed", "separate"], default="separate",
@@ -232,11 +237,148 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ our arm
+def tf32_peak(dev, n=8192, reps=10):
+    """Dense TF32 tensor-core throughput of this GPU, measured here: a torch fp32
+    n x n x n matmul with TF32 allowed, best of `reps` (burst), 2 n^3 FLOPs each."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn((n, n), device=dev, dtype=torch.float32)
+        b = torch.randn((n, n), device=dev, dtype=torch.float32)
+        c = torch.empty((n, n), device=dev, dtype=torch.float32)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def step_times(step, steps, stream):
+    """Runs `steps` steps with a CUDA event between consecutive steps (on the launching
+    stream) and returns the per-step milliseconds."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
+def dist_stats(ms):
+    """Median and 10th / 90th percentiles of per-step times (ms)."""
+    xs = sorted(ms)
+    q = lambda f: xs[min(len(xs) - 1, max(0, int(round(f * (len(xs) - 1)))))]
+    return {"median_ms": statistics.median(xs), "p10_ms": q(0.10), "p90_ms": q(0.90), "n": len(xs)}
+
+
+class LayerSet:
+    """Device (and pinned host) buffers of every layer of a workload: inputs, outputs
+    and one shared backward workspace, as a training step would hold them."""
+
+    def __init__(self, w, layers, dev, pinned: bool):
+        import torch
+
+        import causal_gqa_flash_attention_gb300 as ne
+        from causal_gqa_flash_attention_gb300 import synthetic
+        self.w = w
+        self.host, self.devs, self.grads_host = [], [], []
+        ws = ne.alloc_workspace(w.B, w.T, w.Hq, w.Hkv, w.D, dev)
+        for L in layers:
+            q, k, v, dO = synthetic.make_inputs(w, layer=L)
+            hq = [t.contiguous().pin_memory() if pinned else t.contiguous() for t in (q, k, v, dO)]
+            if pinned:
+                self.host.append(hq)
+            d = [t.to(dev, non_blocking=False) for t in hq]
+            o = torch.empty_like(d[0])
+            lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
+            dq, dk, dv = torch.empty_like(d[0]), torch.empty_like(d[1]), torch.empty_like(d[2])
+            self.devs.append(dict(q=d[0], k=d[1], v=d[2], dO=d[3], o=o, lse=lse, ws=ws, dq=dq, dk=dk, dv=dv))
+        if pinned:
+            self.grads_host = [[torch.empty_like(t).pin_memory() for t in (h[0], h[1], h[2])] for h in self.host]
+
+    def run_layer(self, b):
+        import causal_gqa_flash_attention_gb300 as ne
+        ne.attn_fwd(b["q"], b["k"], b["v"], self.w.theta, o=b["o"], lse=b["lse"])
+        ne.attn_bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["dO"], self.w.theta, workspace=b["ws"],
+                    dq=b["dq"], dk=b["dk"], dv=b["dv"])
+
+    def step(self):
+        for b in self.devs:
+            self.run_layer(b)
+
+    def step_l2_hot(self):
+        """The same number of layers, all on layer 0's buffers (L2-resident inputs)."""
+        for _ in self.devs:
+            self.run_layer(self.devs[0])
+
+
+def graph_step_ms(ls, stream, steps):
+    """One step captured into a CUDA graph and replayed: per-replay milliseconds."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        ls.step()                     # warm the side stream (no first-call work inside capture)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=side):
+        ls.step()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    return step_times(g.replay, steps, torch.cuda.current_stream())
+
+
+def sweep_point(wid, dev, steps, peak):
+    """TFLOP/s of one sequence-sweep workload (one layer per step, inputs resident),
+    with the per-kernel split from the library's phase timing."""
+    import torch
+
+    import causal_gqa_flash_attention_gb300 as ne
+    from causal_gqa_flash_attention_gb300 import synthetic
+    w = synthetic.WORKLOADS[wid]
+    ls = LayerSet(w, [0], dev, pinned=False)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        ls.step()
+    torch.cuda.synchronize(dev)
+    ms = step_times(ls.step, steps, stream)
+    ne.profile_enable(True)
+    for _ in range(steps):
+        ls.step()
+    ph = ne.profile_totals()
+    ne.profile_enable(False)
+    st = dist_stats(ms)
+    tf = w.flops() / (st["median_ms"] * 1e-3) / 1e12
+    avg = lambda k: ph[k][0] / ph[k][1] if ph[k][1] else None
+    out = {"workload": w.name, "tflops": tf, "pct_of_peak": tf / peak, **st,
+           "fwd_ms": avg("attn_fwd"), "bwd_main_ms": avg("attn_bwd"),
+           "fwd_tflops": w.flops_fwd() / (avg("attn_fwd") * 1e-3) / 1e12 if avg("attn_fwd") else None,
+           "bwd_main_tflops": w.flops_bwd() / (avg("attn_bwd") * 1e-3) / 1e12 if avg("attn_bwd") else None}
+    del ls
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w):
     import torch
 
     import causal_gqa_flash_attention_gb300 as ne
-    from causal_gqa_flash_attention_gb300 import _build, synthetic
+    from causal_gqa_flash_attention_gb300 import _build
 
     hz = Harness("nccl")
     torch.cuda.set_device(hz.local_rank)
@@ -246,29 +388,18 @@ def run_ours(args, w):
     hz.barrier()
     ne.load()
     layers = shard_layers(w.layers, hz.world, hz.rank)
-    dt = w.torch_dtype
+    if args.bare:
+        run_bare(args, w, dev)
+        hz.close()
+        return
 
     # Inputs resident in HBM (device arm) and pinned host copies (end-to-end arm).  The
     # backward scratch (Delta and the fp32 dQ accumulator) is one buffer for all layers,
     # as a training step would allocate it; every layer has its own inputs and outputs.
-    host, devs = [], []
-    ws = ne.alloc_workspace(w.B, w.T, w.Hq, w.Hkv, w.D, dev)
-    for L in layers:
-        q, k, v, dO = synthetic.make_inputs(w, layer=L)
-        hq = [t.contiguous().pin_memory() for t in (q, k, v, dO)]
-        host.append(hq)
-        d = [t.to(dev, non_blocking=False) for t in hq]
-        o = torch.empty_like(d[0])
-        lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
-        dq, dk, dv = torch.empty_like(d[0]), torch.empty_like(d[1]), torch.empty_like(d[2])
-        devs.append(dict(q=d[0], k=d[1], v=d[2], dO=d[3], o=o, lse=lse, ws=ws, dq=dq, dk=dk, dv=dv))
-    grads_host = [[torch.empty_like(t).pin_memory() for t in (h[0], h[1], h[2])] for h in host]
+    ls = LayerSet(w, layers, dev, pinned=True)
+    devs, host, grads_host = ls.devs, ls.host, ls.grads_host
     stream = torch.cuda.current_stream(dev)
-    def step():
-        for b in devs:
-            ne.attn_fwd(b["q"], b["k"], b["v"], w.theta, o=b["o"], lse=b["lse"])
-            ne.attn_bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["dO"], w.theta, workspace=b["ws"],
-                        dq=b["dq"], dk=b["dk"], dv=b["dv"])
+    step = ls.step
 
     # End-to-end step: every layer's inputs go host -> device on a copy stream, its
     # forward and backward run on the compute stream, and its gradients go device -> host
@@ -292,9 +423,7 @@ def run_ours(args, w):
                 ev_in[i].record(h2d_s)
             stream.wait_event(ev_in[i])
             stream.wait_event(ev_out[i])
-            ne.attn_fwd(b["q"], b["k"], b["v"], w.theta, o=b["o"], lse=b["lse"])
-            ne.attn_bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["dO"], w.theta, workspace=b["ws"],
-                        dq=b["dq"], dk=b["dk"], dv=b["dv"])
+            ls.run_layer(b)
             ev_comp[i].record(stream)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(ev_comp[i])
@@ -302,8 +431,8 @@ def run_ours(args, w):
                     h.copy_(b[name], non_blocking=True)
                 ev_out[i].record(d2h_s)
 
-    # Clocks are sampled from the warm-up through the end-to-end region, so that even a
-    # short timed region lies inside the sampled window.
+    # Clocks are sampled from the warm-up through the last extra measurement, so the
+    # timed region lies inside the sampled window.
     clocks = ClockSampler(hz.local_rank)
     clocks.start()
     clocks.wait_first()
@@ -324,14 +453,11 @@ def run_ours(args, w):
     ne.profile_enable(args.phase_timing == "timed")
     hz.barrier()
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    # The timed region: exactly K steps, one CUDA event between consecutive steps, so the
+    # per-step distribution comes from the same run as the mean.
+    per_step = step_times(step, args.steps, stream)
     hz.barrier()
-    ms_local = e0.elapsed_time(e1) / args.steps
+    ms_local = sum(per_step) / args.steps
     if args.phase_timing == "separate":
         ne.profile_enable(True)
         for _ in range(args.steps):
@@ -342,6 +468,14 @@ def run_ours(args, w):
     if ne.get_device_error() != ne.NE_OK:
         raise RuntimeError("device error during timing: " + ne.last_error())
     ms = hz.max(ms_local, dev)
+
+    # Beside the eager number: the same step replayed from a CUDA graph, and an L2-hot
+    # step whose layers all reuse layer 0's buffers (labelled: not the headline).
+    extra_steps = max(args.steps, 50)
+    graph_ms = graph_step_ms(ls, stream, extra_steps)
+    for _ in range(3):
+        ls.step_l2_hot()
+    hot_ms = step_times(ls.step_l2_hot, extra_steps, stream)
 
     # End-to-end: host buffers, H2D of the inputs and D2H of the gradients inside the step.
     for _ in range(2):
@@ -360,8 +494,17 @@ def run_ours(args, w):
     g1.record(stream)
     torch.cuda.synchronize(dev)
     hz.barrier()
-    clk = clocks.stop()
     e2e_ms = hz.max(g0.elapsed_time(g1) / e2, dev)
+
+    peaks = measured_peaks()
+    tf32 = tf32_peak(dev) if w.dtype == "f32" or not args.no_sweep else None
+    # The sequence-length sweep points at T >= 2048 (one layer per step, resident inputs)
+    # ride along in the default line so that a long-sequence number exists for every run.
+    sweep = {}
+    if not args.no_sweep and w.wid == 2:
+        for wid in (52, 53, 54):
+            sweep[f"T{synthetic_T(wid)}"] = sweep_point(wid, dev, 10, peaks["bf16_tflops"])
+    clk = clocks.stop()
 
     flops_step = w.flops() * len(layers)
     total_flops = flops_step * hz.world
@@ -371,12 +514,14 @@ def run_ours(args, w):
     h2d = sum(t.numel() * es for h in host for t in h)
     d2h = sum(t.numel() * es for g in grads_host for t in g)
 
-    peaks = measured_peaks()
+    # The peak of the path's own dtype: bf16 for bf16 tensors, the TF32 rate measured
+    # above for fp32 tensors (they run on TF32 tensor cores).
+    peak = peaks["bf16_tflops"] if w.dtype == "bf16" else tf32
+    peak_name = "bf16 burst" if w.dtype == "bf16" else "tf32 burst (torch fp32 matmul 8192^3, TF32 on, measured here)"
     # Per-kernel averages over the timed region; the dominant kernel is the one with the
     # largest share.  Algorithmic FLOPs per launch: forward 4 D P, backward main 10 D P
     # with P = T(T+1)/2 B Hq; bytes per launch (HBM-bound preprocess/epilogue) from
     # compulsory_bytes().
-    peak = peaks["bf16_tflops"]
     avg = {k: (v[0] / v[1] if v[1] else 0.0) for k, v in phases.items()}
     total = sum(v[0] for v in phases.values()) or 1.0
     share = {k: v[0] / total for k, v in phases.items()}
@@ -397,6 +542,8 @@ def run_ours(args, w):
                      if avg["bwd_post"] else None, "unit": "GB/s"},
     }
     kernels = {k: v for k, v in kernels.items() if phases[k][1]}   # the kernels this path launches
+    for k in kernels:
+        kernels[k]["launches"] = phases[k][1]
     dom = max(kernels, key=lambda k: kernels[k]["share"])
     dk = kernels[dom]
     dom_peak = peak if dk["unit"] == "TFLOP/s" else peaks["hbm_gbs"]
@@ -404,6 +551,8 @@ def run_ours(args, w):
         ("attn_bwd_tf32.cu" if w.dtype == "f32" else "attn_bwd.cu")
     src = {"attn_fwd": "attn_fwd.cu", "attn_bwd": bwd_main_src, "bwd_pre": "attn_bwd.cu", "bwd_post": "attn_bwd.cu"}[dom]
     traffic = profiled_traffic(os.path.join(ROOT, "causal_gqa_flash_attention_gb300", "csrc", src), f"{dom}:{w.name}")
+    st = dist_stats(per_step)
+    gst, hst = dist_stats(graph_ms), dist_stats(hot_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": hz.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -415,14 +564,26 @@ def run_ours(args, w):
                          f"one shared backward workspace",
                    "parallelism": f"replicas x{hz.world}"},
         "pct_of_peak": value / hz.world / peak,
+        "timing": {
+            "eager": {**st, "tflops_at_median": flops_step / (st["median_ms"] * 1e-3) / 1e12,
+                      "what": "the timed region: per-step CUDA events, layer-distinct buffers"},
+            "graph": {**gst, "tflops_at_median": flops_step / (gst["median_ms"] * 1e-3) / 1e12,
+                      "what": "one step captured in a CUDA graph, replayed"},
+            "l2_hot": {**hst, "tflops_at_median": flops_step / (hst["median_ms"] * 1e-3) / 1e12,
+                       "what": "L2-HOT, not the headline: every layer on layer 0's buffers"},
+        },
         "roofline": {"kernel": dom, "bound": dk["bound"], "achieved": dk["achieved"], "peak": dom_peak,
                      "unit": dk["unit"], "frac": dk["achieved"] / dom_peak,
-                     "peak_source": f"{peaks['source']} " + ("bf16 burst" if dk["unit"] == "TFLOP/s" else "HBM copy"),
+                     "peak_source": (f"{peaks['source']} " + peak_name) if dk["unit"] == "TFLOP/s"
+                     else f"{peaks['source']} HBM copy",
                      "traffic": traffic, "per_launch_ms": dk["ms"],
                      "timing": ("CUDA events around every launch over the timed region" if args.phase_timing == "timed"
                                 else f"CUDA events around every launch over {args.steps} steps run right after "
                                      "the timed region (same work, same stream)")},
         "kernels": kernels,
+        "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "tf32_tflops_measured": tf32,
+                  "source": peaks["source"]},
+        "sweep": sweep,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": sum(v[1] for v in phases.values()),
@@ -435,6 +596,29 @@ def run_ours(args, w):
     if hz.rank == 0:
         print(json.dumps(line), flush=True)
     hz.close()
+
+
+def run_bare(args, w, dev):
+    """--bare: warm-up, then K steps of layer 0 of the workload, and one short line.
+    This is the command the ncu captures run (few launches, nothing else)."""
+    import torch
+
+    import causal_gqa_flash_attention_gb300 as ne
+    ls = LayerSet(w, [0], dev, pinned=False)
+    for _ in range(args.warmup):
+        ls.step()
+    torch.cuda.synchronize(dev)
+    ms = step_times(ls.step, args.steps, torch.cuda.current_stream(dev))
+    if ne.get_device_error() != ne.NE_OK:
+        raise RuntimeError("device error: " + ne.last_error())
+    st = dist_stats(ms)
+    print(json.dumps({"bare": True, "workload": w.name, **st,
+                      "tflops_at_median": w.flops() / (st["median_ms"] * 1e-3) / 1e12}), flush=True)
+
+
+def synthetic_T(wid):
+    from causal_gqa_flash_attention_gb300 import synthetic
+    return synthetic.WORKLOADS[wid].T
 
 
 # ------------------------------------------------------------------ decode step
