@@ -263,6 +263,14 @@ def tf32_peak(dev, n=8192, reps=10):
         torch.backends.cuda.matmul.allow_tf32 = prev
 
 
+def kernel_work(w):
+    """Algorithmic FLOPs per launch of each tensor-core kernel, P = T(T+1)/2 B Hq causal
+    pairs: the forward 4 D P, the backward main kernel 10 D P (S recomputed, dP, dV, dK,
+    dQ)."""
+    P = w.pairs * w.B * w.Hq
+    return {"attn_fwd": 4 * w.D * P, "attn_bwd": 10 * w.D * P}
+
+
 def step_times(step, steps, stream):
     """Runs `steps` steps with a CUDA event between consecutive steps (on the launching
     stream) and returns the per-step milliseconds."""
@@ -365,10 +373,12 @@ def sweep_point(wid, dev, steps, peak):
     st = dist_stats(ms)
     tf = w.flops() / (st["median_ms"] * 1e-3) / 1e12
     avg = lambda k: ph[k][0] / ph[k][1] if ph[k][1] else None
+    kw = kernel_work(w)
+    tfl = lambda k: kw[k] / (avg(k) * 1e-3) / 1e12 if avg(k) else None
     out = {"workload": w.name, "tflops": tf, "pct_of_peak": tf / peak, **st,
            "fwd_ms": avg("attn_fwd"), "bwd_main_ms": avg("attn_bwd"),
-           "fwd_tflops": w.flops_fwd() / (avg("attn_fwd") * 1e-3) / 1e12 if avg("attn_fwd") else None,
-           "bwd_main_tflops": w.flops_bwd() / (avg("attn_bwd") * 1e-3) / 1e12 if avg("attn_bwd") else None}
+           "bwd_pre_ms": avg("bwd_pre"), "bwd_post_ms": avg("bwd_post"),
+           "fwd_tflops": tfl("attn_fwd"), "bwd_main_tflops": tfl("attn_bwd")}
     del ls
     torch.cuda.empty_cache()
     return out
@@ -527,13 +537,13 @@ def run_ours(args, w):
     share = {k: v[0] / total for k, v in phases.items()}
     cb = w.compulsory_bytes()
     acc_bytes = w.B * w.T * w.Hq * w.D * 4
+    kw = kernel_work(w)
+    tfl = lambda k: kw[k] / (avg[k] * 1e-3) / 1e12 if avg[k] else None
     kernels = {
         "attn_fwd": {"ms": avg["attn_fwd"], "share": share["attn_fwd"], "bound": "tensor",
-                     "achieved": w.flops_fwd() / (avg["attn_fwd"] * 1e-3) / 1e12 if avg["attn_fwd"] else None,
-                     "unit": "TFLOP/s"},
+                     "achieved": tfl("attn_fwd"), "unit": "TFLOP/s"},
         "attn_bwd": {"ms": avg["attn_bwd"], "share": share["attn_bwd"], "bound": "tensor",
-                     "achieved": w.flops_bwd() / (avg["attn_bwd"] * 1e-3) / 1e12 if avg["attn_bwd"] else None,
-                     "unit": "TFLOP/s"},
+                     "achieved": tfl("attn_bwd"), "unit": "TFLOP/s"},
         "bwd_pre": {"ms": avg["bwd_pre"], "share": share["bwd_pre"], "bound": "hbm",
                     "achieved": (cb["pre"] + acc_bytes) / (avg["bwd_pre"] * 1e-3) / 1e9 if avg["bwd_pre"] else None,
                     "unit": "GB/s"},
@@ -609,11 +619,18 @@ def run_bare(args, w, dev):
         ls.step()
     torch.cuda.synchronize(dev)
     ms = step_times(ls.step, args.steps, torch.cuda.current_stream(dev))
+    ne.profile_enable(True)
+    for _ in range(args.steps):
+        ls.step()
+    ph = ne.profile_totals()
+    ne.profile_enable(False)
     if ne.get_device_error() != ne.NE_OK:
         raise RuntimeError("device error: " + ne.last_error())
     st = dist_stats(ms)
+    per_kernel = {k: v[0] / v[1] for k, v in ph.items() if v[1]}
     print(json.dumps({"bare": True, "workload": w.name, **st,
-                      "tflops_at_median": w.flops() / (st["median_ms"] * 1e-3) / 1e12}), flush=True)
+                      "tflops_at_median": w.flops() / (st["median_ms"] * 1e-3) / 1e12,
+                      "kernel_ms": per_kernel}), flush=True)
 
 
 def synthetic_T(wid):
