@@ -32,7 +32,8 @@ EXPORTS = (
     "ne_attn_bwd_f32", "ne_status_string", "ne_last_error", "ne_get_device_error",
     "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown", "ne_attn_bwd_noalloc",
     "ne_profile_enable", "ne_profile_totals", "ne_attn_decode_workspace_size", "ne_attn_decode",
-    "ne_attn_decode_f32", "ne_noalloc_get_device_error",
+    "ne_attn_decode_f32", "ne_noalloc_get_device_error", "ne_attn_fwd_varlen", "ne_attn_fwd_varlen_f32",
+    "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32",
 )
 
 
@@ -69,6 +70,10 @@ def load(path: str | None = None):
         lib.ne_set_wait_timeout_ms.restype = None
         lib.ne_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         lib.ne_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 5 + [d, vp]
+        lib.ne_attn_fwd_varlen.argtypes = [vp] * 6 + [i] * 5 + [d, vp]
+        lib.ne_attn_fwd_varlen_f32.argtypes = lib.ne_attn_fwd_varlen.argtypes
+        lib.ne_attn_bwd_varlen.argtypes = [vp] * 10 + [i] * 5 + [d, vp, sz, vp]
+        lib.ne_attn_bwd_varlen_f32.argtypes = lib.ne_attn_bwd_varlen.argtypes
         lib.ne_noalloc_get_device_error.argtypes = [vp]
         lib.ne_profile_enable.argtypes = [i]
         lib.ne_profile_enable.restype = None
@@ -82,7 +87,8 @@ def load(path: str | None = None):
         lib.ne_attn_decode_f32.argtypes = lib.ne_attn_decode.argtypes
         for f in ("ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd", "ne_attn_bwd_f32",
                   "ne_get_device_error", "ne_selftest_wait_timeout", "ne_attn_bwd_noalloc", "ne_attn_decode",
-                  "ne_noalloc_get_device_error",
+                  "ne_noalloc_get_device_error", "ne_attn_fwd_varlen", "ne_attn_fwd_varlen_f32",
+                  "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32",
                   "ne_attn_decode_f32"):
             getattr(lib, f).restype = i
         _lib = lib
@@ -140,6 +146,28 @@ def attn_fwd(q, k, v, theta: float = 10000.0, o=None, lse=None):
     return o, lse
 
 
+def _check_lens(seq_lens, B, device):
+    if seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,) or not seq_lens.is_cuda \
+            or not seq_lens.is_contiguous() or seq_lens.device != device:
+        raise ValueError("seq_lens must be a contiguous int32 CUDA tensor [B] on the tensors' device")
+
+
+def attn_fwd_varlen(q, k, v, seq_lens, theta: float = 10000.0, o=None, lse=None):
+    """Forward over a padded batch of sequences of lengths seq_lens (int32 [B] on the
+    device): returns (o, lse); padding rows get o = 0 and lse = -inf."""
+    lib = load()
+    B, T, Hq, Hkv, D = _dims(q, k, v)
+    _check_lens(seq_lens, B, q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    fn = lib.ne_attn_fwd_varlen if q.dtype == torch.bfloat16 else lib.ne_attn_fwd_varlen_f32
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), _ptr(o), _ptr(lse), B, T, Hq, Hkv, D, float(theta),
+              _stream(q)))
+    return o, lse
+
+
 def workspace_size(B, T, Hq, Hkv, D) -> int:
     return int(load().ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D))
 
@@ -165,6 +193,30 @@ def attn_bwd(q, k, v, o, lse, dO, theta: float = 10000.0, workspace=None, dq=Non
     dv = torch.empty_like(v) if dv is None else dv
     fn = lib.ne_attn_bwd if q.dtype == torch.bfloat16 else lib.ne_attn_bwd_f32
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+              B, T, Hq, Hkv, D, float(theta), _ptr(workspace), workspace.numel() * workspace.element_size(),
+              _stream(q)))
+    return dq, dk, dv
+
+
+def attn_bwd_varlen(q, k, v, o, lse, dO, seq_lens, theta: float = 10000.0, workspace=None, dq=None, dk=None,
+                    dv=None):
+    """Backward over a padded batch (see attn_fwd_varlen): returns (dq, dk, dv); padding
+    positions get zero gradients."""
+    lib = load()
+    B, T, Hq, Hkv, D = _dims(q, k, v)
+    _check_lens(seq_lens, B, q.device)
+    for t in (o, dO):
+        if tuple(t.shape) != tuple(q.shape) or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("o and dO must match q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, T) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, Hq, T]")
+    if workspace is None:
+        workspace = alloc_workspace(B, T, Hq, Hkv, D, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    fn = lib.ne_attn_bwd_varlen if q.dtype == torch.bfloat16 else lib.ne_attn_bwd_varlen_f32
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(seq_lens), _ptr(dq), _ptr(dk), _ptr(dv),
               B, T, Hq, Hkv, D, float(theta), _ptr(workspace), workspace.numel() * workspace.element_size(),
               _stream(q)))
     return dq, dk, dv

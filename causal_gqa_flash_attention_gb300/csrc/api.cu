@@ -37,7 +37,7 @@ ne_status cuda_fail(cudaError_t e, const char* what) {
 // ------------------------------------------------------------------ per-device state
 struct DeviceState {
     int* err_word = nullptr;                                           // device int
-    std::map<std::tuple<int, int, uint64_t>, float2*> rope;            // (T, D, theta bits)
+    std::map<std::tuple<int, int, int, uint64_t>, float2*> rope;       // (T, D, pairs per row, theta bits)
 };
 
 std::mutex g_mu;
@@ -80,12 +80,14 @@ ne_status error_word(int dev, int** out) {
     return NE_OK;
 }
 
-// Cached interleaved (cos, sin) table [T, D/2] for the current device.  Built on
-// `st` by the rope kernel the first time; that first build synchronises `st`.
-ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const float2** out) {
+// Cached interleaved (cos, sin) table [T, ld] (ld >= D/2 pairs per row; pairs past D/2
+// hold angle 0) for the current device.  Built on `st` by the rope kernel the first
+// time; that first build synchronises `st`.
+ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const float2** out, int ld = 0) {
+    if (ld < D / 2) ld = D / 2;
     uint64_t tb;
     std::memcpy(&tb, &theta, sizeof(tb));
-    const auto key = std::make_tuple(T, D, tb);
+    const auto key = std::make_tuple(T, D, ld, tb);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto& m = g_dev[dev].rope;
@@ -103,10 +105,10 @@ ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const
                     T, D, theta);
     float2* buf = nullptr;
     const int rows = ne::rope_table_rows(T);
-    size_t bytes = (size_t)rows * (D / 2) * sizeof(float2);
+    size_t bytes = (size_t)rows * ld * sizeof(float2);
     cudaError_t e = cudaMalloc(&buf, bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(rope table)");
-    e = ne::launch_rope_table(nullptr, nullptr, buf, rows, D, theta, st);
+    e = ne::launch_rope_table(nullptr, nullptr, buf, rows, D, theta, st, ld);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         cudaFree(buf);
@@ -207,9 +209,9 @@ ne_status check_shape(int B, int T, int Hq, int Hkv, int D, double theta, bool f
         return fail(NE_ERR_INVALID_ARG, "need Hq > 0, Hkv > 0 and Hq %% Hkv == 0 (Hq=%d Hkv=%d)", Hq, Hkv);
     if (!(theta > 0.0) || !std::isfinite(theta)) return fail(NE_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
     if (D <= 0 || D % 2 != 0) return fail(NE_ERR_INVALID_ARG, "D must be even and > 0 (D=%d)", D);
-    if (f32 ? (D != 32 && D != 64) : (D != 64 && D != 128))
+    if (f32 ? (D != 32 && D != 64) : (D != 32 && D != 64 && D != 128))
         return fail(NE_ERR_UNSUPPORTED, "head_dim D=%d is not supported for %s (supported: %s)", D,
-                    f32 ? "f32" : "bf16", f32 ? "32, 64" : "64, 128");
+                    f32 ? "f32" : "bf16", f32 ? "32, 64" : "32, 64, 128");
     const long long elems = (long long)B * T * Hq * D;
     if (elems >= (1LL << 31)) return fail(NE_ERR_INVALID_ARG, "B*T*Hq*D must be < 2^31");
     return NE_OK;
@@ -240,22 +242,35 @@ BwdWs bwd_ws_layout(int B, int T, int Hq, int D) {
 }
 size_t bwd_ws_bytes(int B, int T, int Hq, int D) { return bwd_ws_layout(B, T, Hq, D).total; }
 // The bf16 head_dim-64 kernel reads Q rotated ahead of time by the preprocess kernel.
-bool bwd_uses_q16(bool f32, int D) { return !f32 && D == 64; }
+bool bwd_uses_q16(bool f32, int D) { return !f32 && D <= 64; }
+// bf16 head_dim 32 runs on the 64-wide kernels with the upper 32 columns zero (128-byte
+// TMA boxes over 64-byte rows read zeros there and clip stores); their RoPE table has
+// 32 (cos, sin) pairs per row, the last 16 at angle 0.
+int rope_ld(bool f32, int D) { return !f32 && D == 32 ? 32 : D / 2; }
 
 // ------------------------------------------------------------------ forward / backward
+// Per-sequence lengths of a variable-length call: a device int32 array [B], 4-byte aligned.
+ne_status check_seq_lens(const int* seq_lens) {
+    if (!seq_lens || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0)
+        return fail(NE_ERR_INVALID_ARG, "seq_lens must be a non-null, 4-byte aligned device pointer");
+    return NE_OK;
+}
+
+// seq_lens: null, or (variable-length calls) the device lengths [B] of the sequences.
 ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
-                        int Hq, int Hkv, int D, double theta, cudaStream_t st) {
+                        int Hq, int Hkv, int D, double theta, const int* seq_lens, bool varlen, cudaStream_t st) {
     g_last_error.clear();
     ne_status s = check_shape(B, T, Hq, Hkv, D, theta, f32);
     if (s != NE_OK) return s;
     if (B == 0 || T == 0) return NE_OK;
     if ((s = check_ptrs({q, k, v, o, lse})) != NE_OK) return s;
+    if (varlen && (s = check_seq_lens(seq_lens)) != NE_OK) return s;
     int dev;
     if ((s = current_device(&dev)) != NE_OK) return s;
     int* err;
     if ((s = error_word(dev, &err)) != NE_OK) return s;
     const float2* rope;
-    if ((s = rope_cache(dev, T, D, theta, st, &rope)) != NE_OK) return s;
+    if ((s = rope_cache(dev, T, D, theta, st, &rope, rope_ld(f32, D))) != NE_OK) return s;
     CUtensorMap tq, tk, tv, to;
     const int kv_rows = ne::fwd_kv_box_rows(f32, D);
     if ((s = map_bthd(&tq, q, f32, B, T, Hq, D, 128)) != NE_OK) return s;
@@ -275,6 +290,8 @@ ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, v
     a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     a.err = err;
     a.timeout_ns = timeout_ns();
+    a.seq_lens = seq_lens;
+    a.dr = D;
     cudaError_t e = timed(0, st, [&] { return ne::launch_fwd(f32, D, B, tq, tk, tv, to, a, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
     return NE_OK;
@@ -282,12 +299,13 @@ ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, v
 
 ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, const void* o, const float* lse,
                         const void* dO, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
-                        double theta, void* ws, size_t ws_bytes, cudaStream_t st) {
+                        double theta, void* ws, size_t ws_bytes, const int* seq_lens, bool varlen, cudaStream_t st) {
     g_last_error.clear();
     ne_status s = check_shape(B, T, Hq, Hkv, D, theta, f32);
     if (s != NE_OK) return s;
     if (B == 0 || T == 0) return NE_OK;
     if ((s = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv})) != NE_OK) return s;
+    if (varlen && (s = check_seq_lens(seq_lens)) != NE_OK) return s;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
         return fail(NE_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
     const size_t need = bwd_ws_bytes(B, T, Hq, D);
@@ -298,7 +316,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     int* err;
     if ((s = error_word(dev, &err)) != NE_OK) return s;
     const float2* rope;
-    if ((s = rope_cache(dev, T, D, theta, st, &rope)) != NE_OK) return s;
+    if ((s = rope_cache(dev, T, D, theta, st, &rope, rope_ld(f32, D))) != NE_OK) return s;
     const BwdWs wl = bwd_ws_layout(B, T, Hq, D);
     float* delta = static_cast<float*>(ws);
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.acc);
@@ -306,7 +324,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     const long long rows = (long long)B * T * Hq;
 
     ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, err,
-                      ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T)};
+                      ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T), seq_lens, rope_ld(f32, D)};
     cudaError_t e = timed(1, st, [&] { return ne::launch_bwd_pre(f32, pa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
 
@@ -317,7 +335,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     if ((s = map_bthd(&tv, v, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tdo, dO, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
     std::memset(&tdq, 0, sizeof(tdq));
-    if (!f32 && D == 64 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
+    if (!f32 && D <= 64 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
     ne::BwdArgs a;
     a.lse = lse;
     a.delta = delta;
@@ -334,6 +352,8 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     a.scale = (float)(1.0 / std::sqrt((double)D));
     a.err = err;
     a.timeout_ns = timeout_ns();
+    a.seq_lens = seq_lens;
+    a.dr = D;
     e = timed(2, st, [&] {
         return f32 ? ne::launch_bwd_tf32(D, B, tq, tk, tv, tdo, a, st)
                    : ne::launch_bwd(f32, D, B, tq, tk, tv, tdo, tdq, a, st);
@@ -341,7 +361,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
 
     ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale, ne::make_fastdiv((uint32_t)Hq),
-                          ne::make_fastdiv((uint32_t)T)};
+                          ne::make_fastdiv((uint32_t)T), rope_ld(f32, D)};
     e = timed(3, st, [&] { return ne::launch_bwd_post(f32, qa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dq epilogue launch");
     return NE_OK;
@@ -367,6 +387,8 @@ ne_status attn_decode_impl(bool f32, const void* q, const void* k, const void* v
     // Head, head_dim and theta rules as for the forward; the cache is indexed in 64 bits.
     ne_status s = check_shape(B, 1, Hq, Hkv, D, theta, f32);
     if (s != NE_OK) return s;
+    if (!f32 && D == 32)
+        return fail(NE_ERR_UNSUPPORTED, "decode supports head_dim 64 and 128 for bf16 (32 and 64 for f32)");
     if (B > 65535) return fail(NE_ERR_INVALID_ARG, "decode needs B <= 65535 (B=%d)", B);
     if (B == 0) return NE_OK;
     if (Tmax < 1 || Tmax > (1 << 30))
@@ -424,6 +446,10 @@ ne_status read_and_clear(int* err) {
     if (h == ne::SITE_DECODE_LEN)
         return fail(NE_ERR_INVALID_ARG,
                     "a decode call got a seq_lens entry outside [1, T_max]; it was clamped and the outputs of "
+                    "that sequence are invalid");
+    if (h == ne::SITE_VARLEN_LEN)
+        return fail(NE_ERR_INVALID_ARG,
+                    "a variable-length call got a seq_lens entry outside [0, T]; it was clamped and the outputs of "
                     "that sequence are invalid");
     if (h == ne::SITE_RANGE)
         return fail(NE_ERR_INVALID_ARG,
@@ -500,12 +526,12 @@ ne_status ne_rope_table(float* cos_out, float* sin_out, int T, int D, double the
 
 ne_status ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
                       int Hkv, int D, double rope_theta, ne_stream_t stream) {
-    return attn_fwd_impl(false, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, (cudaStream_t)stream);
+    return attn_fwd_impl(false, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, nullptr, false, (cudaStream_t)stream);
 }
 
 ne_status ne_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int T,
                           int Hq, int Hkv, int D, double rope_theta, ne_stream_t stream) {
-    return attn_fwd_impl(true, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, (cudaStream_t)stream);
+    return attn_fwd_impl(true, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, nullptr, false, (cudaStream_t)stream);
 }
 
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D) {
@@ -517,14 +543,41 @@ ne_status ne_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D, double rope_theta,
                       void* workspace, size_t workspace_bytes, ne_stream_t stream) {
     return attn_bwd_impl(false, q, k, v, o, lse, dO, dq, dk, dv, B, T, Hq, Hkv, D, rope_theta, workspace,
-                         workspace_bytes, (cudaStream_t)stream);
+                         workspace_bytes, nullptr, false, (cudaStream_t)stream);
 }
 
 ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const float* o, const float* lse,
                           const float* dO, float* dq, float* dk, float* dv, int B, int T, int Hq, int Hkv, int D,
                           double rope_theta, void* workspace, size_t workspace_bytes, ne_stream_t stream) {
     return attn_bwd_impl(true, q, k, v, o, lse, dO, dq, dk, dv, B, T, Hq, Hkv, D, rope_theta, workspace,
-                         workspace_bytes, (cudaStream_t)stream);
+                         workspace_bytes, nullptr, false, (cudaStream_t)stream);
+}
+
+ne_status ne_attn_fwd_varlen(const void* q, const void* k, const void* v, const int* seq_lens, void* o, float* lse,
+                             int B, int T, int Hq, int Hkv, int D, double rope_theta, ne_stream_t stream) {
+    return attn_fwd_impl(false, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, seq_lens, true, (cudaStream_t)stream);
+}
+
+ne_status ne_attn_fwd_varlen_f32(const float* q, const float* k, const float* v, const int* seq_lens, float* o,
+                                 float* lse, int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                                 ne_stream_t stream) {
+    return attn_fwd_impl(true, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, seq_lens, true, (cudaStream_t)stream);
+}
+
+ne_status ne_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dO, const int* seq_lens, void* dq, void* dk, void* dv, int B, int T, int Hq,
+                             int Hkv, int D, double rope_theta, void* workspace, size_t workspace_bytes,
+                             ne_stream_t stream) {
+    return attn_bwd_impl(false, q, k, v, o, lse, dO, dq, dk, dv, B, T, Hq, Hkv, D, rope_theta, workspace,
+                         workspace_bytes, seq_lens, true, (cudaStream_t)stream);
+}
+
+ne_status ne_attn_bwd_varlen_f32(const float* q, const float* k, const float* v, const float* o, const float* lse,
+                                 const float* dO, const int* seq_lens, float* dq, float* dk, float* dv, int B, int T,
+                                 int Hq, int Hkv, int D, double rope_theta, void* workspace, size_t workspace_bytes,
+                                 ne_stream_t stream) {
+    return attn_bwd_impl(true, q, k, v, o, lse, dO, dq, dk, dv, B, T, Hq, Hkv, D, rope_theta, workspace,
+                         workspace_bytes, seq_lens, true, (cudaStream_t)stream);
 }
 
 size_t ne_attn_decode_workspace_size(int B, int T_max, int Hq, int Hkv, int D) {
@@ -651,7 +704,8 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     if (s != NE_OK) return s;
     if (B == 0 || T == 0) return NE_OK;
     if ((s = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv})) != NE_OK) return s;
-    const size_t rope_bytes = round_up((size_t)ne::rope_table_rows(T) * (D / 2) * sizeof(float2), 256);
+    const int ld = rope_ld(false, D);
+    const size_t rope_bytes = round_up((size_t)ne::rope_table_rows(T) * ld * sizeof(float2), 256);
     const size_t delta_bytes = round_up((size_t)B * Hq * T * sizeof(float), 256);
     const size_t acc_bytes = round_up((size_t)B * T * Hq * D * sizeof(float), 256);
     const size_t q16_bytes = bwd_uses_q16(false, D) ? (size_t)B * T * Hq * D * 2 : 0;
@@ -672,10 +726,10 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     const long long rows = (long long)B * T * Hq;
 
     // The table is rebuilt on every call: the scratch keeps whatever the last call left.
-    cudaError_t e = ne::launch_rope_table(nullptr, nullptr, rope, ne::rope_table_rows(T), D, rope_theta, st);
+    cudaError_t e = ne::launch_rope_table(nullptr, nullptr, rope, ne::rope_table_rows(T), D, rope_theta, st, ld);
     if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
     ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, err,   // also zeroes dq_acc
-                      ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T)};
+                      ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T), nullptr, ld};
     e = ne::launch_bwd_pre(false, pa, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
     CUtensorMap tq, tk, tv, tdo, tdq;
@@ -685,7 +739,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     if ((s = map_bthd(&tv, v, false, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tdo, dO, false, B, T, Hq, D, q_rows)) != NE_OK) return s;
     std::memset(&tdq, 0, sizeof(tdq));
-    if (D == 64 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
+    if (D <= 64 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
     ne::BwdArgs a;
     a.lse = lse;
     a.delta = delta;
@@ -702,10 +756,12 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     a.scale = (float)(1.0 / std::sqrt((double)D));
     a.err = err;                // the static error word of the allocation-free calls
     a.timeout_ns = timeout_ns();
+    a.seq_lens = nullptr;
+    a.dr = D;
     e = ne::launch_bwd(false, D, B, tq, tk, tv, tdo, tdq, a, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
     ne::BwdPostArgs qa{dq_acc, dq, rope, rows, T, Hq, D, a.scale, ne::make_fastdiv((uint32_t)Hq),
-                          ne::make_fastdiv((uint32_t)T)};
+                          ne::make_fastdiv((uint32_t)T), ld};
     e = ne::launch_bwd_post(false, qa, st);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dq epilogue launch");
     return NE_OK;

@@ -85,8 +85,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
                     const uint32_t row = r0 + k * nw * RPW;
                     if (row >= rows) continue;
                     const uint32_t bt = fast_div(row, a.div_hq);
-                    const uint32_t t = bt - fast_div(bt, a.div_t) * (uint32_t)a.T;
-                    const float4* cs4 = reinterpret_cast<const float4*>(a.rope + (size_t)t * (D / 2) + 4 * li);
+                    const uint32_t bb = fast_div(bt, a.div_t);
+                    const uint32_t t = bt - bb * (uint32_t)a.T;
+                    // Padding positions (past the sequence's length) get R Q = 0.
+                    const bool pad = (int)t >= seq_len(a.seq_lens, (int)bb, a.T);
+                    const float4* cs4 = reinterpret_cast<const float4*>(a.rope + (size_t)t * a.rope_ld + 4 * li);
                     const float4 c01 = __ldg(cs4), c23 = __ldg(cs4 + 1);
                     const float cs[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
                     const uint32_t wq[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
                     for (int pr = 0; pr < 4; ++pr) {
                         const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[pr]));
                         const float c = cs[2 * pr], sn = cs[2 * pr + 1];
-                        const float y0 = x.x * c - x.y * sn, y1 = x.x * sn + x.y * c;
+                        const float y0 = pad ? 0.f : x.x * c - x.y * sn, y1 = pad ? 0.f : x.x * sn + x.y * c;
                         ovf |= fmaxf(fabsf(y0), fabsf(y1)) > 65504.f;
                         const __half2 h = __floats2half2_rn(y0, y1);
                         o16[pr] = *reinterpret_cast<const uint32_t*>(&h);
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
             if (row < rows && li == 0) {
                 const uint32_t bt = fast_div(row, a.div_hq), b = fast_div(bt, a.div_t);
                 const uint32_t h = row - bt * (uint32_t)a.Hq, t = bt - b * (uint32_t)a.T;
-                a.delta[(b * (uint32_t)a.Hq + h) * (uint32_t)a.T + t] = acc;
+                a.delta[(b * (uint32_t)a.Hq + h) * (uint32_t)a.T + t] = (int)t < seq_len(a.seq_lens, (int)b, a.T) ? acc : 0.f;
             }
         }
     }
@@ -171,8 +174,8 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdPostArgs a) {
                 const uint32_t t = bt - fast_div(bt, a.div_t) * (uint32_t)a.T;
                 g[k][0] = acc4[idx * 2];
                 g[k][1] = acc4[idx * 2 + 1];
-                cs[k][0] = __ldg(rope4 + (size_t)t * (D / 4) + 2 * c8);
-                cs[k][1] = __ldg(rope4 + (size_t)t * (D / 4) + 2 * c8 + 1);
+                cs[k][0] = __ldg(rope4 + (size_t)t * (a.rope_ld / 2) + 2 * c8);
+                cs[k][1] = __ldg(rope4 + (size_t)t * (a.rope_ld / 2) + 2 * c8 + 1);
             }
         }
 #pragma unroll
@@ -275,9 +278,12 @@ __global__ void __launch_bounds__(512, 1)
     const int hkv = blockIdx.x, b = blockIdx.y, j = blockIdx.z;
     const int T = a.T, G = a.G;
     const int kv0 = j * C::BKV;
-    const int n_qt = (T + C::BQ - 1) / C::BQ;
+    // Query tiles end at the sequence's length (T without per-sequence lengths); a key
+    // tile wholly past it has no query tile and writes zero gradients.
+    const int len = seq_len(a.seq_lens, b, T);
+    const int n_qt = (len + C::BQ - 1) / C::BQ;
     const int i_first = kv0 / C::BQ;
-    const int per_head = n_qt - i_first;
+    const int per_head = n_qt > i_first ? n_qt - i_first : 0;
     const int n_it = G * per_head;
 
     if (tid == 0) {
@@ -484,7 +490,7 @@ __global__ void __launch_bounds__(512, 1)
         };
         bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
         if (ok) {
-            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_BF16_F16>(sK, sK16, kv0, T, r, a.rope);
+            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_BF16_F16>(sK, sK16, kv0, T, r, a.rope, len);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready));
         }
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(512, 1)
                 if (C::DS_ALIASES_Q16 && it > 0 &&
                     !(ok = mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE)))
                     break;
-                ovf |= rope_tile_smem<D, C::BQ, 128, ROPE_BF16_F16>(stage_q(s), stage_q16(s), q0, T, r, a.rope);
+                ovf |= rope_tile_smem<D, C::BQ, 128, ROPE_BF16_F16>(stage_q(s), stage_q16(s), q0, T, r, a.rope, len);
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&bar_q_ready[s]));
             }
@@ -523,8 +529,8 @@ __global__ void __launch_bounds__(512, 1)
             const int h = hkv * G + it / per_head;
             const int qpos = (i_first + it % per_head) * C::BQ + cbase + (r & 63);
             const size_t rix = ((size_t)b * a.Hq + h) * T + qpos;
-            lv = qpos < T ? a.lse[rix] * 1.4426950408889634f : 0.f;
-            dv = qpos < T ? a.delta[rix] : 0.f;
+            lv = qpos < len ? a.lse[rix] * 1.4426950408889634f : 0.f;
+            dv = qpos < len ? a.delta[rix] : 0.f;
         };
         auto publish = [&](int it, float lv, float dv) {
             if (r < 64) {
@@ -535,7 +541,7 @@ __global__ void __launch_bounds__(512, 1)
         };
         {
             float lv, dv;
-            if (r < 64) row_vals(0, lv, dv);
+            if (r < 64 && n_it > 0) row_vals(0, lv, dv);
             publish(0, lv, dv);
         }
         for (int it = 0; it < n_it; ++it) {
@@ -545,7 +551,8 @@ __global__ void __launch_bounds__(512, 1)
             if (!mbar_wait_warp(smem_u32(&bar_rows[sb]), (it >> 1) & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
             float lv_n = 0.f, dv_n = 0.f;
             if (it + 1 < n_it && r < 64) row_vals(it + 1, lv_n, dv_n);    // in flight during this step
-            const bool diag = kv0 + C::BKV - 1 > q0;
+            // Per-element masks: the causal diagonal, and queries past the length (padding).
+            const bool diag = kv0 + C::BKV - 1 > q0 || q0 + C::BQ > len;
             if (!mbar_wait_warp(smem_u32(&bar_s_full), it & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
             if (!mbar_wait_warp(smem_u32(&bar_dp_full), it & 1, w, SITE_BWD_DP_FULL)) { ok = false; break; }
             if (it > 0 && !mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE)) { ok = false; break; }
@@ -570,7 +577,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
-                        if (diag && kvpos > q0 + cbase + c + e + k) p[k] = 0.f;
+                        if (diag && (kvpos > q0 + cbase + c + e + k || q0 + cbase + c + e + k >= len)) p[k] = 0.f;
                         gg[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
                     }
                     pk[e >> 1] = pack_bf162(p[0], p[1]);
@@ -620,6 +627,8 @@ __global__ void __launch_bounds__(512, 1)
         if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
             tc_fence_after();
             const bool valid = kvpos < T;
+            // Keys past the sequence's length (or a tile with no query tile) get zeros.
+            const bool live = kvpos < len && n_it > 0;
             const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -628,6 +637,10 @@ __global__ void __launch_bounds__(512, 1)
                 tmem_wait_ld();
                 reg_fence32(x);
                 if (!valid) continue;
+                if (!live) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = 0u;
+                }
                 uint32_t pk[16];
                 if (g == 0) {
                     const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)kvpos * (D / 2) + c / 2);
@@ -684,6 +697,7 @@ cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st) {
     if (a.rows == 0) return cudaSuccess;
     const dim3 g(grid_for(a.rows * 8, 256)), blk(256);
     if (!tf32) {
+        if (a.D == 32) return launch_k(bwd_pre_kernel<__nv_bfloat16, 32>, g, blk, 0, st, a);
         if (a.D == 64) return launch_k(bwd_pre_kernel<__nv_bfloat16, 64>, g, blk, 0, st, a);
         if (a.D == 128) return launch_k(bwd_pre_kernel<__nv_bfloat16, 128>, g, blk, 0, st, a);
     } else {
@@ -697,6 +711,7 @@ cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st) {
     if (a.rows == 0) return cudaSuccess;
     const dim3 g(grid_for(a.rows * (a.D / 8), 256)), blk(256);
     if (!tf32) {
+        if (a.D == 32) return launch_k(bwd_post_kernel<__nv_bfloat16, 32>, g, blk, 0, st, a);
         if (a.D == 64) return launch_k(bwd_post_kernel<__nv_bfloat16, 64>, g, blk, 0, st, a);
         if (a.D == 128) return launch_k(bwd_post_kernel<__nv_bfloat16, 128>, g, blk, 0, st, a);
     } else {
@@ -708,14 +723,14 @@ cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st) {
 
 int bwd_q_box_rows(bool tf32, int D) {
     if (tf32) return bwd_tf32_q_box_rows();
-    return D == 64 ? bwd_d64_q_box_rows() : BwdCfg<128>::BQ;
+    return D <= 64 ? bwd_d64_q_box_rows() : BwdCfg<128>::BQ;
 }
 
 cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
                        cudaStream_t st) {
     if (tf32) return cudaErrorNotSupported;
-    if (D == 64) return launch_bwd_d64(B, tq, tk, tv, tdo, tdq, a, st);
+    if (D == 64 || D == 32) return launch_bwd_d64(B, tq, tk, tv, tdo, tdq, a, st);   // 32: zero-padded to 64
     if (D == 128) return launch_bwd_t<128>(B, tq, tk, tv, tdo, a, st);
     return cudaErrorInvalidValue;
 }

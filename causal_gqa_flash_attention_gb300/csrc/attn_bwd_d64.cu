@@ -99,7 +99,7 @@ struct TileWalk {
 // as infinity.
 template <bool MASK>
 __device__ __forceinline__ void grad_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* lse2,
-                                           const float* delta, float sl2, int kl, uint32_t (&pk)[16],
+                                           const float* delta, float sl2, int kl, int qlim, uint32_t (&pk)[16],
                                            uint32_t (&dk)[16], __half2& amax2) {
     const float4* l4 = reinterpret_cast<const float4*>(lse2);
     const float4* d4 = reinterpret_cast<const float4*>(delta);
@@ -111,7 +111,7 @@ __device__ __forceinline__ void grad_chunk(const uint32_t (&sr)[32], const uint3
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
-            if (MASK && kl > e + k) p[k] = 0.f;
+            if (MASK && (kl > e + k || e + k >= qlim)) p[k] = 0.f;
             ds[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
         }
         pk[e >> 1] = pack_bf162(p[0], p[1]);
@@ -163,8 +163,11 @@ __global__ void __launch_bounds__(512, 1)
     const int hkv = blockIdx.x, b = blockIdx.y, j = blockIdx.z;
     const int T = a.T, G = a.G;
     const int kv0 = j * C::BKV;
-    const int n_qt = (T + C::BT - 1) / C::BT;
-    const int per_head = n_qt - j;                   // 128-query tiles on or after the diagonal
+    // Query tiles end at the sequence's length (T without per-sequence lengths); a key
+    // tile wholly past it has no query tile and writes zero gradients.
+    const int len = seq_len(a.seq_lens, b, T);
+    const int n_qt = (len + C::BT - 1) / C::BT;
+    const int per_head = n_qt > j ? n_qt - j : 0;    // 128-query tiles on or after the diagonal
     const int n_tiles = G * per_head;
     const int n_hs = 2 * n_tiles;
 
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(512, 1)
         bool ovf = false;
         bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
         if (ok) {
-            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_F16, true>(sK, nullptr, kv0, T, r, a.rope);
+            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_F16, true>(sK, nullptr, kv0, T, r, a.rope, len);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready));
         }
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(512, 1)
                 const size_t rix = ((size_t)b * a.Hq + tw.h) * T + qpos;
                 lv[k] = 0.f;
                 dv[k] = 0.f;
-                if (qpos < T) {
+                if (qpos < len) {
                     lv[k] = __ldg(a.lse + rix);
                     dv[k] = __ldg(a.delta + rix);
                 }
@@ -452,8 +455,10 @@ __global__ void __launch_bounds__(512, 1)
                 const int qc = q0 + 32 * c;
                 const float* lrow = &s_lse[sw][buf][32 * c];
                 const float* drow = &s_delta[sw][buf][32 * c];
-                if (kw < qc) grad_chunk<false>(sr, dr, lrow, drow, sl2, -1, pk, dk, amax2);
-                else grad_chunk<true>(sr, dr, lrow, drow, sl2, kw == qc ? lane : 32, pk, dk, amax2);
+                // Queries of the chunk at or past the sequence's length are padding (masked).
+                const int qlim = len - qc;
+                if (kw < qc && qlim >= 32) grad_chunk<false>(sr, dr, lrow, drow, sl2, -1, 32, pk, dk, amax2);
+                else grad_chunk<true>(sr, dr, lrow, drow, sl2, kw < qc ? -1 : (kw == qc ? lane : 32), qlim, pk, dk, amax2);
                 if (c == 0) {
                     // P^T buffer g is free once dV of half-step hs-2 has read it: that
                     // half-step's stage release, committed after its dK' (issued after its
@@ -487,14 +492,22 @@ __global__ void __launch_bounds__(512, 1)
         if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
             tc_fence_after();
             const bool valid = kvpos < T;
-            const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
+            // Keys past the sequence's length (or a tile with no query tile) get zeros.
+            const bool live = kvpos < len && n_hs > 0;
+            // The tensors' row is a.dr wide: at head_dim 32 the kernel runs zero-padded to
+            // 64 columns and stores only the first 32.
+            const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * a.dr;
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
+            for (int c = 0; c < a.dr; c += 32) {
                 uint32_t x[32];
                 tmem_ld32(lt + (g == 0 ? C::DK_COL : C::DV_COL) + c, x);
                 tmem_wait_ld();
                 reg_fence32(x);
                 if (!valid) continue;
+                if (!live) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = 0u;
+                }
                 uint32_t pk[16];
                 if (g == 0) {
                     const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)kvpos * (D / 2) + c / 2);

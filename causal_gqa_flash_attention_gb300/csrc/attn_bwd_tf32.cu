@@ -101,9 +101,12 @@ __global__ void __launch_bounds__(384, 1)
     const int hkv = blockIdx.x, b = blockIdx.y, j = blockIdx.z;
     const int T = a.T, G = a.G;
     const int kv0 = j * C::BKV;
-    const int n_qt = (T + C::BQ - 1) / C::BQ;
+    // Query tiles end at the sequence's length (T without per-sequence lengths); a key
+    // tile wholly past it has no query tile and writes zero gradients.
+    const int len = seq_len(a.seq_lens, b, T);
+    const int n_qt = (len + C::BQ - 1) / C::BQ;
     const int i_first = kv0 / C::BQ;
-    const int per_head = n_qt - i_first;
+    const int per_head = n_qt > i_first ? n_qt - i_first : 0;
     const int n_it = G * per_head;
     auto step_h = [&](int it) { return hkv * G + it / per_head; };
     auto step_q0 = [&](int it) { return (i_first + it % per_head) * C::BQ; };
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(384, 1)
         };
         bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
         if (ok) {
-            rope_tile_smem<D, C::BKV, 128, ROPE_TF32>(sK, nullptr, kv0, T, r, a.rope);
+            rope_tile_smem<D, C::BKV, 128, ROPE_TF32>(sK, nullptr, kv0, T, r, a.rope, len);
             round_tf32<C::KV_BYTES>(sV, r);
             ok = group_sync();
         }
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int it = 0; ok && it <= n_it; ++it) {
             if (it < n_it) {
                 if (!(ok = mbar_wait_warp(smem_u32(&bar_qdo_full), it & 1, w, SITE_BWD_QDO_FULL))) break;
-                rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(sQ, nullptr, step_q0(it), T, r, a.rope);
+                rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(sQ, nullptr, step_q0(it), T, r, a.rope, len);
                 round_tf32<C::Q_BYTES>(sO, r);
                 if (!(ok = group_sync())) break;
                 transpose_f32<D, C::BQ>(sQ, sQT, r);
@@ -272,8 +275,8 @@ __global__ void __launch_bounds__(384, 1)
         auto row_vals = [&](int it, float& lv, float& dv) {
             const int qpos = step_q0(it) + r;
             const size_t rix = ((size_t)b * a.Hq + step_h(it)) * T + qpos;
-            lv = qpos < T ? a.lse[rix] * 1.4426950408889634f : 0.f;
-            dv = qpos < T ? a.delta[rix] : 0.f;
+            lv = qpos < len ? a.lse[rix] * 1.4426950408889634f : 0.f;
+            dv = qpos < len ? a.delta[rix] : 0.f;
         };
         auto publish = [&](int it, float lv, float dv) {
             if (r < C::BQ) {
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(384, 1)
         };
         {
             float lv = 0.f, dv = 0.f;
-            if (r < C::BQ) row_vals(0, lv, dv);
+            if (r < C::BQ && n_it > 0) row_vals(0, lv, dv);
             publish(0, lv, dv);
         }
         for (int it = 0; it < n_it; ++it) {
@@ -299,10 +302,11 @@ __global__ void __launch_bounds__(384, 1)
             tmem_ld_cols<2>(lt + C::S_COL, sr);
             tmem_ld_cols<2>(lt + C::DP_COL, dr);
             const bool diag = kv0 + C::BKV - 1 > q0;
+            const bool tail = q0 + C::BQ > len;          // queries past the length are padding
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 float p = ex2(fmaf(__uint_as_float(sr[c]), sl2, -s_lse[sb][c]));
-                if (diag && kvpos > q0 + c) p = 0.f;
+                if ((diag && kvpos > q0 + c) || (tail && q0 + c >= len)) p = 0.f;
                 const float g = p * (__uint_as_float(dr[c]) - s_delta[sb][c]);
                 sr[c] = f32_to_tf32_rna(p);
                 dr[c] = f32_to_tf32_rna(g);
@@ -324,6 +328,8 @@ __global__ void __launch_bounds__(384, 1)
         if (ok && mbar_wait_warp(smem_u32(&bar_dkv_full), 0, w, SITE_BWD_DKV)) {
             tc_fence_after();
             const bool valid = kvpos < T;
+            // Keys past the sequence's length (or a tile with no query tile) get zeros.
+            const bool live = kvpos < len && n_it > 0;
             const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -334,6 +340,10 @@ __global__ void __launch_bounds__(384, 1)
                 reg_fence32(kr);
                 reg_fence32(vr);
                 if (!valid) continue;
+                if (!live) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) kr[e] = vr[e] = 0u;
+                }
                 const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)kvpos * (D / 2) + c / 2);
                 float4* dkp = reinterpret_cast<float4*>(static_cast<float*>(a.dk) + orow + c);
                 float4* dvp = reinterpret_cast<float4*>(static_cast<float*>(a.dv) + orow + c);

@@ -82,10 +82,22 @@ struct FwdCfg {
 // TMEM column of S buffer `buf` (0/1) of subtile u.
 __device__ __forceinline__ uint32_t s_col(int u, int buf) { return (uint32_t)((u * 2 + buf) * 64); }
 
+// Zeroes rows zero_row .. ROWS-1 of a [ROWS x NCH*128 bytes] tile in the 128-byte-swizzled
+// layout (padding past a sequence's length); thread t of NT.
+template <int ROWS, int NCH, int NT>
+__device__ __forceinline__ void zero_rows(uint8_t* base, int zero_row, int t) {
+    for (int idx = t; idx < ROWS * NCH * 8; idx += NT) {
+        const int c = idx / (ROWS * 8), rem = idx - c * (ROWS * 8), row = rem >> 3;
+        if (row >= zero_row)
+            *reinterpret_cast<uint4*>(base + c * ROWS * 128 + sw128_offset(row, rem & 7)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 // TF32 only: Vt[d][r] = tf32(V[r][d]) for a [ROWS x D] fp32 tile, written K-major (key
-// index contiguous, 32 keys per 128-byte chunk); NT threads.
+// index contiguous, 32 keys per 128-byte chunk); NT threads.  Keys zero_row and later
+// (padding) are written as zeros.
 template <int D, int ROWS, int NT>
-__device__ __forceinline__ void transpose_v_tf32(const uint8_t* src, uint8_t* dst, int t) {
+__device__ __forceinline__ void transpose_v_tf32(const uint8_t* src, uint8_t* dst, int t, int zero_row) {
     constexpr int UNITS = D * ROWS / 4;       // 16-byte units of the transposed tile
     constexpr int UPR = ROWS / 4;             // units per transposed row
 #pragma unroll 4
@@ -96,7 +108,7 @@ __device__ __forceinline__ void transpose_v_tf32(const uint8_t* src, uint8_t* ds
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const uint8_t* s = src + (d >> 5) * ROWS * 128 + sw128_offset(r0 + k, (d & 31) >> 2) + (d & 3) * 4;
-            w[k] = f32_to_tf32_rna(*reinterpret_cast<const float*>(s));
+            w[k] = r0 + k < zero_row ? f32_to_tf32_rna(*reinterpret_cast<const float*>(s)) : 0u;
         }
         *reinterpret_cast<uint4*>(dst + (r0 >> 5) * D * 128 + sw128_offset(d, (r0 & 31) >> 2)) =
             make_uint4(w[0], w[1], w[2], w[3]);
@@ -203,9 +215,10 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
 // subtiles), numbered heaviest first (the pair holding the latest query rows).
 struct FwdUnit {
     int b, h, q0;
-    int n_u[2];    // key tiles of subtile u (0: subtile beyond T)
+    int len;       // the sequence's length (T without per-sequence lengths)
+    int n_u[2];    // key tiles of subtile u (0: subtile at or past the length)
     int n_kv;      // key tiles the unit loads: max(n_u)
-    int n_qsub;    // subtiles inside T
+    int n_qsub;    // subtiles holding positions before the length (at least 1)
 };
 
 template <int BM, int BN>
@@ -216,10 +229,11 @@ __device__ __forceinline__ FwdUnit fwd_unit(int U, const FwdArgs& a) {
     f.h = rem % a.Hq;
     f.b = rem / a.Hq;
     f.q0 = (a.n_qt - 1 - rank) * 2 * BM;
+    f.len = seq_len(a.seq_lens, f.b, a.T);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int qu = f.q0 + u * BM;
-        f.n_u[u] = qu < a.T ? min(qu + BM - 1, a.T - 1) / BN + 1 : 0;
+        f.n_u[u] = qu < f.len ? min(qu + BM - 1, f.len - 1) / BN + 1 : 0;
     }
     f.n_kv = max(f.n_u[0], f.n_u[1]);
     f.n_qsub = f.n_u[1] > 0 ? 2 : 1;
@@ -349,6 +363,7 @@ __global__ void __launch_bounds__(480, 1)
                 if (k >= C::NQB &&
                     !(ok = mbar_wait(smem_u32(&bar_q_empty[qb]), ((k / C::NQB) - 1) & 1, w, SITE_FWD_Q)))
                     break;
+                if (seq_len_bad(a.seq_lens, f.b, T)) report_error(a.err, SITE_VARLEN_LEN);
                 const uint32_t qf = smem_u32(&bar_q_full[qb]);
                 mbar_arrive_expect_tx(qf, f.n_qsub * C::Q_BYTES);
                 for (int u = 0; u < f.n_qsub; ++u)
@@ -509,8 +524,10 @@ __global__ void __launch_bounds__(480, 1)
             rq.load_base(qc, f.q0 + C::BM, T, a.rope);
             rk.load_base(kn, 0, T, a.rope);
             if (!(ok = mbar_wait_warp(smem_u32(&bar_q_full[k % C::NQB]), (k / C::NQB) & 1, w, SITE_FWD_Q))) break;
-            rq.template apply<false>(qbuf, nullptr, qa);
-            if (f.n_qsub == 2) rq.template apply<false>(qbuf + C::Q_BYTES, nullptr, qc);
+            // Rows past the sequence's length (padding) are zeroed, so whatever the caller
+            // left there never reaches an MMA.
+            rq.template apply<false>(qbuf, nullptr, qa, f.len - f.q0);
+            if (f.n_qsub == 2) rq.template apply<false>(qbuf + C::Q_BYTES, nullptr, qc, f.len - f.q0 - C::BM);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_q_ready[k % C::NQB]));
             for (int j = 0; j < f.n_kv; ++j, ++g) {
@@ -520,8 +537,13 @@ __global__ void __launch_bounds__(480, 1)
                 for (int e = 0; e < RopeK::F4; ++e) cur[e] = kn[e];
                 if (j + 1 < f.n_kv) rk.load_base(kn, (j + 1) * C::BN, T, a.rope);   // one tile early
                 if (!(ok = mbar_wait_warp(smem_u32(&bar_kv_full[s]), (g / C::NS) & 1, w, SITE_FWD_KV_FULL))) break;
-                if constexpr (TF32) transpose_v_tf32<D, C::BN, C::ROPE_THREADS>(stage_v(s), stage_vt(s), rt);
-                rk.template apply<false>(stage_k(s), nullptr, cur);
+                const int kz = f.len - j * C::BN;      // first padding row of the tile
+                if constexpr (TF32) {
+                    transpose_v_tf32<D, C::BN, C::ROPE_THREADS>(stage_v(s), stage_vt(s), rt, kz);
+                } else if (kz < C::BN) {
+                    zero_rows<C::BN, C::NCH, C::ROPE_THREADS>(stage_v(s), kz, rt);
+                }
+                rk.template apply<false>(stage_k(s), nullptr, cur, kz);
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&bar_k_ready[s]));
             }
@@ -549,7 +571,7 @@ __global__ void __launch_bounds__(480, 1)
                 n_kv = f.n_kv;
             }
             const int qb = k % C::NQB;
-            if (n == 0) {                             // subtile beyond T: nothing to store
+            if (n == 0) {                             // subtile at or past the sequence's length
                 // Its release of the Q buffer must count toward this unit's phase, so it
                 // waits until the unit's Q has landed (the buffer's previous phase is
                 // then complete).
@@ -559,6 +581,17 @@ __global__ void __launch_bounds__(480, 1)
                     if (rel) mbar_arrive(smem_u32(&bar_q_empty[qb]));
                 }
                 if (!(ok = __all_sync(0xffffffffu, rel))) break;
+                // Padding rows inside T: O = 0 and LSE = -inf (a softmax over no keys).
+                const int qpos = qsub0 + r;
+                if (qpos < T) {
+                    const FwdUnit f = fwd_unit<C::BM, C::BN>(fwd_unit_index(k, a.n_units), a);
+                    const size_t row = ((size_t)f.b * T + qpos) * a.Hq + f.h;
+                    // The tensors' row is a.dr wide (bf16 head_dim 32 runs zero-padded to 64).
+                    const int rb = a.dr * C::ES;
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) + row * rb);
+                    for (int e = 0; e < rb / 16; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+                    a.lse[((size_t)f.b * a.Hq + f.h) * T + qpos] = kNegInf;
+                }
                 continue;
             }
             const int qpos = qsub0 + r;
@@ -584,7 +617,10 @@ __global__ void __launch_bounds__(480, 1)
             tc_fence_after();
             const FwdUnit f = fwd_unit<C::BM, C::BN>(fwd_unit_index(k, a.n_units), a);
             uint8_t* sQu = q_buf(k) + u * C::Q_BYTES;
-            const float inv_l = 1.f / st.l;
+            // Padding rows (past the sequence's length) store O = 0 and LSE = -inf; their
+            // accumulators are finite (their Q, and the padding K and V, were zeroed).
+            const bool live = qpos < f.len;
+            const float inv_l = live ? 1.f / st.l : 0.f;
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
                 uint32_t orow[32];
@@ -613,7 +649,9 @@ __global__ void __launch_bounds__(480, 1)
             tc_fence_before();
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_o_staged[u]));
-            if (qpos < T) a.lse[((size_t)f.b * a.Hq + f.h) * T + qpos] = (st.m_used + log2f(st.l)) * 0.6931471805599453f;
+            if (qpos < T)
+                a.lse[((size_t)f.b * a.Hq + f.h) * T + qpos] =
+                    live ? (st.m_used + log2f(st.l)) * 0.6931471805599453f : kNegInf;
             bool stored = true;
             if (r == 0) {
                 stored = mbar_wait(smem_u32(&bar_o_staged[u]), n_epi & 1, w, SITE_FWD_O_DONE);
@@ -664,7 +702,9 @@ int fwd_kv_box_rows(bool tf32, int D) { return 64; }
 cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
     if (!tf32) {
-        if (D == 64) return launch_fwd_t<false, 64>(B, tq, tk, tv, to, a, st);
+        // head_dim 32 runs the 64-wide kernel: its 128-byte TMA boxes read the upper 32
+        // columns as zeros and the O store clips them.
+        if (D == 64 || D == 32) return launch_fwd_t<false, 64>(B, tq, tk, tv, to, a, st);
         if (D == 128) return launch_fwd_t<false, 128>(B, tq, tk, tv, to, a, st);
     } else {
         if (D == 32) return launch_fwd_t<true, 32>(B, tq, tk, tv, to, a, st);

@@ -21,7 +21,22 @@ enum WaitSite : int {
     SITE_RANGE = 0x401,
     // Not a wait: a decode call got a sequence length outside [1, T_max].
     SITE_DECODE_LEN = 0x402,
+    // Not a wait: a variable-length call got a sequence length outside [0, T].
+    SITE_VARLEN_LEN = 0x403,
 };
+
+// Length of sequence b: T when the call has no per-sequence lengths, else seq_lens[b]
+// clamped to [0, T] (the caller reports a length outside that range).
+__device__ __forceinline__ int seq_len(const int* seq_lens, int b, int T) {
+    if (!seq_lens) return T;
+    const int l = __ldg(seq_lens + b);
+    return l < 0 ? 0 : (l > T ? T : l);
+}
+__device__ __forceinline__ bool seq_len_bad(const int* seq_lens, int b, int T) {
+    if (!seq_lens) return false;
+    const int l = __ldg(seq_lens + b);
+    return l < 0 || l > T;
+}
 
 // Rows of the interleaved RoPE table the kernels read: at least this many (shorter
 // sequences get a padded table), because the in-kernel angle-addition steps read
@@ -55,6 +70,8 @@ struct FwdArgs {
     float scale_log2;        // log2(e) / sqrt(D)
     int* err;
     unsigned long long timeout_ns;
+    const int* seq_lens;     // [B] per-sequence lengths (positions at or past are padding), or null
+    int dr;                  // the tensors' head_dim (bf16 32 runs the 64-wide kernel, zero-padded)
 };
 
 struct BwdPreArgs {
@@ -69,6 +86,8 @@ struct BwdPreArgs {
     const float2* rope;      // [T, D/2] (cos, sin), when q16 is set
     int* err;                // device error word (an fp16 overflow of R Q), may be null
     FastDiv div_hq, div_t;   // by Hq and by T (row = (b T + t) Hq + h)
+    const int* seq_lens;     // [B] or null: Delta and R Q are zero at padding positions
+    int rope_ld;             // (cos, sin) pairs per row of `rope` (>= D/2)
 };
 
 struct BwdArgs {
@@ -83,6 +102,8 @@ struct BwdArgs {
     float scale;             // 1 / sqrt(D)
     int* err;
     unsigned long long timeout_ns;
+    const int* seq_lens;     // [B] or null: padding queries and keys get zero gradients
+    int dr;                  // the tensors' head_dim (bf16 32 runs the 64-wide kernel, zero-padded)
 };
 
 struct BwdPostArgs {
@@ -93,6 +114,7 @@ struct BwdPostArgs {
     int T, Hq, D;
     float scale;
     FastDiv div_hq, div_t;   // by Hq and by T
+    int rope_ld;             // (cos, sin) pairs per row of `rope` (>= D/2)
 };
 
 struct DecodeArgs {
@@ -145,8 +167,9 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // Tile rows of the key/value tensor maps the forward kernel expects.
 int fwd_kv_box_rows(bool tf32, int D);
 // Launchers: return cudaSuccess or the launch error.
+// ld: (cos, sin) pairs per table row (default D/2); pairs D/2 .. ld-1 get angle 0.
 cudaError_t launch_rope_table(float* cos_out, float* sin_out, float2* interleaved, int T, int D,
-                              double theta, cudaStream_t st);
+                              double theta, cudaStream_t st, int ld = 0);
 cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st);

@@ -7,20 +7,24 @@
 
 namespace ne {
 
+// ld >= half pairs per table row: pairs i >= half (the zero-padded head columns of a
+// head_dim run on a wider kernel) get angle 0, i.e. (cos, sin) = (1, 0).
 __global__ void rope_table_kernel(float* __restrict__ cos_out, float* __restrict__ sin_out,
-                                  float2* __restrict__ interleaved, int T, int half, double theta,
+                                  float2* __restrict__ interleaved, int T, int half, int ld, double theta,
                                   double inv_half) {
     griddep_launch_dependents();
     griddep_wait();   // an earlier kernel may still read a table this call overwrites
-    const long long n = (long long)T * half;
+    const long long n = (long long)T * ld;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
          idx += (long long)gridDim.x * blockDim.x) {
-        const int t = (int)(idx / half);
-        const int i = (int)(idx % half);
-        // theta^(-2i/D) = theta^(-i/half)
-        const double w = pow(theta, -(double)i * inv_half);
-        double s, c;
-        sincos((double)t * w, &s, &c);
+        const int t = (int)(idx / ld);
+        const int i = (int)(idx % ld);
+        double s = 0.0, c = 1.0;
+        if (i < half) {
+            // theta^(-2i/D) = theta^(-i/half)
+            const double w = pow(theta, -(double)i * inv_half);
+            sincos((double)t * w, &s, &c);
+        }
         if (cos_out) cos_out[idx] = (float)c;
         if (sin_out) sin_out[idx] = (float)s;
         if (interleaved) interleaved[idx] = make_float2((float)c, (float)s);
@@ -28,13 +32,14 @@ __global__ void rope_table_kernel(float* __restrict__ cos_out, float* __restrict
 }
 
 cudaError_t launch_rope_table(float* cos_out, float* sin_out, float2* interleaved, int T, int D,
-                              double theta, cudaStream_t st) {
+                              double theta, cudaStream_t st, int ld) {
     const int half = D / 2;
-    const long long n = (long long)T * half;
+    if (ld < half) ld = half;
+    const long long n = (long long)T * ld;
     if (n == 0) return cudaSuccess;
     int blocks = (int)((n + 255) / 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
-    return launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st, cos_out, sin_out, interleaved, T, half,
+    return launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st, cos_out, sin_out, interleaved, T, half, ld,
                     theta, 1.0 / (double)half);
 }
 

@@ -72,15 +72,17 @@ struct RopeTile {
         for (int e = 0; e < F4; ++e) b[e] = __ldg(bp + e);
     }
     // Rotates the tile; with CHECK, returns true if an fp16 output would have overflowed
-    // (without, the caller detects overflow downstream and this returns false).
+    // (without, the caller detects overflow downstream and this returns false).  Rows
+    // zero_row and later (padding past a sequence's length) are written as zeros.
     template <bool CHECK = true>
-    __device__ __forceinline__ bool apply(uint8_t* base, uint8_t* dst16, float4 (&b)[F4]) const {
+    __device__ __forceinline__ bool apply(uint8_t* base, uint8_t* dst16, float4 (&b)[F4],
+                                          int zero_row = ROWS) const {
         float amax = 0.f;
 #pragma unroll
         for (int k = 0; k < KSTEPS; ++k) {
             const int row = r0 + k * RSTEP;
             const uint32_t off = (unit >> 3) * ROWS * 128 + sw128_offset(row, unit & 7);
-            const uint4 raw = *reinterpret_cast<const uint4*>(base + off);
+            const uint4 raw = row < zero_row ? *reinterpret_cast<const uint4*>(base + off) : make_uint4(0u, 0u, 0u, 0u);
             if constexpr (MODE == ROPE_TF32) {
                 const float4 cs = b[0];
                 const float x0 = __uint_as_float(raw.x), x1 = __uint_as_float(raw.y);
@@ -122,15 +124,16 @@ struct RopeTile {
     }
 };
 
-// One-shot form: rotate rows [pos0, pos0 + ROWS) of a tile with thread t of NT.
+// One-shot form: rotate rows [pos0, pos0 + ROWS) of a tile with thread t of NT.  Rows at
+// positions len and later (padding of a shorter sequence) are written as zeros.
 template <int D, int ROWS, int NT, int MODE, bool CHECK = true>
 __device__ __forceinline__ bool rope_tile_smem(uint8_t* base, uint8_t* dst16, int pos0, int T, int t,
-                                               const float2* __restrict__ rope) {
+                                               const float2* __restrict__ rope, int len) {
     RopeTile<D, ROWS, NT, MODE> rt;
     rt.init(t, rope);
     float4 b[RopeTile<D, ROWS, NT, MODE>::F4];
     rt.load_base(b, pos0, T, rope);
-    return rt.template apply<CHECK>(base, dst16, b);
+    return rt.template apply<CHECK>(base, dst16, b, len - pos0);
 }
 
 }  // namespace ne

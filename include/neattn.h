@@ -26,7 +26,9 @@
  * tensor cores with fp32 accumulation.  Outputs have the input dtype, lse is fp32.
  *
  * Supported shapes: B >= 0, T >= 0 (any T, ragged tails included), Hq % Hkv == 0,
- * D in {64, 128} for bf16 and {32, 64} for f32 (others return NE_ERR_UNSUPPORTED),
+ * D in {32, 64, 128} for bf16 and {32, 64} for f32 (others return NE_ERR_UNSUPPORTED;
+ * bf16 32 runs on the head_dim-64 kernels with zero-padded columns; fp32 128 does not
+ * fit the kernels' shared memory: a 128-row fp32 tile of 128 columns is 64 KB),
  * B * T * max(Hq, 1) * D < 2^31.  Every tensor pointer must be 16-byte aligned.
  *
  * Ownership: the caller owns every tensor and the backward workspace.  The library
@@ -102,6 +104,38 @@ ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const 
                           int B, int T, int Hq, int Hkv, int D, double rope_theta,
                           void* workspace, size_t workspace_bytes, ne_stream_t stream);
 
+/* Variable-length sequences in a padded batch: the supervised fine-tuning data of
+ * "NanoEuler: C와 CUDA로 밑바닥부터 구축한 GPT-2 규모의 LLM" (2단계 학습 프로세스, SFT bullet)
+ * pads sequences of different lengths to one T, and the padding must not take part.
+ * Same tensors and layouts as ne_attn_fwd / ne_attn_bwd, plus
+ *   seq_lens [B] int32 (device memory, 4-byte aligned): sequence b occupies positions
+ *            0 .. seq_lens[b]-1 of row b; positions seq_lens[b] .. T-1 are padding.
+ * The valid positions of sequence b get the results of the same call on that sequence
+ * alone with T = seq_lens[b] (RoPE positions start at 0 in every row).
+ * Padding never takes part: no valid query attends to a padding key, padding queries
+ * and keys get zero outputs and gradients (o, dq, dk, dv = 0) and lse = -inf (the log of
+ * an empty sum).  Padding entries of q and k are not read as values (the kernels zero
+ * them before any MMA); padding entries of v and dO must be finite (e.g. zeros, as
+ * padding usually is): they meet zero weights inside tensor-core products, where a NaN
+ * or infinity would still propagate.  A length outside [0, T] is clamped on the device
+ * and reported by ne_get_device_error() as NE_ERR_INVALID_ARG; a length of 0 is an
+ * empty sequence.  The backward takes the workspace of ne_attn_bwd. */
+ne_status ne_attn_fwd_varlen(const void* q, const void* k, const void* v, const int* seq_lens, void* o,
+                             float* lse, int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                             ne_stream_t stream);
+ne_status ne_attn_fwd_varlen_f32(const float* q, const float* k, const float* v, const int* seq_lens,
+                                 float* o, float* lse, int B, int T, int Hq, int Hkv, int D,
+                                 double rope_theta, ne_stream_t stream);
+ne_status ne_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dO, const int* seq_lens, void* dq, void* dk,
+                             void* dv, int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                             void* workspace, size_t workspace_bytes, ne_stream_t stream);
+ne_status ne_attn_bwd_varlen_f32(const float* q, const float* k, const float* v, const float* o,
+                                 const float* lse, const float* dO, const int* seq_lens, float* dq,
+                                 float* dk, float* dv, int B, int T, int Hq, int Hkv, int D,
+                                 double rope_theta, void* workspace, size_t workspace_bytes,
+                                 ne_stream_t stream);
+
 /* Backward that allocates nothing (there is no counterpart of this call on the
  * pages: it is a deployment convenience).  Same computation, arguments and outputs
  * as ne_attn_bwd for bf16 tensors, but without a workspace argument: its scratch
@@ -112,8 +146,8 @@ ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const 
  * whose own allocator already owns the device's free memory, or real-time loops that
  * forbid allocation after start-up.  It calls no cudaMalloc, cudaFree or allocating
  * library routine.
- *  - Limit: round256(T*(D/2)*8) + round256(B*Hq*T*4) + round256(B*T*Hq*D*4)
- *    + (D == 64 ? B*T*Hq*D*2 : 0) <= 50331648 bytes (the GPU-pipeline shape B=16 T=512
+ *  - Limit: round256(max(T,64)*P*8) + round256(B*Hq*T*4) + round256(B*T*Hq*D*4)
+ *    + (D <= 64 ? B*T*Hq*D*2 : 0) <= 50331648 bytes, P = max(D,64)/2 (the GPU-pipeline shape B=16 T=512
  *    Hq=12 D=64 uses 38.3 MB); larger shapes
  *    return NE_ERR_INVALID_ARG before anything is enqueued.
  *  - The first call on a device looks up the array's device address (once per

@@ -202,3 +202,39 @@ def test_bad_arguments_raise():
     with pytest.raises(ne.NeError) as ei:
         ne.attn_fwd(q, k, k)
     assert ei.value.status == ne.NE_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- bf16, head_dim 32
+# The small model's head size (dim 128 with 4 query heads, "NanoEuler: C와 CUDA로 밑바닥부터
+# 구축한 GPT-2 규모의 LLM", 모델 구성).  It runs on the head_dim-64 kernels with the upper
+# 32 columns zero, so these cases also pin that the padding never reaches an output row.
+@pytest.mark.parametrize("T", [1, 5, 128, 129, 300])
+def test_bf16_d32_small_model_heads_ragged_T(T):
+    q, k, v, dO = synthetic.make_custom(2, T, 4, 2, 32, torch.bfloat16, seed=41 + T)
+    check(q, k, v, dO, "bf16")
+
+
+def test_bf16_d32_theta_500_and_gqa_group_4():
+    q, k, v, dO = synthetic.make_custom(1, 257, 8, 2, 32, torch.bfloat16, seed=43)
+    check(q, k, v, dO, "bf16", theta=500.0)
+
+
+def test_bf16_d32_does_not_write_past_its_rows():
+    """Outputs are [.., 32] wide; a store of the 64-wide kernel's padded columns would
+    overwrite the next head's row.  Surround the outputs with a canary and check it."""
+    B, T, Hq, Hkv, D = 1, 130, 3, 1, 32
+    q, k, v, dO = (t.cuda() for t in synthetic.make_custom(B, T, Hq, Hkv, D, torch.bfloat16, seed=44))
+    canary = 7.0
+    big = torch.full((B * T * Hq * D + 64,), canary, dtype=torch.bfloat16, device="cuda")
+    o = big[:B * T * Hq * D].view(B, T, Hq, D)
+    o2, lse = ne.attn_fwd(q, k, v, o=o)
+    dq_buf = torch.full((B * T * Hq * D + 64,), canary, dtype=torch.bfloat16, device="cuda")
+    dk_buf = torch.full((B * T * Hkv * D + 64,), canary, dtype=torch.bfloat16, device="cuda")
+    dv_buf = torch.full((B * T * Hkv * D + 64,), canary, dtype=torch.bfloat16, device="cuda")
+    ne.attn_bwd(q, k, v, o2, lse, dO, dq=dq_buf[:B * T * Hq * D].view(B, T, Hq, D),
+                dk=dk_buf[:B * T * Hkv * D].view(B, T, Hkv, D), dv=dv_buf[:B * T * Hkv * D].view(B, T, Hkv, D))
+    torch.cuda.synchronize()
+    assert ne.get_device_error() == ne.NE_OK
+    for buf, n in ((big, B * T * Hq * D), (dq_buf, B * T * Hq * D), (dk_buf, B * T * Hkv * D),
+                   (dv_buf, B * T * Hkv * D)):
+        assert torch.all(buf[n:] == canary)
