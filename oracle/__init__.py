@@ -72,9 +72,10 @@ def _load():
                                               ctypes.c_double]
             lib.ne_ref_attn_krows.argtypes = [dp, dp, dp, dp, i, i, ip, i, dp, dp, i, i, i, i, i,
                                               ctypes.c_double]
+            lib.ne_ref_qkv_prologue.argtypes = [dp] * 6 + [i] * 6 + [ctypes.c_double, ctypes.c_double, i]
             for f in (lib.ne_ref_rope_table, lib.ne_ref_rope_apply, lib.ne_ref_attn_fwd,
                       lib.ne_ref_attn_bwd, lib.ne_ref_attn_qrows, lib.ne_ref_attn_krows,
-                      lib.ne_ref_num_threads):
+                      lib.ne_ref_num_threads, lib.ne_ref_qkv_prologue):
                 f.restype = ctypes.c_int
             lib.ne_ref_num_threads.argtypes = []
             _lib = lib
@@ -201,3 +202,22 @@ def attn_krows(q, k, v, dO, b: int, g: int, rows, theta: float = 10000.0):
     if rc != 0:
         raise ValueError("bad attn_krows arguments")
     return dk, dv
+
+
+def qkv_prologue(x, gamma, w, Hq: int, Hkv: int, D: int, eps: float = 1e-5, theta: float = 10000.0,
+                 rotate: bool = True):
+    """RMSNorm (gain gamma, no bias) -> one bias-free projection w [(Hq + 2 Hkv) D, dim]
+    -> split into q, k, v heads -> RoPE on q and k when `rotate`.  x [B, T, dim];
+    returns q [B, T, Hq, D], k and v [B, T, Hkv, D], all float64."""
+    x, gamma, w = _f64(x), _f64(gamma), _f64(w)
+    B, T, dim = x.shape
+    if gamma.shape != (dim,) or w.shape != ((Hq + 2 * Hkv) * D, dim):
+        raise ValueError("shape mismatch")
+    q = np.zeros((B, T, Hq, D), np.float64)
+    k = np.zeros((B, T, Hkv, D), np.float64)
+    v = np.zeros((B, T, Hkv, D), np.float64)
+    rc = _load().ne_ref_qkv_prologue(_ptr(x), _ptr(gamma), _ptr(w), _ptr(q), _ptr(k), _ptr(v), B, T, dim, Hq,
+                                     Hkv, D, float(eps), float(theta), 1 if rotate else 0)
+    if rc != 0:
+        raise ValueError("bad prologue shape")
+    return q, k, v

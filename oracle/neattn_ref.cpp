@@ -365,6 +365,47 @@ int ne_ref_attn_krows(const double* q, const double* k, const double* v, const d
     return 0;
 }
 
+/* The steps before attention in every layer ("NanoEuler: C와 CUDA로 밑바닥부터 구축한
+ * GPT-2 규모의 LLM", 기술 사양: RMSNorm as pre-normalization without bias, RoPE on queries
+ * and keys; the model uses no biases at all).  For token row m of x [B*T, dim]:
+ *   r_m  = sqrt(mean_c x_mc^2 + eps)                     (RMSNorm, gain gamma [dim])
+ *   xh_m = x_m / r_m * gamma
+ *   y_m  = W xh_m,  W [(Hq + 2 Hkv) D, dim]              (one bias-free projection)
+ * and y_m splits into q (rows 0 .. Hq D - 1 of W), k (next Hkv D) and v (last Hkv D),
+ * each head D wide.  With rotate, q and k are rotated by R_t, t = m mod T (the RoPE of
+ * the attention above); v never is.  Outputs q [B, T, Hq, D], k and v [B, T, Hkv, D]. */
+int ne_ref_qkv_prologue(const double* x, const double* gamma, const double* w, double* q, double* k, double* v,
+                        int B, int T, int dim, int Hq, int Hkv, int D, double eps, double theta, int rotate) {
+    if (bad_shape(B, T, Hq, Hkv, D) || dim <= 0 || !(eps >= 0.0)) return 1;
+    const int N = (Hq + 2 * Hkv) * D;
+    const int64_t M = (int64_t)B * T;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const double* xm = x + m * dim;
+        double ss = 0.0;
+        for (int c = 0; c < dim; ++c) ss += xm[c] * xm[c];
+        const double r = std::sqrt(ss / (double)dim + eps);
+        std::vector<double> xh((size_t)dim), y((size_t)N), yr((size_t)D);
+        for (int c = 0; c < dim; ++c) xh[c] = xm[c] / r * gamma[c];
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int c = 0; c < dim; ++c) acc += w[(int64_t)n * dim + c] * xh[c];
+            y[n] = acc;
+        }
+        const int t = (int)(m % T);
+        for (int h = 0; h < Hq + 2 * Hkv; ++h) {
+            const double* yh = &y[(size_t)h * D];
+            const bool rot = rotate && h < Hq + Hkv;
+            if (rot) rotate_row(yh, yr.data(), t, D, theta);
+            const double* src = rot ? yr.data() : yh;
+            double* dst = h < Hq ? q + (m * Hq + h) * D
+                                 : (h < Hq + Hkv ? k + (m * Hkv + (h - Hq)) * D : v + (m * Hkv + (h - Hq - Hkv)) * D);
+            for (int d = 0; d < D; ++d) dst[d] = src[d];
+        }
+    }
+    return 0;
+}
+
 int ne_ref_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -344,3 +344,43 @@ def test_decode_reading_is_a_row_of_the_causal_attention(oracle_mod):
             np.testing.assert_allclose(o_row[0], o_pre[0, L - 1, h], rtol=0, atol=1e-13)
             np.testing.assert_allclose(o_row[0], o_full[0, L - 1, h], rtol=0, atol=1e-13)
             assert abs(l_row[0] - lse_full[0, h, L - 1]) < 1e-13 and abs(lse_pre[0, h, L - 1] - l_row[0]) < 1e-13
+
+
+# ---------------------------------------------------------------- RMSNorm -> QKV -> RoPE prologue
+
+def test_prologue_rows_have_unit_rms_and_ignore_the_row_scale(oracle_mod):
+    """With a unit gain, an identity projection and eps = 0, q | k | v of a token row is
+    x / rms(x): its root mean square is exactly 1, and scaling the row changes nothing."""
+    Hq, Hkv, D = 2, 1, 4
+    dim = (Hq + 2 * Hkv) * D
+    x = _rand((2, 3, dim), 61) * 5.0
+    gamma, w = np.ones(dim), np.eye(dim)
+    q, k, v = oracle_mod.qkv_prologue(x, gamma, w, Hq, Hkv, D, eps=0.0, rotate=False)
+    y = np.concatenate([q.reshape(2, 3, -1), k.reshape(2, 3, -1), v.reshape(2, 3, -1)], axis=-1)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=0, atol=1e-14)
+    q2, k2, v2 = oracle_mod.qkv_prologue(x * 7.25, gamma, w, Hq, Hkv, D, eps=0.0, rotate=False)
+    for a, b in ((q, q2), (k, k2), (v, v2)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
+
+
+def test_prologue_matches_torch_rms_norm_matmul_and_rope(oracle_mod):
+    """PyTorch's fp64 rms_norm (gain gamma, eps) and matmul, split into heads in the
+    order q, k, v, then RoPE on q and k by the oracle's rotation (pinned above)."""
+    B, T, Hq, Hkv, D, dim = 2, 9, 4, 2, 8, 24
+    x = _rand((B, T, dim), 62)
+    gamma = _rand((dim,), 63)
+    w = _rand(((Hq + 2 * Hkv) * D, dim), 64)
+    xt = torch.from_numpy(x)
+    y = (torch.nn.functional.rms_norm(xt, (dim,), weight=torch.from_numpy(gamma), eps=1e-5)
+         @ torch.from_numpy(w).T).numpy()
+    qu = y[..., :Hq * D].reshape(B, T, Hq, D)
+    ku = y[..., Hq * D:(Hq + Hkv) * D].reshape(B, T, Hkv, D)
+    vu = y[..., (Hq + Hkv) * D:].reshape(B, T, Hkv, D)
+    for theta in (10000.0, 500.0):
+        q, k, v = oracle_mod.qkv_prologue(x, gamma, w, Hq, Hkv, D, eps=1e-5, theta=theta, rotate=True)
+        np.testing.assert_allclose(q, oracle_mod.rope_apply(qu, theta), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(k, oracle_mod.rope_apply(ku, theta), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(v, vu, rtol=0, atol=1e-12)
+    q, k, v = oracle_mod.qkv_prologue(x, gamma, w, Hq, Hkv, D, eps=1e-5, rotate=False)
+    for a, b in ((q, qu), (k, ku), (v, vu)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)

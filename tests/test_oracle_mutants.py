@@ -39,6 +39,8 @@ INDEPENDENT_PINS = (
     "test_backward_matches_central_finite_differences",
     "test_matches_torch_sdpa_fp64_with_autograd",
     "test_row_sampled_oracle_zero_queries_closed_form",
+    "test_prologue_rows_have_unit_rms_and_ignore_the_row_scale",
+    "test_prologue_matches_torch_rms_norm_matmul_and_rope",
 )
 ROW_CONSISTENCY_PIN = "test_row_sampled_oracle_matches_full_oracle"
 
@@ -97,6 +99,15 @@ MUTANTS = [
        "accv += P[(size_t)i * T + j] * dO[idx4(b, i, g * G, d, T, Hq, D)];", 0)]),
     ("dk_drops_diagonal", "full", [("for (int i = j; i < T; ++i) {", "for (int i = j + 1; i < T; ++i) {", 0)]),
     # row-sampled entry points
+    # RMSNorm -> QKV projection -> RoPE prologue
+    ("rms_sum_not_mean", "full", [("std::sqrt(ss / (double)dim + eps)", "std::sqrt(ss + eps)", 0)]),
+    ("rms_eps_outside_sqrt", "full", [("std::sqrt(ss / (double)dim + eps)", "std::sqrt(ss / (double)dim) + eps", 0)]),
+    ("rms_gain_ignored", "full", [("xh[c] = xm[c] / r * gamma[c];", "xh[c] = xm[c] / r;", 0)]),
+    ("projection_transposed", "full", [("acc += w[(int64_t)n * dim + c] * xh[c];", "acc += w[(int64_t)c * N + n] * xh[c];", 0)]),
+    ("kv_split_swapped", "full", [("(h < Hq + Hkv ? k + (m * Hkv + (h - Hq)) * D : v + (m * Hkv + (h - Hq - Hkv)) * D)",
+                                   "(h < Hq + Hkv ? v + (m * Hkv + (h - Hq)) * D : k + (m * Hkv + (h - Hq - Hkv)) * D)", 0)]),
+    ("prologue_rotates_v", "full", [("const bool rot = rotate && h < Hq + Hkv;", "const bool rot = rotate != 0;", 0)]),
+    ("prologue_position_across_batch", "full", [("const int t = (int)(m % T);", "const int t = (int)m;", 0)]),
     ("rows_dq_drops_delta", "rows", [("const double ds = P[j] * (dP[j] - dl);", "const double ds = P[j] * dP[j];", 0)]),
     ("rows_gqa_heads_interleaved", "rows", [("const int g = h / (Hq / Hkv);", "const int g = h % Hkv;", 0)]),
     ("rows_lse_drops_row_max", "rows", [("const double l = m + std::log(sum);", "const double l = std::log(sum);", 0)]),
