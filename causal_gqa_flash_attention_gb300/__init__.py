@@ -33,7 +33,7 @@ EXPORTS = (
     "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown", "ne_attn_bwd_noalloc",
     "ne_profile_enable", "ne_profile_totals", "ne_attn_decode_workspace_size", "ne_attn_decode",
     "ne_attn_decode_f32", "ne_noalloc_get_device_error", "ne_attn_fwd_varlen", "ne_attn_fwd_varlen_f32",
-    "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32",
+    "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32", "ne_qkv_prologue",
 )
 
 
@@ -74,6 +74,7 @@ def load(path: str | None = None):
         lib.ne_attn_fwd_varlen_f32.argtypes = lib.ne_attn_fwd_varlen.argtypes
         lib.ne_attn_bwd_varlen.argtypes = [vp] * 10 + [i] * 5 + [d, vp, sz, vp]
         lib.ne_attn_bwd_varlen_f32.argtypes = lib.ne_attn_bwd_varlen.argtypes
+        lib.ne_qkv_prologue.argtypes = [vp] * 6 + [i] * 6 + [d, d, i, vp]
         lib.ne_noalloc_get_device_error.argtypes = [vp]
         lib.ne_profile_enable.argtypes = [i]
         lib.ne_profile_enable.restype = None
@@ -88,7 +89,7 @@ def load(path: str | None = None):
         for f in ("ne_rope_table", "ne_attn_fwd", "ne_attn_fwd_f32", "ne_attn_bwd", "ne_attn_bwd_f32",
                   "ne_get_device_error", "ne_selftest_wait_timeout", "ne_attn_bwd_noalloc", "ne_attn_decode",
                   "ne_noalloc_get_device_error", "ne_attn_fwd_varlen", "ne_attn_fwd_varlen_f32",
-                  "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32",
+                  "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32", "ne_qkv_prologue",
                   "ne_attn_decode_f32"):
             getattr(lib, f).restype = i
         _lib = lib
@@ -220,6 +221,29 @@ def attn_bwd_varlen(q, k, v, o, lse, dO, seq_lens, theta: float = 10000.0, works
               B, T, Hq, Hkv, D, float(theta), _ptr(workspace), workspace.numel() * workspace.element_size(),
               _stream(q)))
     return dq, dk, dv
+
+
+def qkv_prologue(x, gamma, w, Hq: int, Hkv: int, D: int, eps: float = 1e-5, theta: float = 10000.0,
+                 rotate: bool = False, q=None, k=None, v=None):
+    """RMSNorm (gain gamma) -> projection w [(Hq + 2 Hkv) D, dim] -> q, k, v heads, RoPE
+    on q and k when `rotate` (the attention calls take the unrotated form).  x [B, T, dim]
+    bf16; returns q [B, T, Hq, D], k and v [B, T, Hkv, D] bf16."""
+    lib = load()
+    if x.dim() != 3:
+        raise ValueError("x must be [B, T, dim]")
+    B, T, dim = x.shape
+    N = (Hq + 2 * Hkv) * D
+    for t in (x, gamma, w):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16 or t.device != x.device:
+            raise ValueError("x, gamma and w must be contiguous bf16 CUDA tensors on one device")
+    if tuple(gamma.shape) != (dim,) or tuple(w.shape) != (N, dim):
+        raise ValueError(f"gamma must be [dim] and w [(Hq + 2 Hkv) D, dim] = [{N}, {dim}]")
+    q = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device=x.device) if q is None else q
+    k = torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=x.device) if k is None else k
+    v = torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=x.device) if v is None else v
+    _check(lib.ne_qkv_prologue(_ptr(x), _ptr(gamma), _ptr(w), _ptr(q), _ptr(k), _ptr(v), B, T, dim, Hq, Hkv, D,
+                               float(eps), float(theta), 1 if rotate else 0, _stream(x)))
+    return q, k, v
 
 
 def decode_workspace_size(B, T_max, Hq, Hkv, D) -> int:

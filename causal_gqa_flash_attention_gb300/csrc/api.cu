@@ -200,6 +200,23 @@ ne_status map_bthd(CUtensorMap* m, const void* ptr, bool f32, int B, int T, int 
     return NE_OK;
 }
 
+// Tiled map over a row-major bf16 matrix [rows, cols]: box = (64 columns = 128 bytes,
+// box_rows rows), 128-byte swizzle, zero fill out of bounds.
+ne_status map_rows_bf16(CUtensorMap* m, const void* ptr, long long rows, int cols, int box_rows) {
+    EncodeTiledFn enc;
+    ne_status s = encode_fn(&enc);
+    if (s != NE_OK) return s;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return NE_OK;
+}
+
 // ------------------------------------------------------------------ validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -597,6 +614,57 @@ ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* 
                              void* workspace, size_t workspace_bytes, ne_stream_t stream) {
     return attn_decode_impl(true, q, k_cache, v_cache, seq_lens, o, lse, B, T_max, Hq, Hkv, D, rope_theta,
                             workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void* q, void* k, void* v, int B, int T,
+                          int dim, int Hq, int Hkv, int D, double eps, double rope_theta, int rotate,
+                          ne_stream_t stream) {
+    g_last_error.clear();
+    cudaStream_t st = (cudaStream_t)stream;
+    if (B < 0 || T < 0) return fail(NE_ERR_INVALID_ARG, "B and T must be >= 0 (B=%d T=%d)", B, T);
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+        return fail(NE_ERR_INVALID_ARG, "need Hq > 0, Hkv > 0 and Hq %% Hkv == 0 (Hq=%d Hkv=%d)", Hq, Hkv);
+    if (D != 32 && D != 64 && D != 128)
+        return fail(NE_ERR_UNSUPPORTED, "head_dim D=%d is not supported (supported: 32, 64, 128)", D);
+    if (dim <= 0 || dim % 8 != 0) return fail(NE_ERR_INVALID_ARG, "dim must be a positive multiple of 8 (dim=%d)", dim);
+    if (!(eps >= 0.0) || !std::isfinite(eps)) return fail(NE_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
+        return fail(NE_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    const long long M = (long long)B * T;
+    const long long N = (long long)(Hq + 2 * Hkv) * D;
+    if (M * dim >= (1LL << 31) || M * N >= (1LL << 31) || (M + 127) / 128 > 65535)
+        return fail(NE_ERR_INVALID_ARG, "shape too large: B*T*dim and B*T*(Hq+2Hkv)*D must be < 2^31");
+    if (M == 0) return NE_OK;
+    ne_status s;
+    if ((s = check_ptrs({x, gamma, w, q, k, v})) != NE_OK) return s;
+    int dev;
+    if ((s = current_device(&dev)) != NE_OK) return s;
+    int* err;
+    if ((s = error_word(dev, &err)) != NE_OK) return s;
+    const float2* rope;
+    if ((s = rope_cache(dev, T, D, rope_theta, st, &rope)) != NE_OK) return s;
+    CUtensorMap tx, tw;
+    if ((s = map_rows_bf16(&tx, x, M, dim, 128)) != NE_OK) return s;
+    if ((s = map_rows_bf16(&tw, w, N, dim, ne::prologue_tile_n())) != NE_OK) return s;
+    ne::ProArgs a;
+    a.gamma = gamma;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.rope = rope;
+    a.M = (int)M;
+    a.T = T;
+    a.dim = dim;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.eps = (float)eps;
+    a.rotate = rotate;
+    a.err = err;
+    a.timeout_ns = timeout_ns();
+    cudaError_t e = ne::launch_qkv_prologue(tx, tw, a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "qkv prologue launch");
+    return NE_OK;
 }
 
 const char* ne_status_string(ne_status s) {

@@ -17,6 +17,7 @@ enum WaitSite : int {
     SITE_BWD_DP_FULL, SITE_BWD_DS_READY, SITE_BWD_DS_FREE, SITE_BWD_DQ_FULL, SITE_BWD_DQ_FREE,
     SITE_BWD_DKV, SITE_BWD_DRAIN,
     SITE_SELFTEST = 0x301,
+    SITE_PRO_EMPTY = 0x501, SITE_PRO_READY, SITE_PRO_FULL, SITE_PRO_ACC, SITE_PRO_DRAIN,
     // Not a wait: a rotated q/k value exceeded the fp16 range of the logit operand.
     SITE_RANGE = 0x401,
     // Not a wait: a decode call got a sequence length outside [1, T_max].
@@ -106,6 +107,20 @@ struct BwdArgs {
     int dr;                  // the tensors' head_dim (bf16 32 runs the 64-wide kernel, zero-padded)
 };
 
+// RMSNorm -> QKV projection -> RoPE prologue (qkv_prologue.cu), bf16 tensors.
+struct ProArgs {
+    const void* gamma;       // [dim] RMSNorm gain
+    void* q;                 // [B,T,Hq,D]
+    void* k;                 // [B,T,Hkv,D]
+    void* v;                 // [B,T,Hkv,D]
+    const float2* rope;      // [>= T, D/2] (cos, sin)
+    int M, T, dim, Hq, Hkv, D;   // M = B * T token rows
+    float eps;
+    int rotate;              // nonzero: RoPE on the query and key heads
+    int* err;
+    unsigned long long timeout_ns;
+};
+
 struct BwdPostArgs {
     const float* dq_acc;     // [B,T,Hq,D]
     void* dq;                // [B,T,Hq,D]
@@ -164,6 +179,10 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Prologue: tx maps x [M, dim] bf16 with (64 x 128) boxes, tw maps W [N, dim] bf16 with
+// (64 x prologue_tile_n()) boxes.
+int prologue_tile_n();
+cudaError_t launch_qkv_prologue(const CUtensorMap& tx, const CUtensorMap& tw, const ProArgs& a, cudaStream_t st);
 // Tile rows of the key/value tensor maps the forward kernel expects.
 int fwd_kv_box_rows(bool tf32, int D);
 // Launchers: return cudaSuccess or the launch error.

@@ -1,0 +1,219 @@
+// qkv_prologue.cu -- the steps before attention in every layer, fused into one tcgen05
+// GEMM: RMSNorm (pre-normalization, gain gamma, no bias), one bias-free projection to the
+// query, key and value heads, and RoPE on the query and key heads ("NanoEuler: C와 CUDA로
+// 밑바닥부터 구축한 GPT-2 규모의 LLM", 기술 사양: RMSNorm, RoPE and GQA bullets; the pages
+// run this projection on cuBLAS TF32 tensor cores, 커널 구현).  For token row m:
+//   r_m = sqrt(mean_c x_mc^2 + eps),   y_m = W (x_m o gamma) / r_m
+// with W [(Hq + 2 Hkv) D, dim] (query heads, then key heads, then value heads).  Since
+// 1/r_m is one factor per output row, it is applied to the fp32 accumulator in the
+// epilogue; gamma multiplies the x tile in shared memory before the MMA reads it.
+//
+// One CTA per 128-row x 256-column output tile; the dim (K) axis streams through an
+// NS-stage ring of 64-column chunks (x: 128 rows, W: 256 rows, 128 bytes each,
+// 128-byte-swizzled by TMA).  Warp roles (192 threads):
+//   warp 0      TMA producer.
+//   warp 1      TMEM owner (256 columns) and UMMA issuer: M128 N256 K16, 4 per chunk.
+//   warps 2-5   thread = token row = TMEM lane: per chunk, the row's sum of squares and
+//               x o gamma written back in place (bf16); at the end the epilogue:
+//               acc / r_m, RoPE on query and key heads (position m mod T), bf16 stores.
+// Every wait is bounded; a CTA that gives up records an error code, drains its own copies
+// and MMAs and frees its TMEM.
+#include <cuda_bf16.h>
+#include "kernels.h"
+#include "ptx.cuh"
+#include "rope_smem.cuh"
+
+namespace ne {
+
+namespace {
+
+struct ProCfg {
+    static constexpr int BM = 128;                  // token rows per tile
+    static constexpr int BN = 256;                  // output features per tile
+    static constexpr int BK = 64;                   // dim elements per chunk (128 bytes)
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int NS = 4;
+    static constexpr int SMEM = 1024 + NS * STAGE;
+    static constexpr int THREADS = 192;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+__global__ void __launch_bounds__(192, 1)
+    qkv_prologue_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                        const ProArgs a) {
+    using C = ProCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    auto st_a = [&](int s) { return smem + s * C::STAGE; };
+    auto st_b = [&](int s) { return smem + s * C::STAGE + C::A_BYTES; };
+
+    __shared__ __align__(8) uint64_t bar_full[C::NS], bar_ready[C::NS], bar_empty[C::NS];
+    __shared__ __align__(8) uint64_t bar_acc;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * C::BN, m0 = blockIdx.y * C::BM;
+    const int nk = (a.dim + C::BK - 1) / C::BK;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_ready[s]), 128);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&bar_acc), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(smem_u32(&tmem_slot), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    griddep_launch_dependents();   // after the TMEM allocation
+    griddep_wait();
+    const uint32_t tm = tmem_slot;
+    const WaitCtx w{a.err, &abort_flag, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_x);
+            tma_prefetch_desc(&tm_w);
+            int issued = 0;
+            for (int kc = 0; kc < nk; ++kc) {
+                const int s = kc % C::NS;
+                if (kc >= C::NS && !mbar_wait(smem_u32(&bar_empty[s]), ((kc / C::NS) - 1) & 1, w, SITE_PRO_EMPTY))
+                    break;
+                const uint32_t f = smem_u32(&bar_full[s]);
+                mbar_arrive_expect_tx(f, C::STAGE);
+                tma_load_2d(smem_u32(st_a(s)), &tm_x, f, kc * C::BK, m0);
+                tma_load_2d(smem_u32(st_b(s)), &tm_w, f, kc * C::BK, n0);
+                ++issued;
+            }
+            // Teardown: every copy this CTA started must have landed before exit.
+            for (int kc = max(0, issued - C::NS); kc < issued; ++kc)
+                mbar_wait_drain(smem_u32(&bar_full[kc % C::NS]), (kc / C::NS) & 1, w, SITE_PRO_DRAIN);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ UMMA issuer
+        constexpr uint32_t id = idesc_make(FMT_BF16, 128, C::BN, false, false);
+        const uint64_t da0 = sdesc(smem_u32(st_a(0)), 16, 1024), db0 = sdesc(smem_u32(st_b(0)), 16, 1024);
+        for (int kc = 0; kc < nk; ++kc) {
+            const int s = kc % C::NS;
+            if (!mbar_wait_warp(smem_u32(&bar_ready[s]), (kc / C::NS) & 1, w, SITE_PRO_READY)) break;
+            tc_fence_after();
+            const uint64_t da = sdesc_add(da0, s * C::STAGE), db = sdesc_add(db0, s * C::STAGE);
+#pragma unroll
+            for (int ks = 0; ks < C::BK / 16; ++ks)   // K = dim, 16 per step (32 bytes)
+                umma_ss_e<false>(tm, sdesc_add(da, ks * 32), sdesc_add(db, ks * 32), id, (kc > 0 || ks > 0) ? 1u : 0u);
+            umma_commit_e(smem_u32(&bar_empty[s]));
+        }
+        umma_commit_e(smem_u32(&bar_acc));   // also the teardown's: every MMA of this CTA
+    } else {
+        // ------------------------------------------------------------ norm, gain; epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;              // token row of the tile = TMEM lane
+        const int m = m0 + r;
+        const uint32_t lt = tm + ((uint32_t)(quarter * 32) << 16);
+        const uint4* g4 = reinterpret_cast<const uint4*>(a.gamma);
+        float ss = 0.f;
+        bool ok = true;
+        for (int kc = 0; kc < nk; ++kc) {
+            const int s = kc % C::NS;
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_full[s]), (kc / C::NS) & 1, w, SITE_PRO_FULL))) break;
+            uint8_t* arow = st_a(s);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c0 = kc * C::BK + 8 * u;      // dim index of the unit's first element
+                uint4* p = reinterpret_cast<uint4*>(arow + sw128_offset(r, u));
+                const uint4 xv = *p;
+                // Past dim the tile holds TMA's zero fill; its gain is taken as 0.
+                const uint4 gv = c0 < a.dim ? __ldg(g4 + (c0 >> 3)) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[e]));
+                    const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+                    ss = fmaf(xf.x, xf.x, fmaf(xf.y, xf.y, ss));
+                    o[e] = pack_bf162(xf.x * gf.x, xf.y * gf.y);
+                }
+                *p = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_ready[s]));
+        }
+        if (ok && mbar_wait_warp(smem_u32(&bar_acc), 0, w, SITE_PRO_ACC)) {
+            tc_fence_after();
+            const float inv_r = rsqrtf(ss / (float)a.dim + a.eps);
+            const int t = m % a.T;
+            const int nh = a.Hq + 2 * a.Hkv, D = a.D;
+#pragma unroll 1
+            for (int c = 0; c < C::BN; c += 32) {
+                uint32_t x[32];
+                tmem_ld32(lt + c, x);
+                tmem_wait_ld();
+                reg_fence32(x);
+                const int n = n0 + c;                   // first output feature of the chunk
+                if (m >= a.M || n >= nh * D) continue;
+                const int h = n / D, e0 = n - h * D;    // head and column within it (32 | D)
+                float y[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) y[e] = __uint_as_float(x[e]) * inv_r;
+                if (a.rotate && h < a.Hq + a.Hkv) {     // RoPE on query and key heads
+                    const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)t * (D / 2) + e0 / 2);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 cs = __ldg(tab + e / 4);
+                        const float y0 = y[e], y1 = y[e + 1], y2 = y[e + 2], y3 = y[e + 3];
+                        y[e] = y0 * cs.x - y1 * cs.y;
+                        y[e + 1] = y0 * cs.y + y1 * cs.x;
+                        y[e + 2] = y2 * cs.z - y3 * cs.w;
+                        y[e + 3] = y2 * cs.w + y3 * cs.z;
+                    }
+                }
+                __nv_bfloat16* dst = h < a.Hq ? static_cast<__nv_bfloat16*>(a.q) + ((size_t)m * a.Hq + h) * D
+                                     : h < a.Hq + a.Hkv
+                                         ? static_cast<__nv_bfloat16*>(a.k) + ((size_t)m * a.Hkv + (h - a.Hq)) * D
+                                         : static_cast<__nv_bfloat16*>(a.v) + ((size_t)m * a.Hkv + (h - a.Hq - a.Hkv)) * D;
+                uint4* d4 = reinterpret_cast<uint4*>(dst + e0);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    d4[u] = make_uint4(pack_bf162(y[8 * u], y[8 * u + 1]), pack_bf162(y[8 * u + 2], y[8 * u + 3]),
+                                       pack_bf162(y[8 * u + 4], y[8 * u + 5]), pack_bf162(y[8 * u + 6], y[8 * u + 7]));
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        mbar_wait_drain(smem_u32(&bar_acc), 0, w, SITE_PRO_DRAIN);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tm, 256);
+    }
+}
+
+}  // namespace
+
+int prologue_tile_n() { return ProCfg::BN; }
+
+cudaError_t launch_qkv_prologue(const CUtensorMap& tx, const CUtensorMap& tw, const ProArgs& a, cudaStream_t st) {
+    auto kfn = qkv_prologue_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ProCfg::SMEM);
+    if (e != cudaSuccess) return e;
+    const int N = (a.Hq + 2 * a.Hkv) * a.D;
+    dim3 grid((N + ProCfg::BN - 1) / ProCfg::BN, (a.M + ProCfg::BM - 1) / ProCfg::BM);
+    return launch_k(kfn, grid, dim3(ProCfg::THREADS), ProCfg::SMEM, st, tx, tw, a);
+}
+
+}  // namespace ne

@@ -143,3 +143,13 @@ def make_decode(B, T_max, Hq, Hkv, D, dtype=torch.bfloat16, seed=1, lens=None, t
             k[b, int(lens[b]):] = tail
             v[b, int(lens[b]):] = tail
     return q, k, v, lens
+
+
+def make_prologue(B, T, dim, Hq, Hkv, D, seed=1):
+    """Inputs of the RMSNorm -> QKV -> RoPE prologue, bf16 on the CPU: x [B, T, dim]
+    i.i.d. N(0, 1); gamma [dim] = 1 + N(0, 0.1^2) (a trained RMSNorm gain stays near 1);
+    w [(Hq + 2 Hkv) D, dim] i.i.d. N(0, 1/dim) (unit-variance outputs)."""
+    x = randn((B, T, dim), seed * 16 + 4, 1.0, torch.bfloat16)
+    gamma = (1.0 + randn((dim,), seed * 16 + 5, 0.1, torch.float32)).to(torch.bfloat16)
+    w = randn(((Hq + 2 * Hkv) * D, dim), seed * 16 + 6, dim ** -0.5, torch.bfloat16)
+    return x, gamma, w

@@ -206,6 +206,27 @@ ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* 
                              int Hq, int Hkv, int D, double rope_theta, void* workspace,
                              size_t workspace_bytes, ne_stream_t stream);
 
+/* The steps before attention in every layer, fused into one tensor-core GEMM ("NanoEuler:
+ * C와 CUDA로 밑바닥부터 구축한 GPT-2 규모의 LLM", 기술 사양: RMSNorm as pre-normalization
+ * without bias, RoPE on queries and keys; the model has no biases): for token row m of x,
+ *   r_m = sqrt(mean_c x_mc^2 + eps),   y_m = W (x_m o gamma) / r_m,
+ * split into query heads (rows 0 .. Hq*D-1 of W), key heads (next Hkv*D rows) and value
+ * heads (last Hkv*D rows).  With rotate != 0 the query and key heads are rotated by the
+ * RoPE of the attention calls (position m mod T, theta rope_theta); the attention calls
+ * take unrotated q and k (they rotate as their tiles load), so the form they consume is
+ * rotate = 0.
+ *   x     [B, T, dim] bf16 (in)          gamma [dim] bf16 (in)
+ *   w     [(Hq + 2 Hkv) * D, dim] bf16, row-major (in: row n holds output feature n)
+ *   q     [B, T, Hq, D] bf16 (out)       k, v  [B, T, Hkv, D] bf16 (out)
+ * Arithmetic: bf16 tensor-core products with fp32 accumulation; x o gamma is rounded to
+ * bf16 before the product, the root-mean-square is fp32.  Supported: D in {32, 64, 128},
+ * dim a multiple of 8, Hq % Hkv == 0, B*T*dim and B*T*(Hq + 2 Hkv)*D below 2^31, eps
+ * >= 0.  Pointers 16-byte aligned.  The first call for a new (device, T, D, theta)
+ * builds its RoPE table and synchronises `stream` once (as the attention calls do). */
+ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void* q, void* k, void* v,
+                          int B, int T, int dim, int Hq, int Hkv, int D, double eps,
+                          double rope_theta, int rotate, ne_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* ne_status_string(ne_status s);
 /* Detail of the last error on the calling thread ("" if none). */

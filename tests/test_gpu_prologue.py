@@ -1,0 +1,87 @@
+"""GPU parity of the fused RMSNorm -> QKV projection -> RoPE prologue (ne_qkv_prologue)
+against the fp64 oracle (oracle.qkv_prologue, pinned in test_oracle.py).
+
+Bound: relative Frobenius error <= 5e-3 per output (q, k, v), the bound of the bf16
+attention outputs: the products are bf16 with fp32 accumulation, x o gamma and the
+outputs are rounded to bf16 (about 2^-9 relative each).
+"""
+import numpy as np
+import pytest
+import torch
+
+import causal_gqa_flash_attention_gb300 as ne
+from causal_gqa_flash_attention_gb300 import _build, synthetic
+
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build()
+    ne.load()
+
+
+def rel(x, ref):
+    x = np.asarray(x, np.float64).ravel()
+    ref = np.asarray(ref, np.float64).ravel()
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+def check(B, T, dim, Hq, Hkv, D, rotate, eps=1e-5, theta=10000.0, seed=3, rows=None):
+    import oracle
+    x, gamma, w = synthetic.make_prologue(B, T, dim, Hq, Hkv, D, seed=seed)
+    q, k, v = ne.qkv_prologue(x.cuda(), gamma.cuda(), w.cuda(), Hq, Hkv, D, eps, theta, rotate)
+    torch.cuda.synchronize()
+    assert ne.get_device_error() == ne.NE_OK, ne.last_error()
+    f = lambda t: t.double().cpu().numpy()
+    sel = slice(None) if rows is None else rows            # batch rows the oracle computes
+    q_r, k_r, v_r = oracle.qkv_prologue(f(x[sel]), f(gamma), f(w), Hq, Hkv, D, eps, theta, rotate)
+    errs = {"q": rel(f(q[sel]), q_r), "k": rel(f(k[sel]), k_r), "v": rel(f(v[sel]), v_r)}
+    print((B, T, dim, Hq, Hkv, D, rotate), errs)
+    for name, e in errs.items():
+        assert e <= TOL, (name, errs)
+    for t in (q, k, v):
+        assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+def test_small_model_shape(rotate):
+    """dim 128, 4/2 heads of 32, context 128 (the small model of the config table)."""
+    check(4, 128, 128, 4, 2, 32, rotate)
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+def test_gpu_pipeline_shape_two_sequences(rotate):
+    """dim 768, 12/4 heads of 64, T = 512 (the GPU-pipeline model), all rows checked."""
+    check(2, 512, 768, 12, 4, 64, rotate)
+
+
+def test_gpu_pipeline_full_batch_sampled_sequences():
+    """The full B = 16 batch at once; the first and last sequences are checked."""
+    check(16, 512, 768, 12, 4, 64, True, rows=[0, 15])
+
+
+def test_ragged_rows_and_dim_tail_head_dim_128_theta_500():
+    """B*T = 231 rows (not a multiple of the 128-row tile), dim = 200 (not a multiple of
+    the 64-wide chunk), head_dim 128, theta 500, eps 1e-6."""
+    check(3, 77, 200, 4, 1, 128, True, eps=1e-6, theta=500.0)
+
+
+def test_output_feeds_the_attention_forward():
+    """The unrotated outputs are what ne_attn_fwd takes: chained, they match the oracle's
+    prologue followed by its attention."""
+    import oracle
+    B, T, dim, Hq, Hkv, D = 2, 200, 256, 4, 2, 64
+    x, gamma, w = synthetic.make_prologue(B, T, dim, Hq, Hkv, D, seed=9)
+    q, k, v = ne.qkv_prologue(x.cuda(), gamma.cuda(), w.cuda(), Hq, Hkv, D)
+    o, lse = ne.attn_fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert ne.get_device_error() == ne.NE_OK
+    f = lambda t: t.double().cpu().numpy()
+    q_r, k_r, v_r = oracle.qkv_prologue(f(x), f(gamma), f(w), Hq, Hkv, D, rotate=False)
+    o_r, _ = oracle.attn_fwd(q_r, k_r, v_r)
+    assert rel(f(o), o_r) <= 1e-2
