@@ -46,6 +46,9 @@ def parse():
                         "line: the command profilers run")
     p.add_argument("--decode", action="store_true",
                    help="time the decode step over a KV cache instead (cache-read GB/s)")
+    p.add_argument("--prologue", action="store_true",
+                   help="only the fused RMSNorm -> QKV -> RoPE prologue at the GPU-pipeline shape (K steps of 16 "
+                        "layers), then a short line")
     p.add_argument("--phase-timing", choices=["timed", "separate"], default="separate",
                    help="per-kernel CUDA events inside the timed region, or (default) in as many profiled "
                         "steps right after it: events between kernels cost ~20%% and disable the overlap of "
@@ -787,6 +790,20 @@ def main():
     w = synthetic.WORKLOADS[args.workload]
     if args.decode and args.impl == "ours":
         run_decode(args)
+        return
+    if args.prologue and args.impl == "ours":
+        import torch
+
+        import causal_gqa_flash_attention_gb300 as ne
+        from causal_gqa_flash_attention_gb300 import _build
+        _build.build()
+        ne.load()
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        line = prologue_point(dev, args.steps, measured_peaks()["bf16_tflops"])
+        if ne.get_device_error() != ne.NE_OK:
+            raise RuntimeError("device error: " + ne.last_error())
+        print(json.dumps({"prologue": True, **line}), flush=True)
         return
     if args.impl == "reference":
         run_reference(args, w)

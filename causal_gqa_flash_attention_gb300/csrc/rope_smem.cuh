@@ -71,9 +71,11 @@ struct RopeTile {
 #pragma unroll
         for (int e = 0; e < F4; ++e) b[e] = __ldg(bp + e);
     }
-    // Rotates the tile; with CHECK, returns true if an fp16 output would have overflowed
-    // (without, the caller detects overflow downstream and this returns false).  Rows
-    // zero_row and later (padding past a sequence's length) are written as zeros.
+    // Rotates the tile; with CHECK, returns true if an fp16 output of a row before
+    // zero_row would have overflowed (without, the caller detects overflow downstream and
+    // this returns false).  Rows zero_row and later (padding past a sequence's length) are
+    // then overwritten with zeros; the rotation itself reads every row unconditionally, so
+    // the common case (no padding in the tile) runs the plain loop.
     template <bool CHECK = true>
     __device__ __forceinline__ bool apply(uint8_t* base, uint8_t* dst16, float4 (&b)[F4],
                                           int zero_row = ROWS) const {
@@ -82,7 +84,7 @@ struct RopeTile {
         for (int k = 0; k < KSTEPS; ++k) {
             const int row = r0 + k * RSTEP;
             const uint32_t off = (unit >> 3) * ROWS * 128 + sw128_offset(row, unit & 7);
-            const uint4 raw = row < zero_row ? *reinterpret_cast<const uint4*>(base + off) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 raw = *reinterpret_cast<const uint4*>(base + off);
             if constexpr (MODE == ROPE_TF32) {
                 const float4 cs = b[0];
                 const float x0 = __uint_as_float(raw.x), x1 = __uint_as_float(raw.y);
@@ -100,7 +102,7 @@ struct RopeTile {
                     const float x0 = __low2float(v), x1 = __high2float(v);
                     const float c = cs[2 * p], s = cs[2 * p + 1];
                     const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
-                    if constexpr (CHECK) amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+                    if constexpr (CHECK) amax = fmaxf(amax, row < zero_row ? fmaxf(fabsf(y0), fabsf(y1)) : 0.f);
                     o16[p] = pack_half2(y0, y1);
                     if constexpr (MODE == ROPE_BF16_F16) ob[p] = pack_bf162(y0, y1);
                 }
@@ -118,6 +120,16 @@ struct RopeTile {
                     b[e] = make_float4(c.x * s.x - c.y * s.y, c.y * s.x + c.x * s.y,
                                        c.z * s.z - c.w * s.w, c.w * s.z + c.z * s.w);
                 }
+            }
+        }
+        if (zero_row < ROWS) {      // padding rows: zeros in every output
+#pragma unroll
+            for (int k = 0; k < KSTEPS; ++k) {
+                const int row = r0 + k * RSTEP;
+                if (row < zero_row) continue;
+                const uint32_t off = (unit >> 3) * ROWS * 128 + sw128_offset(row, unit & 7);
+                *reinterpret_cast<uint4*>(base + off) = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (MODE == ROPE_BF16_F16) *reinterpret_cast<uint4*>(dst16 + off) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         return amax > 65504.f;   // largest finite fp16
