@@ -309,6 +309,8 @@ ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, v
     a.timeout_ns = timeout_ns();
     a.seq_lens = seq_lens;
     a.dr = D;
+    a.div_bh = ne::make_fastdiv((uint32_t)(B * Hq));   // B, Hq >= 1 here
+    a.div_hq = ne::make_fastdiv((uint32_t)Hq);
     cudaError_t e = timed(0, st, [&] { return ne::launch_fwd(f32, D, B, tq, tk, tv, to, a, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
     return NE_OK;

@@ -43,7 +43,7 @@ namespace {
 // order.  Each warp zeroes the accumulator rows of the units it reads: interleaving the
 // zero stores with the loads row by row kept HBM busier than a zeroing sweep followed by
 // the loads.
-template <typename Tin, int D>
+template <typename Tin, int D, bool VL>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
     constexpr int EPV = 16 / sizeof(Tin);        // elements per 16-byte vector
     constexpr int LPR = D / EPV;                 // lanes per row (8 or 16)
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
                     const uint32_t bb = fast_div(bt, a.div_t);
                     const uint32_t t = bt - bb * (uint32_t)a.T;
                     // Padding positions (past the sequence's length) get R Q = 0.
-                    const bool pad = (int)t >= seq_len(a.seq_lens, (int)bb, a.T);
+                    const bool pad = VL && (int)t >= seq_len(a.seq_lens, (int)bb, a.T);
                     const float4* cs4 = reinterpret_cast<const float4*>(a.rope + (size_t)t * a.rope_ld + 4 * li);
                     const float4 c01 = __ldg(cs4), c23 = __ldg(cs4 + 1);
                     const float cs[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
                     for (int pr = 0; pr < 4; ++pr) {
                         const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[pr]));
                         const float c = cs[2 * pr], sn = cs[2 * pr + 1];
-                        const float y0 = pad ? 0.f : x.x * c - x.y * sn, y1 = pad ? 0.f : x.x * sn + x.y * c;
+                        const float y0 = pad ? 0.f : rot0(x.x, x.y, c, sn), y1 = pad ? 0.f : rot1(x.x, x.y, c, sn);
                         ovf |= fmaxf(fabsf(y0), fabsf(y1)) > 65504.f;
                         const __half2 h = __floats2half2_rn(y0, y1);
                         o16[pr] = *reinterpret_cast<const uint32_t*>(&h);
@@ -140,7 +140,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
             if (row < rows && li == 0) {
                 const uint32_t bt = fast_div(row, a.div_hq), b = fast_div(bt, a.div_t);
                 const uint32_t h = row - bt * (uint32_t)a.Hq, t = bt - b * (uint32_t)a.T;
-                a.delta[(b * (uint32_t)a.Hq + h) * (uint32_t)a.T + t] = (int)t < seq_len(a.seq_lens, (int)b, a.T) ? acc : 0.f;
+                a.delta[(b * (uint32_t)a.Hq + h) * (uint32_t)a.T + t] =
+                    !VL || (int)t < seq_len(a.seq_lens, (int)b, a.T) ? acc : 0.f;
             }
         }
     }
@@ -249,7 +250,9 @@ struct BwdCfg {
     static_assert(DS_BYTES == Q_BYTES || !DS_ALIASES_Q16, "alias needs equal sizes");
 };
 
-template <int D>
+// VL: per-sequence lengths (padded batch).  Without them every length is T, rows past T
+// arrive as TMA's zero fill, and the padding code compiles away.
+template <int D, bool VL>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(512, 1)
     const int kv0 = j * C::BKV;
     // Query tiles end at the sequence's length (T without per-sequence lengths); a key
     // tile wholly past it has no query tile and writes zero gradients.
-    const int len = seq_len(a.seq_lens, b, T);
+    const int len = VL ? seq_len(a.seq_lens, b, T) : T;
     const int n_qt = (len + C::BQ - 1) / C::BQ;
     const int i_first = kv0 / C::BQ;
     const int per_head = n_qt > i_first ? n_qt - i_first : 0;
@@ -308,6 +311,12 @@ __global__ void __launch_bounds__(512, 1)
         }
         abort_flag = 0;
         fence_mbar_init();
+        // The tensor maps are kernel parameters, not outputs of an earlier kernel: fetch
+        // them before the dependency wait, under the previous kernel's tail.
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
     }
     if (warp == 1) {
         __syncwarp();
@@ -329,10 +338,6 @@ __global__ void __launch_bounds__(512, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_do);
             const uint32_t kvf = smem_u32(&bar_kv_full);
             mbar_arrive_expect_tx(kvf, 2 * C::KV_BYTES);
             for (int c = 0; c < C::NCH; ++c) {
@@ -490,7 +495,8 @@ __global__ void __launch_bounds__(512, 1)
         };
         bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
         if (ok) {
-            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_BF16_F16>(sK, sK16, kv0, T, r, a.rope, len);
+            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_BF16_F16>(sK, sK16, kv0, T, r, a.rope,
+                                                                 VL ? len : kv0 + C::BKV);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready));
         }
@@ -504,7 +510,8 @@ __global__ void __launch_bounds__(512, 1)
                 if (C::DS_ALIASES_Q16 && it > 0 &&
                     !(ok = mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE)))
                     break;
-                ovf |= rope_tile_smem<D, C::BQ, 128, ROPE_BF16_F16>(stage_q(s), stage_q16(s), q0, T, r, a.rope, len);
+                ovf |= rope_tile_smem<D, C::BQ, 128, ROPE_BF16_F16>(stage_q(s), stage_q16(s), q0, T, r, a.rope,
+                                                                    VL ? len : q0 + C::BQ);
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&bar_q_ready[s]));
             }
@@ -552,7 +559,7 @@ __global__ void __launch_bounds__(512, 1)
             float lv_n = 0.f, dv_n = 0.f;
             if (it + 1 < n_it && r < 64) row_vals(it + 1, lv_n, dv_n);    // in flight during this step
             // Per-element masks: the causal diagonal, and queries past the length (padding).
-            const bool diag = kv0 + C::BKV - 1 > q0 || q0 + C::BQ > len;
+            const bool diag = kv0 + C::BKV - 1 > q0 || (VL && q0 + C::BQ > len);
             if (!mbar_wait_warp(smem_u32(&bar_s_full), it & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
             if (!mbar_wait_warp(smem_u32(&bar_dp_full), it & 1, w, SITE_BWD_DP_FULL)) { ok = false; break; }
             if (it > 0 && !mbar_wait_warp(smem_u32(&bar_ds_free), (it - 1) & 1, w, SITE_BWD_DS_FREE)) { ok = false; break; }
@@ -577,7 +584,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
-                        if (diag && (kvpos > q0 + cbase + c + e + k || q0 + cbase + c + e + k >= len)) p[k] = 0.f;
+                        if (diag && (kvpos > q0 + cbase + c + e + k || (VL && q0 + cbase + c + e + k >= len))) p[k] = 0.f;
                         gg[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
                     }
                     pk[e >> 1] = pack_bf162(p[0], p[1]);
@@ -628,7 +635,7 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after();
             const bool valid = kvpos < T;
             // Keys past the sequence's length (or a tile with no query tile) get zeros.
-            const bool live = kvpos < len && n_it > 0;
+            const bool live = !VL || (kvpos < len && n_it > 0);
             const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -649,8 +656,9 @@ __global__ void __launch_bounds__(512, 1)
                         const float4 cs = __ldg(tab + e / 4);
                         const float g0 = __uint_as_float(x[e]) * a.scale, g1 = __uint_as_float(x[e + 1]) * a.scale;
                         const float g2 = __uint_as_float(x[e + 2]) * a.scale, g3 = __uint_as_float(x[e + 3]) * a.scale;
-                        pk[e >> 1] = pack_bf162(g0 * cs.x + g1 * cs.y, -g0 * cs.y + g1 * cs.x);
-                        pk[(e >> 1) + 1] = pack_bf162(g2 * cs.z + g3 * cs.w, -g2 * cs.w + g3 * cs.z);
+                        // R^T: the rotation by -angle.
+                        pk[e >> 1] = pack_bf162(rot0(g0, g1, cs.x, -cs.y), rot1(g0, g1, cs.x, -cs.y));
+                        pk[(e >> 1) + 1] = pack_bf162(rot0(g2, g3, cs.z, -cs.w), rot1(g2, g3, cs.z, -cs.w));
                     }
                 } else {
 #pragma unroll
@@ -674,15 +682,22 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-template <int D>
-cudaError_t launch_bwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+template <int D, bool VL>
+cudaError_t launch_bwd_vl(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
     using C = BwdCfg<D>;
-    auto kfn = attn_bwd_kernel<D>;
+    auto kfn = attn_bwd_kernel<D, VL>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Hkv, B, a.n_kvt);
     return launch_k(kfn, grid, dim3(C::THREADS), C::SMEM, st, tq, tk, tv, tdo, a);
+}
+
+template <int D>
+cudaError_t launch_bwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+    return a.seq_lens ? launch_bwd_vl<D, true>(B, tq, tk, tv, tdo, a, st)
+                      : launch_bwd_vl<D, false>(B, tq, tk, tv, tdo, a, st);
 }
 
 int grid_for(long long work, int per_block) {
@@ -693,18 +708,23 @@ int grid_for(long long work, int per_block) {
 
 }  // namespace
 
-cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st) {
-    if (a.rows == 0) return cudaSuccess;
+template <bool VL>
+cudaError_t launch_bwd_pre_vl(bool tf32, const BwdPreArgs& a, cudaStream_t st) {
     const dim3 g(grid_for(a.rows * 8, 256)), blk(256);
     if (!tf32) {
-        if (a.D == 32) return launch_k(bwd_pre_kernel<__nv_bfloat16, 32>, g, blk, 0, st, a);
-        if (a.D == 64) return launch_k(bwd_pre_kernel<__nv_bfloat16, 64>, g, blk, 0, st, a);
-        if (a.D == 128) return launch_k(bwd_pre_kernel<__nv_bfloat16, 128>, g, blk, 0, st, a);
+        if (a.D == 32) return launch_k(bwd_pre_kernel<__nv_bfloat16, 32, VL>, g, blk, 0, st, a);
+        if (a.D == 64) return launch_k(bwd_pre_kernel<__nv_bfloat16, 64, VL>, g, blk, 0, st, a);
+        if (a.D == 128) return launch_k(bwd_pre_kernel<__nv_bfloat16, 128, VL>, g, blk, 0, st, a);
     } else {
-        if (a.D == 32) return launch_k(bwd_pre_kernel<float, 32>, g, blk, 0, st, a);
-        if (a.D == 64) return launch_k(bwd_pre_kernel<float, 64>, g, blk, 0, st, a);
+        if (a.D == 32) return launch_k(bwd_pre_kernel<float, 32, VL>, g, blk, 0, st, a);
+        if (a.D == 64) return launch_k(bwd_pre_kernel<float, 64, VL>, g, blk, 0, st, a);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st) {
+    if (a.rows == 0) return cudaSuccess;
+    return a.seq_lens ? launch_bwd_pre_vl<true>(tf32, a, st) : launch_bwd_pre_vl<false>(tf32, a, st);
 }
 
 cudaError_t launch_bwd_post(bool tf32, const BwdPostArgs& a, cudaStream_t st) {

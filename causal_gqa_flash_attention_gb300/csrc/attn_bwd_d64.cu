@@ -128,6 +128,9 @@ __device__ __forceinline__ uint32_t dp_col(int b) { return (uint32_t)(128 * b + 
 // Packed P^T of buffer b: 64 queries in 32 columns.
 __device__ __forceinline__ uint32_t pt_col(int b) { return (uint32_t)(Bwd64::PT_COL + 32 * b); }
 
+// VL: per-sequence lengths (padded batch).  Without them every length is T, rows past T
+// arrive as TMA's zero fill, and the padding code compiles away.
+template <bool VL>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_d64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(512, 1)
     const int kv0 = j * C::BKV;
     // Query tiles end at the sequence's length (T without per-sequence lengths); a key
     // tile wholly past it has no query tile and writes zero gradients.
-    const int len = seq_len(a.seq_lens, b, T);
+    const int len = VL ? seq_len(a.seq_lens, b, T) : T;
     const int n_qt = (len + C::BT - 1) / C::BT;
     const int per_head = n_qt > j ? n_qt - j : 0;    // 128-query tiles on or after the diagonal
     const int n_tiles = G * per_head;
@@ -194,6 +197,13 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(smem_u32(&bar_staged), 128);
         abort_flag = 0;
         fence_mbar_init();
+        // The tensor maps are kernel parameters, not outputs of an earlier kernel: fetch
+        // them before the dependency wait, under the previous kernel's tail.
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dq);
     }
     if (warp == 1) {
         __syncwarp();
@@ -218,10 +228,6 @@ __global__ void __launch_bounds__(512, 1)
         // ------------------------------------------------------------ TMA producer + dQ' issuer
         const uint32_t kvf = smem_u32(&bar_kv_full);
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_do);
             mbar_arrive_expect_tx(kvf, 2 * C::KV_BYTES);
             tma_load_4d(smem_u32(sK), &tm_k, kvf, 0, hkv, kv0, b);
             tma_load_4d(smem_u32(sV), &tm_v, kvf, 0, hkv, kv0, b);
@@ -333,11 +339,11 @@ __global__ void __launch_bounds__(512, 1)
         bool ovf = false;
         bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
         if (ok) {
-            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_F16, true>(sK, nullptr, kv0, T, r, a.rope, len);
+            ovf |= rope_tile_smem<D, C::BKV, 128, ROPE_F16, true>(sK, nullptr, kv0, T, r, a.rope,
+                                                                   VL ? len : kv0 + C::BKV);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready));
         }
-        if (r == 0) tma_prefetch_desc(&tm_dq);
         TileWalk dw;
         dw.init(hkv, G, j);
         for (int tau = 0; ok && tau < n_tiles; ++tau, dw.next(j, n_qt)) {
@@ -456,7 +462,7 @@ __global__ void __launch_bounds__(512, 1)
                 const float* lrow = &s_lse[sw][buf][32 * c];
                 const float* drow = &s_delta[sw][buf][32 * c];
                 // Queries of the chunk at or past the sequence's length are padding (masked).
-                const int qlim = len - qc;
+                const int qlim = VL ? len - qc : 32;
                 if (kw < qc && qlim >= 32) grad_chunk<false>(sr, dr, lrow, drow, sl2, -1, 32, pk, dk, amax2);
                 else grad_chunk<true>(sr, dr, lrow, drow, sl2, kw < qc ? -1 : (kw == qc ? lane : 32), qlim, pk, dk, amax2);
                 if (c == 0) {
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after();
             const bool valid = kvpos < T;
             // Keys past the sequence's length (or a tile with no query tile) get zeros.
-            const bool live = kvpos < len && n_hs > 0;
+            const bool live = !VL || (kvpos < len && n_hs > 0);
             // The tensors' row is a.dr wide: at head_dim 32 the kernel runs zero-padded to
             // 64 columns and stores only the first 32.
             const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * a.dr;
@@ -516,8 +522,9 @@ __global__ void __launch_bounds__(512, 1)
                         const float4 cs = __ldg(tab + e / 4);
                         const float g0 = __uint_as_float(x[e]) * a.scale, g1 = __uint_as_float(x[e + 1]) * a.scale;
                         const float g2 = __uint_as_float(x[e + 2]) * a.scale, g3 = __uint_as_float(x[e + 3]) * a.scale;
-                        pk[e >> 1] = pack_bf162(g0 * cs.x + g1 * cs.y, -g0 * cs.y + g1 * cs.x);
-                        pk[(e >> 1) + 1] = pack_bf162(g2 * cs.z + g3 * cs.w, -g2 * cs.w + g3 * cs.z);
+                        // R^T: the rotation by -angle.
+                        pk[e >> 1] = pack_bf162(rot0(g0, g1, cs.x, -cs.y), rot1(g0, g1, cs.x, -cs.y));
+                        pk[(e >> 1) + 1] = pack_bf162(rot0(g2, g3, cs.z, -cs.w), rot1(g2, g3, cs.z, -cs.w));
                     }
                 } else {
 #pragma unroll
@@ -547,7 +554,7 @@ int bwd_d64_q_box_rows() { return Bwd64::BH; }
 
 cudaError_t launch_bwd_d64(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t st) {
-    auto kfn = attn_bwd_d64_kernel;
+    auto kfn = a.seq_lens ? attn_bwd_d64_kernel<true> : attn_bwd_d64_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Bwd64::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Hkv, B, a.n_kvt);

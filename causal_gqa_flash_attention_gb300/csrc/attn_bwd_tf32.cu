@@ -72,7 +72,9 @@ __device__ __forceinline__ void round_tf32(uint8_t* p, int t) {
     }
 }
 
-template <int D>
+// VL: per-sequence lengths (padded batch).  Without them every length is T, rows past T
+// arrive as TMA's zero fill, and the padding code compiles away.
+template <int D, bool VL>
 __global__ void __launch_bounds__(384, 1)
     attn_bwd_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(384, 1)
     const int kv0 = j * C::BKV;
     // Query tiles end at the sequence's length (T without per-sequence lengths); a key
     // tile wholly past it has no query tile and writes zero gradients.
-    const int len = seq_len(a.seq_lens, b, T);
+    const int len = VL ? seq_len(a.seq_lens, b, T) : T;
     const int n_qt = (len + C::BQ - 1) / C::BQ;
     const int i_first = kv0 / C::BQ;
     const int per_head = n_qt > i_first ? n_qt - i_first : 0;
@@ -128,6 +130,12 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(smem_u32(&bar_rows[1]), 128);
         abort_flag = 0;
         fence_mbar_init();
+        // The tensor maps are kernel parameters, not outputs of an earlier kernel: fetch
+        // them before the dependency wait, under the previous kernel's tail.
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
     }
     if (warp == 1) {
         __syncwarp();
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(384, 1)
         };
         bool ok = mbar_wait_warp(smem_u32(&bar_kv_full), 0, w, SITE_BWD_KV);
         if (ok) {
-            rope_tile_smem<D, C::BKV, 128, ROPE_TF32>(sK, nullptr, kv0, T, r, a.rope, len);
+            rope_tile_smem<D, C::BKV, 128, ROPE_TF32>(sK, nullptr, kv0, T, r, a.rope, VL ? len : kv0 + C::BKV);
             round_tf32<C::KV_BYTES>(sV, r);
             ok = group_sync();
         }
@@ -255,7 +263,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int it = 0; ok && it <= n_it; ++it) {
             if (it < n_it) {
                 if (!(ok = mbar_wait_warp(smem_u32(&bar_qdo_full), it & 1, w, SITE_BWD_QDO_FULL))) break;
-                rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(sQ, nullptr, step_q0(it), T, r, a.rope, len);
+                rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(sQ, nullptr, step_q0(it), T, r, a.rope,
+                                                         VL ? len : step_q0(it) + C::BQ);
                 round_tf32<C::Q_BYTES>(sO, r);
                 if (!(ok = group_sync())) break;
                 transpose_f32<D, C::BQ>(sQ, sQT, r);
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(384, 1)
             tmem_ld_cols<2>(lt + C::S_COL, sr);
             tmem_ld_cols<2>(lt + C::DP_COL, dr);
             const bool diag = kv0 + C::BKV - 1 > q0;
-            const bool tail = q0 + C::BQ > len;          // queries past the length are padding
+            const bool tail = VL && q0 + C::BQ > len;          // queries past the length are padding
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 float p = ex2(fmaf(__uint_as_float(sr[c]), sl2, -s_lse[sb][c]));
@@ -329,7 +338,7 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
             const bool valid = kvpos < T;
             // Keys past the sequence's length (or a tile with no query tile) get zeros.
-            const bool live = kvpos < len && n_it > 0;
+            const bool live = !VL || (kvpos < len && n_it > 0);
             const size_t orow = (((size_t)b * T + (valid ? kvpos : 0)) * a.Hkv + hkv) * D;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -352,8 +361,8 @@ __global__ void __launch_bounds__(384, 1)
                     const float4 cs = __ldg(tab + e / 4);
                     const float g0 = __uint_as_float(kr[e]) * a.scale, g1 = __uint_as_float(kr[e + 1]) * a.scale;
                     const float g2 = __uint_as_float(kr[e + 2]) * a.scale, g3 = __uint_as_float(kr[e + 3]) * a.scale;
-                    dkp[e / 4] = make_float4(g0 * cs.x + g1 * cs.y, -g0 * cs.y + g1 * cs.x, g2 * cs.z + g3 * cs.w,
-                                             -g2 * cs.w + g3 * cs.z);
+                    dkp[e / 4] = make_float4(rot0(g0, g1, cs.x, -cs.y), rot1(g0, g1, cs.x, -cs.y),   // R^T
+                                             rot0(g2, g3, cs.z, -cs.w), rot1(g2, g3, cs.z, -cs.w));
                     dvp[e / 4] = make_float4(__uint_as_float(vr[e]), __uint_as_float(vr[e + 1]),
                                              __uint_as_float(vr[e + 2]), __uint_as_float(vr[e + 3]));
                 }
@@ -376,7 +385,7 @@ template <int D>
 cudaError_t launch_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
     using C = BwdTf32Cfg<D>;
-    auto kfn = attn_bwd_tf32_kernel<D>;
+    auto kfn = a.seq_lens ? attn_bwd_tf32_kernel<D, true> : attn_bwd_tf32_kernel<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Hkv, B, a.n_kvt);

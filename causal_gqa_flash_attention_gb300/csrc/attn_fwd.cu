@@ -137,16 +137,17 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
         for (int e = 0; e < C::BN; ++e)
             if (kv0 + e > qpos) sr[e] = __float_as_uint(kNegInf);
     }
-    // Row max over 8 independent chains (a single dependent chain would serialise on
-    // the max latency: one warp per SMSP runs this).
-    float m8[8];
+    // Row max with three-input maxima over four independent chains (a single dependent
+    // chain would serialise on the max latency).
+    float m4[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) m8[k] = __uint_as_float(sr[k]);
+    for (int k = 0; k < 4; ++k) m4[k] = __uint_as_float(sr[k]);
 #pragma unroll
-    for (int e = 8; e < C::BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sr[e]));
-    const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-    const float m_tile = mx * sl2;
+    for (int e = 4; e < C::BN; e += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], __uint_as_float(sr[e + k]), __uint_as_float(sr[e + 4 + k]));
+    const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+    const float m_tile = __fmul_rn(mx, sl2);   // (not contracted into a use below)
     // An fp16 operand that overflowed (|rotated q or k| > 65504) turns logits into inf or
     // NaN; a finite row max rules that out for the whole row (masked rows are -inf).
     if (!(fabsf(mx) < __int_as_float(0x7f800000)) && !(mx == kNegInf)) report_error(w.err, SITE_RANGE);
@@ -161,7 +162,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
     if (j == 0) st.m_used = m_tile;
     if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2(st.m_used - m_tile) : 1.f;
-        st.l *= alpha;
+        st.l = __fmul_rn(st.l, alpha);   // (no FMA contraction with the sum below)
         if (need) st.m_used = m_tile;
         if (!mbar_wait_warp(smem_u32(&bar_kv_empty[(g - 1) % C::NS]), ((g - 1) / C::NS) & 1, w, SITE_FWD_O_DONE))
             return false;
@@ -178,6 +179,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
         }
     }
     float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     const float neg_m = -st.m_used;
     const uint32_t sc = lt + s_col(u, t & 1);
 #pragma unroll
@@ -192,19 +194,25 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
             }
             tmem_st32(sc + c, pk);
         } else {
+            // Two scores per instruction: the exponent argument and the partial sums run
+            // as packed f32x2 FMA / add.
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, neg_m));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[c + e + 1]), sl2, neg_m));
-                s8[e & 7] += p0;
-                s8[(e + 1) & 7] += p1;
-                pk[e >> 1] = pack_bf162(p0, p1);
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c + e]), __uint_as_float(sr[c + e + 1])),
+                                            make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+                const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                s2[(e >> 1) & 3] = __fadd2_rn(s2[(e >> 1) & 3], pp);
+                pk[e >> 1] = pack_bf162(pp.x, pp.y);
             }
             tmem_st16(sc + (c >> 1), pk);
         }
     }
-    st.l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+    if constexpr (!TF32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s8[2 * k] += s2[k].x + s2[k].y;
+    }
+    st.l = __fadd_rn(st.l, ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(smem_u32(&bar_p_ready[u * 2 + (t & 1)]));
@@ -221,15 +229,16 @@ struct FwdUnit {
     int n_qsub;    // subtiles holding positions before the length (at least 1)
 };
 
-template <int BM, int BN>
+template <int BM, int BN, bool VL>
 __device__ __forceinline__ FwdUnit fwd_unit(int U, const FwdArgs& a) {
     FwdUnit f;
-    const int n_bh = a.B * a.Hq;
-    const int rank = U / n_bh, rem = U - rank * n_bh;
-    f.h = rem % a.Hq;
-    f.b = rem / a.Hq;
+    // Multiply-shift divisions: this decode is inlined in every role, and the generic
+    // integer-divide sequences made up much of the kernel's code.
+    const int rank = (int)fast_div((uint32_t)U, a.div_bh), rem = U - rank * (a.B * a.Hq);
+    f.b = (int)fast_div((uint32_t)rem, a.div_hq);
+    f.h = rem - f.b * a.Hq;
     f.q0 = (a.n_qt - 1 - rank) * 2 * BM;
-    f.len = seq_len(a.seq_lens, f.b, a.T);
+    f.len = VL ? seq_len(a.seq_lens, f.b, a.T) : a.T;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int qu = f.q0 + u * BM;
@@ -251,14 +260,14 @@ __device__ __forceinline__ int fwd_unit_index(int k, int n_units) {
 // Walks one subtile's tiles over the CTA's units in order, skipping units where the
 // subtile lies beyond T: unit iteration k (-1 at the end), tile j of n, and kvb, the
 // index of the unit's first K/V tile in the CTA's K/V sequence.
-template <int BM, int BN>
+template <int BM, int BN, bool VL>
 struct FwdWalk {
     int k, j, n, n_kv, kvb;
     __device__ __forceinline__ void load(int kk, int u, const FwdArgs& a) {
         const int U = fwd_unit_index(kk, a.n_units);
         k = U < 0 ? -1 : kk;
         if (U >= 0) {
-            const FwdUnit f = fwd_unit<BM, BN>(U, a);
+            const FwdUnit f = fwd_unit<BM, BN, VL>(U, a);
             n = u == 0 ? f.n_u[0] : f.n_u[1];   // (a select: no local-memory array)
             n_kv = f.n_kv;
         }
@@ -285,7 +294,9 @@ struct FwdWalk {
     }
 };
 
-template <bool TF32, int D>
+// VL: per-sequence lengths (padded batch).  Without them every length is T, rows past T
+// arrive as TMA's zero fill, and the padding code below compiles away.
+template <bool TF32, int D, bool VL>
 __global__ void __launch_bounds__(480, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -327,6 +338,12 @@ __global__ void __launch_bounds__(480, 1)
         }
         abort_flag = 0;
         fence_mbar_init();
+        // The tensor maps are kernel parameters, not outputs of an earlier kernel: fetch
+        // them before the dependency wait, under the previous kernel's tail.
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
     }
     if (warp == 1) {
         __syncwarp();
@@ -348,22 +365,19 @@ __global__ void __launch_bounds__(480, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
             int issued = 0;                           // K/V tiles loaded so far
             int last_k0 = -1, last_k1 = -1;           // last unit loaded into Q buffer 0 / 1
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int U = fwd_unit_index(k, a.n_units);
                 if (U < 0) break;
-                const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+                const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(U, a);
                 const int qb = k % C::NQB;
                 // The Q buffer is free once both epilogues of unit k - NQB stored their O.
                 if (k >= C::NQB &&
                     !(ok = mbar_wait(smem_u32(&bar_q_empty[qb]), ((k / C::NQB) - 1) & 1, w, SITE_FWD_Q)))
                     break;
-                if (seq_len_bad(a.seq_lens, f.b, T)) report_error(a.err, SITE_VARLEN_LEN);
+                if (VL && seq_len_bad(a.seq_lens, f.b, T)) report_error(a.err, SITE_VARLEN_LEN);
                 const uint32_t qf = smem_u32(&bar_q_full[qb]);
                 mbar_arrive_expect_tx(qf, f.n_qsub * C::Q_BYTES);
                 for (int u = 0; u < f.n_qsub; ++u)
@@ -397,8 +411,12 @@ __global__ void __launch_bounds__(480, 1)
         }
     } else if (warp < 3) {
         // ------------------------------------------------------------ UMMA issuers
-        // Each subtile has its own issuing warp (1 + u); the whole warp runs the loop and
-        // one elected lane issues.  Tiles are numbered t = 0, 1, ... over all units of the
+        // Each subtile has its own issuing warp (1 + u).  The whole warp runs the loop, so
+        // the UMMA operands stay warp-uniform, and one elected lane issues each batch (the
+        // UMMAs of a tile and their commit) in one branch: an election per UMMA, or a loop
+        // run by one lane alone (operands no longer provably uniform), took several times
+        // the instructions, and this role's steps are on the kernel's critical path (the
+        // instruction cache is shared with the softmax and RoPE warps).  Tiles are numbered t = 0, 1, ... over all units of the
         // CTA; S(t) goes to S buffer t % 2, two tiles ahead of the softmax, and overwrites
         // P(t-2), whose PV the same lane issued earlier (one thread's UMMAs execute in
         // order).
@@ -419,7 +437,7 @@ __global__ void __launch_bounds__(480, 1)
         };
         int t_s = 0;                                  // S tiles issued
         int qr_next = 0;                              // first unit whose Q' this issuer has not waited for
-        auto issue_s = [&](const FwdWalk<C::BM, C::BN>& c) -> bool {
+        auto issue_s = [&](const FwdWalk<C::BM, C::BN, VL>& c) -> bool {
             // Q' of the unit (and of any unit skipped since the last one: every phase of
             // the Q-ready barriers is waited for in order, so a parity never aliases).
             for (; c.j == 0 && qr_next <= c.k; ++qr_next)
@@ -430,13 +448,16 @@ __global__ void __launch_bounds__(480, 1)
             const uint64_t dq = sdesc_add(dq0, (c.k % C::NQB) * C::QBUF);
             const uint64_t dk = sdesc_add(dk0, (g % C::NS) * C::STAGE_BYTES);
             const uint32_t dcol = tm + s_col(u, t_s & 1);
+            if (elect_one()) {
 #pragma unroll
-            for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
-                const uint32_t byte = ks * 32;
-                umma_ss_e<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
-                                sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
+                for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
+                    const uint32_t byte = ks * 32;
+                    umma_ss<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
+                                  sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
+                }
+                umma_commit(smem_u32(&bar_s_full[u * 2 + (t_s & 1)]));
             }
-            umma_commit_e(smem_u32(&bar_s_full[u * 2 + (t_s & 1)]));
+            __syncwarp();
             ++t_s;
             return true;
         };
@@ -446,17 +467,20 @@ __global__ void __launch_bounds__(480, 1)
             tc_fence_after();
             const uint64_t dv = sdesc_add(dv0, (g % C::NS) * C::STAGE_BYTES);
             const uint32_t pcol = tm + s_col(u, t & 1);
+            if (elect_one()) {
 #pragma unroll
-            for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
-                // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
-                // MN-major, PV_ROWS keys per K-step.
-                const uint32_t off = TF32 ? ((ks * 32) >> 7) * D * 128 + ((ks * 32) & 127) : ks * C::PV_ROWS * 128;
-                umma_ts_e<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
+                    // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
+                    // MN-major, PV_ROWS keys per K-step.
+                    const uint32_t off = TF32 ? ((ks * 32) >> 7) * D * 128 + ((ks * 32) & 127) : ks * C::PV_ROWS * 128;
+                    umma_ts<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                if (last) umma_commit(smem_u32(&bar_o_final[u]));
             }
-            if (last) umma_commit_e(smem_u32(&bar_o_final[u]));
+            __syncwarp();
             return true;
         };
-        FwdWalk<C::BM, C::BN> sw;                     // the next tile to issue S for
+        FwdWalk<C::BM, C::BN, VL> sw;                     // the next tile to issue S for
         sw.init(u, a);
         int t = 0, g = 0;                             // PV tiles issued; K/V tiles passed
         // S runs at most two tiles ahead of PV.  With one Q buffer the next unit's Q can
@@ -467,36 +491,47 @@ __global__ void __launch_bounds__(480, 1)
         // n_kv - n_u + 1 <= 3 stages of the unit, and NS >= 4 lets the next unit's first
         // K/V tile load regardless.
         auto may_issue = [&](int k_cur) { return sw.k >= 0 && t_s < t + 2 && (C::NQB == 2 || sw.k <= k_cur); };
-        bool ok = true;
-        while (ok && may_issue(0)) {
-            ok = issue_s(sw);
-            sw.advance(u, a);
-        }
-        // Every K/V stage is released by both issuers, in order.  A tile beyond the
-        // subtile's diagonal is released without use, but only once the stage really
-        // holds it (k_ready), so the release never runs a phase ahead.
-        for (int k = 0; ok; ++k) {
-            const int U = fwd_unit_index(k, a.n_units);
-            if (U < 0) break;
-            const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
-            for (int j = 0; ok && j < f.n_kv; ++j, ++g) {
-                const int n = u == 0 ? f.n_u[0] : f.n_u[1];
-                if (j < n) {
-                    if (!(ok = issue_pv(t, j, g, j == n - 1))) break;
-                    ++t;
-                    umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
-                    while (ok && may_issue(k)) {
-                        ok = issue_s(sw);
-                        sw.advance(u, a);
-                    }
-                } else {
-                    if (!(ok = k_ready(g))) break;
-                    umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
-                }
+        // The PV walk: every K/V tile g of every unit in order, tile jp of unit kp, of
+        // which the first np are this subtile's (the rest lie beyond its diagonal).
+        int kp = 0, jp = 0, np = 0, nkv = 0;
+        auto load_pv = [&]() -> bool {
+            for (;; ++kp) {                           // units with no K/V tile load nothing
+                const int U = fwd_unit_index(kp, a.n_units);
+                if (U < 0) return false;
+                const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(U, a);
+                np = u == 0 ? f.n_u[0] : f.n_u[1];
+                nkv = f.n_kv;
+                if (nkv > 0) return true;
             }
-            while (ok && may_issue(k + 1)) {
+        };
+        bool more = load_pv();
+        bool ok = true;
+        // One loop with one S site and one PV site: every issue decision of the role in a
+        // single short body, so the warp's code stays in the instruction cache while the
+        // softmax warps on the same SM sub-partition run theirs.  After each PV (and at
+        // the start) every S the two-tile window allows goes first.  Every K/V stage is
+        // released by both issuers, in order; a tile beyond the subtile's diagonal is
+        // released without use, but only once the stage really holds it (k_ready), so the
+        // release never runs a phase ahead.
+        while (ok) {
+            if (may_issue(kp)) {
                 ok = issue_s(sw);
                 sw.advance(u, a);
+                continue;
+            }
+            if (!more) break;
+            if (jp < np) {
+                if (!(ok = issue_pv(t, jp, g, jp == np - 1))) break;
+                ++t;
+            } else if (!(ok = k_ready(g))) {
+                break;
+            }
+            umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
+            ++g;
+            if (++jp == nkv) {
+                jp = 0;
+                ++kp;
+                more = load_pv();
             }
         }
         umma_commit_e(smem_u32(&bar_final));
@@ -516,7 +551,7 @@ __global__ void __launch_bounds__(480, 1)
         for (int k = 0; ok; ++k) {
             const int U = fwd_unit_index(k, a.n_units);
             if (U < 0) break;
-            const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+            const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(U, a);
             uint8_t* qbuf = q_buf(k);
             // The table rows are fetched before the wait, so their latency overlaps it.
             float4 qa[RopeQ::F4], qc[RopeQ::F4], kn[RopeK::F4];
@@ -526,8 +561,14 @@ __global__ void __launch_bounds__(480, 1)
             if (!(ok = mbar_wait_warp(smem_u32(&bar_q_full[k % C::NQB]), (k / C::NQB) & 1, w, SITE_FWD_Q))) break;
             // Rows past the sequence's length (padding) are zeroed, so whatever the caller
             // left there never reaches an MMA.
-            rq.template apply<false>(qbuf, nullptr, qa, f.len - f.q0);
-            if (f.n_qsub == 2) rq.template apply<false>(qbuf + C::Q_BYTES, nullptr, qc, f.len - f.q0 - C::BM);
+            // One copy of the rotation code for both subtiles (instruction cache).
+#pragma unroll 1
+            for (int s2 = 0; s2 < f.n_qsub; ++s2) {
+                float4 qb[RopeQ::F4];
+#pragma unroll
+                for (int e = 0; e < RopeQ::F4; ++e) qb[e] = s2 ? qc[e] : qa[e];
+                rq.template apply<false>(qbuf + s2 * C::Q_BYTES, nullptr, qb, VL ? f.len - f.q0 - s2 * C::BM : C::BM);
+            }
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_q_ready[k % C::NQB]));
             for (int j = 0; j < f.n_kv; ++j, ++g) {
@@ -537,10 +578,10 @@ __global__ void __launch_bounds__(480, 1)
                 for (int e = 0; e < RopeK::F4; ++e) cur[e] = kn[e];
                 if (j + 1 < f.n_kv) rk.load_base(kn, (j + 1) * C::BN, T, a.rope);   // one tile early
                 if (!(ok = mbar_wait_warp(smem_u32(&bar_kv_full[s]), (g / C::NS) & 1, w, SITE_FWD_KV_FULL))) break;
-                const int kz = f.len - j * C::BN;      // first padding row of the tile
+                const int kz = VL ? f.len - j * C::BN : C::BN;   // first padding row of the tile
                 if constexpr (TF32) {
                     transpose_v_tf32<D, C::BN, C::ROPE_THREADS>(stage_v(s), stage_vt(s), rt, kz);
-                } else if (kz < C::BN) {
+                } else if (VL && kz < C::BN) {
                     zero_rows<C::BN, C::NCH, C::ROPE_THREADS>(stage_v(s), kz, rt);
                 }
                 rk.template apply<false>(stage_k(s), nullptr, cur, kz);
@@ -548,7 +589,7 @@ __global__ void __launch_bounds__(480, 1)
                 mbar_arrive(smem_u32(&bar_k_ready[s]));
             }
         }
-    } else if (warp < 12) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ softmax (subtile u)
         const int u = (warp - 4) >> 2;
         const int r = tid - 128 - 128 * u;            // query row = TMEM lane
@@ -565,7 +606,7 @@ __global__ void __launch_bounds__(480, 1)
             {
                 const int U = fwd_unit_index(k, a.n_units);
                 if (U < 0) break;
-                const FwdUnit f = fwd_unit<C::BM, C::BN>(U, a);
+                const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(U, a);
                 n = u == 0 ? f.n_u[0] : f.n_u[1];
                 qsub0 = f.q0 + u * C::BM;
                 n_kv = f.n_kv;
@@ -583,8 +624,8 @@ __global__ void __launch_bounds__(480, 1)
                 if (!(ok = __all_sync(0xffffffffu, rel))) break;
                 // Padding rows inside T: O = 0 and LSE = -inf (a softmax over no keys).
                 const int qpos = qsub0 + r;
-                if (qpos < T) {
-                    const FwdUnit f = fwd_unit<C::BM, C::BN>(fwd_unit_index(k, a.n_units), a);
+                if (VL && qpos < T) {
+                    const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(fwd_unit_index(k, a.n_units), a);
                     const size_t row = ((size_t)f.b * T + qpos) * a.Hq + f.h;
                     // The tensors' row is a.dr wide (bf16 head_dim 32 runs zero-padded to 64).
                     const int rb = a.dr * C::ES;
@@ -615,11 +656,11 @@ __global__ void __launch_bounds__(480, 1)
             // the older one would then name a phase that is still to come.
             if (!(ok = mbar_wait_warp(smem_u32(&bar_o_final[u]), n_epi & 1, w, SITE_FWD_O_DONE))) break;
             tc_fence_after();
-            const FwdUnit f = fwd_unit<C::BM, C::BN>(fwd_unit_index(k, a.n_units), a);
+            const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(fwd_unit_index(k, a.n_units), a);
             uint8_t* sQu = q_buf(k) + u * C::Q_BYTES;
             // Padding rows (past the sequence's length) store O = 0 and LSE = -inf; their
             // accumulators are finite (their Q, and the padding K and V, were zeroed).
-            const bool live = qpos < f.len;
+            const bool live = !VL || qpos < f.len;
             const float inv_l = live ? 1.f / st.l : 0.f;
 #pragma unroll
             for (int c = 0; c < D; c += 32) {
@@ -680,11 +721,11 @@ __global__ void __launch_bounds__(480, 1)
     }
 }
 
-template <bool TF32, int D>
+template <bool TF32, int D, bool VL>
 cudaError_t launch_fwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
     using C = FwdCfg<TF32, D>;
-    auto kfn = attn_fwd_kernel<TF32, D>;
+    auto kfn = attn_fwd_kernel<TF32, D, VL>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -699,18 +740,25 @@ cudaError_t launch_fwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, co
 
 int fwd_kv_box_rows(bool tf32, int D) { return 64; }
 
-cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
+template <bool VL>
+cudaError_t launch_fwd_vl(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
     if (!tf32) {
         // head_dim 32 runs the 64-wide kernel: its 128-byte TMA boxes read the upper 32
         // columns as zeros and the O store clips them.
-        if (D == 64 || D == 32) return launch_fwd_t<false, 64>(B, tq, tk, tv, to, a, st);
-        if (D == 128) return launch_fwd_t<false, 128>(B, tq, tk, tv, to, a, st);
+        if (D == 64 || D == 32) return launch_fwd_t<false, 64, VL>(B, tq, tk, tv, to, a, st);
+        if (D == 128) return launch_fwd_t<false, 128, VL>(B, tq, tk, tv, to, a, st);
     } else {
-        if (D == 32) return launch_fwd_t<true, 32>(B, tq, tk, tv, to, a, st);
-        if (D == 64) return launch_fwd_t<true, 64>(B, tq, tk, tv, to, a, st);
+        if (D == 32) return launch_fwd_t<true, 32, VL>(B, tq, tk, tv, to, a, st);
+        if (D == 64) return launch_fwd_t<true, 64, VL>(B, tq, tk, tv, to, a, st);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
+    return a.seq_lens ? launch_fwd_vl<true>(tf32, D, B, tq, tk, tv, to, a, st)
+                      : launch_fwd_vl<false>(tf32, D, B, tq, tk, tv, to, a, st);
 }
 
 }  // namespace ne

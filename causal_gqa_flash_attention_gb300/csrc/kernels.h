@@ -73,6 +73,7 @@ struct FwdArgs {
     unsigned long long timeout_ns;
     const int* seq_lens;     // [B] per-sequence lengths (positions at or past are padding), or null
     int dr;                  // the tensors' head_dim (bf16 32 runs the 64-wide kernel, zero-padded)
+    FastDiv div_bh, div_hq;  // by B * Hq and by Hq (the unit decode)
 };
 
 struct BwdPreArgs {

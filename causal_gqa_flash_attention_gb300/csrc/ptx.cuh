@@ -240,6 +240,14 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
             : "memory");
     }
 }
+// True in one lane of a converged warp (the lowest).  The warp computes the UMMA operands
+// together, so they stay warp-uniform, and the elected lane issues a whole batch.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile("{\n .reg .pred e;\n .reg .b32 r;\n elect.sync r|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}\n"
+                 : "=r"(p));
+    return p != 0;
+}
 // Arrive once on `bar` when every UMMA this thread issued so far has completed.
 // Warp-collective forms: the whole warp runs the issuing loop (so descriptors stay
 // warp-uniform) and elect.sync picks the one lane (always the lowest) that issues.  The
@@ -402,6 +410,13 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef NE_S8
 
 // 2^x on the special-function unit (flush-to-zero; exp2(-inf) = 0).
+// max(a, b, c) in one three-input instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float m;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -42,6 +42,16 @@ __device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The rotation (x0, x1) -> (x0 c - x1 s, x0 s + x1 c) with its roundings fixed by
+// explicit intrinsics: left to the compiler, the contraction of a product into an FMA
+// may differ between two instantiations of the same kernel, and so would the results.
+__device__ __forceinline__ float rot0(float x0, float x1, float c, float s) {
+    return __fmaf_rn(x0, c, __fmul_rn(-x1, s));
+}
+__device__ __forceinline__ float rot1(float x0, float x1, float c, float s) {
+    return __fmaf_rn(x0, s, __fmul_rn(x1, c));
+}
+
 template <int D, int ROWS, int NT, int MODE>
 struct RopeTile {
     static constexpr int ES = MODE == ROPE_TF32 ? 4 : 2;
@@ -90,8 +100,8 @@ struct RopeTile {
                 const float x0 = __uint_as_float(raw.x), x1 = __uint_as_float(raw.y);
                 const float x2 = __uint_as_float(raw.z), x3 = __uint_as_float(raw.w);
                 *reinterpret_cast<uint4*>(base + off) =
-                    make_uint4(f32_to_tf32_rna(x0 * cs.x - x1 * cs.y), f32_to_tf32_rna(x0 * cs.y + x1 * cs.x),
-                               f32_to_tf32_rna(x2 * cs.z - x3 * cs.w), f32_to_tf32_rna(x2 * cs.w + x3 * cs.z));
+                    make_uint4(f32_to_tf32_rna(rot0(x0, x1, cs.x, cs.y)), f32_to_tf32_rna(rot1(x0, x1, cs.x, cs.y)),
+                               f32_to_tf32_rna(rot0(x2, x3, cs.z, cs.w)), f32_to_tf32_rna(rot1(x2, x3, cs.z, cs.w)));
             } else {
                 const float cs[8] = {b[0].x, b[0].y, b[0].z, b[0].w, b[1].x, b[1].y, b[1].z, b[1].w};
                 const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -101,7 +111,7 @@ struct RopeTile {
                     const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[p]);
                     const float x0 = __low2float(v), x1 = __high2float(v);
                     const float c = cs[2 * p], s = cs[2 * p + 1];
-                    const float y0 = x0 * c - x1 * s, y1 = x0 * s + x1 * c;
+                    const float y0 = rot0(x0, x1, c, s), y1 = rot1(x0, x1, c, s);
                     if constexpr (CHECK) amax = fmaxf(amax, row < zero_row ? fmaxf(fabsf(y0), fabsf(y1)) : 0.f);
                     o16[p] = pack_half2(y0, y1);
                     if constexpr (MODE == ROPE_BF16_F16) ob[p] = pack_bf162(y0, y1);
@@ -117,8 +127,8 @@ struct RopeTile {
 #pragma unroll
                 for (int e = 0; e < F4; ++e) {
                     const float4 c = b[e], s = step[e];
-                    b[e] = make_float4(c.x * s.x - c.y * s.y, c.y * s.x + c.x * s.y,
-                                       c.z * s.z - c.w * s.w, c.w * s.z + c.z * s.w);
+                    b[e] = make_float4(rot0(c.x, c.y, s.x, s.y), rot1(c.x, c.y, s.x, s.y),
+                                       rot0(c.z, c.w, s.z, s.w), rot1(c.z, c.w, s.z, s.w));
                 }
             }
         }
