@@ -33,7 +33,8 @@ EXPORTS = (
     "ne_set_wait_timeout_ms", "ne_selftest_wait_timeout", "ne_shutdown", "ne_attn_bwd_noalloc",
     "ne_profile_enable", "ne_profile_totals", "ne_attn_decode_workspace_size", "ne_attn_decode",
     "ne_attn_decode_f32", "ne_noalloc_get_device_error", "ne_attn_fwd_varlen", "ne_attn_fwd_varlen_f32",
-    "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32", "ne_qkv_prologue",
+    "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32", "ne_qkv_prologue", "ne_attn_fwd_train",
+    "ne_attn_fwd_train_f32", "ne_attn_bwd_train", "ne_attn_bwd_train_f32",
 )
 
 
@@ -75,6 +76,10 @@ def load(path: str | None = None):
         lib.ne_attn_bwd_varlen.argtypes = [vp] * 10 + [i] * 5 + [d, vp, sz, vp]
         lib.ne_attn_bwd_varlen_f32.argtypes = lib.ne_attn_bwd_varlen.argtypes
         lib.ne_qkv_prologue.argtypes = [vp] * 6 + [i] * 6 + [d, d, i, vp]
+        lib.ne_attn_fwd_train.argtypes = [vp] * 6 + [sz] + [i] * 5 + [d, vp]
+        lib.ne_attn_fwd_train_f32.argtypes = lib.ne_attn_fwd_train.argtypes
+        lib.ne_attn_bwd_train.argtypes = lib.ne_attn_bwd.argtypes
+        lib.ne_attn_bwd_train_f32.argtypes = lib.ne_attn_bwd.argtypes
         lib.ne_noalloc_get_device_error.argtypes = [vp]
         lib.ne_profile_enable.argtypes = [i]
         lib.ne_profile_enable.restype = None
@@ -193,6 +198,40 @@ def attn_bwd(q, k, v, o, lse, dO, theta: float = 10000.0, workspace=None, dq=Non
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     fn = lib.ne_attn_bwd if q.dtype == torch.bfloat16 else lib.ne_attn_bwd_f32
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+              B, T, Hq, Hkv, D, float(theta), _ptr(workspace), workspace.numel() * workspace.element_size(),
+              _stream(q)))
+    return dq, dk, dv
+
+
+def attn_fwd_train(q, k, v, workspace, theta: float = 10000.0, o=None, lse=None):
+    """Training forward: what attn_fwd returns, and (bf16, head_dim 32/64) the backward
+    workspace filled for attn_bwd_train of the same layer (see include/neattn.h)."""
+    lib = load()
+    B, T, Hq, Hkv, D = _dims(q, k, v)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    fn = lib.ne_attn_fwd_train if q.dtype == torch.bfloat16 else lib.ne_attn_fwd_train_f32
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+              workspace.numel() * workspace.element_size(), B, T, Hq, Hkv, D, float(theta), _stream(q)))
+    return o, lse
+
+
+def attn_bwd_train(q, k, v, o, lse, dO, workspace, theta: float = 10000.0, dq=None, dk=None, dv=None):
+    """Backward after attn_fwd_train on the same workspace: returns (dq, dk, dv)."""
+    lib = load()
+    B, T, Hq, Hkv, D = _dims(q, k, v)
+    for t in (o, dO):
+        if tuple(t.shape) != tuple(q.shape) or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("o and dO must match q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, T) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, Hq, T]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    fn = lib.ne_attn_bwd_train if q.dtype == torch.bfloat16 else lib.ne_attn_bwd_train_f32
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
               B, T, Hq, Hkv, D, float(theta), _ptr(workspace), workspace.numel() * workspace.element_size(),
               _stream(q)))

@@ -273,15 +273,29 @@ ne_status check_seq_lens(const int* seq_lens) {
     return NE_OK;
 }
 
+// The backward workspace must be non-null, 256-byte aligned and large enough.
+ne_status check_ws(const void* ws, size_t ws_bytes, int B, int T, int Hq, int D) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return fail(NE_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+    const size_t need = bwd_ws_bytes(B, T, Hq, D);
+    if (ws_bytes < need)
+        return fail(NE_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", ws_bytes, need);
+    return NE_OK;
+}
+
 // seq_lens: null, or (variable-length calls) the device lengths [B] of the sequences.
+// ws: null, or (training forward) the backward workspace that receives R Q and a zeroed
+// dQ' accumulator where the backward uses them (bf16, head_dim 32 or 64).
 ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
-                        int Hq, int Hkv, int D, double theta, const int* seq_lens, bool varlen, cudaStream_t st) {
+                        int Hq, int Hkv, int D, double theta, const int* seq_lens, bool varlen, cudaStream_t st,
+                        void* ws = nullptr, size_t ws_bytes = 0, bool train = false) {
     g_last_error.clear();
     ne_status s = check_shape(B, T, Hq, Hkv, D, theta, f32);
     if (s != NE_OK) return s;
     if (B == 0 || T == 0) return NE_OK;
     if ((s = check_ptrs({q, k, v, o, lse})) != NE_OK) return s;
     if (varlen && (s = check_seq_lens(seq_lens)) != NE_OK) return s;
+    if (train && (s = check_ws(ws, ws_bytes, B, T, Hq, D)) != NE_OK) return s;
     int dev;
     if ((s = current_device(&dev)) != NE_OK) return s;
     int* err;
@@ -311,25 +325,35 @@ ne_status attn_fwd_impl(bool f32, const void* q, const void* k, const void* v, v
     a.dr = D;
     a.div_bh = ne::make_fastdiv((uint32_t)(B * Hq));   // B, Hq >= 1 here
     a.div_hq = ne::make_fastdiv((uint32_t)Hq);
-    cudaError_t e = timed(0, st, [&] { return ne::launch_fwd(f32, D, B, tq, tk, tv, to, a, st); });
+    // The training forward fills the backward's R Q and zeroes its dQ' accumulator where
+    // the backward reads them (bf16 head_dim <= 64); elsewhere it is the plain forward.
+    a.save = train && bwd_uses_q16(f32, D) ? 1 : 0;
+    CUtensorMap tq16, tdqz;
+    std::memset(&tq16, 0, sizeof(tq16));
+    std::memset(&tdqz, 0, sizeof(tdqz));
+    if (a.save) {
+        const BwdWs wl = bwd_ws_layout(B, T, Hq, D);
+        if ((s = map_bthd(&tq16, static_cast<char*>(ws) + wl.q16, false, B, T, Hq, D, 128, true)) != NE_OK) return s;
+        if ((s = map_bthd(&tdqz, static_cast<char*>(ws) + wl.acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
+    }
+    cudaError_t e = timed(0, st, [&] { return ne::launch_fwd(f32, D, B, tq, tk, tv, to, tq16, tdqz, a, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
     return NE_OK;
 }
 
+// train: the workspace holds what the training forward left there (R Q and the zeroed
+// dQ' accumulator, for bf16 head_dim <= 64), so the preprocess pass only forms Delta.
 ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, const void* o, const float* lse,
                         const void* dO, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
-                        double theta, void* ws, size_t ws_bytes, const int* seq_lens, bool varlen, cudaStream_t st) {
+                        double theta, void* ws, size_t ws_bytes, const int* seq_lens, bool varlen, cudaStream_t st,
+                        bool train = false) {
     g_last_error.clear();
     ne_status s = check_shape(B, T, Hq, Hkv, D, theta, f32);
     if (s != NE_OK) return s;
     if (B == 0 || T == 0) return NE_OK;
     if ((s = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv})) != NE_OK) return s;
     if (varlen && (s = check_seq_lens(seq_lens)) != NE_OK) return s;
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
-        return fail(NE_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
-    const size_t need = bwd_ws_bytes(B, T, Hq, D);
-    if (ws_bytes < need)
-        return fail(NE_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", ws_bytes, need);
+    if ((s = check_ws(ws, ws_bytes, B, T, Hq, D)) != NE_OK) return s;
     int dev;
     if ((s = current_device(&dev)) != NE_OK) return s;
     int* err;
@@ -342,8 +366,9 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     void* q16 = bwd_uses_q16(f32, D) ? static_cast<char*>(ws) + wl.q16 : nullptr;
     const long long rows = (long long)B * T * Hq;
 
-    ne::BwdPreArgs pa{o, dO, delta, dq_acc, rows, T, Hq, D, q, q16, rope, err,
-                      ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T), seq_lens, rope_ld(f32, D)};
+    const bool prepared = train && q16 != nullptr;   // R Q stored and dQ' zeroed by the forward
+    ne::BwdPreArgs pa{o, dO, delta, prepared ? nullptr : dq_acc, rows, T, Hq, D, q, prepared ? nullptr : q16, rope,
+                      err, ne::make_fastdiv((uint32_t)Hq), ne::make_fastdiv((uint32_t)T), seq_lens, rope_ld(f32, D)};
     cudaError_t e = timed(1, st, [&] { return ne::launch_bwd_pre(f32, pa, st); });
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
 
@@ -551,6 +576,35 @@ ne_status ne_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
 ne_status ne_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int T,
                           int Hq, int Hkv, int D, double rope_theta, ne_stream_t stream) {
     return attn_fwd_impl(true, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, nullptr, false, (cudaStream_t)stream);
+}
+
+ne_status ne_attn_fwd_train(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                            size_t workspace_bytes, int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                            ne_stream_t stream) {
+    return attn_fwd_impl(false, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, nullptr, false, (cudaStream_t)stream,
+                         workspace, workspace_bytes, true);
+}
+
+ne_status ne_attn_fwd_train_f32(const float* q, const float* k, const float* v, float* o, float* lse, void* workspace,
+                                size_t workspace_bytes, int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                                ne_stream_t stream) {
+    return attn_fwd_impl(true, q, k, v, o, lse, B, T, Hq, Hkv, D, rope_theta, nullptr, false, (cudaStream_t)stream,
+                         workspace, workspace_bytes, true);
+}
+
+ne_status ne_attn_bwd_train(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dO, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
+                            double rope_theta, void* workspace, size_t workspace_bytes, ne_stream_t stream) {
+    return attn_bwd_impl(false, q, k, v, o, lse, dO, dq, dk, dv, B, T, Hq, Hkv, D, rope_theta, workspace,
+                         workspace_bytes, nullptr, false, (cudaStream_t)stream, true);
+}
+
+ne_status ne_attn_bwd_train_f32(const float* q, const float* k, const float* v, const float* o, const float* lse,
+                                const float* dO, float* dq, float* dk, float* dv, int B, int T, int Hq, int Hkv,
+                                int D, double rope_theta, void* workspace, size_t workspace_bytes,
+                                ne_stream_t stream) {
+    return attn_bwd_impl(true, q, k, v, o, lse, dO, dq, dk, dv, B, T, Hq, Hkv, D, rope_theta, workspace,
+                         workspace_bytes, nullptr, false, (cudaStream_t)stream, true);
 }
 
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D) {

@@ -43,12 +43,16 @@ namespace {
 // order.  Each warp zeroes the accumulator rows of the units it reads: interleaving the
 // zero stores with the loads row by row kept HBM busier than a zeroing sweep followed by
 // the loads.
-template <typename Tin, int D, bool VL>
+// DELTA_ONLY (after the training forward, which stored R Q and zeroed the accumulator):
+// the pass only reads O and dO, so it keeps four row units in flight per thread.
+template <typename Tin, int D, bool VL, bool DELTA_ONLY = false>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
     constexpr int EPV = 16 / sizeof(Tin);        // elements per 16-byte vector
     constexpr int LPR = D / EPV;                 // lanes per row (8 or 16)
     constexpr int RPW = 32 / LPR;                // rows per warp unit
-    constexpr int U = 1;                         // units per pass (more were slower when measured)
+    // Units per pass: with the rotation and the zero stores one was fastest when measured;
+    // the loads alone need more in flight.
+    constexpr int U = DELTA_ONLY ? 4 : 1;
     constexpr int ZPL = D / 4 / LPR;             // 16-byte zero stores per lane per row
     griddep_launch_dependents();
     griddep_wait();
@@ -62,7 +66,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
     const uint32_t rows = (uint32_t)a.rows;
     const uint4* o4 = static_cast<const uint4*>(a.o);
     const uint4* g4 = static_cast<const uint4*>(a.dO);
-    const bool rot = sizeof(Tin) == 2 && a.q16 != nullptr;
+    const bool rot = !DELTA_ONLY && sizeof(Tin) == 2 && a.q16 != nullptr;
     bool ovf = false;
     for (uint32_t r0 = wg * RPW + sub; r0 - sub < rows; r0 += nw * RPW * U) {
         uint4 ov[U], gv[U], qv[U];
@@ -110,7 +114,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreArgs a) {
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const uint32_t row = r0 + k * nw * RPW;
-            if (row < rows) {
+            if (!DELTA_ONLY && row < rows && a.dq_acc) {
                 float4* z = reinterpret_cast<float4*>(a.dq_acc + (size_t)row * D);
 #pragma unroll
                 for (int e = 0; e < ZPL; ++e) z[li + e * LPR] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -711,6 +715,10 @@ int grid_for(long long work, int per_block) {
 template <bool VL>
 cudaError_t launch_bwd_pre_vl(bool tf32, const BwdPreArgs& a, cudaStream_t st) {
     const dim3 g(grid_for(a.rows * 8, 256)), blk(256);
+    if (!tf32 && !a.q16 && !a.dq_acc) {          // after the training forward (bf16, D <= 64)
+        if (a.D == 32) return launch_k(bwd_pre_kernel<__nv_bfloat16, 32, VL, true>, g, blk, 0, st, a);
+        if (a.D == 64) return launch_k(bwd_pre_kernel<__nv_bfloat16, 64, VL, true>, g, blk, 0, st, a);
+    }
     if (!tf32) {
         if (a.D == 32) return launch_k(bwd_pre_kernel<__nv_bfloat16, 32, VL>, g, blk, 0, st, a);
         if (a.D == 64) return launch_k(bwd_pre_kernel<__nv_bfloat16, 64, VL>, g, blk, 0, st, a);

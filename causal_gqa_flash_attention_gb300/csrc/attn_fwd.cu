@@ -79,6 +79,10 @@ struct FwdCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
+// Bytes of the zero tile the training forward stores into the dQ' accumulator (fp32:
+// 128 rows x 32 columns per store).
+constexpr int kZeroTileBytes = 128 * 128;
+
 // TMEM column of S buffer `buf` (0/1) of subtile u.
 __device__ __forceinline__ uint32_t s_col(int u, int buf) { return (uint32_t)((u * 2 + buf) * 64); }
 
@@ -296,16 +300,24 @@ struct FwdWalk {
 
 // VL: per-sequence lengths (padded batch).  Without them every length is T, rows past T
 // arrive as TMA's zero fill, and the padding code below compiles away.
-template <bool TF32, int D, bool VL>
+// SAVE (training forward, bf16 head_dim <= 64): the rotated fp16 queries R Q, which the
+// backward uses as its logit and dK' operand, are stored from shared memory once rotated
+// (tm_q16), and the backward's fp32 dQ' accumulator rows of each unit are zeroed by TMA
+// stores of a zero tile (tm_dqz).  This kernel leaves HBM mostly idle, so the backward's
+// preprocess pass no longer reads Q or writes these 37.8 MB (B16 T512 Hq12 D64).
+template <bool TF32, int D, bool VL, bool SAVE>
 __global__ void __launch_bounds__(480, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const __grid_constant__ CUtensorMap tm_q16, const __grid_constant__ CUtensorMap tm_dqz,
                     const FwdArgs a) {
     using C = FwdCfg<TF32, D>;
+    static_assert(!SAVE || (!TF32 && D == 64 && !VL), "the training forward is the bf16 head_dim-64 kernel");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;                               // NQB x (Q0 | Q1), later O staging
     uint8_t* sStage = sQ + C::NQB * C::QBUF;          // NS x (K | V | Vt)
+    uint8_t* sZero = sStage + C::NS * C::STAGE_BYTES;  // SAVE: a zero tile [128 rows x 128 bytes]
 
     __shared__ __align__(8) uint64_t bar_final;
     __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_ready[2], bar_q_empty[2];   // [Q buffer]
@@ -344,6 +356,15 @@ __global__ void __launch_bounds__(480, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_o);
+        if constexpr (SAVE) {
+            tma_prefetch_desc(&tm_q16);
+            tma_prefetch_desc(&tm_dqz);
+        }
+    }
+    if constexpr (SAVE) {
+        for (int i = tid; i < kZeroTileBytes / 16; i += C::THREADS)
+            reinterpret_cast<uint4*>(sZero)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();      // read by TMA stores after the barrier below
     }
     if (warp == 1) {
         __syncwarp();
@@ -384,6 +405,13 @@ __global__ void __launch_bounds__(480, 1)
                     for (int c = 0; c < C::NCH; ++c)
                         tma_load_4d(smem_u32(q_buf(k) + u * C::Q_BYTES + c * C::BM * 128), &tm_q, qf, c * C::EPC,
                                     f.h, f.q0 + u * C::BM, f.b);
+                if constexpr (SAVE) {
+                    // The unit's dQ' accumulator rows (fp32, 32 columns per store).
+                    for (int u = 0; u < f.n_qsub; ++u)
+                        for (int c0 = 0; c0 < a.dr; c0 += 32)
+                            tma_store_4d(&tm_dqz, smem_u32(sZero), c0, f.h, f.q0 + u * C::BM, f.b);
+                    bulk_commit_group();
+                }
                 if (qb == 0) last_k0 = k;
                 else last_k1 = k;
                 const int hkv = f.h / a.G;
@@ -408,6 +436,7 @@ __global__ void __launch_bounds__(480, 1)
             if (last_k1 >= 0) mbar_wait_drain(smem_u32(&bar_q_full[1]), (last_k1 / C::NQB) & 1, w, SITE_FWD_DRAIN);
             for (int g = max(0, issued - C::NS); g < issued; ++g)
                 mbar_wait_drain(smem_u32(&bar_kv_full[g % C::NS]), (g / C::NS) & 1, w, SITE_FWD_DRAIN);
+            if constexpr (SAVE) bulk_wait_group0();   // the zero stores have completed
         }
     } else if (warp < 3) {
         // ------------------------------------------------------------ UMMA issuers
@@ -570,6 +599,18 @@ __global__ void __launch_bounds__(480, 1)
                 rq.template apply<false>(qbuf + s2 * C::Q_BYTES, nullptr, qb, VL ? f.len - f.q0 - s2 * C::BM : C::BM);
             }
             fence_proxy_async_smem();
+            if constexpr (SAVE) {
+                // Every rotation of the unit is done (the four RoPE warps), then one thread
+                // stores R Q and waits until TMA has read it: the buffer later stages O, and
+                // that happens after this unit's S MMAs, which wait for the arrival below.
+                named_bar_sync(1, C::ROPE_THREADS);
+                if (rt == 0) {
+                    for (int s2 = 0; s2 < f.n_qsub; ++s2)
+                        tma_store_4d(&tm_q16, smem_u32(qbuf + s2 * C::Q_BYTES), 0, f.h, f.q0 + s2 * C::BM, f.b);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                }
+            }
             mbar_arrive(smem_u32(&bar_q_ready[k % C::NQB]));
             for (int j = 0; j < f.n_kv; ++j, ++g) {
                 const int s = g % C::NS;
@@ -588,6 +629,9 @@ __global__ void __launch_bounds__(480, 1)
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&bar_k_ready[s]));
             }
+        }
+        if constexpr (SAVE) {
+            if (rt == 0) bulk_wait_group0();   // the R Q stores have completed
         }
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ softmax (subtile u)
@@ -721,19 +765,22 @@ __global__ void __launch_bounds__(480, 1)
     }
 }
 
-template <bool TF32, int D, bool VL>
+template <bool TF32, int D, bool VL, bool SAVE = false>
 cudaError_t launch_fwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
+                         const CUtensorMap& to, const CUtensorMap& tq16, const CUtensorMap& tdqz, const FwdArgs& a,
+                         cudaStream_t st) {
     using C = FwdCfg<TF32, D>;
-    auto kfn = attn_fwd_kernel<TF32, D, VL>;
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    auto kfn = attn_fwd_kernel<TF32, D, VL, SAVE>;
+    constexpr int smem = C::SMEM + (SAVE ? kZeroTileBytes : 0);
+    static_assert(smem <= 227 * 1024, "shared memory");
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     // One CTA per SM (the shared memory allows no second), each walking its units.
     dim3 grid(a.n_units < sms ? a.n_units : sms);
-    return launch_k(kfn, grid, dim3(C::THREADS), C::SMEM, st, tq, tk, tv, to, a);
+    return launch_k(kfn, grid, dim3(C::THREADS), smem, st, tq, tk, tv, to, tq16, tdqz, a);
 }
 
 }  // namespace
@@ -742,23 +789,29 @@ int fwd_kv_box_rows(bool tf32, int D) { return 64; }
 
 template <bool VL>
 cudaError_t launch_fwd_vl(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
+                          const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tq16,
+                          const CUtensorMap& tdqz, const FwdArgs& a, cudaStream_t st) {
     if (!tf32) {
         // head_dim 32 runs the 64-wide kernel: its 128-byte TMA boxes read the upper 32
         // columns as zeros and the O store clips them.
-        if (D == 64 || D == 32) return launch_fwd_t<false, 64, VL>(B, tq, tk, tv, to, a, st);
-        if (D == 128) return launch_fwd_t<false, 128, VL>(B, tq, tk, tv, to, a, st);
+        if (D == 64 || D == 32) return launch_fwd_t<false, 64, VL>(B, tq, tk, tv, to, tq16, tdqz, a, st);
+        if (D == 128) return launch_fwd_t<false, 128, VL>(B, tq, tk, tv, to, tq16, tdqz, a, st);
     } else {
-        if (D == 32) return launch_fwd_t<true, 32, VL>(B, tq, tk, tv, to, a, st);
-        if (D == 64) return launch_fwd_t<true, 64, VL>(B, tq, tk, tv, to, a, st);
+        if (D == 32) return launch_fwd_t<true, 32, VL>(B, tq, tk, tv, to, tq16, tdqz, a, st);
+        if (D == 64) return launch_fwd_t<true, 64, VL>(B, tq, tk, tv, to, tq16, tdqz, a, st);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
-    return a.seq_lens ? launch_fwd_vl<true>(tf32, D, B, tq, tk, tv, to, a, st)
-                      : launch_fwd_vl<false>(tf32, D, B, tq, tk, tv, to, a, st);
+                       const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tq16,
+                       const CUtensorMap& tdqz, const FwdArgs& a, cudaStream_t st) {
+    if (a.save) {
+        if (tf32 || !(D == 64 || D == 32) || a.seq_lens) return cudaErrorInvalidValue;
+        return launch_fwd_t<false, 64, false, true>(B, tq, tk, tv, to, tq16, tdqz, a, st);
+    }
+    return a.seq_lens ? launch_fwd_vl<true>(tf32, D, B, tq, tk, tv, to, tq16, tdqz, a, st)
+                      : launch_fwd_vl<false>(tf32, D, B, tq, tk, tv, to, tq16, tdqz, a, st);
 }
 
 }  // namespace ne

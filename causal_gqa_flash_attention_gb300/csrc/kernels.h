@@ -74,13 +74,14 @@ struct FwdArgs {
     const int* seq_lens;     // [B] per-sequence lengths (positions at or past are padding), or null
     int dr;                  // the tensors' head_dim (bf16 32 runs the 64-wide kernel, zero-padded)
     FastDiv div_bh, div_hq;  // by B * Hq and by Hq (the unit decode)
+    int save;                // training forward: store R Q (fp16) and zero the dQ' accumulator
 };
 
 struct BwdPreArgs {
     const void* o;           // [B,T,Hq,D]
     const void* dO;          // [B,T,Hq,D]
     float* delta;            // [B,Hq,T]
-    float* dq_acc;           // [B,T,Hq,D] fp32, zeroed here
+    float* dq_acc;           // [B,T,Hq,D] fp32, zeroed here (null: zeroed by the training forward)
     long long rows;          // B*T*Hq
     int T, Hq, D;
     const void* q;           // [B,T,Hq,D] bf16: rotated into q16 when q16 is set
@@ -190,8 +191,11 @@ int fwd_kv_box_rows(bool tf32, int D);
 // ld: (cos, sin) pairs per table row (default D/2); pairs D/2 .. ld-1 get angle 0.
 cudaError_t launch_rope_table(float* cos_out, float* sin_out, float2* interleaved, int T, int D,
                               double theta, cudaStream_t st, int ld = 0);
+// `tq16` / `tdqz` map the backward workspace's fp16 R Q and fp32 dQ' accumulator; read only
+// when a.save is set (bf16 head_dim 32/64, no per-sequence lengths).
 cudaError_t launch_fwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
+                       const CUtensorMap& tv, const CUtensorMap& to, const CUtensorMap& tq16,
+                       const CUtensorMap& tdqz, const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_pre(bool tf32, const BwdPreArgs& a, cudaStream_t st);
 // `tdq` maps the fp32 dQ accumulator (used by the head_dim-64 kernel).
 cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUtensorMap& tk,

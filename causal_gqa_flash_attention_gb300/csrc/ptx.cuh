@@ -181,6 +181,10 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 __device__ __forceinline__ void bulk_wait_group0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Barrier `id` (1..15; 0 is __syncthreads) over `count` threads, whole warps.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // ------------------------------------------------------------------ tcgen05: TMEM
 // Allocation must be issued by one full warp; the column count is a power of two >= 32.

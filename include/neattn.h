@@ -104,6 +104,34 @@ ne_status ne_attn_bwd_f32(const float* q, const float* k, const float* v, const 
                           int B, int T, int Hq, int Hkv, int D, double rope_theta,
                           void* workspace, size_t workspace_bytes, ne_stream_t stream);
 
+/* Training pair: the forward and backward of one layer sharing that layer's backward
+ * workspace (the pages train with the forward and backward kernels of 커널 구현 and
+ * 검증 및 안정성, same page).  ne_attn_fwd_train computes what ne_attn_fwd computes and,
+ * for bf16 head_dim 32 and 64, also fills the workspace for the later backward: the
+ * rotated queries R Q as fp16 and a zeroed fp32 dQ accumulator (the forward rotates the
+ * queries anyway, and its HBM is mostly idle).  ne_attn_bwd_train then computes what
+ * ne_attn_bwd computes while skipping that work, so its preprocess pass only forms Delta.
+ * Same arguments as ne_attn_fwd / ne_attn_bwd plus the workspace (as for ne_attn_bwd:
+ * ne_attn_bwd_workspace_size() bytes, 256-byte aligned, caller-owned).  Contract: the
+ * backward must get the same workspace, the same q, k, v, shape and theta, and nothing
+ * may write the workspace between the two calls (one workspace per layer in flight).
+ * For f32 tensors and head_dim 128 the pair is exactly ne_attn_fwd + ne_attn_bwd (the
+ * forward leaves the workspace alone and the backward fills it itself). */
+ne_status ne_attn_fwd_train(const void* q, const void* k, const void* v, void* o, float* lse,
+                            void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int D,
+                            double rope_theta, ne_stream_t stream);
+ne_status ne_attn_fwd_train_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                                void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                                int D, double rope_theta, ne_stream_t stream);
+ne_status ne_attn_bwd_train(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                            int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                            void* workspace, size_t workspace_bytes, ne_stream_t stream);
+ne_status ne_attn_bwd_train_f32(const float* q, const float* k, const float* v, const float* o,
+                                const float* lse, const float* dO, float* dq, float* dk, float* dv,
+                                int B, int T, int Hq, int Hkv, int D, double rope_theta,
+                                void* workspace, size_t workspace_bytes, ne_stream_t stream);
+
 /* Variable-length sequences in a padded batch: the supervised fine-tuning data of
  * "NanoEuler: C와 CUDA로 밑바닥부터 구축한 GPT-2 규모의 LLM" (2단계 학습 프로세스, SFT bullet)
  * pads sequences of different lengths to one T, and the padding must not take part.
