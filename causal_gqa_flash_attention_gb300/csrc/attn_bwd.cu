@@ -544,9 +544,9 @@ __global__ void __launch_bounds__(512, 1)
             dv = qpos < len ? a.delta[rix] : 0.f;
         };
         auto publish = [&](int it, float lv, float dv) {
-            if (r < 64) {
-                s_lse[it & 1][cbase + r] = lv;
-                s_delta[it & 1][cbase + r] = dv;
+            if (r < 64) {                         // negated: added by packed FMA / add
+                s_lse[it & 1][cbase + r] = -lv;
+                s_delta[it & 1][cbase + r] = -dv;
             }
             mbar_arrive(smem_u32(&bar_rows[it & 1]));
         };
@@ -580,17 +580,27 @@ __global__ void __launch_bounds__(512, 1)
                 uint32_t pk[8], dk[8];
                 const float4* l4 = reinterpret_cast<const float4*>(&s_lse[sb][cbase + c]);
                 const float4* d4 = reinterpret_cast<const float4*>(&s_delta[sb][cbase + c]);
+                const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
                 for (int e = 0; e < 16; e += 4) {
+                    // -LSE log2(e) and -Delta (negated when staged): the exponent argument,
+                    // dP - Delta and P (dP - Delta) run as packed f32x2 pairs of queries.
                     const float4 lv = l4[e >> 2], dv = d4[e >> 2];   // broadcast reads
-                    const float lq[4] = {lv.x, lv.y, lv.z, lv.w}, dq[4] = {dv.x, dv.y, dv.z, dv.w};
-                    float p[4], gg[4];
+                    const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                                  sl2v, make_float2(lv.x, lv.y));
+                    const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])),
+                                                  sl2v, make_float2(lv.z, lv.w));
+                    float p[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
+                    for (int k = 0; k < 4; ++k)
                         if (diag && (kvpos > q0 + cbase + c + e + k || (VL && q0 + cbase + c + e + k >= len))) p[k] = 0.f;
-                        gg[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
-                    }
+                    const float2 g01 = __fmul2_rn(make_float2(p[0], p[1]),
+                                                  __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                                             make_float2(dv.x, dv.y)));
+                    const float2 g23 = __fmul2_rn(make_float2(p[2], p[3]),
+                                                  __fadd2_rn(make_float2(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                                             make_float2(dv.z, dv.w)));
+                    const float gg[4] = {g01.x, g01.y, g23.x, g23.y};
                     pk[e >> 1] = pack_bf162(p[0], p[1]);
                     pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
                     dk[e >> 1] = pack_bf162(gg[0], gg[1]);

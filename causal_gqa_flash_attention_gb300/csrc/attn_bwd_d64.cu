@@ -97,23 +97,36 @@ struct TileWalk {
 // follows every query (the chunk is all zero).
 // amax2 keeps the largest |dS| as packed fp16, so a value past the fp16 range shows up
 // as infinity.
+// nlse2 and ndelta hold -LSE log2(e) and -Delta of the chunk's queries, so that the
+// exponent argument, dP - Delta and the product P (dP - Delta) run as packed f32x2
+// instructions, two queries each.
 template <bool MASK>
-__device__ __forceinline__ void grad_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* lse2,
-                                           const float* delta, float sl2, int kl, int qlim, uint32_t (&pk)[16],
+__device__ __forceinline__ void grad_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float* nlse2,
+                                           const float* ndelta, float sl2, int kl, int qlim, uint32_t (&pk)[16],
                                            uint32_t (&dk)[16], __half2& amax2) {
-    const float4* l4 = reinterpret_cast<const float4*>(lse2);
-    const float4* d4 = reinterpret_cast<const float4*>(delta);
+    const float4* l4 = reinterpret_cast<const float4*>(nlse2);
+    const float4* d4 = reinterpret_cast<const float4*>(ndelta);
+    const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
         const float4 lq4 = l4[e >> 2], dq4 = d4[e >> 2];   // broadcast reads
-        const float lq[4] = {lq4.x, lq4.y, lq4.z, lq4.w}, dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w};
-        float p[4], ds[4];
+        const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2v,
+                                      make_float2(lq4.x, lq4.y));
+        const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2v,
+                                      make_float2(lq4.z, lq4.w));
+        float p[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
+        if (MASK) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            p[k] = ex2(fmaf(__uint_as_float(sr[e + k]), sl2, -lq[k]));
-            if (MASK && (kl > e + k || e + k >= qlim)) p[k] = 0.f;
-            ds[k] = p[k] * (__uint_as_float(dr[e + k]) - dq[k]);
+            for (int k = 0; k < 4; ++k)
+                if (kl > e + k || e + k >= qlim) p[k] = 0.f;
         }
+        const float2 g01 = __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                      make_float2(dq4.x, dq4.y));
+        const float2 g23 = __fadd2_rn(make_float2(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                      make_float2(dq4.z, dq4.w));
+        const float2 d01 = __fmul2_rn(make_float2(p[0], p[1]), g01);
+        const float2 d23 = __fmul2_rn(make_float2(p[2], p[3]), g23);
+        const float ds[4] = {d01.x, d01.y, d23.x, d23.y};
         pk[e >> 1] = pack_bf162(p[0], p[1]);
         pk[(e >> 1) + 1] = pack_bf162(p[2], p[3]);
         dk[e >> 1] = pack_half2(ds[0], ds[1]);
@@ -222,8 +235,9 @@ __global__ void __launch_bounds__(512, 1)
     auto mndesc = [](const void* p, uint32_t lbo) { return sdesc(smem_u32(p), lbo, 1024); };  // MN-major
 
     // The issuing warps (0-3) run their loops with all 32 lanes, so that descriptors and
-    // loop state stay warp-uniform; elect.sync picks the lane that issues each MMA and
-    // commit, and lane 0 issues the TMA copies.
+    // loop state stay warp-uniform; one elected lane issues each batch of MMAs and their
+    // commits in one branch (an election per MMA took several times the instructions),
+    // and lane 0 issues the TMA copies.
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer + dQ' issuer
         const uint32_t kvf = smem_u32(&bar_kv_full);
@@ -264,12 +278,15 @@ __global__ void __launch_bounds__(512, 1)
                 break;
             tc_fence_after();
             const uint64_t dSmn = mndesc(ds_tile(tb), C::DS_CHUNK);
+            if (elect_one()) {
 #pragma unroll
-            for (int ks = 0; ks < C::BKV / 16; ++ks)        // dQ' = dS K', K = key rows
-                umma_ss_e<false>(tm + C::DQ_COL, sdesc_add(dSmn, ks * 16 * 128), sdesc_add(dKmn, ks * 16 * 128),
-                                 id_dq, ks > 0);
-            umma_commit_e(smem_u32(&bar_dq_full));
-            umma_commit_e(smem_u32(&bar_ds_free[tb]));
+                for (int ks = 0; ks < C::BKV / 16; ++ks)    // dQ' = dS K', K = key rows
+                    umma_ss<false>(tm + C::DQ_COL, sdesc_add(dSmn, ks * 16 * 128), sdesc_add(dKmn, ks * 16 * 128),
+                                   id_dq, ks > 0);
+                umma_commit(smem_u32(&bar_dq_full));
+                umma_commit(smem_u32(&bar_ds_free[tb]));
+            }
+            __syncwarp();
             for (int hs = 2 * tau + C::NQS; ok && hs < 2 * tau + C::NQS + 2 && hs < n_hs; ++hs) ok = load(hs);
         }
         umma_commit_e(smem_u32(&bar_final));
@@ -300,11 +317,14 @@ __global__ void __launch_bounds__(512, 1)
                 break;
             tc_fence_after();
             const uint64_t dB = sdesc_add(dB0, s * C::STAGE_BYTES);
+            const uint32_t dcol = tm + (is_s ? s_col(bf) : dp_col(bf));
+            if (elect_one()) {                              // one elected lane issues the batch
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)            // K = head_dim: 16 per step (32 bytes)
-                umma_ss_e<false>(tm + (is_s ? s_col(bf) : dp_col(bf)), sdesc_add(dA, ks * 32), sdesc_add(dB, ks * 32),
-                                 id, ks > 0);
-            umma_commit_e(smem_u32(&bar_sdp_full[bf]));
+                for (int ks = 0; ks < D / 16; ++ks)        // K = head_dim: 16 per step (32 bytes)
+                    umma_ss<false>(dcol, sdesc_add(dA, ks * 32), sdesc_add(dB, ks * 32), id, ks > 0);
+                umma_commit(smem_u32(&bar_sdp_full[bf]));
+            }
+            __syncwarp();
         }
         umma_commit_e(smem_u32(&bar_final));
     } else if (warp == 3) {
@@ -318,17 +338,20 @@ __global__ void __launch_bounds__(512, 1)
             if (!(ok = mbar_wait_warp(smem_u32(&bar_ds_half[half]), tau & 1, w, SITE_BWD_DS_READY))) break;
             tc_fence_after();
             const uint64_t dOmn = sdesc_add(dOmn0, s * C::STAGE_BYTES), dQmn = sdesc_add(dQmn0, s * C::STAGE_BYTES);
-#pragma unroll
-            for (int ks = 0; ks < C::BH / 16; ++ks)         // dV += P^T dO (P^T from TMEM), K = queries
-                umma_ts_e<false>(tm + C::DV_COL, tm + pt_col(half) + 8 * ks, sdesc_add(dOmn, ks * 16 * 128), id_dv,
-                                 (hs > 0 || ks > 0) ? 1u : 0u);
             const uint64_t dDS = kdesc(ds_tile(tb) + half * C::DS_CHUNK);
+            if (elect_one()) {
 #pragma unroll
-            for (int ks = 0; ks < C::BH / 16; ++ks)         // dK' += dS^T Q', K = queries
-                umma_ss_e<false>(tm + C::DK_COL, sdesc_add(dDS, ks * 32), sdesc_add(dQmn, ks * 16 * 128), id_dk,
-                                 (hs > 0 || ks > 0) ? 1u : 0u);
-            umma_commit_e(smem_u32(&bar_qdo_empty[s]));
-            if (half == 1) umma_commit_e(smem_u32(&bar_ds_free[tb]));
+                for (int ks = 0; ks < C::BH / 16; ++ks)     // dV += P^T dO (P^T from TMEM), K = queries
+                    umma_ts<false>(tm + C::DV_COL, tm + pt_col(half) + 8 * ks, sdesc_add(dOmn, ks * 16 * 128), id_dv,
+                                   (hs > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < C::BH / 16; ++ks)     // dK' += dS^T Q', K = queries
+                    umma_ss<false>(tm + C::DK_COL, sdesc_add(dDS, ks * 32), sdesc_add(dQmn, ks * 16 * 128), id_dk,
+                                   (hs > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&bar_qdo_empty[s]));
+                if (half == 1) umma_commit(smem_u32(&bar_ds_free[tb]));
+            }
+            __syncwarp();
         }
         umma_commit_e(smem_u32(&bar_dkv_full));
         umma_commit_e(smem_u32(&bar_final));
@@ -422,9 +445,9 @@ __global__ void __launch_bounds__(512, 1)
         auto publish = [&](int hs, const float (&lv)[2], const float (&dv)[2]) {
             const int buf = (hs >> 1) & 1;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                s_lse[sw][buf][lane + 32 * k] = lv[k] * 1.4426950408889634f;
-                s_delta[sw][buf][lane + 32 * k] = dv[k];
+            for (int k = 0; k < 2; ++k) {       // negated: added by packed FMA / add
+                s_lse[sw][buf][lane + 32 * k] = -(lv[k] * 1.4426950408889634f);
+                s_delta[sw][buf][lane + 32 * k] = -dv[k];
             }
             __syncwarp();
         };
