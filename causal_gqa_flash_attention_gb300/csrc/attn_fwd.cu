@@ -441,14 +441,17 @@ __global__ void __launch_bounds__(480, 1)
     } else if (warp < 3) {
         // ------------------------------------------------------------ UMMA issuers
         // Each subtile has its own issuing warp (1 + u).  The whole warp runs the loop, so
-        // the UMMA operands stay warp-uniform, and one elected lane issues each batch (the
-        // UMMAs of a tile and their commit) in one branch: an election per UMMA, or a loop
-        // run by one lane alone (operands no longer provably uniform), took several times
-        // the instructions, and this role's steps are on the kernel's critical path (the
-        // instruction cache is shared with the softmax and RoPE warps).  Tiles are numbered t = 0, 1, ... over all units of the
-        // CTA; S(t) goes to S buffer t % 2, two tiles ahead of the softmax, and overwrites
-        // P(t-2), whose PV the same lane issued earlier (one thread's UMMAs execute in
-        // order).
+        // the UMMA operands stay warp-uniform, and one elected lane issues each batch in
+        // one branch: an election per UMMA, or a loop run by one lane alone (operands no
+        // longer provably uniform), took several times the instructions.  This role's
+        // steps are the kernel's critical path: clock64 traces put a 64-key tile at ~1.7K
+        // cycles with the softmax work removed, almost all of it waits, elections and
+        // bookkeeping between UMMA batches.  So the PV of a tile and the S the two-tile
+        // window then admits go out as one batch when the S can go at once (its K' tile
+        // rotated, its Q' already waited for).
+        // Tiles are numbered t = 0, 1, ... over all units of the CTA; S(t) goes to S
+        // buffer t % 2, two tiles ahead of the softmax, and overwrites P(t-2), whose PV
+        // the same lane issued earlier (one thread's UMMAs execute in order).
         const int u = warp - 1;
         constexpr uint32_t id_s = idesc_make(C::FMT_S, 128, C::BN, false, false);
         constexpr uint32_t id_o = idesc_make(C::FMT_PV, 128, D, false, !TF32);
@@ -466,51 +469,31 @@ __global__ void __launch_bounds__(480, 1)
         };
         int t_s = 0;                                  // S tiles issued
         int qr_next = 0;                              // first unit whose Q' this issuer has not waited for
-        auto issue_s = [&](const FwdWalk<C::BM, C::BN, VL>& c) -> bool {
-            // Q' of the unit (and of any unit skipped since the last one: every phase of
-            // the Q-ready barriers is waited for in order, so a parity never aliases).
-            for (; c.j == 0 && qr_next <= c.k; ++qr_next)
-                if (!mbar_wait_warp(smem_u32(&bar_q_ready[qr_next % C::NQB]), (qr_next / C::NQB) & 1, w, SITE_FWD_Q))
-                    return false;
-            const int g = c.kvb + c.j;
-            if (!k_ready(g)) return false;
-            const uint64_t dq = sdesc_add(dq0, (c.k % C::NQB) * C::QBUF);
+        FwdWalk<C::BM, C::BN, VL> sw;                 // the next tile to issue S for
+        sw.init(u, a);
+        // S(t_s) of tile sw: the UMMAs and the commit (run by the elected lane).
+        auto s_mmas = [&]() {
+            const int g = sw.kvb + sw.j;
+            const uint64_t dq = sdesc_add(dq0, (sw.k % C::NQB) * C::QBUF);
             const uint64_t dk = sdesc_add(dk0, (g % C::NS) * C::STAGE_BYTES);
             const uint32_t dcol = tm + s_col(u, t_s & 1);
-            if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
-                    const uint32_t byte = ks * 32;
-                    umma_ss<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
-                                  sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
-                }
-                umma_commit(smem_u32(&bar_s_full[u * 2 + (t_s & 1)]));
+            for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
+                const uint32_t byte = ks * 32;
+                umma_ss<TF32>(dcol, sdesc_add(dq, (byte >> 7) * C::BM * 128 + (byte & 127)),
+                              sdesc_add(dk, (byte >> 7) * C::BN * 128 + (byte & 127)), id_s, ks > 0);
             }
-            __syncwarp();
-            ++t_s;
-            return true;
+            umma_commit(smem_u32(&bar_s_full[u * 2 + (t_s & 1)]));
         };
-        auto issue_pv = [&](int t, int j, int g, bool last) -> bool {
-            if (!mbar_wait_warp(smem_u32(&bar_p_ready[u * 2 + (t & 1)]), (t >> 1) & 1, w, SITE_FWD_P_READY))
-                return false;
-            tc_fence_after();
-            const uint64_t dv = sdesc_add(dv0, (g % C::NS) * C::STAGE_BYTES);
-            const uint32_t pcol = tm + s_col(u, t & 1);
-            if (elect_one()) {
-#pragma unroll
-                for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
-                    // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
-                    // MN-major, PV_ROWS keys per K-step.
-                    const uint32_t off = TF32 ? ((ks * 32) >> 7) * D * 128 + ((ks * 32) & 127) : ks * C::PV_ROWS * 128;
-                    umma_ts<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (j > 0 || ks > 0) ? 1u : 0u);
-                }
-                if (last) umma_commit(smem_u32(&bar_o_final[u]));
-            }
-            __syncwarp();
-            return true;
+        // The waits S(t_s) needs: Q' of its unit (and of any unit skipped since the last
+        // one: every phase of the Q-ready barriers is waited for in order, so a parity
+        // never aliases) and its rotated K' tile.
+        auto s_waits = [&]() -> bool {
+            for (; sw.j == 0 && qr_next <= sw.k; ++qr_next)
+                if (!mbar_wait_warp(smem_u32(&bar_q_ready[qr_next % C::NQB]), (qr_next / C::NQB) & 1, w, SITE_FWD_Q))
+                    return false;
+            return k_ready(sw.kvb + sw.j);
         };
-        FwdWalk<C::BM, C::BN, VL> sw;                     // the next tile to issue S for
-        sw.init(u, a);
         int t = 0, g = 0;                             // PV tiles issued; K/V tiles passed
         // S runs at most two tiles ahead of PV.  With one Q buffer the next unit's Q can
         // only land after this unit's epilogues, which wait for this unit's last PVs, so
@@ -519,7 +502,9 @@ __global__ void __launch_bounds__(480, 1)
         // inside the loop, where this issuer has released all but the last
         // n_kv - n_u + 1 <= 3 stages of the unit, and NS >= 4 lets the next unit's first
         // K/V tile load regardless.
-        auto may_issue = [&](int k_cur) { return sw.k >= 0 && t_s < t + 2 && (C::NQB == 2 || sw.k <= k_cur); };
+        auto may_issue = [&](int k_cur, int t_pv) {
+            return sw.k >= 0 && t_s < t_pv + 2 && (C::NQB == 2 || sw.k <= k_cur);
+        };
         // The PV walk: every K/V tile g of every unit in order, tile jp of unit kp, of
         // which the first np are this subtile's (the rest lie beyond its diagonal).
         int kp = 0, jp = 0, np = 0, nkv = 0;
@@ -535,27 +520,60 @@ __global__ void __launch_bounds__(480, 1)
         };
         bool more = load_pv();
         bool ok = true;
-        // One loop with one S site and one PV site: every issue decision of the role in a
-        // single short body, so the warp's code stays in the instruction cache while the
-        // softmax warps on the same SM sub-partition run theirs.  After each PV (and at
-        // the start) every S the two-tile window allows goes first.  Every K/V stage is
-        // released by both issuers, in order; a tile beyond the subtile's diagonal is
-        // released without use, but only once the stage really holds it (k_ready), so the
-        // release never runs a phase ahead.
+        // One loop: every issue decision of the role in one short body, so the warp's code
+        // stays in the instruction cache beside the softmax and RoPE warps' code.  Every
+        // K/V stage is released by both issuers, in order; a tile beyond the subtile's
+        // diagonal is released without use, but only once the stage really holds it
+        // (k_ready), so the release never runs a phase ahead.
         while (ok) {
-            if (may_issue(kp)) {
-                ok = issue_s(sw);
+            if (may_issue(kp, t)) {                   // an S on its own (start, unit change)
+                if (!(ok = s_waits())) break;
+                if (elect_one()) s_mmas();
+                __syncwarp();
+                ++t_s;
                 sw.advance(u, a);
                 continue;
             }
             if (!more) break;
+            const uint32_t kv_empty = smem_u32(&bar_kv_empty[g % C::NS]);
             if (jp < np) {
-                if (!(ok = issue_pv(t, jp, g, jp == np - 1))) break;
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_p_ready[u * 2 + (t & 1)]), (t >> 1) & 1, w,
+                                          SITE_FWD_P_READY)))
+                    break;
+                // The S this PV admits joins the batch if it needs no wait: its unit's Q'
+                // was waited for and its K' tile is already rotated (a test, not a wait).
+                bool fuse = may_issue(kp, t + 1) && !(sw.j == 0 && qr_next <= sw.k);
+                if (fuse) {
+                    const int gs = sw.kvb + sw.j;
+                    fuse = __all_sync(0xffffffffu, mbar_test(smem_u32(&bar_k_ready[gs % C::NS]), (gs / C::NS) & 1));
+                }
+                tc_fence_after();
+                const uint64_t dv = sdesc_add(dv0, (g % C::NS) * C::STAGE_BYTES);
+                const uint32_t pcol = tm + s_col(u, t & 1);
+                const bool last = jp == np - 1;
+                if (elect_one()) {
+#pragma unroll
+                    for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
+                        // TF32: V^T [D x BN] K-major, 32 keys per chunk; bf16: V [BN x D]
+                        // MN-major, PV_ROWS keys per K-step.
+                        const uint32_t off =
+                            TF32 ? ((ks * 32) >> 7) * D * 128 + ((ks * 32) & 127) : ks * C::PV_ROWS * 128;
+                        umma_ts<TF32>(ocol, pcol + ks * 8, sdesc_add(dv, off), id_o, (jp > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    if (last) umma_commit(smem_u32(&bar_o_final[u]));
+                    umma_commit(kv_empty);
+                    if (fuse) s_mmas();
+                }
+                __syncwarp();
                 ++t;
-            } else if (!(ok = k_ready(g))) {
-                break;
+                if (fuse) {
+                    ++t_s;
+                    sw.advance(u, a);
+                }
+            } else {
+                if (!(ok = k_ready(g))) break;
+                umma_commit_e(kv_empty);
             }
-            umma_commit_e(smem_u32(&bar_kv_empty[g % C::NS]));
             ++g;
             if (++jp == nkv) {
                 jp = 0;
