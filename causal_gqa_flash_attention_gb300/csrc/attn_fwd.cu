@@ -321,6 +321,7 @@ __global__ void __launch_bounds__(480, 1)
 
     __shared__ __align__(8) uint64_t bar_final;
     __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_ready[2], bar_q_empty[2];   // [Q buffer]
+    __shared__ __align__(8) uint64_t bar_q16_read[2];  // [Q buffer] SAVE: the R Q store has read it
     __shared__ __align__(8) uint64_t bar_o_final[2], bar_o_staged[2];  // [subtile]
     __shared__ __align__(8) uint64_t bar_s_full[4], bar_p_ready[4];     // [u * 2 + buffer]
     __shared__ __align__(8) uint64_t bar_kv_full[C::NS], bar_k_ready[C::NS], bar_kv_empty[C::NS];
@@ -336,6 +337,7 @@ __global__ void __launch_bounds__(480, 1)
             mbar_init(smem_u32(&bar_q_full[i]), 1);
             mbar_init(smem_u32(&bar_q_ready[i]), C::ROPE_THREADS);
             mbar_init(smem_u32(&bar_q_empty[i]), 2);     // one arrival per subtile epilogue
+            mbar_init(smem_u32(&bar_q16_read[i]), 1);    // the storing RoPE thread
             mbar_init(smem_u32(&bar_o_final[i]), 1);     // the last PV of a unit
             mbar_init(smem_u32(&bar_o_staged[i]), 128);
         }
@@ -405,13 +407,19 @@ __global__ void __launch_bounds__(480, 1)
                     for (int c = 0; c < C::NCH; ++c)
                         tma_load_4d(smem_u32(q_buf(k) + u * C::Q_BYTES + c * C::BM * 128), &tm_q, qf, c * C::EPC,
                                     f.h, f.q0 + u * C::BM, f.b);
-                if constexpr (SAVE) {
-                    // The unit's dQ' accumulator rows (fp32, 32 columns per store).
-                    for (int u = 0; u < f.n_qsub; ++u)
-                        for (int c0 = 0; c0 < a.dr; c0 += 32)
-                            tma_store_4d(&tm_dqz, smem_u32(sZero), c0, f.h, f.q0 + u * C::BM, f.b);
-                    bulk_commit_group();
-                }
+                // Training forward: the unit's dQ' accumulator rows are zeroed by stores of
+                // the zero tile (fp32, 128 rows x 32 columns each), one after each K/V tile
+                // request rather than all at once ahead of them.
+                int zs = 0;
+                const int n_zs = SAVE ? f.n_qsub * ((a.dr + 31) / 32) : 0;
+                auto zero_store = [&]() {
+                    if (zs < n_zs) {
+                        const int per = (a.dr + 31) / 32;
+                        tma_store_4d(&tm_dqz, smem_u32(sZero), (zs % per) * 32, f.h, f.q0 + (zs / per) * C::BM, f.b);
+                        bulk_commit_group();
+                        ++zs;
+                    }
+                };
                 if (qb == 0) last_k0 = k;
                 else last_k1 = k;
                 const int hkv = f.h / a.G;
@@ -429,7 +437,10 @@ __global__ void __launch_bounds__(480, 1)
                                     f.b);
                     }
                     ++issued;
+                    if constexpr (SAVE) zero_store();
                 }
+                if constexpr (SAVE)
+                    while (ok && zs < n_zs) zero_store();
             }
             // Teardown: every copy this CTA started must have landed before exit.
             if (last_k0 >= 0) mbar_wait_drain(smem_u32(&bar_q_full[0]), (last_k0 / C::NQB) & 1, w, SITE_FWD_DRAIN);
@@ -595,11 +606,20 @@ __global__ void __launch_bounds__(480, 1)
         rq.init(rt, a.rope);
         int g = 0;
         bool ok = true;
+        int q16_pending = -1;                         // SAVE: unit whose R Q store may still be reading
+        auto q16_release = [&]() {
+            if (SAVE && rt == 0 && q16_pending >= 0) {
+                bulk_wait_group_read0();
+                mbar_arrive(smem_u32(&bar_q16_read[q16_pending % C::NQB]));
+                q16_pending = -1;
+            }
+        };
         for (int k = 0; ok; ++k) {
             const int U = fwd_unit_index(k, a.n_units);
             if (U < 0) break;
             const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(U, a);
             uint8_t* qbuf = q_buf(k);
+            q16_release();
             // The table rows are fetched before the wait, so their latency overlaps it.
             float4 qa[RopeQ::F4], qc[RopeQ::F4], kn[RopeK::F4];
             rq.load_base(qa, f.q0, T, a.rope);
@@ -619,14 +639,15 @@ __global__ void __launch_bounds__(480, 1)
             fence_proxy_async_smem();
             if constexpr (SAVE) {
                 // Every rotation of the unit is done (the four RoPE warps), then one thread
-                // stores R Q and waits until TMA has read it: the buffer later stages O, and
-                // that happens after this unit's S MMAs, which wait for the arrival below.
+                // stores R Q.  The buffer later stages the unit's O: the epilogue waits for
+                // bar_q16_read, which this thread arrives on once TMA has read the tile (at
+                // its next unit, or after its loop): waiting here delayed the unit's S.
                 named_bar_sync(1, C::ROPE_THREADS);
                 if (rt == 0) {
                     for (int s2 = 0; s2 < f.n_qsub; ++s2)
                         tma_store_4d(&tm_q16, smem_u32(qbuf + s2 * C::Q_BYTES), 0, f.h, f.q0 + s2 * C::BM, f.b);
                     bulk_commit_group();
-                    bulk_wait_group_read0();
+                    q16_pending = k;
                 }
             }
             mbar_arrive(smem_u32(&bar_q_ready[k % C::NQB]));
@@ -649,6 +670,7 @@ __global__ void __launch_bounds__(480, 1)
             }
         }
         if constexpr (SAVE) {
+            q16_release();
             if (rt == 0) bulk_wait_group0();   // the R Q stores have completed
         }
     } else if (warp >= 4 && warp < 12) {
@@ -717,6 +739,9 @@ __global__ void __launch_bounds__(480, 1)
             // last two PVs may have completed before this wait starts, and the parity of
             // the older one would then name a phase that is still to come.
             if (!(ok = mbar_wait_warp(smem_u32(&bar_o_final[u]), n_epi & 1, w, SITE_FWD_O_DONE))) break;
+            // Training forward: the R Q store of this unit has read the buffer O is staged in.
+            if (SAVE && !(ok = mbar_wait_warp(smem_u32(&bar_q16_read[qb]), (k / C::NQB) & 1, w, SITE_FWD_O_DONE)))
+                break;
             tc_fence_after();
             const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(fwd_unit_index(k, a.n_units), a);
             uint8_t* sQu = q_buf(k) + u * C::Q_BYTES;
