@@ -392,7 +392,8 @@ def sweep_point(wid, dev, steps, peak):
 def prologue_point(dev, steps, peak, layers=16):
     """The fused RMSNorm -> QKV projection -> RoPE prologue at the GPU-pipeline shape
     (x [16, 512, 768] bf16, 12/4 heads of 64), one call per layer on distinct buffers:
-    2 M N K FLOPs per call, M = 8192 tokens, N = 1280 features, K = 768."""
+    2 M N K FLOPs per call, M = 8192 tokens, N = 1280 features, K = 768 (the call includes
+    its small pass folding the gain into the weights)."""
     import torch
 
     import causal_gqa_flash_attention_gb300 as ne
@@ -405,9 +406,12 @@ def prologue_point(dev, steps, peak, layers=16):
                      torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=dev),
                      torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=dev)))
 
+    n_ws = int(ne.load().ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D))
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)      # W diag(gamma), rewritten by each call
+
     def step():
         for x, g, wt, q, k, v in bufs:
-            ne.qkv_prologue(x, g, wt, Hq, Hkv, D, rotate=True, q=q, k=k, v=v)
+            ne.qkv_prologue(x, g, wt, Hq, Hkv, D, rotate=True, q=q, k=k, v=v, workspace=ws)
 
     for _ in range(3):
         step()

@@ -34,7 +34,7 @@ EXPORTS = (
     "ne_profile_enable", "ne_profile_totals", "ne_attn_decode_workspace_size", "ne_attn_decode",
     "ne_attn_decode_f32", "ne_noalloc_get_device_error", "ne_attn_fwd_varlen", "ne_attn_fwd_varlen_f32",
     "ne_attn_bwd_varlen", "ne_attn_bwd_varlen_f32", "ne_qkv_prologue", "ne_attn_fwd_train",
-    "ne_attn_fwd_train_f32", "ne_attn_bwd_train", "ne_attn_bwd_train_f32",
+    "ne_attn_fwd_train_f32", "ne_attn_bwd_train", "ne_attn_bwd_train_f32", "ne_qkv_prologue_workspace_size",
 )
 
 
@@ -75,7 +75,9 @@ def load(path: str | None = None):
         lib.ne_attn_fwd_varlen_f32.argtypes = lib.ne_attn_fwd_varlen.argtypes
         lib.ne_attn_bwd_varlen.argtypes = [vp] * 10 + [i] * 5 + [d, vp, sz, vp]
         lib.ne_attn_bwd_varlen_f32.argtypes = lib.ne_attn_bwd_varlen.argtypes
-        lib.ne_qkv_prologue.argtypes = [vp] * 6 + [i] * 6 + [d, d, i, vp]
+        lib.ne_qkv_prologue.argtypes = [vp] * 6 + [i] * 6 + [d, d, i, vp, sz, vp]
+        lib.ne_qkv_prologue_workspace_size.argtypes = [i] * 4
+        lib.ne_qkv_prologue_workspace_size.restype = sz
         lib.ne_attn_fwd_train.argtypes = [vp] * 6 + [sz] + [i] * 5 + [d, vp]
         lib.ne_attn_fwd_train_f32.argtypes = lib.ne_attn_fwd_train.argtypes
         lib.ne_attn_bwd_train.argtypes = lib.ne_attn_bwd.argtypes
@@ -263,7 +265,7 @@ def attn_bwd_varlen(q, k, v, o, lse, dO, seq_lens, theta: float = 10000.0, works
 
 
 def qkv_prologue(x, gamma, w, Hq: int, Hkv: int, D: int, eps: float = 1e-5, theta: float = 10000.0,
-                 rotate: bool = False, q=None, k=None, v=None):
+                 rotate: bool = False, q=None, k=None, v=None, workspace=None):
     """RMSNorm (gain gamma) -> projection w [(Hq + 2 Hkv) D, dim] -> q, k, v heads, RoPE
     on q and k when `rotate` (the attention calls take the unrotated form).  x [B, T, dim]
     bf16; returns q [B, T, Hq, D], k and v [B, T, Hkv, D] bf16."""
@@ -280,8 +282,12 @@ def qkv_prologue(x, gamma, w, Hq: int, Hkv: int, D: int, eps: float = 1e-5, thet
     q = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device=x.device) if q is None else q
     k = torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=x.device) if k is None else k
     v = torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=x.device) if v is None else v
+    if workspace is None:
+        n = int(lib.ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D))
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=x.device)
     _check(lib.ne_qkv_prologue(_ptr(x), _ptr(gamma), _ptr(w), _ptr(q), _ptr(k), _ptr(v), B, T, dim, Hq, Hkv, D,
-                               float(eps), float(theta), 1 if rotate else 0, _stream(x)))
+                               float(eps), float(theta), 1 if rotate else 0, _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(x)))
     return q, k, v
 
 

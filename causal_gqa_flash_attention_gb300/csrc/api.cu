@@ -672,9 +672,14 @@ ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* 
                             workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
+size_t ne_qkv_prologue_workspace_size(int dim, int Hq, int Hkv, int D) {
+    if (dim <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
+    return round_up((size_t)(Hq + 2 * Hkv) * D * dim * 2, 256);
+}
+
 ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void* q, void* k, void* v, int B, int T,
                           int dim, int Hq, int Hkv, int D, double eps, double rope_theta, int rotate,
-                          ne_stream_t stream) {
+                          void* workspace, size_t workspace_bytes, ne_stream_t stream) {
     g_last_error.clear();
     cudaStream_t st = (cudaStream_t)stream;
     if (B < 0 || T < 0) return fail(NE_ERR_INVALID_ARG, "B and T must be >= 0 (B=%d T=%d)", B, T);
@@ -693,6 +698,13 @@ ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void*
     if (M == 0) return NE_OK;
     ne_status s;
     if ((s = check_ptrs({x, gamma, w, q, k, v})) != NE_OK) return s;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(NE_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+    if (workspace_bytes < ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D))
+        return fail(NE_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes,
+                    ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D));
+    if ((reinterpret_cast<uintptr_t>(gamma) & 15u) != 0 || (reinterpret_cast<uintptr_t>(w) & 15u) != 0)
+        return fail(NE_ERR_INVALID_ARG, "gamma and w must be 16-byte aligned");
     int dev;
     if ((s = current_device(&dev)) != NE_OK) return s;
     int* err;
@@ -701,9 +713,11 @@ ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void*
     if ((s = rope_cache(dev, T, D, rope_theta, st, &rope)) != NE_OK) return s;
     CUtensorMap tx, tw;
     if ((s = map_rows_bf16(&tx, x, M, dim, 128)) != NE_OK) return s;
-    if ((s = map_rows_bf16(&tw, w, N, dim, ne::prologue_tile_n())) != NE_OK) return s;
+    // The gain folded into the weights: W' = W diag(gamma) in the workspace.
+    cudaError_t e = ne::launch_gain_weights(w, gamma, workspace, N, dim, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gain weights launch");
+    if ((s = map_rows_bf16(&tw, workspace, N, dim, ne::prologue_tile_n())) != NE_OK) return s;
     ne::ProArgs a;
-    a.gamma = gamma;
     a.q = q;
     a.k = k;
     a.v = v;
@@ -718,7 +732,7 @@ ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void*
     a.rotate = rotate;
     a.err = err;
     a.timeout_ns = timeout_ns();
-    cudaError_t e = ne::launch_qkv_prologue(tx, tw, a, st);
+    e = ne::launch_qkv_prologue(tx, tw, a, st);
     if (e != cudaSuccess) return cuda_fail(e, "qkv prologue launch");
     return NE_OK;
 }

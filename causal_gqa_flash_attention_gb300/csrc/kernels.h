@@ -111,7 +111,6 @@ struct BwdArgs {
 
 // RMSNorm -> QKV projection -> RoPE prologue (qkv_prologue.cu), bf16 tensors.
 struct ProArgs {
-    const void* gamma;       // [dim] RMSNorm gain
     void* q;                 // [B,T,Hq,D]
     void* k;                 // [B,T,Hkv,D]
     void* v;                 // [B,T,Hkv,D]
@@ -185,6 +184,8 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // (64 x prologue_tile_n()) boxes.
 int prologue_tile_n();
 cudaError_t launch_qkv_prologue(const CUtensorMap& tx, const CUtensorMap& tw, const ProArgs& a, cudaStream_t st);
+// wg [N, dim] = w [N, dim] times gamma [dim] along each row (bf16); dim % 8 == 0.
+cudaError_t launch_gain_weights(const void* w, const void* gamma, void* wg, long long N, int dim, cudaStream_t st);
 // Tile rows of the key/value tensor maps the forward kernel expects.
 int fwd_kv_box_rows(bool tf32, int D);
 // Launchers: return cudaSuccess or the launch error.

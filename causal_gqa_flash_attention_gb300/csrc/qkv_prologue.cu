@@ -6,16 +6,21 @@
 //   r_m = sqrt(mean_c x_mc^2 + eps),   y_m = W (x_m o gamma) / r_m
 // with W [(Hq + 2 Hkv) D, dim] (query heads, then key heads, then value heads).  Since
 // 1/r_m is one factor per output row, it is applied to the fp32 accumulator in the
-// epilogue; gamma multiplies the x tile in shared memory before the MMA reads it.
+// epilogue; gamma is folded into the weights once per call (W' = W diag(gamma), a small
+// pass into the caller's workspace), so x goes from TMA straight to the MMA.
 //
 // One CTA per 128-row x 256-column output tile; the dim (K) axis streams through an
 // NS-stage ring of 64-column chunks (x: 128 rows, W: 256 rows, 128 bytes each,
 // 128-byte-swizzled by TMA).  Warp roles (192 threads):
 //   warp 0      TMA producer.
 //   warp 1      TMEM owner (256 columns) and UMMA issuer: M128 N256 K16, 4 per chunk.
-//   warps 2-5   thread = token row = TMEM lane: per chunk, the row's sum of squares and
-//               x o gamma written back in place (bf16); at the end the epilogue:
-//               acc / r_m, RoPE on query and key heads (position m mod T), bf16 stores.
+//   warps 2-5   thread = token row = TMEM lane: per chunk, the row's sum of squares
+//               (read beside the MMA, which needs no wait for it); at the end the
+//               epilogue: acc / r_m, RoPE on query and key heads (position m mod T),
+//               bf16 stores.  A stage is free once both the MMAs and these warps read it.
+// clock64 traces of the first version, which multiplied x by gamma in place between TMA
+// and MMA, showed that pass (~2.2K cycles a chunk on one warp per SM sub-partition) and
+// an epilogue that waited on a table load per chunk (~15K cycles) as the whole cost.
 // Every wait is bounded; a CTA that gives up records an error code, drains its own copies
 // and MMAs and frees its TMEM.
 #include <cuda_bf16.h>
@@ -40,6 +45,7 @@ struct ProCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
+template <int D>
 __global__ void __launch_bounds__(192, 1)
     qkv_prologue_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                         const ProArgs a) {
@@ -49,7 +55,7 @@ __global__ void __launch_bounds__(192, 1)
     auto st_a = [&](int s) { return smem + s * C::STAGE; };
     auto st_b = [&](int s) { return smem + s * C::STAGE + C::A_BYTES; };
 
-    __shared__ __align__(8) uint64_t bar_full[C::NS], bar_ready[C::NS], bar_empty[C::NS];
+    __shared__ __align__(8) uint64_t bar_full[C::NS], bar_empty[C::NS];
     __shared__ __align__(8) uint64_t bar_acc;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -61,8 +67,7 @@ __global__ void __launch_bounds__(192, 1)
     if (tid == 0) {
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
-            mbar_init(smem_u32(&bar_ready[s]), 128);
-            mbar_init(smem_u32(&bar_empty[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), 1 + 128);   // the MMA commit and the norm threads
         }
         mbar_init(smem_u32(&bar_acc), 1);
         abort_flag = 0;
@@ -107,13 +112,16 @@ __global__ void __launch_bounds__(192, 1)
         const uint64_t da0 = sdesc(smem_u32(st_a(0)), 16, 1024), db0 = sdesc(smem_u32(st_b(0)), 16, 1024);
         for (int kc = 0; kc < nk; ++kc) {
             const int s = kc % C::NS;
-            if (!mbar_wait_warp(smem_u32(&bar_ready[s]), (kc / C::NS) & 1, w, SITE_PRO_READY)) break;
+            if (!mbar_wait_warp(smem_u32(&bar_full[s]), (kc / C::NS) & 1, w, SITE_PRO_FULL)) break;
             tc_fence_after();
             const uint64_t da = sdesc_add(da0, s * C::STAGE), db = sdesc_add(db0, s * C::STAGE);
+            if (elect_one()) {                        // one elected lane issues the batch
 #pragma unroll
-            for (int ks = 0; ks < C::BK / 16; ++ks)   // K = dim, 16 per step (32 bytes)
-                umma_ss_e<false>(tm, sdesc_add(da, ks * 32), sdesc_add(db, ks * 32), id, (kc > 0 || ks > 0) ? 1u : 0u);
-            umma_commit_e(smem_u32(&bar_empty[s]));
+                for (int ks = 0; ks < C::BK / 16; ++ks)   // K = dim, 16 per step (32 bytes)
+                    umma_ss<false>(tm, sdesc_add(da, ks * 32), sdesc_add(db, ks * 32), id, (kc > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&bar_empty[s]));
+            }
+            __syncwarp();
         }
         umma_commit_e(smem_u32(&bar_acc));   // also the teardown's: every MMA of this CTA
     } else {
@@ -122,40 +130,45 @@ __global__ void __launch_bounds__(192, 1)
         const int r = quarter * 32 + lane;              // token row of the tile = TMEM lane
         const int m = m0 + r;
         const uint32_t lt = tm + ((uint32_t)(quarter * 32) << 16);
-        const uint4* g4 = reinterpret_cast<const uint4*>(a.gamma);
-        float ss = 0.f;
+        // The (cos, sin) table row of this token's position, D/2 pairs, fetched before the
+        // main loop so its latency hides under it: a load waited on per 32-column chunk set
+        // the epilogue's pace.
+        float4 tabr[D / 4];
+        {
+            const float4* tr = reinterpret_cast<const float4*>(a.rope + (size_t)(m % a.T) * (D / 2));
+#pragma unroll
+            for (int e = 0; e < D / 4; ++e)
+                tabr[e] = a.rotate && m < a.M ? __ldg(tr + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float2 ss2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};       // independent sums (past dim: TMA's zero fill)
         bool ok = true;
         for (int kc = 0; kc < nk; ++kc) {
             const int s = kc % C::NS;
             if (!(ok = mbar_wait_warp(smem_u32(&bar_full[s]), (kc / C::NS) & 1, w, SITE_PRO_FULL))) break;
-            uint8_t* arow = st_a(s);
+            const uint8_t* arow = st_a(s);
+            uint4 xv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) xv[u] = *reinterpret_cast<const uint4*>(arow + sw128_offset(r, u));
+            mbar_arrive(smem_u32(&bar_empty[s]));       // read: the stage may take the next chunk
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int c0 = kc * C::BK + 8 * u;      // dim index of the unit's first element
-                uint4* p = reinterpret_cast<uint4*>(arow + sw128_offset(r, u));
-                const uint4 xv = *p;
-                // Past dim the tile holds TMA's zero fill; its gain is taken as 0.
-                const uint4 gv = c0 < a.dim ? __ldg(g4 + (c0 >> 3)) : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                uint32_t o[4];
+                const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[e]));
-                    const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
-                    ss = fmaf(xf.x, xf.x, fmaf(xf.y, xf.y, ss));
-                    o[e] = pack_bf162(xf.x * gf.x, xf.y * gf.y);
+                    ss2[e] = __ffma2_rn(xf, xf, ss2[e]);
                 }
-                *p = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bar_ready[s]));
         }
+        const float ss = ((ss2[0].x + ss2[0].y) + (ss2[1].x + ss2[1].y)) + ((ss2[2].x + ss2[2].y) + (ss2[3].x + ss2[3].y));
         if (ok && mbar_wait_warp(smem_u32(&bar_acc), 0, w, SITE_PRO_ACC)) {
             tc_fence_after();
             const float inv_r = rsqrtf(ss / (float)a.dim + a.eps);
-            const int t = m % a.T;
-            const int nh = a.Hq + 2 * a.Hkv, D = a.D;
-#pragma unroll 1
+            const int nh = a.Hq + 2 * a.Hkv;
+            // Unrolled over the tile's chunks so each chunk's table pairs are registers
+            // named at compile time (32 columns = 16 pairs; the tile starts on a head).
+#pragma unroll
             for (int c = 0; c < C::BN; c += 32) {
                 uint32_t x[32];
                 tmem_ld32(lt + c, x);
@@ -164,19 +177,19 @@ __global__ void __launch_bounds__(192, 1)
                 const int n = n0 + c;                   // first output feature of the chunk
                 if (m >= a.M || n >= nh * D) continue;
                 const int h = n / D, e0 = n - h * D;    // head and column within it (32 | D)
+                static_assert(C::BN % D == 0 || D % C::BN == 0, "chunks line up with heads");
                 float y[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) y[e] = __uint_as_float(x[e]) * inv_r;
                 if (a.rotate && h < a.Hq + a.Hkv) {     // RoPE on query and key heads
-                    const float4* tab = reinterpret_cast<const float4*>(a.rope + (size_t)t * (D / 2) + e0 / 2);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 cs = __ldg(tab + e / 4);
+                        const float4 cs = tabr[((c % D) + e) / 4];
                         const float y0 = y[e], y1 = y[e + 1], y2 = y[e + 2], y3 = y[e + 3];
-                        y[e] = y0 * cs.x - y1 * cs.y;
-                        y[e + 1] = y0 * cs.y + y1 * cs.x;
-                        y[e + 2] = y2 * cs.z - y3 * cs.w;
-                        y[e + 3] = y2 * cs.w + y3 * cs.z;
+                        y[e] = rot0(y0, y1, cs.x, cs.y);
+                        y[e + 1] = rot1(y0, y1, cs.x, cs.y);
+                        y[e + 2] = rot0(y2, y3, cs.z, cs.w);
+                        y[e + 3] = rot1(y2, y3, cs.z, cs.w);
                     }
                 }
                 __nv_bfloat16* dst = h < a.Hq ? static_cast<__nv_bfloat16*>(a.q) + ((size_t)m * a.Hq + h) * D
@@ -203,12 +216,45 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+// W' = W diag(gamma): row n, column c of the projection times the gain of input column c,
+// rounded to bf16; 8 elements (16 bytes) per thread step.
+__global__ void __launch_bounds__(256) gain_weights_kernel(const __nv_bfloat16* __restrict__ w,
+                                                           const __nv_bfloat16* __restrict__ gamma,
+                                                           __nv_bfloat16* __restrict__ wg, long long n8, int dim8) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const uint4* w4 = reinterpret_cast<const uint4*>(w);
+    const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+    uint4* o4 = reinterpret_cast<uint4*>(wg);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+        const uint4 wv = w4[i], gv = __ldg(g4 + (int)(i % dim8));
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ww[e]));
+            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+            o[e] = pack_bf162(wf.x * gf.x, wf.y * gf.y);
+        }
+        o4[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 }  // namespace
 
 int prologue_tile_n() { return ProCfg::BN; }
 
+cudaError_t launch_gain_weights(const void* w, const void* gamma, void* wg, long long N, int dim, cudaStream_t st) {
+    const long long n8 = N * dim / 8;
+    long long blocks = (n8 + 255) / 256;
+    if (blocks > 152 * 4) blocks = 152 * 4;
+    return launch_k(gain_weights_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                    static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(gamma),
+                    static_cast<__nv_bfloat16*>(wg), n8, dim / 8);
+}
+
 cudaError_t launch_qkv_prologue(const CUtensorMap& tx, const CUtensorMap& tw, const ProArgs& a, cudaStream_t st) {
-    auto kfn = qkv_prologue_kernel;
+    auto kfn = a.D == 32 ? qkv_prologue_kernel<32> : a.D == 64 ? qkv_prologue_kernel<64> : qkv_prologue_kernel<128>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ProCfg::SMEM);
     if (e != cudaSuccess) return e;
     const int N = (a.Hq + 2 * a.Hkv) * a.D;

@@ -246,14 +246,20 @@ ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* 
  *   x     [B, T, dim] bf16 (in)          gamma [dim] bf16 (in)
  *   w     [(Hq + 2 Hkv) * D, dim] bf16, row-major (in: row n holds output feature n)
  *   q     [B, T, Hq, D] bf16 (out)       k, v  [B, T, Hkv, D] bf16 (out)
- * Arithmetic: bf16 tensor-core products with fp32 accumulation; x o gamma is rounded to
- * bf16 before the product, the root-mean-square is fp32.  Supported: D in {32, 64, 128},
- * dim a multiple of 8, Hq % Hkv == 0, B*T*dim and B*T*(Hq + 2 Hkv)*D below 2^31, eps
- * >= 0.  Pointers 16-byte aligned.  The first call for a new (device, T, D, theta)
- * builds its RoPE table and synchronises `stream` once (as the attention calls do). */
+ *   workspace: caller-owned device scratch of ne_qkv_prologue_workspace_size() bytes,
+ *              256-byte aligned; it receives W diag(gamma) (bf16) and is rewritten by
+ *              every call.
+ * Arithmetic: bf16 tensor-core products with fp32 accumulation; the gain is folded into
+ * the weights (W diag(gamma), rounded to bf16, formed on the device by each call), the
+ * root-mean-square is fp32.  Supported: D in {32, 64, 128}, dim a multiple of 8,
+ * Hq % Hkv == 0, B*T*dim and B*T*(Hq + 2 Hkv)*D below 2^31, eps >= 0.  Pointers 16-byte
+ * aligned.  The first call for a new (device, T, D, theta) builds its RoPE table and
+ * synchronises `stream` once (as the attention calls do). */
+size_t ne_qkv_prologue_workspace_size(int dim, int Hq, int Hkv, int D);
 ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void* q, void* k, void* v,
                           int B, int T, int dim, int Hq, int Hkv, int D, double eps,
-                          double rope_theta, int rotate, ne_stream_t stream);
+                          double rope_theta, int rotate, void* workspace, size_t workspace_bytes,
+                          ne_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* ne_status_string(ne_status s);

@@ -2,8 +2,9 @@
 against the fp64 oracle (oracle.qkv_prologue, pinned in test_oracle.py).
 
 Bound: relative Frobenius error <= 5e-3 per output (q, k, v), the bound of the bf16
-attention outputs: the products are bf16 with fp32 accumulation, x o gamma and the
-outputs are rounded to bf16 (about 2^-9 relative each).
+attention outputs: the products are bf16 with fp32 accumulation, W diag(gamma) (the
+gain folded into the weights) and the outputs are rounded to bf16 (about 2^-9 relative
+each).
 """
 import numpy as np
 import pytest
@@ -85,3 +86,20 @@ def test_output_feeds_the_attention_forward():
     q_r, k_r, v_r = oracle.qkv_prologue(f(x), f(gamma), f(w), Hq, Hkv, D, rotate=False)
     o_r, _ = oracle.attn_fwd(q_r, k_r, v_r)
     assert rel(f(o), o_r) <= 1e-2
+
+
+def test_workspace_is_rewritten_by_every_call():
+    """A workspace holding 0xFF bytes (NaN as bf16) and then another call's weights gives
+    the oracle's result: the call forms its own W diag(gamma) first."""
+    import oracle
+    B, T, dim, Hq, Hkv, D = 1, 200, 256, 4, 2, 64
+    n = int(ne.load().ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D))
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")
+    f = lambda t: t.double().cpu().numpy()
+    for seed in (8, 9):
+        x, gamma, w = synthetic.make_prologue(B, T, dim, Hq, Hkv, D, seed=seed)
+        q, k, v = ne.qkv_prologue(x.cuda(), gamma.cuda(), w.cuda(), Hq, Hkv, D, rotate=True, workspace=ws)
+        torch.cuda.synchronize()
+        q_r, k_r, v_r = oracle.qkv_prologue(f(x), f(gamma), f(w), Hq, Hkv, D, 1e-5, 10000.0, True)
+        for got, ref in ((q, q_r), (k, k_r), (v, v_r)):
+            assert rel(f(got), ref) <= TOL
