@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/neattn.h: argument validation, status
 // codes, per-device caches (RoPE tables, device error word), TMA tensor-map encoding
 // and kernel launches.  No compute happens here; every step runs in the kernels.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -37,7 +38,12 @@ ne_status cuda_fail(cudaError_t e, const char* what) {
 // ------------------------------------------------------------------ per-device state
 struct DeviceState {
     int* err_word = nullptr;                                           // device int
-    std::map<std::tuple<int, int, int, uint64_t>, float2*> rope;       // (T, D, pairs per row, theta bits)
+    // RoPE tables per (D, pairs per row, theta bits): rows and pointer.  A table serves
+    // every T up to its rows; a longer T builds one twice as long (or T's), and the
+    // shorter one is kept until ne_shutdown (a kernel in flight may still read it), so
+    // a caller whose T grows step by step costs at most twice the largest table.
+    std::map<std::tuple<int, int, uint64_t>, std::pair<int, float2*>> rope;
+    std::vector<float2*> rope_retired;
 };
 
 std::mutex g_mu;
@@ -87,14 +93,19 @@ ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const
     if (ld < D / 2) ld = D / 2;
     uint64_t tb;
     std::memcpy(&tb, &theta, sizeof(tb));
-    const auto key = std::make_tuple(T, D, ld, tb);
+    const auto key = std::make_tuple(D, ld, tb);
+    const int need = ne::rope_table_rows(T);
+    int rows = need;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto& m = g_dev[dev].rope;
         auto it = m.find(key);
         if (it != m.end()) {
-            *out = it->second;
-            return NE_OK;
+            if (it->second.first >= need) {
+                *out = it->second.second;
+                return NE_OK;
+            }
+            rows = std::max(need, 2 * it->second.first);   // geometric growth
         }
     }
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -104,7 +115,6 @@ ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const
                     "make one call before capturing",
                     T, D, theta);
     float2* buf = nullptr;
-    const int rows = ne::rope_table_rows(T);
     size_t bytes = (size_t)rows * ld * sizeof(float2);
     cudaError_t e = cudaMalloc(&buf, bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(rope table)");
@@ -117,11 +127,12 @@ ne_status rope_cache(int dev, int T, int D, double theta, cudaStream_t st, const
     std::lock_guard<std::mutex> lk(g_mu);
     auto& m = g_dev[dev].rope;
     auto it = m.find(key);
-    if (it != m.end()) {   // another thread won the race
+    if (it != m.end() && it->second.first >= need) {   // another thread won the race
         cudaFree(buf);
-        *out = it->second;
+        *out = it->second.second;
     } else {
-        m[key] = buf;
+        if (it != m.end()) g_dev[dev].rope_retired.push_back(it->second.second);
+        m[key] = std::make_pair(rows, buf);
         *out = buf;
     }
     return NE_OK;
@@ -827,7 +838,8 @@ void ne_shutdown(void) {
     for (auto& kv : g_dev) {
         cudaSetDevice(kv.first);
         if (kv.second.err_word) cudaFree(kv.second.err_word);
-        for (auto& r : kv.second.rope) cudaFree(r.second);
+        for (auto& r : kv.second.rope) cudaFree(r.second.second);
+        for (float2* p : kv.second.rope_retired) cudaFree(p);
     }
     g_dev.clear();
     cudaSetDevice(cur);

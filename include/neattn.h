@@ -32,14 +32,18 @@
  * B * T * max(Hq, 1) * D < 2^31.  Every tensor pointer must be 16-byte aligned.
  *
  * Ownership: the caller owns every tensor and the backward workspace.  The library
- * owns only small per-device caches (RoPE tables per (T, D, theta), one device error
- * word), created on first use and released by ne_shutdown().  All pointers are device
+ * owns only small per-device caches (RoPE tables per (D, theta), one device error
+ * word), created on first use and released by ne_shutdown().  A table serves every T up
+ * to its length; a call with a longer T builds one of twice the length (or T's), and the
+ * shorter table is kept until ne_shutdown() (kernels in flight may still read it), so a
+ * caller whose T grows step by step (a growing KV cache) holds at most about twice the
+ * largest table (T * D/2 * 8 bytes).  All pointers are device
  * pointers unless stated otherwise.
  *
  * Streams: every call enqueues its kernels on `stream` (NULL = legacy default stream)
- * and returns without synchronising, except that the first call for a new
- * (device, T, D, theta) builds its RoPE table and synchronises `stream` once; make
- * that first call before any stream capture.  Argument errors return before anything
+ * and returns without synchronising, except that a call that needs a new or longer RoPE
+ * table for its (device, D, theta) builds it and synchronises `stream` once; make such
+ * a call (the longest T) before any stream capture.  Argument errors return before anything
  * is enqueued.  Device-side failures (a bounded wait inside a kernel that ran out,
  * see ne_get_device_error) are reported asynchronously.
  *
@@ -253,8 +257,8 @@ ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* 
  * the weights (W diag(gamma), rounded to bf16, formed on the device by each call), the
  * root-mean-square is fp32.  Supported: D in {32, 64, 128}, dim a multiple of 8,
  * Hq % Hkv == 0, B*T*dim and B*T*(Hq + 2 Hkv)*D below 2^31, eps >= 0.  Pointers 16-byte
- * aligned.  The first call for a new (device, T, D, theta) builds its RoPE table and
- * synchronises `stream` once (as the attention calls do). */
+ * aligned.  A call that needs a new or longer RoPE table builds it and synchronises
+ * `stream` once (as the attention calls do). */
 size_t ne_qkv_prologue_workspace_size(int dim, int Hq, int Hkv, int D);
 ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void* q, void* k, void* v,
                           int B, int T, int dim, int Hq, int Hkv, int D, double eps,
