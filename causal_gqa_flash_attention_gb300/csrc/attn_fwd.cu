@@ -33,6 +33,7 @@
 // only after their epilogue has read the previous unit's O_u.
 // Every wait is bounded (WaitCtx); a CTA that gives up records an error code, drains
 // its own copies and MMAs, frees its TMEM and exits.
+#include <climits>
 #include <cuda_bf16.h>
 #include "kernels.h"
 #include "ptx.cuh"
@@ -496,25 +497,48 @@ __global__ void __launch_bounds__(480, 1)
             }
             umma_commit(smem_u32(&bar_s_full[u * 2 + (t_s & 1)]));
         };
-        // The waits S(t_s) needs: Q' of its unit (and of any unit skipped since the last
-        // one: every phase of the Q-ready barriers is waited for in order, so a parity
-        // never aliases) and its rotated K' tile.
-        auto s_waits = [&]() -> bool {
-            for (; sw.j == 0 && qr_next <= sw.k; ++qr_next)
+        // Waits, in unit order, for the rotated Q of units qr_next .. upto.  A unit where
+        // this subtile has no rows frees its Q buffer here (one of the buffer's two
+        // releases; its softmax warps take no part): then the buffer's next phase needs
+        // this issuer to have seen the current one, on every path, and neither this
+        // issuer's nor the RoPE warps' waits on the Q barriers can fall a phase behind
+        // (a run of units with no rows at all could otherwise cycle a buffer twice before
+        // they looked).
+        auto q_sync = [&](int upto) -> bool {
+            for (; qr_next <= upto; ++qr_next) {
+                const int U = fwd_unit_index(qr_next, a.n_units);
+                if (U < 0) break;
                 if (!mbar_wait_warp(smem_u32(&bar_q_ready[qr_next % C::NQB]), (qr_next / C::NQB) & 1, w, SITE_FWD_Q))
                     return false;
+                const FwdUnit f = fwd_unit<C::BM, C::BN, VL>(U, a);
+                if ((u == 0 ? f.n_u[0] : f.n_u[1]) == 0 && lane == 0)
+                    mbar_arrive(smem_u32(&bar_q_empty[qr_next % C::NQB]));
+                __syncwarp();
+            }
+            return true;
+        };
+        // The waits S(t_s) needs: Q' of its unit (and of every unit before it) and its
+        // rotated K' tile.
+        auto s_waits = [&]() -> bool {
+            if (sw.j == 0 && !q_sync(sw.k)) return false;
             return k_ready(sw.kvb + sw.j);
         };
         int t = 0, g = 0;                             // PV tiles issued; K/V tiles passed
-        // S runs at most two tiles ahead of PV.  With one Q buffer the next unit's Q can
-        // only land after this unit's epilogues, which wait for this unit's last PVs, so
-        // S of the next unit waits until the current unit's loop is done.  With two, the
-        // next unit's Q depends only on the unit before this one; its S may then wait
-        // inside the loop, where this issuer has released all but the last
-        // n_kv - n_u + 1 <= 3 stages of the unit, and NS >= 4 lets the next unit's first
-        // K/V tile load regardless.
-        auto may_issue = [&](int k_cur, int t_pv) {
-            return sw.k >= 0 && t_s < t_pv + 2 && (C::NQB == 2 || sw.k <= k_cur);
+        // S runs at most two tiles ahead of PV, and an S wait must never depend on this
+        // issuer's own later steps:
+        // - unit: the Q of unit k lands once the epilogues of unit k - NQB have read O,
+        //   which needs this issuer's PVs of that unit, so S stays within NQB - 1 units
+        //   of the PV walk (k_cur);
+        // - K/V tile: the tile g_s loads into the stage of tile g_s - NS, which this
+        //   issuer has released only below g_rel (the PV walk's tiles, including those
+        //   beyond its diagonal, which it releases without use), so g_s < g_rel + NS.
+        //   (The producer loads every Q after the K/V tiles of the unit before it, so
+        //   this bound also covers the Q load.)
+        // A subtile with no tiles in several units in a row (its rows past the sequence)
+        // would otherwise wait for the Q or K of a unit two or more ahead while still
+        // holding the stages of the units between.
+        auto may_issue = [&](int k_cur, int t_pv, int g_rel) {
+            return sw.k >= 0 && t_s < t_pv + 2 && sw.k <= k_cur + (C::NQB - 1) && sw.kvb + sw.j < g_rel + C::NS;
         };
         // The PV walk: every K/V tile g of every unit in order, tile jp of unit kp, of
         // which the first np are this subtile's (the rest lie beyond its diagonal).
@@ -530,14 +554,14 @@ __global__ void __launch_bounds__(480, 1)
             }
         };
         bool more = load_pv();
-        bool ok = true;
+        bool ok = q_sync(more ? kp : INT_MAX);
         // One loop: every issue decision of the role in one short body, so the warp's code
         // stays in the instruction cache beside the softmax and RoPE warps' code.  Every
         // K/V stage is released by both issuers, in order; a tile beyond the subtile's
         // diagonal is released without use, but only once the stage really holds it
         // (k_ready), so the release never runs a phase ahead.
         while (ok) {
-            if (may_issue(kp, t)) {                   // an S on its own (start, unit change)
+            if (may_issue(kp, t, g)) {                // an S on its own (start, unit change)
                 if (!(ok = s_waits())) break;
                 if (elect_one()) s_mmas();
                 __syncwarp();
@@ -553,7 +577,7 @@ __global__ void __launch_bounds__(480, 1)
                     break;
                 // The S this PV admits joins the batch if it needs no wait: its unit's Q'
                 // was waited for and its K' tile is already rotated (a test, not a wait).
-                bool fuse = may_issue(kp, t + 1) && !(sw.j == 0 && qr_next <= sw.k);
+                bool fuse = may_issue(kp, t + 1, g + 1) && !(sw.j == 0 && qr_next <= sw.k);
                 if (fuse) {
                     const int gs = sw.kvb + sw.j;
                     fuse = __all_sync(0xffffffffu, mbar_test(smem_u32(&bar_k_ready[gs % C::NS]), (gs / C::NS) & 1));
@@ -590,8 +614,10 @@ __global__ void __launch_bounds__(480, 1)
                 jp = 0;
                 ++kp;
                 more = load_pv();
+                if (!(ok = q_sync(more ? kp : INT_MAX))) break;
             }
         }
+        if (ok) q_sync(INT_MAX);
         umma_commit_e(smem_u32(&bar_final));
     } else if (warp == 3 || warp >= 12) {
         // ------------------------------------------------------------ RoPE on Q and K (+ V^T)
@@ -697,15 +723,7 @@ __global__ void __launch_bounds__(480, 1)
             }
             const int qb = k % C::NQB;
             if (n == 0) {                             // subtile at or past the sequence's length
-                // Its release of the Q buffer must count toward this unit's phase, so it
-                // waits until the unit's Q has landed (the buffer's previous phase is
-                // then complete).
-                bool rel = true;
-                if (r == 0) {
-                    rel = mbar_wait(smem_u32(&bar_q_full[qb]), (k / C::NQB) & 1, w, SITE_FWD_Q);
-                    if (rel) mbar_arrive(smem_u32(&bar_q_empty[qb]));
-                }
-                if (!(ok = __all_sync(0xffffffffu, rel))) break;
+                // (Its issuer frees the unit's Q buffer for it.)
                 // Padding rows inside T: O = 0 and LSE = -inf (a softmax over no keys).
                 const int qpos = qsub0 + r;
                 if (VL && qpos < T) {

@@ -54,7 +54,7 @@ def run_gpu(q, k, v, dO, theta=10000.0, bwd=True):
         dq, dk, dv = ne.attn_bwd(qd, kd, vd, o, lse, dOd, theta)
         out.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
-    assert ne.get_device_error() == ne.NE_OK
+    assert ne.get_device_error() == ne.NE_OK, ne.last_error()
     return {kk: f64(vv) for kk, vv in out.items()}
 
 
@@ -132,6 +132,20 @@ def test_bf16_deterministic_dk_dv():
         assert np.array_equal(a[name], b[name]), name
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,dtype", [
+    (8, 64, 64, 8, 64, torch.bfloat16),     # 512 one-tile units: S runs across several units
+    (4, 320, 48, 8, 64, torch.bfloat16),    # 384 units of 8 and 2 tiles, ragged second unit
+    (6, 100, 64, 16, 32, torch.bfloat16),   # head_dim 32 (run zero-padded to 64)
+    (8, 64, 64, 8, 64, torch.float32),
+])
+def test_many_units_per_cta(B, T, Hq, Hkv, D, dtype):
+    """More work units than 2.5 per SM: every CTA of the persistent forward crosses unit
+    boundaries several times (the small cases above give a CTA one unit at most), with
+    subtiles of one key tile, where the S issue runs furthest ahead of the PV issue."""
+    q, k, v, dO = synthetic.make_custom(B, T, Hq, Hkv, D, dtype, seed=B * 10 + T + D)
+    check(q, k, v, dO, "bf16" if dtype == torch.bfloat16 else "f32")
+
+
 # ---------------------------------------------------------------- f32 (TF32)
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,D", [
@@ -174,7 +188,7 @@ def test_other_rope_theta_matches_oracle(dtype):
 # ---------------------------------------------------------------- error paths
 
 def test_bounded_wait_times_out_and_reports():
-    assert ne.get_device_error() == ne.NE_OK
+    assert ne.get_device_error() == ne.NE_OK, ne.last_error()
     ne.selftest_wait_timeout(20)
     assert ne.get_device_error() == ne.NE_ERR_DEVICE_TIMEOUT
     assert "bounded wait" in ne.last_error()
@@ -193,7 +207,7 @@ def test_rotated_values_beyond_fp16_range_are_reported():
     ne.attn_fwd(qd, kd, vd)
     assert ne.get_device_error() == ne.NE_ERR_INVALID_ARG
     assert "fp16" in ne.last_error()
-    assert ne.get_device_error() == ne.NE_OK
+    assert ne.get_device_error() == ne.NE_OK, ne.last_error()
 
 
 def test_bad_arguments_raise():
@@ -234,7 +248,7 @@ def test_bf16_d32_does_not_write_past_its_rows():
     ne.attn_bwd(q, k, v, o2, lse, dO, dq=dq_buf[:B * T * Hq * D].view(B, T, Hq, D),
                 dk=dk_buf[:B * T * Hkv * D].view(B, T, Hkv, D), dv=dv_buf[:B * T * Hkv * D].view(B, T, Hkv, D))
     torch.cuda.synchronize()
-    assert ne.get_device_error() == ne.NE_OK
+    assert ne.get_device_error() == ne.NE_OK, ne.last_error()
     for buf, n in ((big, B * T * Hq * D), (dq_buf, B * T * Hq * D), (dk_buf, B * T * Hkv * D),
                    (dv_buf, B * T * Hkv * D)):
         assert torch.all(buf[n:] == canary)

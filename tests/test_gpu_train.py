@@ -75,6 +75,23 @@ def test_train_pair_matches_oracle(D, dtype, T):
         assert errs[n] <= tol["grad"], errs
 
 
+def test_train_pair_many_units_per_cta():
+    """384 units (8 and 2 key tiles): every CTA of the training forward stores R Q and
+    zeroes dQ' for several units in turn."""
+    import oracle
+    B, T, Hq, Hkv, D = 4, 320, 48, 8, 64
+    q, k, v, dO = synthetic.make_custom(B, T, Hq, Hkv, D, torch.bfloat16, seed=41)
+    o, lse, dq, dk, dv = train_pair(*(t.cuda() for t in (q, k, v, dO)))
+    qd, kd, vd, dOd = (f64(t) for t in (q, k, v, dO))
+    o_r, lse_r = oracle.attn_fwd(qd, kd, vd)
+    dq_r, dk_r, dv_r = oracle.attn_bwd(qd, kd, vd, dOd)
+    tol = TOL[torch.bfloat16]
+    assert rel(f64(o), o_r) <= tol["o"]
+    assert float(np.max(np.abs(f64(lse) - lse_r))) <= tol["lse"]
+    for a, b in ((dq, dq_r), (dk, dk_r), (dv, dv_r)):
+        assert rel(f64(a), b) <= tol["grad"]
+
+
 def test_train_pair_equals_regular_pair_at_the_gpu_pipeline_shape():
     w = synthetic.WORKLOADS[2]
     q, k, v, dO = (t.cuda() for t in synthetic.make_inputs(w, layer=0))

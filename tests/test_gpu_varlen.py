@@ -97,6 +97,14 @@ def test_varlen_bf16_d64_gpu_pipeline_heads_with_empty_sequence():
     check_varlen(4, 384, 12, 4, 64, torch.bfloat16, [0, 383, 64, 256])
 
 
+def test_varlen_bf16_d64_many_units_per_cta():
+    """Sixteen sequences of mixed lengths over 48 heads: 576 units, several per CTA,
+    among them empty subtiles and one-tile subtiles, so the persistent forward's S issue
+    crosses unit boundaries ahead of its PV issue many times."""
+    lens = [1, 64, 65, 300, 320, 0, 129, 200, 17, 256, 257, 320, 64, 90, 310, 2]
+    check_varlen(16, 320, 48, 8, 64, torch.bfloat16, lens)
+
+
 def test_varlen_bf16_d128():
     check_varlen(4, 256, 8, 2, 128, torch.bfloat16, [1, 77, 200, 256])
 
