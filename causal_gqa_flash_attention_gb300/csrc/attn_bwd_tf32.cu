@@ -44,10 +44,14 @@ struct BwdTf32Cfg {
 // swizzled layout (both K-major, 32 elements per 128-byte chunk); 128 threads.
 template <int D, int ROWS>
 __device__ __forceinline__ void transpose_f32(const uint8_t* src, uint8_t* dst, int t) {
-    constexpr int UNITS = D * ROWS / 4, UPR = ROWS / 4;
+    constexpr int UNITS = D * ROWS / 4;
+    // A warp takes 32 consecutive columns d of the same four rows: conflict-free reads
+    // (one row, every bank once under the 128-byte swizzle) and writes (eight rows d per
+    // quarter-warp at swizzle-spread chunk positions).  Rows fastest put a warp's reads
+    // on two or four banks.
 #pragma unroll 4
     for (int ul = t; ul < UNITS; ul += 128) {
-        const int d = ul / UPR, r0 = 4 * (ul % UPR);
+        const int d = ul % D, r0 = 4 * (ul / D);
         uint32_t w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)

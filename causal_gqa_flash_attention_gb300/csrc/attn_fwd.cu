@@ -104,10 +104,13 @@ __device__ __forceinline__ void zero_rows(uint8_t* base, int zero_row, int t) {
 template <int D, int ROWS, int NT>
 __device__ __forceinline__ void transpose_v_tf32(const uint8_t* src, uint8_t* dst, int t, int zero_row) {
     constexpr int UNITS = D * ROWS / 4;       // 16-byte units of the transposed tile
-    constexpr int UPR = ROWS / 4;             // units per transposed row
+    // A warp takes 32 consecutive columns d of the same four keys: its reads of one key
+    // row cover eight 16-byte chunks x four words (every bank once in the 128-byte
+    // swizzle) and its 16-byte writes go to eight rows d per quarter-warp, whose chunk
+    // positions the swizzle spreads.  (Keys fastest put a warp's reads on two banks.)
 #pragma unroll 4
     for (int ul = t; ul < UNITS; ul += NT) {
-        const int d = ul / UPR, u = ul % UPR;  // transposed row d, keys 4u .. 4u+3
+        const int d = ul % D, u = ul / D;      // transposed row d, keys 4u .. 4u+3
         const int r0 = 4 * u;
         uint32_t w[4];
 #pragma unroll
