@@ -16,8 +16,13 @@
 // Warp roles (384 threads): warp 0 TMA; warp 1 TMEM allocator and UMMA issuer (all
 // products, in order, so every TMEM and smem reuse is ordered by the one issuer);
 // warps 4-7 RoPE, TF32 rounding and transposes, then the dQ drain; warps 8-11 P^T, dS^T
-// and dS (thread = key row) and the dK/dV epilogue.  One Q/dO stage: TF32 is the
-// precision path, not the throughput path.
+// and dS (thread = key row) and the dK/dV epilogue.
+// Two Q' | dO stages (one for Q'^T | dO^T): step it's tiles load into stage it % 2 as
+// soon as the S^T / dP^T products of step it - 2 have read it, and are rotated and
+// rounded in place while step it - 1 runs; only the transposes wait, for the dK product
+// of step it - 1 (the last reader of Q'^T and dO^T).  With one stage, each step began
+// with the load, rotation and transposes of its tiles after every product of the step
+// before had completed.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "rope_smem.cuh"
@@ -33,8 +38,9 @@ struct BwdTf32Cfg {
     static constexpr int NCH = ROWB / 128;            // 128-byte chunks per row
     static constexpr int KV_BYTES = BKV * ROWB;       // K', V, K'^T
     static constexpr int Q_BYTES = BQ * ROWB;         // Q', Q'^T, dO, dO^T
+    static constexpr int STAGE_BYTES = 2 * Q_BYTES;   // one Q' | dO stage (two stages)
     static constexpr int DS_BYTES = BQ * BKV * 4;     // dS [query][key]
-    static constexpr int SMEM = 1024 + 3 * KV_BYTES + 4 * Q_BYTES + DS_BYTES;
+    static constexpr int SMEM = 1024 + 3 * KV_BYTES + 2 * STAGE_BYTES + 2 * Q_BYTES + DS_BYTES;
     static constexpr int S_COL = 0, DP_COL = 64, DV_COL = 128, DK_COL = 128 + D, DQ_COL = 128 + 2 * D;
     static constexpr int TMEM_COLS = 128 + 3 * D <= 256 ? 256 : 512;
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -89,14 +95,16 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* sK = smem;                       // K' [128][D]
     uint8_t* sKT = sK + C::KV_BYTES;          // K'^T [D][128]
     uint8_t* sV = sKT + C::KV_BYTES;          // V [128][D]
-    uint8_t* sQ = sV + C::KV_BYTES;           // Q' [64][D]
-    uint8_t* sQT = sQ + C::Q_BYTES;           // Q'^T [D][64]
-    uint8_t* sO = sQT + C::Q_BYTES;           // dO [64][D]
-    uint8_t* sOT = sO + C::Q_BYTES;           // dO^T [D][64]
+    uint8_t* sStage = sV + C::KV_BYTES;       // stage s: Q' [64][D] | dO [64][D]
+    uint8_t* sQT = sStage + 2 * C::STAGE_BYTES;   // Q'^T [D][64]
+    uint8_t* sOT = sQT + C::Q_BYTES;          // dO^T [D][64]
     uint8_t* sdS = sOT + C::Q_BYTES;          // dS [64][128]
+    auto stage_q = [&](int it) { return sStage + (it & 1) * C::STAGE_BYTES; };
+    auto stage_o = [&](int it) { return sStage + (it & 1) * C::STAGE_BYTES + C::Q_BYTES; };
 
-    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_qdo_full, bar_q_ready, bar_qdo_empty, bar_s_full,
-        bar_ds_ready, bar_dq_full, bar_dq_free, bar_dkv_full, bar_final, bar_aux;
+    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_q_ready, bar_qt_free, bar_s_full, bar_ds_ready,
+        bar_dq_full, bar_dq_free, bar_dkv_full, bar_final, bar_aux;
+    __shared__ __align__(8) uint64_t bar_stage_full[2], bar_stage_free[2];
     __shared__ __align__(8) uint64_t bar_rows[2];
     __shared__ __align__(16) float s_lse[2][C::BQ];
     __shared__ __align__(16) float s_delta[2][C::BQ];
@@ -120,9 +128,12 @@ __global__ void __launch_bounds__(384, 1)
     if (tid == 0) {
         mbar_init(smem_u32(&bar_kv_full), 1);
         mbar_init(smem_u32(&bar_k_ready), 128);
-        mbar_init(smem_u32(&bar_qdo_full), 1);
+        mbar_init(smem_u32(&bar_stage_full[0]), 1);
+        mbar_init(smem_u32(&bar_stage_full[1]), 1);
+        mbar_init(smem_u32(&bar_stage_free[0]), 1);
+        mbar_init(smem_u32(&bar_stage_free[1]), 1);
         mbar_init(smem_u32(&bar_q_ready), 128);
-        mbar_init(smem_u32(&bar_qdo_empty), 1);
+        mbar_init(smem_u32(&bar_qt_free), 1);
         mbar_init(smem_u32(&bar_s_full), 1);
         mbar_init(smem_u32(&bar_ds_ready), 128);
         mbar_init(smem_u32(&bar_dq_full), 1);
@@ -165,17 +176,23 @@ __global__ void __launch_bounds__(384, 1)
             }
             int issued = 0;
             for (int it = 0; it < n_it; ++it) {
-                if (it > 0 && !mbar_wait(smem_u32(&bar_qdo_empty), (it - 1) & 1, w, SITE_BWD_QDO_EMPTY)) break;
-                const uint32_t f = smem_u32(&bar_qdo_full);
+                // Stage it % 2 is free once the S^T and dP^T products of step it - 2 read it.
+                if (it >= 2 && !mbar_wait(smem_u32(&bar_stage_free[it & 1]), ((it >> 1) - 1) & 1, w,
+                                          SITE_BWD_QDO_EMPTY))
+                    break;
+                const uint32_t f = smem_u32(&bar_stage_full[it & 1]);
                 mbar_arrive_expect_tx(f, 2 * C::Q_BYTES);
                 for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_4d(smem_u32(sQ + c * C::BQ * 128), &tm_q, f, c * 32, step_h(it), step_q0(it), b);
-                    tma_load_4d(smem_u32(sO + c * C::BQ * 128), &tm_do, f, c * 32, step_h(it), step_q0(it), b);
+                    tma_load_4d(smem_u32(stage_q(it) + c * C::BQ * 128), &tm_q, f, c * 32, step_h(it), step_q0(it), b);
+                    tma_load_4d(smem_u32(stage_o(it) + c * C::BQ * 128), &tm_do, f, c * 32, step_h(it), step_q0(it), b);
                 }
                 ++issued;
             }
             mbar_wait_drain(kvf, 0, w, SITE_BWD_DRAIN);
-            if (issued > 0) mbar_wait_drain(smem_u32(&bar_qdo_full), (issued - 1) & 1, w, SITE_BWD_DRAIN);
+            // The last load of each stage has landed (earlier ones were waited for by the
+            // RoPE warps before the stage was reused).
+            for (int it = issued - 2 > 0 ? issued - 2 : 0; it < issued; ++it)
+                mbar_wait_drain(smem_u32(&bar_stage_full[it & 1]), (it >> 1) & 1, w, SITE_BWD_DRAIN);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ UMMA issuer (all products)
@@ -184,8 +201,8 @@ __global__ void __launch_bounds__(384, 1)
             constexpr uint32_t id_vk = idesc_make(FMT_TF32, 128, D, false, false);       // dV, dK
             constexpr uint32_t id_q = idesc_make(FMT_TF32, 64, D, false, false);         // dQ (M = 64)
             const uint64_t dK = sdesc(smem_u32(sK), 16, 1024), dKT = sdesc(smem_u32(sKT), 16, 1024);
-            const uint64_t dV = sdesc(smem_u32(sV), 16, 1024), dQ = sdesc(smem_u32(sQ), 16, 1024);
-            const uint64_t dQT = sdesc(smem_u32(sQT), 16, 1024), dO = sdesc(smem_u32(sO), 16, 1024);
+            const uint64_t dV = sdesc(smem_u32(sV), 16, 1024), dQ0 = sdesc(smem_u32(stage_q(0)), 16, 1024);
+            const uint64_t dQT = sdesc(smem_u32(sQT), 16, 1024), dO0 = sdesc(smem_u32(stage_o(0)), 16, 1024);
             const uint64_t dOT = sdesc(smem_u32(sOT), 16, 1024), dS = sdesc(smem_u32(sdS), 16, 1024);
             // K-step ks covers 8 fp32 = 32 bytes of the K dimension: chunk ks/4, offset (ks%4)*32.
             auto koff = [](int ks, int rows) { return (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32); };
@@ -193,6 +210,8 @@ __global__ void __launch_bounds__(384, 1)
             for (int it = 0; ok && it < n_it; ++it) {
                 if (!(ok = mbar_wait(smem_u32(&bar_q_ready), it & 1, w, SITE_BWD_Q_READY))) break;
                 tc_fence_after();
+                const uint64_t dQ = sdesc_add(dQ0, (it & 1) * C::STAGE_BYTES);
+                const uint64_t dO = sdesc_add(dO0, (it & 1) * C::STAGE_BYTES);
 #pragma unroll
                 for (int ks = 0; ks < D / 8; ++ks)
                     umma_ss<true>(tm + C::S_COL, sdesc_add(dK, koff(ks, C::BKV)), sdesc_add(dQ, koff(ks, C::BQ)), id_sp,
@@ -202,6 +221,7 @@ __global__ void __launch_bounds__(384, 1)
                     umma_ss<true>(tm + C::DP_COL, sdesc_add(dV, koff(ks, C::BKV)), sdesc_add(dO, koff(ks, C::BQ)), id_sp,
                                   ks > 0);
                 umma_commit(smem_u32(&bar_s_full));
+                umma_commit(smem_u32(&bar_stage_free[it & 1]));
                 if (!(ok = mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
                 tc_fence_after();
 #pragma unroll
@@ -212,6 +232,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int ks = 0; ks < C::BQ / 8; ++ks)       // dK' += dS^T Q'
                     umma_ts<true>(tm + C::DK_COL, tm + C::DP_COL + ks * 8, sdesc_add(dQT, koff(ks, D)), id_vk,
                                   (it > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&bar_qt_free));        // Q'^T and dO^T are read
                 if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
                 tc_fence_after();
 #pragma unroll
@@ -219,7 +240,6 @@ __global__ void __launch_bounds__(384, 1)
                     umma_ss<true>(tm + C::DQ_COL, sdesc_add(dS, koff(ks, C::BQ)), sdesc_add(dKT, koff(ks, D)), id_q,
                                   ks > 0);
                 umma_commit(smem_u32(&bar_dq_full));
-                umma_commit(smem_u32(&bar_qdo_empty));
             }
             umma_commit(smem_u32(&bar_dkv_full));
             umma_commit(smem_u32(&bar_final));
@@ -266,13 +286,17 @@ __global__ void __launch_bounds__(384, 1)
         }
         for (int it = 0; ok && it <= n_it; ++it) {
             if (it < n_it) {
-                if (!(ok = mbar_wait_warp(smem_u32(&bar_qdo_full), it & 1, w, SITE_BWD_QDO_FULL))) break;
-                rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(sQ, nullptr, step_q0(it), T, r, a.rope,
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_stage_full[it & 1]), (it >> 1) & 1, w, SITE_BWD_QDO_FULL)))
+                    break;
+                rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(stage_q(it), nullptr, step_q0(it), T, r, a.rope,
                                                          VL ? len : step_q0(it) + C::BQ);
-                round_tf32<C::Q_BYTES>(sO, r);
+                round_tf32<C::Q_BYTES>(stage_o(it), r);
                 if (!(ok = group_sync())) break;
-                transpose_f32<D, C::BQ>(sQ, sQT, r);
-                transpose_f32<D, C::BQ>(sO, sOT, r);
+                // Q'^T and dO^T of step it - 1 have been read by its dV and dK products.
+                if (it > 0 && !(ok = mbar_wait_warp(smem_u32(&bar_qt_free), (it - 1) & 1, w, SITE_BWD_Q_READY)))
+                    break;
+                transpose_f32<D, C::BQ>(stage_q(it), sQT, r);
+                transpose_f32<D, C::BQ>(stage_o(it), sOT, r);
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&bar_q_ready));
             }
