@@ -7,8 +7,9 @@
 // over the G query heads and every 64-query tile at or after the diagonal:
 //   S^T  = K' Q'^T           M=128 keys, N=64 queries     A = K', B = Q'
 //   dP^T = V dO^T            M=128, N=64                  A = V,  B = dO
-//   P^T, dS^T (fp32, TF32-rounded) written back to TMEM over S^T and dP^T; dS also to
-//   shared memory as [query][key] (the K-major A of the dQ product)
+//   P^T, dS^T (fp32, TF32-rounded) written back to TMEM over S^T and dP^T (two TMEM
+//   buffers, by step parity); dS also to shared memory as [query][key] (the K-major A
+//   of the dQ product)
 //   dV  += P^T dO            A = P^T (TMEM), B = dO^T     (dO transposed in smem)
 //   dK' += dS^T Q'           A = dS^T (TMEM), B = Q'^T    (Q' transposed in smem)
 //   dQ'_part = dS K'         M=64 queries, N=D, K=128 keys; A = dS, B = K'^T
@@ -17,12 +18,17 @@
 // products, in order, so every TMEM and smem reuse is ordered by the one issuer);
 // warps 4-7 RoPE, TF32 rounding and transposes, then the dQ drain; warps 8-11 P^T, dS^T
 // and dS (thread = key row) and the dK/dV epilogue.
-// Two Q' | dO stages (one for Q'^T | dO^T): step it's tiles load into stage it % 2 as
-// soon as the S^T / dP^T products of step it - 2 have read it, and are rotated and
-// rounded in place while step it - 1 runs; only the transposes wait, for the dK product
-// of step it - 1 (the last reader of Q'^T and dO^T).  With one stage, each step began
-// with the load, rotation and transposes of its tiles after every product of the step
-// before had completed.
+// Two Q' | dO stages (one for Q'^T | dO^T) and two S^T | dP^T buffers in TMEM: step
+// it's tiles load into stage it % 2 once step it - 2 is done with it and are rotated and
+// rounded in place while step it - 1 runs; S^T and dP^T of step it + 1 (whose operands
+// need no transpose) are issued as soon as its tiles are rotated, before the dV, dK and
+// dQ products of step it, so the gradient warps go from one step to the next without
+// waiting for those.  The transposes wait only for the dK product of the step before
+// (the last reader of Q'^T and dO^T), and the gradient warps write dS to shared memory
+// only after the previous step's dQ product has read it.  (With one stage and one
+// buffer, each step began with the load, rotation and transposes of its tiles after
+// every product of the step before had completed: 273 us against 221.5 with two
+// stages at B16 T512.)
 #include "kernels.h"
 #include "ptx.cuh"
 #include "rope_smem.cuh"
@@ -41,8 +47,12 @@ struct BwdTf32Cfg {
     static constexpr int STAGE_BYTES = 2 * Q_BYTES;   // one Q' | dO stage (two stages)
     static constexpr int DS_BYTES = BQ * BKV * 4;     // dS [query][key]
     static constexpr int SMEM = 1024 + 3 * KV_BYTES + 2 * STAGE_BYTES + 2 * Q_BYTES + DS_BYTES;
-    static constexpr int S_COL = 0, DP_COL = 64, DV_COL = 128, DK_COL = 128 + D, DQ_COL = 128 + 2 * D;
-    static constexpr int TMEM_COLS = 128 + 3 * D <= 256 ? 256 : 512;
+    // S^T / P^T of buffer b at 128 b, dP^T / dS^T at 128 b + 64; dV, dK', dQ' after both.
+    static constexpr int DV_COL = 256, DK_COL = 256 + D, DQ_COL = 256 + 2 * D;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(DQ_COL + D <= TMEM_COLS, "TMEM columns");
+    static __device__ __forceinline__ uint32_t s_col(int it) { return (uint32_t)((it & 1) * 128); }
+    static __device__ __forceinline__ uint32_t dp_col(int it) { return (uint32_t)((it & 1) * 128 + 64); }
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -102,9 +112,9 @@ __global__ void __launch_bounds__(384, 1)
     auto stage_q = [&](int it) { return sStage + (it & 1) * C::STAGE_BYTES; };
     auto stage_o = [&](int it) { return sStage + (it & 1) * C::STAGE_BYTES + C::Q_BYTES; };
 
-    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_q_ready, bar_qt_free, bar_s_full, bar_ds_ready,
+    __shared__ __align__(8) uint64_t bar_kv_full, bar_k_ready, bar_q_rot, bar_q_ready, bar_qt_free, bar_ds_ready,
         bar_dq_full, bar_dq_free, bar_dkv_full, bar_final, bar_aux;
-    __shared__ __align__(8) uint64_t bar_stage_full[2], bar_stage_free[2];
+    __shared__ __align__(8) uint64_t bar_stage_full[2], bar_stage_free[2], bar_s_full[2];
     __shared__ __align__(8) uint64_t bar_rows[2];
     __shared__ __align__(16) float s_lse[2][C::BQ];
     __shared__ __align__(16) float s_delta[2][C::BQ];
@@ -130,11 +140,15 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(smem_u32(&bar_k_ready), 128);
         mbar_init(smem_u32(&bar_stage_full[0]), 1);
         mbar_init(smem_u32(&bar_stage_full[1]), 1);
-        mbar_init(smem_u32(&bar_stage_free[0]), 1);
-        mbar_init(smem_u32(&bar_stage_free[1]), 1);
+        // A stage is free once the S^T and dP^T products (a commit) and the transposes
+        // (the 128 RoPE threads) have read it.
+        mbar_init(smem_u32(&bar_stage_free[0]), 129);
+        mbar_init(smem_u32(&bar_stage_free[1]), 129);
+        mbar_init(smem_u32(&bar_q_rot), 128);
         mbar_init(smem_u32(&bar_q_ready), 128);
         mbar_init(smem_u32(&bar_qt_free), 1);
-        mbar_init(smem_u32(&bar_s_full), 1);
+        mbar_init(smem_u32(&bar_s_full[0]), 1);
+        mbar_init(smem_u32(&bar_s_full[1]), 1);
         mbar_init(smem_u32(&bar_ds_ready), 128);
         mbar_init(smem_u32(&bar_dq_full), 1);
         mbar_init(smem_u32(&bar_dq_free), 128);
@@ -176,7 +190,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             int issued = 0;
             for (int it = 0; it < n_it; ++it) {
-                // Stage it % 2 is free once the S^T and dP^T products of step it - 2 read it.
+                // Stage it % 2 is free once step it - 2 has read it.
                 if (it >= 2 && !mbar_wait(smem_u32(&bar_stage_free[it & 1]), ((it >> 1) - 1) & 1, w,
                                           SITE_BWD_QDO_EMPTY))
                     break;
@@ -206,31 +220,39 @@ __global__ void __launch_bounds__(384, 1)
             const uint64_t dOT = sdesc(smem_u32(sOT), 16, 1024), dS = sdesc(smem_u32(sdS), 16, 1024);
             // K-step ks covers 8 fp32 = 32 bytes of the K dimension: chunk ks/4, offset (ks%4)*32.
             auto koff = [](int ks, int rows) { return (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32); };
-            bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV);
-            for (int it = 0; ok && it < n_it; ++it) {
-                if (!(ok = mbar_wait(smem_u32(&bar_q_ready), it & 1, w, SITE_BWD_Q_READY))) break;
+            // S^T and dP^T of step it into TMEM buffer it % 2, once its Q' and dO are
+            // rotated and rounded (their buffer's previous products, dV and dK of step
+            // it - 2, were issued earlier by this thread and run first).
+            auto sdp = [&](int it) -> bool {
+                if (!mbar_wait(smem_u32(&bar_q_rot), it & 1, w, SITE_BWD_Q_READY)) return false;
                 tc_fence_after();
                 const uint64_t dQ = sdesc_add(dQ0, (it & 1) * C::STAGE_BYTES);
                 const uint64_t dO = sdesc_add(dO0, (it & 1) * C::STAGE_BYTES);
 #pragma unroll
                 for (int ks = 0; ks < D / 8; ++ks)
-                    umma_ss<true>(tm + C::S_COL, sdesc_add(dK, koff(ks, C::BKV)), sdesc_add(dQ, koff(ks, C::BQ)), id_sp,
-                                  ks > 0);
+                    umma_ss<true>(tm + C::s_col(it), sdesc_add(dK, koff(ks, C::BKV)), sdesc_add(dQ, koff(ks, C::BQ)),
+                                  id_sp, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < D / 8; ++ks)
-                    umma_ss<true>(tm + C::DP_COL, sdesc_add(dV, koff(ks, C::BKV)), sdesc_add(dO, koff(ks, C::BQ)), id_sp,
-                                  ks > 0);
-                umma_commit(smem_u32(&bar_s_full));
+                    umma_ss<true>(tm + C::dp_col(it), sdesc_add(dV, koff(ks, C::BKV)), sdesc_add(dO, koff(ks, C::BQ)),
+                                  id_sp, ks > 0);
+                umma_commit(smem_u32(&bar_s_full[it & 1]));
                 umma_commit(smem_u32(&bar_stage_free[it & 1]));
+                return true;
+            };
+            bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV) && (n_it == 0 || sdp(0));
+            for (int it = 0; ok && it < n_it; ++it) {
+                if (it + 1 < n_it && !(ok = sdp(it + 1))) break;
                 if (!(ok = mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
+                if (!(ok = mbar_wait(smem_u32(&bar_q_ready), it & 1, w, SITE_BWD_Q_READY))) break;   // transposes
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < C::BQ / 8; ++ks)       // dV += P^T dO, K = queries
-                    umma_ts<true>(tm + C::DV_COL, tm + C::S_COL + ks * 8, sdesc_add(dOT, koff(ks, D)), id_vk,
+                    umma_ts<true>(tm + C::DV_COL, tm + C::s_col(it) + ks * 8, sdesc_add(dOT, koff(ks, D)), id_vk,
                                   (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < C::BQ / 8; ++ks)       // dK' += dS^T Q'
-                    umma_ts<true>(tm + C::DK_COL, tm + C::DP_COL + ks * 8, sdesc_add(dQT, koff(ks, D)), id_vk,
+                    umma_ts<true>(tm + C::DK_COL, tm + C::dp_col(it) + ks * 8, sdesc_add(dQT, koff(ks, D)), id_vk,
                                   (it > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(smem_u32(&bar_qt_free));        // Q'^T and dO^T are read
                 if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
@@ -284,24 +306,31 @@ __global__ void __launch_bounds__(384, 1)
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready));
         }
-        for (int it = 0; ok && it <= n_it; ++it) {
-            if (it < n_it) {
-                if (!(ok = mbar_wait_warp(smem_u32(&bar_stage_full[it & 1]), (it >> 1) & 1, w, SITE_BWD_QDO_FULL)))
-                    break;
-                rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(stage_q(it), nullptr, step_q0(it), T, r, a.rope,
-                                                         VL ? len : step_q0(it) + C::BQ);
-                round_tf32<C::Q_BYTES>(stage_o(it), r);
-                if (!(ok = group_sync())) break;
-                // Q'^T and dO^T of step it - 1 have been read by its dV and dK products.
-                if (it > 0 && !(ok = mbar_wait_warp(smem_u32(&bar_qt_free), (it - 1) & 1, w, SITE_BWD_Q_READY)))
-                    break;
-                transpose_f32<D, C::BQ>(stage_q(it), sQT, r);
-                transpose_f32<D, C::BQ>(stage_o(it), sOT, r);
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&bar_q_ready));
-            }
+        // Rotation and rounding of step it's tiles in place; the q_rot barrier (every
+        // thread of the group) also orders them before the transposes.
+        auto rotate = [&](int it) -> bool {
+            if (!mbar_wait_warp(smem_u32(&bar_stage_full[it & 1]), (it >> 1) & 1, w, SITE_BWD_QDO_FULL)) return false;
+            rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(stage_q(it), nullptr, step_q0(it), T, r, a.rope,
+                                                     VL ? len : step_q0(it) + C::BQ);
+            round_tf32<C::Q_BYTES>(stage_o(it), r);
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_q_rot));
+            return true;
+        };
+        if (ok && n_it > 0) ok = rotate(0);
+        for (int it = 0; ok && it < n_it; ++it) {
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_q_rot), it & 1, w, SITE_BWD_Q_READY))) break;
+            // Q'^T and dO^T of step it - 1 have been read by its dV and dK products.
+            if (it > 0 && !(ok = mbar_wait_warp(smem_u32(&bar_qt_free), (it - 1) & 1, w, SITE_BWD_Q_READY))) break;
+            transpose_f32<D, C::BQ>(stage_q(it), sQT, r);
+            transpose_f32<D, C::BQ>(stage_o(it), sOT, r);
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_q_ready));
+            mbar_arrive(smem_u32(&bar_stage_free[it & 1]));
+            if (it + 1 < n_it && !(ok = rotate(it + 1))) break;
             if (it > 0 && !(ok = drain(it - 1))) break;
         }
+        if (ok && n_it > 0) drain(n_it - 1);
     } else if (warp >= 8) {
         // ------------------------------------------------------------ P^T, dS^T, dS; dK, dV epilogue
         const int r = tid - 256;                       // key row = TMEM lane
@@ -333,11 +362,11 @@ __global__ void __launch_bounds__(384, 1)
             if (!mbar_wait_warp(smem_u32(&bar_rows[sb]), (it >> 1) & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
             float lv_n = 0.f, dv_n = 0.f;
             if (it + 1 < n_it && r < C::BQ) row_vals(it + 1, lv_n, dv_n);
-            if (!mbar_wait_warp(smem_u32(&bar_s_full), it & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
+            if (!mbar_wait_warp(smem_u32(&bar_s_full[it & 1]), (it >> 1) & 1, w, SITE_BWD_S_FULL)) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[64], dr[64];
-            tmem_ld_cols<2>(lt + C::S_COL, sr);
-            tmem_ld_cols<2>(lt + C::DP_COL, dr);
+            tmem_ld_cols<2>(lt + C::s_col(it), sr);
+            tmem_ld_cols<2>(lt + C::dp_col(it), dr);
             const bool diag = kv0 + C::BKV - 1 > q0;
             const bool tail = VL && q0 + C::BQ > len;          // queries past the length are padding
 #pragma unroll
@@ -347,14 +376,17 @@ __global__ void __launch_bounds__(384, 1)
                 const float g = p * (__uint_as_float(dr[c]) - s_delta[sb][c]);
                 sr[c] = f32_to_tf32_rna(p);
                 dr[c] = f32_to_tf32_rna(g);
-                // dS [query c][key r]: key chunk r/32, 4-byte element (r%32) of row c
+            }
+            tmem_st32(lt + C::s_col(it), *reinterpret_cast<uint32_t(*)[32]>(sr));
+            tmem_st32(lt + C::s_col(it) + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            tmem_st32(lt + C::dp_col(it), *reinterpret_cast<uint32_t(*)[32]>(dr));
+            tmem_st32(lt + C::dp_col(it) + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+            // dS to shared memory once the dQ product of step it - 1 has read the buffer.
+            if (it > 0 && !mbar_wait_warp(smem_u32(&bar_dq_full), (it - 1) & 1, w, SITE_BWD_DQ_FULL)) { ok = false; break; }
+#pragma unroll
+            for (int c = 0; c < 64; ++c)   // dS [query c][key r]: key chunk r/32, 4-byte element (r%32) of row c
                 *reinterpret_cast<uint32_t*>(sdS + (r >> 5) * C::BQ * 128 + sw128_offset(c, (r & 31) >> 2) + (r & 3) * 4) =
                     dr[c];
-            }
-            tmem_st32(lt + C::S_COL, *reinterpret_cast<uint32_t(*)[32]>(sr));
-            tmem_st32(lt + C::S_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-            tmem_st32(lt + C::DP_COL, *reinterpret_cast<uint32_t(*)[32]>(dr));
-            tmem_st32(lt + C::DP_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
             fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
