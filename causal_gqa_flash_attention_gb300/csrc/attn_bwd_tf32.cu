@@ -210,7 +210,10 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ UMMA issuer (all products)
-        if (lane == 0) {
+        // The whole warp runs the loop and its waits, so the UMMA operands stay
+        // warp-uniform, and one elected lane issues each batch with its commits (a loop
+        // run by lane 0 alone cost several instructions per UMMA, 48 UMMAs a step).
+        {
             constexpr uint32_t id_sp = idesc_make(FMT_TF32, 128, C::BQ, false, false);   // S^T, dP^T
             constexpr uint32_t id_vk = idesc_make(FMT_TF32, 128, D, false, false);       // dV, dK
             constexpr uint32_t id_q = idesc_make(FMT_TF32, 64, D, false, false);         // dQ (M = 64)
@@ -222,49 +225,61 @@ __global__ void __launch_bounds__(384, 1)
             auto koff = [](int ks, int rows) { return (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32); };
             // S^T and dP^T of step it into TMEM buffer it % 2, once its Q' and dO are
             // rotated and rounded (their buffer's previous products, dV and dK of step
-            // it - 2, were issued earlier by this thread and run first).
+            // it - 2, were issued earlier by this warp and run first).
             auto sdp = [&](int it) -> bool {
-                if (!mbar_wait(smem_u32(&bar_q_rot), it & 1, w, SITE_BWD_Q_READY)) return false;
+                if (!mbar_wait_warp(smem_u32(&bar_q_rot), it & 1, w, SITE_BWD_Q_READY)) return false;
                 tc_fence_after();
                 const uint64_t dQ = sdesc_add(dQ0, (it & 1) * C::STAGE_BYTES);
                 const uint64_t dO = sdesc_add(dO0, (it & 1) * C::STAGE_BYTES);
+                const uint32_t sc = tm + C::s_col(it), dc = tm + C::dp_col(it);
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    umma_ss<true>(tm + C::s_col(it), sdesc_add(dK, koff(ks, C::BKV)), sdesc_add(dQ, koff(ks, C::BQ)),
-                                  id_sp, ks > 0);
+                    for (int ks = 0; ks < D / 8; ++ks)
+                        umma_ss<true>(sc, sdesc_add(dK, koff(ks, C::BKV)), sdesc_add(dQ, koff(ks, C::BQ)), id_sp, ks > 0);
 #pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    umma_ss<true>(tm + C::dp_col(it), sdesc_add(dV, koff(ks, C::BKV)), sdesc_add(dO, koff(ks, C::BQ)),
-                                  id_sp, ks > 0);
-                umma_commit(smem_u32(&bar_s_full[it & 1]));
-                umma_commit(smem_u32(&bar_stage_free[it & 1]));
+                    for (int ks = 0; ks < D / 8; ++ks)
+                        umma_ss<true>(dc, sdesc_add(dV, koff(ks, C::BKV)), sdesc_add(dO, koff(ks, C::BQ)), id_sp, ks > 0);
+                    umma_commit(smem_u32(&bar_s_full[it & 1]));
+                    umma_commit(smem_u32(&bar_stage_free[it & 1]));
+                }
+                __syncwarp();
                 return true;
             };
-            bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV) && (n_it == 0 || sdp(0));
+            bool ok = mbar_wait_warp(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV) && (n_it == 0 || sdp(0));
             for (int it = 0; ok && it < n_it; ++it) {
                 if (it + 1 < n_it && !(ok = sdp(it + 1))) break;
-                if (!(ok = mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
-                if (!(ok = mbar_wait(smem_u32(&bar_q_ready), it & 1, w, SITE_BWD_Q_READY))) break;   // transposes
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_q_ready), it & 1, w, SITE_BWD_Q_READY))) break;   // transposes
                 tc_fence_after();
+                const uint32_t sc = tm + C::s_col(it), dc = tm + C::dp_col(it);
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < C::BQ / 8; ++ks)       // dV += P^T dO, K = queries
-                    umma_ts<true>(tm + C::DV_COL, tm + C::s_col(it) + ks * 8, sdesc_add(dOT, koff(ks, D)), id_vk,
-                                  (it > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < C::BQ / 8; ++ks)   // dV += P^T dO, K = queries
+                        umma_ts<true>(tm + C::DV_COL, sc + ks * 8, sdesc_add(dOT, koff(ks, D)), id_vk,
+                                      (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-                for (int ks = 0; ks < C::BQ / 8; ++ks)       // dK' += dS^T Q'
-                    umma_ts<true>(tm + C::DK_COL, tm + C::dp_col(it) + ks * 8, sdesc_add(dQT, koff(ks, D)), id_vk,
-                                  (it > 0 || ks > 0) ? 1u : 0u);
-                umma_commit(smem_u32(&bar_qt_free));        // Q'^T and dO^T are read
-                if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
+                    for (int ks = 0; ks < C::BQ / 8; ++ks)   // dK' += dS^T Q'
+                        umma_ts<true>(tm + C::DK_COL, dc + ks * 8, sdesc_add(dQT, koff(ks, D)), id_vk,
+                                      (it > 0 || ks > 0) ? 1u : 0u);
+                    umma_commit(smem_u32(&bar_qt_free));    // Q'^T and dO^T are read
+                }
+                __syncwarp();
+                if (it > 0 && !(ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < C::BKV / 8; ++ks)      // dQ'_part = dS K', K = keys
-                    umma_ss<true>(tm + C::DQ_COL, sdesc_add(dS, koff(ks, C::BQ)), sdesc_add(dKT, koff(ks, D)), id_q,
-                                  ks > 0);
-                umma_commit(smem_u32(&bar_dq_full));
+                    for (int ks = 0; ks < C::BKV / 8; ++ks)  // dQ'_part = dS K', K = keys
+                        umma_ss<true>(tm + C::DQ_COL, sdesc_add(dS, koff(ks, C::BQ)), sdesc_add(dKT, koff(ks, D)), id_q,
+                                      ks > 0);
+                    umma_commit(smem_u32(&bar_dq_full));
+                }
+                __syncwarp();
             }
-            umma_commit(smem_u32(&bar_dkv_full));
-            umma_commit(smem_u32(&bar_final));
+            if (elect_one()) {
+                umma_commit(smem_u32(&bar_dkv_full));
+                umma_commit(smem_u32(&bar_final));
+            }
+            __syncwarp();
         }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ RoPE, rounding, transposes; dQ drain
@@ -327,6 +342,11 @@ __global__ void __launch_bounds__(384, 1)
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_q_ready));
             mbar_arrive(smem_u32(&bar_stage_free[it & 1]));
+            // The next rotation completes the next q_rot phase: first the issuer must have
+            // passed this one (its S^T and dP^T of step it are done), or on the first step
+            // q_rot could run two phases past the issuer's wait.
+            if (it + 1 < n_it && !(ok = mbar_wait_warp(smem_u32(&bar_s_full[it & 1]), (it >> 1) & 1, w, SITE_BWD_S_FULL)))
+                break;
             if (it + 1 < n_it && !(ok = rotate(it + 1))) break;
             if (it > 0 && !(ok = drain(it - 1))) break;
         }
