@@ -16,8 +16,11 @@
 // The M=64 accumulator puts query row m in TMEM lane 32*(m/16) + m%16.
 // Warp roles (384 threads): warp 0 TMA; warp 1 TMEM allocator and UMMA issuer (all
 // products, in order, so every TMEM and smem reuse is ordered by the one issuer);
-// warps 4-7 RoPE, TF32 rounding and transposes, then the dQ drain; warps 8-11 P^T, dS^T
-// and dS (thread = key row) and the dK/dV epilogue.
+// warps 4-7 RoPE on K and Q', TF32 rounding of V and dO, the transposes, then the dQ
+// drain; warps 8-11 P^T, dS^T and dS (thread = key row) and the dK/dV epilogue.  (Warps
+// 2-3 taking dO's rounding and transpose measured slower: the roles share the shared-
+// memory bandwidth with the SS products, and the gradient warps slowed by more than the
+// transposes gained.)
 // Two Q' | dO stages (one for Q'^T | dO^T) and two S^T | dP^T buffers in TMEM: step
 // it's tiles load into stage it % 2 once step it - 2 is done with it and are rotated and
 // rounded in place while step it - 1 runs; S^T and dP^T of step it + 1 (whose operands
@@ -57,8 +60,8 @@ struct BwdTf32Cfg {
 };
 
 // dst[d][r] = src[r][d] for a fp32 tile of ROWS rows x D columns in the 128-byte
-// swizzled layout (both K-major, 32 elements per 128-byte chunk); 128 threads.
-template <int D, int ROWS>
+// swizzled layout (both K-major, 32 elements per 128-byte chunk); NT threads.
+template <int D, int ROWS, int NT = 128>
 __device__ __forceinline__ void transpose_f32(const uint8_t* src, uint8_t* dst, int t) {
     constexpr int UNITS = D * ROWS / 4;
     // A warp takes 32 consecutive columns d of the same four rows: conflict-free reads
@@ -66,7 +69,7 @@ __device__ __forceinline__ void transpose_f32(const uint8_t* src, uint8_t* dst, 
     // quarter-warp at swizzle-spread chunk positions).  Rows fastest put a warp's reads
     // on two or four banks.
 #pragma unroll 4
-    for (int ul = t; ul < UNITS; ul += 128) {
+    for (int ul = t; ul < UNITS; ul += NT) {
         const int d = ul % D, r0 = 4 * (ul / D);
         uint32_t w[4];
 #pragma unroll
@@ -78,11 +81,11 @@ __device__ __forceinline__ void transpose_f32(const uint8_t* src, uint8_t* dst, 
     }
 }
 
-// Round a fp32 tile to TF32 (nearest) in place; 128 threads.
-template <int BYTES>
+// Round a fp32 tile to TF32 (nearest) in place; NT threads.
+template <int BYTES, int NT = 128>
 __device__ __forceinline__ void round_tf32(uint8_t* p, int t) {
 #pragma unroll 4
-    for (int i = t; i < BYTES / 16; i += 128) {
+    for (int i = t; i < BYTES / 16; i += NT) {
         uint4 v = reinterpret_cast<uint4*>(p)[i];
         v.x = f32_to_tf32_rna(__uint_as_float(v.x));
         v.y = f32_to_tf32_rna(__uint_as_float(v.y));
@@ -142,8 +145,8 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(smem_u32(&bar_stage_full[1]), 1);
         // A stage is free once the S^T and dP^T products (a commit) and the transposes
         // (the 128 RoPE threads) have read it.
-        mbar_init(smem_u32(&bar_stage_free[0]), 129);
-        mbar_init(smem_u32(&bar_stage_free[1]), 129);
+        mbar_init(smem_u32(&bar_stage_free[0]), 1 + 128);
+        mbar_init(smem_u32(&bar_stage_free[1]), 1 + 128);
         mbar_init(smem_u32(&bar_q_rot), 128);
         mbar_init(smem_u32(&bar_q_ready), 128);
         mbar_init(smem_u32(&bar_qt_free), 1);
@@ -321,15 +324,22 @@ __global__ void __launch_bounds__(384, 1)
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_k_ready));
         }
-        // Rotation and rounding of step it's tiles in place; the q_rot barrier (every
-        // thread of the group) also orders them before the transposes.
+        // Rotation of step it's Q' and rounding of its dO in place; the q_rot barrier
+        // (every thread of the group) also orders them before the transposes.  The table
+        // row of the next step's rotation is fetched right after this one, so its latency
+        // overlaps the transposes and the drain.
+        using RopeQ = RopeTile<D, C::BQ, 128, ROPE_TF32>;
+        RopeQ rq;
+        rq.init(r, a.rope);
+        float4 qbase[RopeQ::F4];
+        if (n_it > 0) rq.load_base(qbase, step_q0(0), T, a.rope);
         auto rotate = [&](int it) -> bool {
             if (!mbar_wait_warp(smem_u32(&bar_stage_full[it & 1]), (it >> 1) & 1, w, SITE_BWD_QDO_FULL)) return false;
-            rope_tile_smem<D, C::BQ, 128, ROPE_TF32>(stage_q(it), nullptr, step_q0(it), T, r, a.rope,
-                                                     VL ? len : step_q0(it) + C::BQ);
+            rq.template apply<false>(stage_q(it), nullptr, qbase, (VL ? len : step_q0(it) + C::BQ) - step_q0(it));
             round_tf32<C::Q_BYTES>(stage_o(it), r);
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bar_q_rot));
+            if (it + 1 < n_it) rq.load_base(qbase, step_q0(it + 1), T, a.rope);
             return true;
         };
         if (ok && n_it > 0) ok = rotate(0);
@@ -390,12 +400,20 @@ __global__ void __launch_bounds__(384, 1)
             const bool diag = kv0 + C::BKV - 1 > q0;
             const bool tail = VL && q0 + C::BQ > len;          // queries past the length are padding
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float p = ex2(fmaf(__uint_as_float(sr[c]), sl2, -s_lse[sb][c]));
-                if ((diag && kvpos > q0 + c) || (tail && q0 + c >= len)) p = 0.f;
-                const float g = p * (__uint_as_float(dr[c]) - s_delta[sb][c]);
-                sr[c] = f32_to_tf32_rna(p);
-                dr[c] = f32_to_tf32_rna(g);
+            for (int c0 = 0; c0 < 64; c0 += 4) {
+                // Four queries' LSE and Delta per 16-byte read.
+                const float4 l4 = *reinterpret_cast<const float4*>(&s_lse[sb][c0]);
+                const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[sb][c0]);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dlt[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = c0 + e;
+                    float p = ex2(fmaf(__uint_as_float(sr[c]), sl2, -lv[e]));
+                    if ((diag && kvpos > q0 + c) || (tail && q0 + c >= len)) p = 0.f;
+                    const float g = p * (__uint_as_float(dr[c]) - dlt[e]);
+                    sr[c] = f32_to_tf32_rna(p);
+                    dr[c] = f32_to_tf32_rna(g);
+                }
             }
             tmem_st32(lt + C::s_col(it), *reinterpret_cast<uint32_t(*)[32]>(sr));
             tmem_st32(lt + C::s_col(it) + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));

@@ -1,12 +1,14 @@
 """A model of the TF32 backward kernel's barrier protocol (csrc/attn_bwd_tf32.cu), run
 on the CPU for every step count a CTA can get.
 
-The four roles of a CTA -- the TMA producer, the UMMA issuer, the RoPE / transpose /
-dQ-drain warps and the gradient warps -- are coroutines running the role's sequence of
-waits and arrivals; MMAs and copies complete at once.  As in the forward's model
+The four roles of a CTA -- the TMA producer, the UMMA issuer, the RoPE / rounding /
+transpose / dQ-drain warps and the gradient warps -- are coroutines running the role's sequence of waits and arrivals (a group of threads
+arrives as one); MMAs and copies complete at once.  As in the forward's model
 (test_fwd_protocol_model.py), the check fails on a deadlock or on a wait evaluated while
 its barrier is neither in the phase waited for nor the one after (mbarrier parity
-aliasing).  Two Q'/dO stages and two S^T/dP^T TMEM buffers: the next step's S^T and dP^T
+aliasing); every arrival also names the phase it is meant for, and one that lands in
+another phase (a role running a step ahead on a barrier that several roles complete)
+fails too.  Two Q'/dO stages and two S^T/dP^T TMEM buffers: the next step's S^T and dP^T
 go out before the current step's dV, dK and dQ.  Kept in step with the kernel by hand.
 """
 import random
@@ -18,8 +20,10 @@ class Bar:
     def __init__(self, name, count):
         self.name, self.count, self.arr, self.phase = name, count, 0, 0
 
-    def arrive(self, n=1):
-        self.arr += n
+    def arrive(self, phase):
+        if phase != self.phase:
+            raise ProtocolError(f"early arrival: {self.name} for phase {phase} in phase {self.phase}")
+        self.arr += 1
         assert self.arr <= self.count, self.name
         if self.arr == self.count:
             self.arr = 0
@@ -46,19 +50,19 @@ def simulate(n_it, rng, rope_waits_for_s=True):
     rows = [bar("rows0", 1), bar("rows1", 1)]
 
     def producer():
-        kv_full.arrive()
+        kv_full.arrive(0)
         for it in range(n_it):
             if it >= 2:
                 yield stage_free[it & 1], (it >> 1) - 1, f"producer: stage for step {it}"
-            stage_full[it & 1].arrive()
+            stage_full[it & 1].arrive(it >> 1)
 
     def issuer():
         yield k_ready, 0, "issuer: K'"
 
         def sdp(it):
             yield q_rot, it, f"issuer: rotated tiles of step {it}"
-            s_full[it & 1].arrive()
-            stage_free[it & 1].arrive()
+            s_full[it & 1].arrive(it >> 1)
+            stage_free[it & 1].arrive(it >> 1)
 
         if n_it:
             yield from sdp(0)
@@ -67,23 +71,23 @@ def simulate(n_it, rng, rope_waits_for_s=True):
                 yield from sdp(it + 1)
             yield ds_ready, it, f"issuer: dS of step {it}"
             yield q_ready, it, f"issuer: transposes of step {it}"
-            qt_free.arrive()
+            qt_free.arrive(it)
             if it > 0:
                 yield dq_free, it - 1, f"issuer: dQ' drained, step {it - 1}"
-            dq_full.arrive()
-        dkv_full.arrive()
+            dq_full.arrive(it)
+        dkv_full.arrive(0)
 
     def rope():
         yield kv_full, 0, "rope: K, V"
-        k_ready.arrive()
+        k_ready.arrive(0)
 
         def rotate(it):
             yield stage_full[it & 1], it >> 1, f"rope: tiles of step {it}"
-            q_rot.arrive()
+            q_rot.arrive(it)
 
         def drain(it):
             yield dq_full, it, f"rope: dQ' of step {it}"
-            dq_free.arrive()
+            dq_free.arrive(it)
 
         if n_it:
             yield from rotate(0)
@@ -91,8 +95,8 @@ def simulate(n_it, rng, rope_waits_for_s=True):
             yield q_rot, it, f"rope: rotation of step {it} (all threads)"
             if it > 0:
                 yield qt_free, it - 1, f"rope: Q'^T free after step {it - 1}"
-            q_ready.arrive()
-            stage_free[it & 1].arrive()
+            q_ready.arrive(it)
+            stage_free[it & 1].arrive(it >> 1)
             if it + 1 < n_it:
                 if rope_waits_for_s:
                     yield s_full[it & 1], it >> 1, f"rope: S^T of step {it} issued"
@@ -103,15 +107,15 @@ def simulate(n_it, rng, rope_waits_for_s=True):
             yield from drain(n_it - 1)
 
     def gradient():
-        rows[0].arrive()
+        rows[0].arrive(0)
         for it in range(n_it):
             yield rows[it & 1], it >> 1, f"gradient: LSE/Delta of step {it}"
             yield s_full[it & 1], it >> 1, f"gradient: S^T of step {it}"
             if it > 0:
                 yield dq_full, it - 1, f"gradient: dS buffer after step {it - 1}"
-            ds_ready.arrive()
+            ds_ready.arrive(it)
             if it + 1 < n_it:
-                rows[(it + 1) & 1].arrive()
+                rows[(it + 1) & 1].arrive((it + 1) >> 1)
         yield dkv_full, 0, "gradient: dK, dV"
 
     roles = {"producer": producer(), "issuer": issuer(), "rope": rope(), "gradient": gradient()}
