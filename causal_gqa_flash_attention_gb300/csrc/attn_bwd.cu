@@ -371,48 +371,58 @@ __global__ void __launch_bounds__(512, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ issuer A: S^T, dP^T
-        if (lane == 0) {
+        // Each issuer warp runs its loop and waits together (UMMA operands stay warp-
+        // uniform) and one elected lane issues each batch with its commits: a loop run by
+        // lane 0 alone cost several instructions per UMMA.
+        {
             constexpr uint32_t id_s = idesc_make(FMT_F16, 128, C::BQ, false, false);   // S^T (fp16 Q', K')
             constexpr uint32_t id_dp = idesc_make(FMT_BF16, 128, C::BQ, false, false); // dP^T
             const uint64_t dK16 = kdesc(sK16), dV = kdesc(sV), dQ0 = kdesc(stage_q(0));
-            bool ok = mbar_wait(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV);
+            bool ok = mbar_wait_warp(smem_u32(&bar_k_ready), 0, w, SITE_BWD_KV);
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it % C::NQS;
                 const uint32_t so = s * C::STAGE_BYTES;
-                if (!(ok = mbar_wait(smem_u32(&bar_q_ready[s]), (it / C::NQS) & 1, w, SITE_BWD_Q_READY))) break;
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_q_ready[s]), (it / C::NQS) & 1, w, SITE_BWD_Q_READY))) break;
                 // The previous step's S^T and dP^T must have been read out of TMEM; when P^T
                 // shares S^T's columns, dV must also have read P^T.
                 if (it > 0) {
                     const uint32_t bar = smem_u32(C::PT_OWN ? &bar_sdp_read : &bar_p_free);
-                    if (!(ok = mbar_wait(bar, (it - 1) & 1, w, SITE_BWD_DS_READY))) break;
+                    if (!(ok = mbar_wait_warp(bar, (it - 1) & 1, w, SITE_BWD_DS_READY))) break;
                 }
                 tc_fence_after();
                 const uint64_t dQ16 = sdesc_add(dQ0, so + C::Q_BYTES), dO = sdesc_add(dQ0, so + 2 * C::Q_BYTES);
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_D; ++ks) {      // S^T = K' Q'^T, K = head_dim
-                    const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
-                    const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
-                    umma_ss<false>(tm + C::S_COL, sdesc_add(dK16, off), sdesc_add(dQ16, offq), id_s, ks > 0);
+                    for (int ks = 0; ks < C::KSTEPS_D; ++ks) {  // S^T = K' Q'^T, K = head_dim
+                        const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
+                        const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
+                        umma_ss<false>(tm + C::S_COL, sdesc_add(dK16, off), sdesc_add(dQ16, offq), id_s, ks > 0);
+                    }
+                    umma_commit(smem_u32(&bar_s_full));
                 }
-                umma_commit(smem_u32(&bar_s_full));
+                __syncwarp();
                 if constexpr (C::DQ_ALIASES_DP) {               // dQ of the previous step sits in dP^T's columns
-                    if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE)))
+                    if (it > 0 && !(ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE)))
                         break;
                     tc_fence_after();
                 }
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_D; ++ks) {      // dP^T = V dO^T
-                    const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
-                    const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
-                    umma_ss<false>(tm + C::DP_COL, sdesc_add(dV, off), sdesc_add(dO, offq), id_dp, ks > 0);
+                    for (int ks = 0; ks < C::KSTEPS_D; ++ks) {  // dP^T = V dO^T
+                        const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
+                        const uint32_t offq = (ks * 32 >> 7) * C::BQ * 128 + (ks * 32 & 127);
+                        umma_ss<false>(tm + C::DP_COL, sdesc_add(dV, off), sdesc_add(dO, offq), id_dp, ks > 0);
+                    }
+                    umma_commit(smem_u32(&bar_dp_full));
                 }
-                umma_commit(smem_u32(&bar_dp_full));
+                __syncwarp();
             }
-            umma_commit(smem_u32(&bar_final));
+            if (elect_one()) umma_commit(smem_u32(&bar_final));
+            __syncwarp();
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ issuer B: dV, dK
-        if (lane == 0) {
+        {
             constexpr uint32_t id_dv = idesc_make(FMT_BF16, 128, D, false, true);      // B MN-major
             const uint64_t dQmn0 = mndesc(stage_q(0), C::BQ * 128), dDS0 = kdesc(sdS);
             bool ok = true;
@@ -420,50 +430,60 @@ __global__ void __launch_bounds__(512, 1)
                 const int s = it % C::NQS;
                 const uint32_t so = s * C::STAGE_BYTES;
                 const uint64_t dDS = sdesc_add(dDS0, C::DS_ALIASES_Q16 ? so : 0);
-                if (!(ok = mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
                 tc_fence_after();
                 const uint64_t dOmn = sdesc_add(dQmn0, so + 2 * C::Q_BYTES), dQmn = sdesc_add(dQmn0, so);
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_Q; ++ks)         // dV += P^T dO (P^T from TMEM)
-                    umma_ts<false>(tm + C::DV_COL, tm + C::pt_col(ks * 16), sdesc_add(dOmn, ks * 16 * 128), id_dv,
-                                   (it > 0 || ks > 0) ? 1u : 0u);
-                umma_commit(smem_u32(&bar_p_free));
+                    for (int ks = 0; ks < C::KSTEPS_Q; ++ks)     // dV += P^T dO (P^T from TMEM)
+                        umma_ts<false>(tm + C::DV_COL, tm + C::pt_col(ks * 16), sdesc_add(dOmn, ks * 16 * 128), id_dv,
+                                       (it > 0 || ks > 0) ? 1u : 0u);
+                    umma_commit(smem_u32(&bar_p_free));
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_Q; ++ks) {       // dK' += dS^T Q'
-                    const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
-                    umma_ss<false>(tm + C::DK_COL, sdesc_add(dDS, off), sdesc_add(dQmn, ks * 16 * 128), id_dv,
-                                   (it > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < C::KSTEPS_Q; ++ks) {   // dK' += dS^T Q'
+                        const uint32_t off = (ks * 32 >> 7) * C::BKV * 128 + (ks * 32 & 127);
+                        umma_ss<false>(tm + C::DK_COL, sdesc_add(dDS, off), sdesc_add(dQmn, ks * 16 * 128), id_dv,
+                                       (it > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    umma_commit(smem_u32(&bar_qdo_empty[s]));
+                    umma_commit(smem_u32(&bar_ds_free));
                 }
-                umma_commit(smem_u32(&bar_qdo_empty[s]));
-                umma_commit(smem_u32(&bar_ds_free));
+                __syncwarp();
             }
-            umma_commit(smem_u32(&bar_dkv_full));
-            umma_commit(smem_u32(&bar_final));
+            if (elect_one()) {
+                umma_commit(smem_u32(&bar_dkv_full));
+                umma_commit(smem_u32(&bar_final));
+            }
+            __syncwarp();
         }
     } else if (warp == 3) {
         // ------------------------------------------------------------ issuer C: dQ
-        if (lane == 0) {
+        {
             constexpr uint32_t id_dq = idesc_make(FMT_BF16, 128, D, true, true);       // A, B MN-major
             const uint64_t dKmn = mndesc(sK, C::BKV * 128), dDSmn0 = mndesc(sdS, C::BKV * 128);
             bool ok = true;
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it % C::NQS;
                 const uint64_t dDSmn = sdesc_add(dDSmn0, C::DS_ALIASES_Q16 ? s * C::STAGE_BYTES : 0);
-                if (!(ok = mbar_wait(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
-                if (it > 0 && !(ok = mbar_wait(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_ds_ready), it & 1, w, SITE_BWD_DS_READY))) break;
+                if (it > 0 && !(ok = mbar_wait_warp(smem_u32(&bar_dq_free), (it - 1) & 1, w, SITE_BWD_DQ_FREE))) break;
                 if constexpr (C::DQ_ALIASES_DP) {               // dQ overwrites dP^T: issuer A's dP^T is done
-                    if (!(ok = mbar_wait(smem_u32(&bar_dp_full), it & 1, w, SITE_BWD_DP_FULL))) break;
+                    if (!(ok = mbar_wait_warp(smem_u32(&bar_dp_full), it & 1, w, SITE_BWD_DP_FULL))) break;
                 }
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < C::KSTEPS_KV; ++ks)        // dQ'_part = dS K'
-                    umma_ss<false>(tm + C::DQ_COL, sdesc_add(dDSmn, ks * 16 * 128), sdesc_add(dKmn, ks * 16 * 128),
-                                   id_dq, ks > 0);
-                umma_commit(smem_u32(&bar_dq_full));
-                umma_commit(smem_u32(&bar_qdo_empty[s]));
-                umma_commit(smem_u32(&bar_ds_free));
+                    for (int ks = 0; ks < C::KSTEPS_KV; ++ks)    // dQ'_part = dS K'
+                        umma_ss<false>(tm + C::DQ_COL, sdesc_add(dDSmn, ks * 16 * 128), sdesc_add(dKmn, ks * 16 * 128),
+                                       id_dq, ks > 0);
+                    umma_commit(smem_u32(&bar_dq_full));
+                    umma_commit(smem_u32(&bar_qdo_empty[s]));
+                    umma_commit(smem_u32(&bar_ds_free));
+                }
+                __syncwarp();
             }
-            umma_commit(smem_u32(&bar_final));
+            if (elect_one()) umma_commit(smem_u32(&bar_final));
+            __syncwarp();
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------ RoPE on K and Q; dQ drain
