@@ -390,7 +390,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     if ((s = map_bthd(&tv, v, f32, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tdo, dO, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
     std::memset(&tdq, 0, sizeof(tdq));
-    if (!f32 && D <= 64 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
+    if (!f32 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
     ne::BwdArgs a;
     a.lse = lse;
     a.delta = delta;
@@ -889,7 +889,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     if ((s = map_bthd(&tv, v, false, B, T, Hkv, D, 128)) != NE_OK) return s;
     if ((s = map_bthd(&tdo, dO, false, B, T, Hq, D, q_rows)) != NE_OK) return s;
     std::memset(&tdq, 0, sizeof(tdq));
-    if (D <= 64 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
+    if ((s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
     ne::BwdArgs a;
     a.lse = lse;
     a.delta = delta;

@@ -228,7 +228,9 @@ struct BwdCfg {
     static constexpr int Q_BYTES = BQ * ROWB;
     static constexpr int STAGE_BYTES = 3 * Q_BYTES; // Q' (bf16) | Q' (fp16) | dO
     static constexpr int DS_BYTES = BKV * BQ * 2;   // dS^T bf16 [key][query]
-    static constexpr int SMEM = 1024 + 3 * KV_BYTES + NQS * STAGE_BYTES + (DS_ALIASES_Q16 ? 0 : DS_BYTES);
+    static constexpr int DQ_STAGE = BQ * 128;       // one 32-column fp32 chunk of dQ' for a bulk reduce-add
+    static constexpr int SMEM =
+        1024 + 3 * KV_BYTES + NQS * STAGE_BYTES + (DS_ALIASES_Q16 ? 0 : DS_BYTES) + DQ_STAGE;
     // TMEM columns
     static constexpr int S_COL = 0;                 // S^T, then P^T (bf16 packed)
     static constexpr int DP_COL = 128;              // dP^T
@@ -260,7 +262,7 @@ template <int D, bool VL>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,6 +271,7 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t* sV = sK16 + C::KV_BYTES;
     uint8_t* sStage = sV + C::KV_BYTES;            // NQS x (Q' bf16 | Q' fp16 | dO)
     uint8_t* sdS = C::DS_ALIASES_Q16 ? sStage + C::Q_BYTES : sStage + C::NQS * C::STAGE_BYTES;
+    uint8_t* sDQ = sStage + C::NQS * C::STAGE_BYTES + (C::DS_ALIASES_Q16 ? 0 : C::DS_BYTES);   // dQ' chunk
     auto stage_q = [&](int s) { return sStage + s * C::STAGE_BYTES; };
     auto stage_q16 = [&](int s) { return sStage + s * C::STAGE_BYTES + C::Q_BYTES; };
 
@@ -276,6 +279,7 @@ __global__ void __launch_bounds__(512, 1)
         bar_p_free, bar_ds_free, bar_dq_full, bar_dq_free, bar_dkv_full, bar_final, bar_sdp_read;
     __shared__ __align__(8) uint64_t bar_qdo_full[C::NQS], bar_q_ready[C::NQS], bar_qdo_empty[C::NQS];
     __shared__ __align__(8) uint64_t bar_rows[2];   // LSE/Delta of a query tile staged (double buffer)
+    __shared__ __align__(8) uint64_t bar_dqs_free, bar_dqs_full;   // dQ' chunk: read by its reduce / staged
     __shared__ __align__(16) float s_lse[2][C::BQ];
     __shared__ __align__(16) float s_delta[2][C::BQ];
     __shared__ uint32_t tmem_slot;
@@ -308,6 +312,8 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(smem_u32(&bar_final), 3);        // one commit per issuer
         mbar_init(smem_u32(&bar_rows[0]), 256);
         mbar_init(smem_u32(&bar_rows[1]), 256);
+        mbar_init(smem_u32(&bar_dqs_free), 1);       // the thread that issued the reduce
+        mbar_init(smem_u32(&bar_dqs_full), 128);     // every row of the chunk
         for (int s = 0; s < C::NQS; ++s) {
             mbar_init(smem_u32(&bar_qdo_full[s]), 1);
             mbar_init(smem_u32(&bar_q_ready[s]), 128);
@@ -321,6 +327,7 @@ __global__ void __launch_bounds__(512, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dq);
     }
     if (warp == 1) {
         __syncwarp();
@@ -490,30 +497,53 @@ __global__ void __launch_bounds__(512, 1)
         // Thread r: RoPE units of the K tile and of every Q tile, and query row r of the dQ
         // partial (TMEM lane r), added into the fp32 accumulator.  The Q of step it+1 is
         // rotated before the dQ of step it is drained.
+        // The drain stages 32 columns of the partial at a time (16 KB) and adds each chunk
+        // with one bulk tensor reduce-add (per-thread 16-byte atomics kept the accumulator's
+        // traffic in flight on every thread and made the drain the longest-stalled role).
+        // Chunk kk (over all steps) waits until the reduce of chunk kk - 1 has read the
+        // staging tile.
         const int r = tid - 128;
         const uint32_t lt = tm + ((uint32_t)((warp & 3) * 32) << 16);
         bool ovf = false;
+        int kk = 0;                                    // dQ' chunks staged so far
         auto drain = [&](int it) -> bool {
             const int h = hkv * G + it / per_head;
-            const int qpos = (i_first + it % per_head) * C::BQ + r;
+            const int q0 = (i_first + it % per_head) * C::BQ;
             if (!mbar_wait_warp(smem_u32(&bar_dq_full), it & 1, w, SITE_BWD_DQ_FULL)) return false;
             tc_fence_after();
-            float* dst = a.dq_acc + (((size_t)b * T + (qpos < T ? qpos : 0)) * a.Hq + h) * D;
-#pragma unroll
-            for (int c = 0; c < D; c += 64) {
-                uint32_t v[64];
-                tmem_ld_cols<2>(lt + C::DQ_COL + c, v);
-                if (c + 64 >= D) {
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32, ++kk) {
+                uint32_t v[32];
+                tmem_ld32(lt + C::DQ_COL + c, v);
+                tmem_wait_ld();
+                reg_fence32(v);
+                if (c + 32 >= D) {
                     tc_fence_before();
                     mbar_arrive(smem_u32(&bar_dq_free));
                 }
-                if (qpos < T) {
-#pragma unroll
-                    for (int e = 0; e < 64; e += 4)
-                        atomicAdd(reinterpret_cast<float4*>(dst + c + e),
-                                  make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                              __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
+                if (kk > 0) {
+                    if (r == 0) {
+                        bulk_wait_group_read0();
+                        mbar_arrive(smem_u32(&bar_dqs_free));
+                    }
+                    if (!mbar_wait_warp(smem_u32(&bar_dqs_free), (kk - 1) & 1, w, SITE_BWD_DQ_FREE)) return false;
                 }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4*>(sDQ + sw128_offset(r, u)) =
+                        make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bar_dqs_full));
+                bool issued = true;
+                if (r == 0) {
+                    issued = mbar_wait(smem_u32(&bar_dqs_full), kk & 1, w, SITE_BWD_DQ_FULL);
+                    if (issued) {
+                        // Rows at or beyond T lie outside the tensor map and are skipped.
+                        tma_reduce_add_4d(&tm_dq, smem_u32(sDQ), c, h, q0, b);
+                        bulk_commit_group();
+                    }
+                }
+                if (!__all_sync(0xffffffffu, issued)) return false;
             }
             return true;
         };
@@ -541,6 +571,7 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (it > 0 && !(ok = drain(it - 1))) break;
         }
+        if (r == 0) bulk_wait_group0();   // the last reduces have completed before the CTA exits
         if (ovf) report_error(a.err, SITE_RANGE);
     } else {
         // ------------------------------------------------------------ P^T, dS^T; dK, dV epilogue
@@ -718,20 +749,20 @@ __global__ void __launch_bounds__(512, 1)
 
 template <int D, bool VL>
 cudaError_t launch_bwd_vl(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t st) {
     using C = BwdCfg<D>;
     auto kfn = attn_bwd_kernel<D, VL>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.Hkv, B, a.n_kvt);
-    return launch_k(kfn, grid, dim3(C::THREADS), C::SMEM, st, tq, tk, tv, tdo, a);
+    return launch_k(kfn, grid, dim3(C::THREADS), C::SMEM, st, tq, tk, tv, tdo, tdq, a);
 }
 
 template <int D>
 cudaError_t launch_bwd_t(int B, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
-    return a.seq_lens ? launch_bwd_vl<D, true>(B, tq, tk, tv, tdo, a, st)
-                      : launch_bwd_vl<D, false>(B, tq, tk, tv, tdo, a, st);
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, cudaStream_t st) {
+    return a.seq_lens ? launch_bwd_vl<D, true>(B, tq, tk, tv, tdo, tdq, a, st)
+                      : launch_bwd_vl<D, false>(B, tq, tk, tv, tdo, tdq, a, st);
 }
 
 int grid_for(long long work, int per_block) {
@@ -789,7 +820,7 @@ cudaError_t launch_bwd(bool tf32, int D, int B, const CUtensorMap& tq, const CUt
                        cudaStream_t st) {
     if (tf32) return cudaErrorNotSupported;
     if (D == 64 || D == 32) return launch_bwd_d64(B, tq, tk, tv, tdo, tdq, a, st);   // 32: zero-padded to 64
-    if (D == 128) return launch_bwd_t<128>(B, tq, tk, tv, tdo, a, st);
+    if (D == 128) return launch_bwd_t<128>(B, tq, tk, tv, tdo, tdq, a, st);
     return cudaErrorInvalidValue;
 }
 
