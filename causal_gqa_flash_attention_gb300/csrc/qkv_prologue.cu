@@ -41,12 +41,12 @@ struct ProCfg {
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int NS = 4;
     static constexpr int SMEM = 1024 + NS * STAGE;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 320;
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     qkv_prologue_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                         const ProArgs a) {
     using C = ProCfg;
@@ -56,26 +56,44 @@ __global__ void __launch_bounds__(192, 1)
     auto st_b = [&](int s) { return smem + s * C::STAGE + C::A_BYTES; };
 
     __shared__ __align__(8) uint64_t bar_full[C::NS], bar_empty[C::NS];
-    __shared__ __align__(8) uint64_t bar_acc;
+    __shared__ __align__(8) uint64_t bar_acc_full[2], bar_acc_empty[2];   // [accumulator]
+    __shared__ __align__(8) uint64_t bar_rn_full[2], bar_rn_empty[2];     // [1/rms slot]
+    __shared__ __align__(8) uint64_t bar_final;
+    __shared__ float s_invr[2][C::BM];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * C::BN, m0 = blockIdx.y * C::BM;
     const int nk = (a.dim + C::BK - 1) / C::BK;
+    const int nh = a.Hq + 2 * a.Hkv;
+    const int tiles_n = (nh * D + C::BN - 1) / C::BN, tiles_m = (a.M + C::BM - 1) / C::BM;
+    const int n_tiles = tiles_n * tiles_m;
+    // This CTA's tiles: blockIdx.x, + gridDim.x, ...  Tile t is (row block t / tiles_n,
+    // column block t % tiles_n), so tiles running at the same time share rows of x in L2.
+    const int my_tiles = n_tiles > (int)blockIdx.x ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto tile_m0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) / tiles_n * C::BM; };
+    auto tile_n0 = [&](int i) { return ((int)blockIdx.x + i * (int)gridDim.x) % tiles_n * C::BN; };
 
     if (tid == 0) {
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
             mbar_init(smem_u32(&bar_empty[s]), 1 + 128);   // the MMA commit and the norm threads
         }
-        mbar_init(smem_u32(&bar_acc), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bar_acc_full[i]), 1);        // the tile's last MMA
+            mbar_init(smem_u32(&bar_acc_empty[i]), 128);     // the epilogue threads
+            mbar_init(smem_u32(&bar_rn_full[i]), 128);       // the norm threads
+            mbar_init(smem_u32(&bar_rn_empty[i]), 128);      // the epilogue threads
+        }
+        mbar_init(smem_u32(&bar_final), 1);
         abort_flag = 0;
         fence_mbar_init();
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
     }
     if (warp == 1) {
         __syncwarp();
-        tmem_alloc(smem_u32(&tmem_slot), 256);
+        tmem_alloc(smem_u32(&tmem_slot), 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -88,92 +106,134 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // One ring over every chunk of every tile of the CTA (chunk g = i nk + kc).
         if (lane == 0) {
-            tma_prefetch_desc(&tm_x);
-            tma_prefetch_desc(&tm_w);
             int issued = 0;
-            for (int kc = 0; kc < nk; ++kc) {
-                const int s = kc % C::NS;
-                if (kc >= C::NS && !mbar_wait(smem_u32(&bar_empty[s]), ((kc / C::NS) - 1) & 1, w, SITE_PRO_EMPTY))
-                    break;
-                const uint32_t f = smem_u32(&bar_full[s]);
-                mbar_arrive_expect_tx(f, C::STAGE);
-                tma_load_2d(smem_u32(st_a(s)), &tm_x, f, kc * C::BK, m0);
-                tma_load_2d(smem_u32(st_b(s)), &tm_w, f, kc * C::BK, n0);
-                ++issued;
+            bool ok = true;
+            for (int i = 0; ok && i < my_tiles; ++i) {
+                const int m0 = tile_m0(i), n0 = tile_n0(i);
+                for (int kc = 0; kc < nk; ++kc) {
+                    const int g = issued, s = g % C::NS;
+                    if (g >= C::NS &&
+                        !(ok = mbar_wait(smem_u32(&bar_empty[s]), ((g / C::NS) - 1) & 1, w, SITE_PRO_EMPTY)))
+                        break;
+                    const uint32_t f = smem_u32(&bar_full[s]);
+                    mbar_arrive_expect_tx(f, C::STAGE);
+                    tma_load_2d(smem_u32(st_a(s)), &tm_x, f, kc * C::BK, m0);
+                    tma_load_2d(smem_u32(st_b(s)), &tm_w, f, kc * C::BK, n0);
+                    ++issued;
+                }
             }
             // Teardown: every copy this CTA started must have landed before exit.
-            for (int kc = max(0, issued - C::NS); kc < issued; ++kc)
-                mbar_wait_drain(smem_u32(&bar_full[kc % C::NS]), (kc / C::NS) & 1, w, SITE_PRO_DRAIN);
+            for (int g = max(0, issued - C::NS); g < issued; ++g)
+                mbar_wait_drain(smem_u32(&bar_full[g % C::NS]), (g / C::NS) & 1, w, SITE_PRO_DRAIN);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ UMMA issuer
+        // Tile i accumulates in TMEM columns 256 (i % 2) .. + 255, once the epilogue has
+        // read tile i - 2 out of them.
         constexpr uint32_t id = idesc_make(FMT_BF16, 128, C::BN, false, false);
         const uint64_t da0 = sdesc(smem_u32(st_a(0)), 16, 1024), db0 = sdesc(smem_u32(st_b(0)), 16, 1024);
-        for (int kc = 0; kc < nk; ++kc) {
-            const int s = kc % C::NS;
-            if (!mbar_wait_warp(smem_u32(&bar_full[s]), (kc / C::NS) & 1, w, SITE_PRO_FULL)) break;
+        bool ok = true;
+        int g = 0;
+        for (int i = 0; ok && i < my_tiles; ++i) {
+            const int ab = i & 1;
+            if (i >= 2 && !(ok = mbar_wait_warp(smem_u32(&bar_acc_empty[ab]), ((i >> 1) - 1) & 1, w, SITE_PRO_ACC)))
+                break;
             tc_fence_after();
-            const uint64_t da = sdesc_add(da0, s * C::STAGE), db = sdesc_add(db0, s * C::STAGE);
-            if (elect_one()) {                        // one elected lane issues the batch
+            const uint32_t acc = tm + 256 * ab;
+            for (int kc = 0; kc < nk; ++kc, ++g) {
+                const int s = g % C::NS;
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_full[s]), (g / C::NS) & 1, w, SITE_PRO_FULL))) break;
+                tc_fence_after();
+                const uint64_t da = sdesc_add(da0, s * C::STAGE), db = sdesc_add(db0, s * C::STAGE);
+                if (elect_one()) {                    // one elected lane issues the batch
 #pragma unroll
-                for (int ks = 0; ks < C::BK / 16; ++ks)   // K = dim, 16 per step (32 bytes)
-                    umma_ss<false>(tm, sdesc_add(da, ks * 32), sdesc_add(db, ks * 32), id, (kc > 0 || ks > 0) ? 1u : 0u);
-                umma_commit(smem_u32(&bar_empty[s]));
+                    for (int ks = 0; ks < C::BK / 16; ++ks)   // K = dim, 16 per step (32 bytes)
+                        umma_ss<false>(acc, sdesc_add(da, ks * 32), sdesc_add(db, ks * 32), id,
+                                       (kc > 0 || ks > 0) ? 1u : 0u);
+                    umma_commit(smem_u32(&bar_empty[s]));
+                    if (kc == nk - 1) umma_commit(smem_u32(&bar_acc_full[ab]));
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
-        umma_commit_e(smem_u32(&bar_acc));   // also the teardown's: every MMA of this CTA
+        umma_commit_e(smem_u32(&bar_final));   // the teardown's: every MMA of this CTA
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ RMS norm of the x rows
+        // Thread r: token row r of the tile, read from every chunk beside the MMA (which
+        // needs no wait for it); 1/r_m goes to the epilogue through a double-buffered slot.
+        const int r = (warp - 6) * 32 + lane;
+        bool ok = true;
+        int g = 0;
+        for (int i = 0; ok && i < my_tiles; ++i) {
+            float2 ss2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};   // independent sums (past dim: TMA's zero fill)
+            for (int kc = 0; kc < nk; ++kc, ++g) {
+                const int s = g % C::NS;
+                if (!(ok = mbar_wait_warp(smem_u32(&bar_full[s]), (g / C::NS) & 1, w, SITE_PRO_FULL))) break;
+                const uint8_t* arow = st_a(s);
+                uint4 xv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) xv[u] = *reinterpret_cast<const uint4*>(arow + sw128_offset(r, u));
+                mbar_arrive(smem_u32(&bar_empty[s]));   // read: the stage may take the next chunk
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[e]));
+                        ss2[e] = __ffma2_rn(xf, xf, ss2[e]);
+                    }
+                }
+            }
+            if (!ok) break;
+            const float ss =
+                ((ss2[0].x + ss2[0].y) + (ss2[1].x + ss2[1].y)) + ((ss2[2].x + ss2[2].y) + (ss2[3].x + ss2[3].y));
+            const int rb = i & 1;
+            if (i >= 2 && !(ok = mbar_wait_warp(smem_u32(&bar_rn_empty[rb]), ((i >> 1) - 1) & 1, w, SITE_PRO_ACC)))
+                break;
+            s_invr[rb][r] = rsqrtf(ss / (float)a.dim + a.eps);
+            mbar_arrive(smem_u32(&bar_rn_full[rb]));
+        }
     } else {
-        // ------------------------------------------------------------ norm, gain; epilogue
+        // ------------------------------------------------------------ epilogue
+        // Thread r: token row r of the tile = TMEM lane (warps 2-5 cover the four lane
+        // quarters).  acc / r_m, RoPE on query and key heads (position m mod T), bf16
+        // stores; the tile's (cos, sin) table row is fetched one tile early.
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;              // token row of the tile = TMEM lane
-        const int m = m0 + r;
+        const int r = quarter * 32 + lane;
         const uint32_t lt = tm + ((uint32_t)(quarter * 32) << 16);
-        // The (cos, sin) table row of this token's position, D/2 pairs, fetched before the
-        // main loop so its latency hides under it: a load waited on per 32-column chunk set
-        // the epilogue's pace.
         float4 tabr[D / 4];
-        {
+        auto fetch_row = [&](int i) {
+            const int m = tile_m0(i) + r;
             const float4* tr = reinterpret_cast<const float4*>(a.rope + (size_t)(m % a.T) * (D / 2));
 #pragma unroll
             for (int e = 0; e < D / 4; ++e)
                 tabr[e] = a.rotate && m < a.M ? __ldg(tr + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float2 ss2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};       // independent sums (past dim: TMA's zero fill)
+        };
+        if (my_tiles > 0) fetch_row(0);
         bool ok = true;
-        for (int kc = 0; kc < nk; ++kc) {
-            const int s = kc % C::NS;
-            if (!(ok = mbar_wait_warp(smem_u32(&bar_full[s]), (kc / C::NS) & 1, w, SITE_PRO_FULL))) break;
-            const uint8_t* arow = st_a(s);
-            uint4 xv[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) xv[u] = *reinterpret_cast<const uint4*>(arow + sw128_offset(r, u));
-            mbar_arrive(smem_u32(&bar_empty[s]));       // read: the stage may take the next chunk
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[e]));
-                    ss2[e] = __ffma2_rn(xf, xf, ss2[e]);
-                }
-            }
-        }
-        const float ss = ((ss2[0].x + ss2[0].y) + (ss2[1].x + ss2[1].y)) + ((ss2[2].x + ss2[2].y) + (ss2[3].x + ss2[3].y));
-        if (ok && mbar_wait_warp(smem_u32(&bar_acc), 0, w, SITE_PRO_ACC)) {
+        for (int i = 0; ok && i < my_tiles; ++i) {
+            const int ab = i & 1;
+            const int m = tile_m0(i) + r, n0 = tile_n0(i);
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_rn_full[ab]), (i >> 1) & 1, w, SITE_PRO_ACC))) break;
+            const float inv_r = s_invr[ab][r];
+            mbar_arrive(smem_u32(&bar_rn_empty[ab]));
+            if (!(ok = mbar_wait_warp(smem_u32(&bar_acc_full[ab]), (i >> 1) & 1, w, SITE_PRO_ACC))) break;
             tc_fence_after();
-            const float inv_r = rsqrtf(ss / (float)a.dim + a.eps);
-            const int nh = a.Hq + 2 * a.Hkv;
             // Unrolled over the tile's chunks so each chunk's table pairs are registers
             // named at compile time (32 columns = 16 pairs; the tile starts on a head).
 #pragma unroll
             for (int c = 0; c < C::BN; c += 32) {
                 uint32_t x[32];
-                tmem_ld32(lt + c, x);
+                tmem_ld32(lt + 256 * ab + c, x);
                 tmem_wait_ld();
                 reg_fence32(x);
+                if (c + 32 == C::BN) {                   // the accumulator may take tile i + 2
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bar_acc_empty[ab]));
+                }
                 const int n = n0 + c;                   // first output feature of the chunk
                 if (m >= a.M || n >= nh * D) continue;
                 const int h = n / D, e0 = n - h * D;    // head and column within it (32 | D)
@@ -202,6 +262,7 @@ __global__ void __launch_bounds__(192, 1)
                     d4[u] = make_uint4(pack_bf162(y[8 * u], y[8 * u + 1]), pack_bf162(y[8 * u + 2], y[8 * u + 3]),
                                        pack_bf162(y[8 * u + 4], y[8 * u + 5]), pack_bf162(y[8 * u + 6], y[8 * u + 7]));
             }
+            if (i + 1 < my_tiles) fetch_row(i + 1);
         }
     }
 
@@ -209,10 +270,10 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        mbar_wait_drain(smem_u32(&bar_acc), 0, w, SITE_PRO_DRAIN);
+        mbar_wait_drain(smem_u32(&bar_final), 0, w, SITE_PRO_DRAIN);
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tm, 256);
+        tmem_dealloc(tm, 512);
     }
 }
 
@@ -258,7 +319,13 @@ cudaError_t launch_qkv_prologue(const CUtensorMap& tx, const CUtensorMap& tw, co
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ProCfg::SMEM);
     if (e != cudaSuccess) return e;
     const int N = (a.Hq + 2 * a.Hkv) * a.D;
-    dim3 grid((N + ProCfg::BN - 1) / ProCfg::BN, (a.M + ProCfg::BM - 1) / ProCfg::BM);
+    const int tiles = ((N + ProCfg::BN - 1) / ProCfg::BN) * ((a.M + ProCfg::BM - 1) / ProCfg::BM);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // Persistent: one CTA per SM (the ring takes most of the shared memory), each walking
+    // its tiles.
+    dim3 grid(tiles < sms ? tiles : sms);
     return launch_k(kfn, grid, dim3(ProCfg::THREADS), ProCfg::SMEM, st, tx, tw, a);
 }
 
