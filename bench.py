@@ -294,9 +294,26 @@ def dist_stats(ms):
     return {"median_ms": statistics.median(xs), "p10_ms": q(0.10), "p90_ms": q(0.90), "n": len(xs)}
 
 
+def flat_views(shapes, dtype, device, pinned=False):
+    """One contiguous allocation holding tensors of the given shapes, each starting on a
+    256-byte boundary, so that a layer's inputs (or gradients) move in one copy."""
+    import math
+
+    import torch
+    al = 256 // torch.empty((), dtype=dtype).element_size()
+    offs, n = [], 0
+    for sh in shapes:
+        offs.append(n)
+        n += (math.prod(sh) + al - 1) // al * al
+    buf = torch.empty(n, dtype=dtype, device=device, pin_memory=pinned)
+    return buf, [buf[o:o + math.prod(sh)].view(sh) for o, sh in zip(offs, shapes)]
+
+
 class LayerSet:
     """Device (and pinned host) buffers of every layer of a workload: inputs, outputs
-    and one shared backward workspace, as a training step would hold them."""
+    and one shared backward workspace, as a training step would hold them.  A layer's
+    q, k, v, dO share one allocation, as do its dq, dk, dv (on the device and, for the
+    end-to-end step, in pinned host memory): one copy moves each set."""
 
     def __init__(self, w, layers, dev, pinned: bool):
         import torch
@@ -305,19 +322,29 @@ class LayerSet:
         from causal_gqa_flash_attention_gb300 import synthetic
         self.w = w
         self.host, self.devs, self.grads_host = [], [], []
+        self.host_flat, self.dev_flat, self.grads_flat, self.grads_host_flat = [], [], [], []
         ws = ne.alloc_workspace(w.B, w.T, w.Hq, w.Hkv, w.D, dev)
         for L in layers:
-            q, k, v, dO = synthetic.make_inputs(w, layer=L)
-            hq = [t.contiguous().pin_memory() if pinned else t.contiguous() for t in (q, k, v, dO)]
+            src = [t.contiguous() for t in synthetic.make_inputs(w, layer=L)]   # q, k, v, dO
+            shapes, dt = [t.shape for t in src], src[0].dtype
+            dflat, d = flat_views(shapes, dt, dev)
+            for x, t in zip(d, src):
+                x.copy_(t)
+            self.dev_flat.append(dflat)
             if pinned:
+                hflat, hq = flat_views(shapes, dt, "cpu", pinned=True)
+                for x, t in zip(hq, src):
+                    x.copy_(t)
                 self.host.append(hq)
-            d = [t.to(dev, non_blocking=False) for t in hq]
+                self.host_flat.append(hflat)
+                ghflat, gh = flat_views(shapes[:3], dt, "cpu", pinned=True)
+                self.grads_host.append(gh)
+                self.grads_host_flat.append(ghflat)
             o = torch.empty_like(d[0])
             lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
-            dq, dk, dv = torch.empty_like(d[0]), torch.empty_like(d[1]), torch.empty_like(d[2])
+            gflat, (dq, dk, dv) = flat_views(shapes[:3], dt, dev)
+            self.grads_flat.append(gflat)
             self.devs.append(dict(q=d[0], k=d[1], v=d[2], dO=d[3], o=o, lse=lse, ws=ws, dq=dq, dk=dk, dv=dv))
-        if pinned:
-            self.grads_host = [[torch.empty_like(t).pin_memory() for t in (h[0], h[1], h[2])] for h in self.host]
 
     def run_layer(self, b):
         """One layer's forward and backward: the training pair, whose forward also fills
@@ -452,9 +479,10 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     step = ls.step
 
-    # End-to-end step: every layer's inputs go host -> device on a copy stream, its
-    # forward and backward run on the compute stream, and its gradients go device -> host
-    # on a third stream, so the copies of one layer overlap the kernels of its neighbours.
+    # End-to-end step: every layer's inputs go host -> device on a copy stream (one copy:
+    # q, k, v, dO share an allocation), its forward and backward run on the compute
+    # stream, and its gradients go device -> host on a third stream (one copy), so the
+    # copies of one layer overlap the kernels of its neighbours.
     # Events keep each layer's buffers safe: an input is overwritten only after the
     # previous step's kernels of that layer consumed it, a gradient only after the previous
     # step's copy-out of it finished.
@@ -469,8 +497,7 @@ def run_ours(args, w):
         for i, b in enumerate(devs):
             with torch.cuda.stream(h2d_s):
                 h2d_s.wait_event(ev_comp[i])
-                for name, h in zip(("q", "k", "v", "dO"), host[i]):
-                    b[name].copy_(h, non_blocking=True)
+                ls.dev_flat[i].copy_(ls.host_flat[i], non_blocking=True)
                 ev_in[i].record(h2d_s)
             stream.wait_event(ev_in[i])
             stream.wait_event(ev_out[i])
@@ -478,8 +505,7 @@ def run_ours(args, w):
             ev_comp[i].record(stream)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(ev_comp[i])
-                for h, name in zip(grads_host[i], ("dq", "dk", "dv")):
-                    h.copy_(b[name], non_blocking=True)
+                ls.grads_host_flat[i].copy_(ls.grads_flat[i], non_blocking=True)
                 ev_out[i].record(d2h_s)
 
     # Clocks are sampled from the warm-up through the last extra measurement, so the
@@ -564,8 +590,8 @@ def run_ours(args, w):
     value = total_flops / (ms * 1e-3) / 1e12
     e2e_val = total_flops / (e2e_ms * 1e-3) / 1e12
     es = 2 if w.dtype == "bf16" else 4
-    h2d = sum(t.numel() * es for h in host for t in h)
-    d2h = sum(t.numel() * es for g in grads_host for t in g)
+    h2d = sum(f.numel() * es for f in ls.host_flat)
+    d2h = sum(f.numel() * es for f in ls.grads_host_flat)
 
     # The peak of the path's own dtype: bf16 for bf16 tensors, the TF32 rate measured
     # above for fp32 tensors (they run on TF32 tensor cores).
