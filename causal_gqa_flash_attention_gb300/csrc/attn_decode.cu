@@ -62,7 +62,9 @@ struct Row16<float> {
 };
 
 // Rotate N consecutive elements (N/2 adjacent pairs, the first pair index e0/2) of a row
-// at position t: (x0, x1) -> (x0 c - x1 s, x0 s + x1 c).
+// at position t: (x0, x1) -> (x0 c - x1 s, x0 s + x1 c), as packed f32x2 operations:
+// (x0, x0) (c, s) + (-x1, x1) (s, c).  The chunk kernel is bound by its instruction
+// stream, so its arithmetic runs two lanes of a float2 per instruction where it can.
 template <int N>
 __device__ __forceinline__ void rotate(float (&x)[N], const float2* __restrict__ rope, int t, int half, int e0) {
     const float4* tab = reinterpret_cast<const float4*>(rope + (size_t)t * half + e0 / 2);
@@ -70,10 +72,14 @@ __device__ __forceinline__ void rotate(float (&x)[N], const float2* __restrict__
     for (int i = 0; i < N / 4; ++i) {
         const float4 cs = __ldg(tab + i);   // (cos, sin) of pairs 2i and 2i+1 of this slice
         const float a0 = x[4 * i], a1 = x[4 * i + 1], b0 = x[4 * i + 2], b1 = x[4 * i + 3];
-        x[4 * i] = a0 * cs.x - a1 * cs.y;
-        x[4 * i + 1] = a0 * cs.y + a1 * cs.x;
-        x[4 * i + 2] = b0 * cs.z - b1 * cs.w;
-        x[4 * i + 3] = b0 * cs.w + b1 * cs.z;
+        const float2 ra = __ffma2_rn(make_float2(-a1, a1), make_float2(cs.y, cs.x),
+                                     __fmul2_rn(make_float2(a0, a0), make_float2(cs.x, cs.y)));
+        const float2 rb = __ffma2_rn(make_float2(-b1, b1), make_float2(cs.w, cs.z),
+                                     __fmul2_rn(make_float2(b0, b0), make_float2(cs.z, cs.w)));
+        x[4 * i] = ra.x;
+        x[4 * i + 1] = ra.y;
+        x[4 * i + 2] = rb.x;
+        x[4 * i + 3] = rb.y;
     }
 }
 
@@ -91,7 +97,7 @@ __device__ __forceinline__ void merge(float& m, float& l, float (&o)[N], float m
 }
 
 template <typename TIn, int D, int HPC>
-__global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, HPC <= 3 ? 4 : 3) attn_decode_kernel(DecodeArgs a) {
     constexpr int EPL = Row16<TIn>::N;    // elements per lane per row
     constexpr int LPK = D / EPL;          // lanes per key row
     constexpr int KPW = 32 / LPK;         // key rows per warp per step
@@ -170,10 +176,11 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
             rotate<EPL>(kf, a.rope, j < j1 ? j : 0, half, e0);
 #pragma unroll
             for (int h = 0; h < HPC; ++h) {
-                float acc = 0.f;
+                float2 acc = make_float2(0.f, 0.f);   // even and odd elements
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc = fmaf(qr[h][e], kf[e], acc);
-                s[u][h] = acc;
+                for (int e = 0; e < EPL; e += 2)
+                    acc = __ffma2_rn(make_float2(qr[h][e], qr[h][e + 1]), make_float2(kf[e], kf[e + 1]), acc);
+                s[u][h] = acc.x + acc.y;
             }
         }
 #pragma unroll
@@ -205,11 +212,13 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
             }
             l[h] = l[h] * c + psum;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                float acc = o[h][e] * c;
+            for (int e = 0; e < EPL; e += 2) {
+                float2 acc = __fmul2_rn(make_float2(o[h][e], o[h][e + 1]), make_float2(c, c));
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) acc = fmaf(p[u], vf[u][e], acc);
-                o[h][e] = acc;
+                for (int u = 0; u < kUnroll; ++u)
+                    acc = __ffma2_rn(make_float2(p[u], p[u]), make_float2(vf[u][e], vf[u][e + 1]), acc);
+                o[h][e] = acc.x;
+                o[h][e + 1] = acc.y;
             }
             m[h] = mx;
         }
