@@ -376,8 +376,8 @@ __global__ void __launch_bounds__(384, 1)
         };
         auto publish = [&](int it, float lv, float dv) {
             if (r < C::BQ) {
-                s_lse[it & 1][r] = lv;
-                s_delta[it & 1][r] = dv;
+                s_lse[it & 1][r] = -lv;     // negated: added by packed FMA / add
+                s_delta[it & 1][r] = -dv;
             }
             mbar_arrive(smem_u32(&bar_rows[it & 1]));
         };
@@ -401,18 +401,27 @@ __global__ void __launch_bounds__(384, 1)
             const bool tail = VL && q0 + C::BQ > len;          // queries past the length are padding
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 4) {
-                // Four queries' LSE and Delta per 16-byte read.
+                // Four queries' -LSE log2(e) and -Delta per 16-byte read; the exponent
+                // argument, dP - Delta and the product run as packed f32x2 pairs of queries.
                 const float4 l4 = *reinterpret_cast<const float4*>(&s_lse[sb][c0]);
                 const float4 d4 = *reinterpret_cast<const float4*>(&s_delta[sb][c0]);
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dlt[4] = {d4.x, d4.y, d4.z, d4.w};
+                const float2 nl[2] = {make_float2(l4.x, l4.y), make_float2(l4.z, l4.w)};
+                const float2 nd[2] = {make_float2(d4.x, d4.y), make_float2(d4.z, d4.w)};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < 4; e += 2) {
                     const int c = c0 + e;
-                    float p = ex2(fmaf(__uint_as_float(sr[c]), sl2, -lv[e]));
-                    if ((diag && kvpos > q0 + c) || (tail && q0 + c >= len)) p = 0.f;
-                    const float g = p * (__uint_as_float(dr[c]) - dlt[e]);
-                    sr[c] = f32_to_tf32_rna(p);
-                    dr[c] = f32_to_tf32_rna(g);
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                                make_float2(sl2, sl2), nl[e >> 1]);
+                    float p0 = ex2(x.x), p1 = ex2(x.y);
+                    if ((diag && kvpos > q0 + c) || (tail && q0 + c >= len)) p0 = 0.f;
+                    if ((diag && kvpos > q0 + c + 1) || (tail && q0 + c + 1 >= len)) p1 = 0.f;
+                    const float2 g = __fmul2_rn(make_float2(p0, p1),
+                                                __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
+                                                           nd[e >> 1]));
+                    sr[c] = f32_to_tf32_rna(p0);
+                    sr[c + 1] = f32_to_tf32_rna(p1);
+                    dr[c] = f32_to_tf32_rna(g.x);
+                    dr[c + 1] = f32_to_tf32_rna(g.y);
                 }
             }
             tmem_st32(lt + C::s_col(it), *reinterpret_cast<uint32_t(*)[32]>(sr));
