@@ -193,12 +193,16 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
 #pragma unroll
     for (int c = 0; c < C::BN; c += 32) {
         if constexpr (TF32) {
+            // Two scores per instruction, as in the bf16 branch.
             uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float p = ex2(fmaf(__uint_as_float(sr[c + e]), sl2, neg_m));
-                s8[e & 7] += p;
-                pk[e] = f32_to_tf32_rna(p);
+            for (int e = 0; e < 32; e += 2) {
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c + e]), __uint_as_float(sr[c + e + 1])),
+                                            make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+                const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                s2[(e >> 1) & 3] = __fadd2_rn(s2[(e >> 1) & 3], pp);
+                pk[e] = f32_to_tf32_rna(pp.x);
+                pk[e + 1] = f32_to_tf32_rna(pp.y);
             }
             tmem_st32(sc + c, pk);
         } else {
@@ -216,10 +220,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[64], int j, int t, i
             tmem_st16(sc + (c >> 1), pk);
         }
     }
-    if constexpr (!TF32) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) s8[2 * k] += s2[k].x + s2[k].y;
-    }
+    for (int k = 0; k < 4; ++k) s8[2 * k] += s2[k].x + s2[k].y;
     st.l = __fadd_rn(st.l, ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
     tmem_wait_st();
     tc_fence_before();
