@@ -72,6 +72,14 @@ def test_ragged_rows_and_dim_tail_head_dim_128_theta_500():
     check(3, 77, 200, 4, 1, 128, True, eps=1e-6, theta=500.0)
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv", [(3, 128, 3, 1), (1, 100, 4, 2)])
+def test_odd_row_blocks_and_column_tail(B, T, Hq, Hkv):
+    """An odd number of row blocks (3) and a single short one (100 rows), and N = 320
+    output features, so the last 256-column tile lies mostly past the rows of W' (TMA's
+    zero fill, nothing stored there)."""
+    check(B, T, 256, Hq, Hkv, 64, True)
+
+
 def test_output_feeds_the_attention_forward():
     """The unrotated outputs are what ne_attn_fwd takes: chained, they match the oracle's
     prologue followed by its attention."""
