@@ -8,6 +8,9 @@ count exact causal pairs: 14 * D * T(T+1)/2 * B * Hq (4 D forward, 10 D backward
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --decode     # the decode step over a KV cache instead: cache-read GB/s
 
+Beside the headline, the default line carries points measured outside its timed region:
+the long-sequence sweep (T 2048, 8192, 16384), the fused prologue and the decode step.
+
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the
 attention of independent sequences needs no exchange); the timed region is bracketed
 by a barrier and the max over ranks is reported.  `--impl reference` times the fp64
@@ -420,7 +423,7 @@ def prologue_point(dev, steps, peak, layers=16):
     """The fused RMSNorm -> QKV projection -> RoPE prologue at the GPU-pipeline shape
     (x [16, 512, 768] bf16, 12/4 heads of 64), one call per layer on distinct buffers:
     2 M N K FLOPs per call, M = 8192 tokens, N = 1280 features, K = 768 (the call includes
-    its small pass folding the gain into the weights)."""
+    its two small passes: the gain folded into the weights, each row's 1/rms)."""
     import torch
 
     import causal_gqa_flash_attention_gb300 as ne
@@ -433,8 +436,8 @@ def prologue_point(dev, steps, peak, layers=16):
                      torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=dev),
                      torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=dev)))
 
-    n_ws = int(ne.load().ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D))
-    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)      # W diag(gamma), rewritten by each call
+    n_ws = int(ne.load().ne_qkv_prologue_workspace_size(B, T, dim, Hq, Hkv, D))
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)      # W diag(gamma) and 1/rms, rewritten by each call
 
     def step():
         for x, g, wt, q, k, v in bufs:
@@ -450,6 +453,38 @@ def prologue_point(dev, steps, peak, layers=16):
     torch.cuda.empty_cache()
     return {"workload": f"RMSNorm->QKV->RoPE prologue B{B} T{T} dim{dim} Hq{Hq} Hkv{Hkv} D{D} bf16 x{layers} layers",
             "tflops": tf, "pct_of_peak": tf / peak, "us_per_call": st["median_ms"] * 1e3 / layers, **st}
+
+
+def decode_point(dev, steps, hbm_peak, layers=4):
+    """The decode step of `--decode` (B8, every sequence's cache 16384 positions, Hq12/Hkv4
+    D64 bf16, distinct 134 MB caches per layer), device-timed only, so that every default
+    run also measures the decode kernel: cache-read GB/s against the HBM copy peak."""
+    import torch
+
+    import causal_gqa_flash_attention_gb300 as ne
+    from causal_gqa_flash_attention_gb300 import synthetic
+    B, T, Hq, Hkv, D = 8, 16384, 12, 4, 64
+    bufs = []
+    for i in range(layers):
+        q, k, v, lens = synthetic.make_decode(B, T, Hq, Hkv, D, torch.bfloat16, seed=100 + i, lens=[T] * B)
+        bufs.append((q.to(dev), k.to(dev), v.to(dev), lens.to(dev), torch.empty_like(q, device=dev),
+                     torch.empty((B, Hq), dtype=torch.float32, device=dev)))
+    ws = torch.empty(max(ne.decode_workspace_size(B, T, Hq, Hkv, D), 256), dtype=torch.uint8, device=dev)
+
+    def step():
+        for q, k, v, lens, o, lse in bufs:
+            ne.attn_decode(q, k, v, lens, o=o, lse=lse, workspace=ws)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    st = dist_stats(step_times(step, steps, torch.cuda.current_stream(dev)))
+    per_layer = B * T * Hkv * D * 2 * 2 + 2 * B * Hq * D * 2 + B * Hq * 4
+    gbs = per_layer * layers / (st["median_ms"] * 1e-3) / 1e9
+    del bufs
+    torch.cuda.empty_cache()
+    return {"workload": f"decode B{B} T_max{T} Hq{Hq} Hkv{Hkv} D{D} bf16 x{layers} layers",
+            "gbs": gbs, "pct_of_hbm": gbs / hbm_peak, "us_per_layer": st["median_ms"] * 1e3 / layers, **st}
 
 
 def run_ours(args, w):
@@ -583,6 +618,7 @@ def run_ours(args, w):
             sweep[f"T{synthetic_T(wid)}"] = sweep_point(wid, dev, 10, peaks["bf16_tflops"])
     # The step before attention (not part of the headline step): the fused prologue.
     prologue = prologue_point(dev, 20, peaks["bf16_tflops"]) if not args.no_sweep and w.wid == 2 else None
+    decode = decode_point(dev, 20, peaks["hbm_gbs"]) if not args.no_sweep and w.wid == 2 else None
     clk = clocks.stop()
 
     flops_step = w.flops() * len(layers)
@@ -669,6 +705,7 @@ def run_ours(args, w):
                   "source": peaks["source"]},
         "sweep": sweep,
         "prologue": prologue,
+        "decode": decode,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": sum(v[1] for v in phases.values()),

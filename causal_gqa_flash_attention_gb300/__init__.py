@@ -76,7 +76,7 @@ def load(path: str | None = None):
         lib.ne_attn_bwd_varlen.argtypes = [vp] * 10 + [i] * 5 + [d, vp, sz, vp]
         lib.ne_attn_bwd_varlen_f32.argtypes = lib.ne_attn_bwd_varlen.argtypes
         lib.ne_qkv_prologue.argtypes = [vp] * 6 + [i] * 6 + [d, d, i, vp, sz, vp]
-        lib.ne_qkv_prologue_workspace_size.argtypes = [i] * 4
+        lib.ne_qkv_prologue_workspace_size.argtypes = [i] * 6
         lib.ne_qkv_prologue_workspace_size.restype = sz
         lib.ne_attn_fwd_train.argtypes = [vp] * 6 + [sz] + [i] * 5 + [d, vp]
         lib.ne_attn_fwd_train_f32.argtypes = lib.ne_attn_fwd_train.argtypes
@@ -283,7 +283,7 @@ def qkv_prologue(x, gamma, w, Hq: int, Hkv: int, D: int, eps: float = 1e-5, thet
     k = torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=x.device) if k is None else k
     v = torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=x.device) if v is None else v
     if workspace is None:
-        n = int(lib.ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D))
+        n = int(lib.ne_qkv_prologue_workspace_size(B, T, dim, Hq, Hkv, D))
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=x.device)
     _check(lib.ne_qkv_prologue(_ptr(x), _ptr(gamma), _ptr(w), _ptr(q), _ptr(k), _ptr(v), B, T, dim, Hq, Hkv, D,
                                float(eps), float(theta), 1 if rotate else 0, _ptr(workspace),

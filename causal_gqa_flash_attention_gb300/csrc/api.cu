@@ -683,9 +683,13 @@ ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* 
                             workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
-size_t ne_qkv_prologue_workspace_size(int dim, int Hq, int Hkv, int D) {
-    if (dim <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
+// W diag(gamma) (bf16), then 1/rms of every token row (fp32).
+static size_t prologue_weight_bytes(int dim, int Hq, int Hkv, int D) {
     return round_up((size_t)(Hq + 2 * Hkv) * D * dim * 2, 256);
+}
+size_t ne_qkv_prologue_workspace_size(int B, int T, int dim, int Hq, int Hkv, int D) {
+    if (B < 0 || T < 0 || dim <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
+    return prologue_weight_bytes(dim, Hq, Hkv, D) + round_up((size_t)B * T * 4, 256);
 }
 
 ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void* q, void* k, void* v, int B, int T,
@@ -711,9 +715,9 @@ ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void*
     if ((s = check_ptrs({x, gamma, w, q, k, v})) != NE_OK) return s;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(NE_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
-    if (workspace_bytes < ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D))
+    if (workspace_bytes < ne_qkv_prologue_workspace_size(B, T, dim, Hq, Hkv, D))
         return fail(NE_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes,
-                    ne_qkv_prologue_workspace_size(dim, Hq, Hkv, D));
+                    ne_qkv_prologue_workspace_size(B, T, dim, Hq, Hkv, D));
     if ((reinterpret_cast<uintptr_t>(gamma) & 15u) != 0 || (reinterpret_cast<uintptr_t>(w) & 15u) != 0)
         return fail(NE_ERR_INVALID_ARG, "gamma and w must be 16-byte aligned");
     int dev;
@@ -727,6 +731,10 @@ ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void*
     // The gain folded into the weights: W' = W diag(gamma) in the workspace.
     cudaError_t e = ne::launch_gain_weights(w, gamma, workspace, N, dim, st);
     if (e != cudaSuccess) return cuda_fail(e, "gain weights launch");
+    // 1/rms of every token row, after the weights in the workspace.
+    float* inv_rms = reinterpret_cast<float*>(static_cast<char*>(workspace) + prologue_weight_bytes(dim, Hq, Hkv, D));
+    e = ne::launch_rms_rows(x, inv_rms, (int)M, dim, (float)eps, st);
+    if (e != cudaSuccess) return cuda_fail(e, "row rms launch");
     if ((s = map_rows_bf16(&tw, workspace, N, dim, ne::prologue_tile_n())) != NE_OK) return s;
     ne::ProArgs a;
     a.q = q;
@@ -739,7 +747,7 @@ ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void*
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.D = D;
-    a.eps = (float)eps;
+    a.inv_rms = inv_rms;
     a.rotate = rotate;
     a.err = err;
     a.timeout_ns = timeout_ns();

@@ -111,12 +111,12 @@ struct BwdArgs {
 
 // RMSNorm -> QKV projection -> RoPE prologue (qkv_prologue.cu), bf16 tensors.
 struct ProArgs {
+    const float* inv_rms;    // [M] 1 / root-mean-square of each token row
     void* q;                 // [B,T,Hq,D]
     void* k;                 // [B,T,Hkv,D]
     void* v;                 // [B,T,Hkv,D]
     const float2* rope;      // [>= T, D/2] (cos, sin)
     int M, T, dim, Hq, Hkv, D;   // M = B * T token rows
-    float eps;
     int rotate;              // nonzero: RoPE on the query and key heads
     int* err;
     unsigned long long timeout_ns;
@@ -184,6 +184,8 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // (64 x prologue_tile_n()) boxes.
 int prologue_tile_n();
 cudaError_t launch_qkv_prologue(const CUtensorMap& tx, const CUtensorMap& tw, const ProArgs& a, cudaStream_t st);
+// inv_rms [M] = 1 / sqrt(mean of the squares of row m of x [M, dim] bf16 + eps); dim % 8 == 0.
+cudaError_t launch_rms_rows(const void* x, float* inv_rms, int M, int dim, float eps, cudaStream_t st);
 // wg [N, dim] = w [N, dim] times gamma [dim] along each row (bf16); dim % 8 == 0.
 cudaError_t launch_gain_weights(const void* w, const void* gamma, void* wg, long long N, int dim, cudaStream_t st);
 // Tile rows of the key/value tensor maps the forward kernel expects.

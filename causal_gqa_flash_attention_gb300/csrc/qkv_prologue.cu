@@ -6,18 +6,27 @@
 //   r_m = sqrt(mean_c x_mc^2 + eps),   y_m = W (x_m o gamma) / r_m
 // with W [(Hq + 2 Hkv) D, dim] (query heads, then key heads, then value heads).  Since
 // 1/r_m is one factor per output row, it is applied to the fp32 accumulator in the
-// epilogue; gamma is folded into the weights once per call (W' = W diag(gamma), a small
-// pass into the caller's workspace), so x goes from TMA straight to the MMA.
+// epilogue; gamma is folded into the weights once per call (W' = W diag(gamma)) and
+// 1/r_m is formed once per row, both by small passes into the caller's workspace before
+// the GEMM, so x goes from TMA straight to the MMA and the GEMM's ring has one reader.
 //
-// One CTA per 128-row x 256-column output tile; the dim (K) axis streams through an
-// NS-stage ring of 64-column chunks (x: 128 rows, W: 256 rows, 128 bytes each,
-// 128-byte-swizzled by TMA).  Warp roles (192 threads):
+// Persistent, one CTA per SM walking 128-row x 256-column output tiles; the dim (K) axis
+// streams through an NS-stage ring of 64-column chunks (x: 128 rows, W': 256 rows, 128
+// bytes each, 128-byte-swizzled by TMA) that only the MMAs read.  Warp roles (192
+// threads):
 //   warp 0      TMA producer.
-//   warp 1      TMEM owner (256 columns) and UMMA issuer: M128 N256 K16, 4 per chunk.
-//   warps 2-5   thread = token row = TMEM lane: per chunk, the row's sum of squares
-//               (read beside the MMA, which needs no wait for it); at the end the
-//               epilogue: acc / r_m, RoPE on query and key heads (position m mod T),
-//               bf16 stores.  A stage is free once both the MMAs and these warps read it.
+//   warp 1      TMEM owner (512 columns) and UMMA issuer: M128 N256 K16, 4 per chunk,
+//               into two accumulators (tile i in columns 256 (i % 2)).
+//   warps 2-5   epilogue, thread = token row = TMEM lane: acc / r_m, RoPE on query and
+//               key heads (position m mod T), bf16 stores; the tile's 1/r_m and (cos,
+//               sin) row are fetched one tile early.
+// An earlier version summed each row's squares inside this kernel, on four more warps
+// reading the ring's x chunks and releasing a stage after their loads.  Under load such
+// a warp at times read a stage already refilled with the chunk four ahead (per-chunk
+// checksums of the rows it read showed it), although its release followed its loads,
+// even with the release made to depend on the loaded data; any change to the warp's
+// timing hid it.  Each row block was also summed once per column tile (five times at
+// the GPU-pipeline shape); the row pass sums it once.
 // clock64 traces of the first version, which multiplied x by gamma in place between TMA
 // and MMA, showed that pass (~2.2K cycles a chunk on one warp per SM sub-partition) and
 // an epilogue that waited on a table load per chunk (~15K cycles) as the whole cost.
@@ -41,12 +50,12 @@ struct ProCfg {
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int NS = 4;
     static constexpr int SMEM = 1024 + NS * STAGE;
-    static constexpr int THREADS = 320;
+    static constexpr int THREADS = 192;
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(192, 1)
     qkv_prologue_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                         const ProArgs a) {
     using C = ProCfg;
@@ -57,9 +66,7 @@ __global__ void __launch_bounds__(320, 1)
 
     __shared__ __align__(8) uint64_t bar_full[C::NS], bar_empty[C::NS];
     __shared__ __align__(8) uint64_t bar_acc_full[2], bar_acc_empty[2];   // [accumulator]
-    __shared__ __align__(8) uint64_t bar_rn_full[2], bar_rn_empty[2];     // [1/rms slot]
     __shared__ __align__(8) uint64_t bar_final;
-    __shared__ float s_invr[2][C::BM];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -77,13 +84,11 @@ __global__ void __launch_bounds__(320, 1)
     if (tid == 0) {
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
-            mbar_init(smem_u32(&bar_empty[s]), 1 + 128);   // the MMA commit and the norm threads
+            mbar_init(smem_u32(&bar_empty[s]), 1);   // the chunk's MMAs have completed
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bar_acc_full[i]), 1);        // the tile's last MMA
             mbar_init(smem_u32(&bar_acc_empty[i]), 128);     // the epilogue threads
-            mbar_init(smem_u32(&bar_rn_full[i]), 128);       // the norm threads
-            mbar_init(smem_u32(&bar_rn_empty[i]), 128);      // the epilogue threads
         }
         mbar_init(smem_u32(&bar_final), 1);
         abort_flag = 0;
@@ -159,43 +164,6 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
         umma_commit_e(smem_u32(&bar_final));   // the teardown's: every MMA of this CTA
-    } else if (warp >= 6) {
-        // ------------------------------------------------------------ RMS norm of the x rows
-        // Thread r: token row r of the tile, read from every chunk beside the MMA (which
-        // needs no wait for it); 1/r_m goes to the epilogue through a double-buffered slot.
-        const int r = (warp - 6) * 32 + lane;
-        bool ok = true;
-        int g = 0;
-        for (int i = 0; ok && i < my_tiles; ++i) {
-            float2 ss2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};   // independent sums (past dim: TMA's zero fill)
-            for (int kc = 0; kc < nk; ++kc, ++g) {
-                const int s = g % C::NS;
-                if (!(ok = mbar_wait_warp(smem_u32(&bar_full[s]), (g / C::NS) & 1, w, SITE_PRO_FULL))) break;
-                const uint8_t* arow = st_a(s);
-                uint4 xv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) xv[u] = *reinterpret_cast<const uint4*>(arow + sw128_offset(r, u));
-                mbar_arrive(smem_u32(&bar_empty[s]));   // read: the stage may take the next chunk
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[e]));
-                        ss2[e] = __ffma2_rn(xf, xf, ss2[e]);
-                    }
-                }
-            }
-            if (!ok) break;
-            const float ss =
-                ((ss2[0].x + ss2[0].y) + (ss2[1].x + ss2[1].y)) + ((ss2[2].x + ss2[2].y) + (ss2[3].x + ss2[3].y));
-            const int rb = i & 1;
-            if (i >= 2 && !(ok = mbar_wait_warp(smem_u32(&bar_rn_empty[rb]), ((i >> 1) - 1) & 1, w, SITE_PRO_ACC)))
-                break;
-            s_invr[rb][r] = rsqrtf(ss / (float)a.dim + a.eps);
-            mbar_arrive(smem_u32(&bar_rn_full[rb]));
-        }
     } else {
         // ------------------------------------------------------------ epilogue
         // Thread r: token row r of the tile = TMEM lane (warps 2-5 cover the four lane
@@ -205,8 +173,10 @@ __global__ void __launch_bounds__(320, 1)
         const int r = quarter * 32 + lane;
         const uint32_t lt = tm + ((uint32_t)(quarter * 32) << 16);
         float4 tabr[D / 4];
+        float invr = 0.f;
         auto fetch_row = [&](int i) {
             const int m = tile_m0(i) + r;
+            invr = m < a.M ? __ldg(a.inv_rms + m) : 0.f;
             const float4* tr = reinterpret_cast<const float4*>(a.rope + (size_t)(m % a.T) * (D / 2));
 #pragma unroll
             for (int e = 0; e < D / 4; ++e)
@@ -217,9 +187,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; ok && i < my_tiles; ++i) {
             const int ab = i & 1;
             const int m = tile_m0(i) + r, n0 = tile_n0(i);
-            if (!(ok = mbar_wait_warp(smem_u32(&bar_rn_full[ab]), (i >> 1) & 1, w, SITE_PRO_ACC))) break;
-            const float inv_r = s_invr[ab][r];
-            mbar_arrive(smem_u32(&bar_rn_empty[ab]));
+            const float inv_r = invr;
             if (!(ok = mbar_wait_warp(smem_u32(&bar_acc_full[ab]), (i >> 1) & 1, w, SITE_PRO_ACC))) break;
             tc_fence_after();
             // Unrolled over the tile's chunks so each chunk's table pairs are registers
@@ -301,7 +269,42 @@ __global__ void __launch_bounds__(256) gain_weights_kernel(const __nv_bfloat16* 
     }
 }
 
+// inv_rms[m] = 1 / sqrt(mean_c x_mc^2 + eps): one warp per row, 16 bytes a lane at a time
+// (dim % 8 == 0), the lanes' sums combined by shuffles.
+__global__ void __launch_bounds__(256) rms_rows_kernel(const __nv_bfloat16* __restrict__ x, float* __restrict__ inv_rms,
+                                                       int M, int dim, float eps) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int lane = threadIdx.x & 31;
+    const int n16 = dim / 8;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int m = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; m < M; m += warps) {
+        const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)m * dim);
+        float2 ss2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        for (int c = lane; c < n16; c += 32) {
+            const uint4 v = __ldg(xr + c);
+            const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[e]));
+                ss2[e] = __ffma2_rn(xf, xf, ss2[e]);
+            }
+        }
+        float ss = ((ss2[0].x + ss2[0].y) + (ss2[1].x + ss2[1].y)) + ((ss2[2].x + ss2[2].y) + (ss2[3].x + ss2[3].y));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) inv_rms[m] = rsqrtf(ss / (float)dim + eps);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_rms_rows(const void* x, float* inv_rms, int M, int dim, float eps, cudaStream_t st) {
+    long long blocks = ((long long)M + 7) / 8;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    return launch_k(rms_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, static_cast<const __nv_bfloat16*>(x),
+                    inv_rms, M, dim, eps);
+}
 
 int prologue_tile_n() { return ProCfg::BN; }
 

@@ -250,16 +250,17 @@ ne_status ne_attn_decode_f32(const float* q, const float* k_cache, const float* 
  *   x     [B, T, dim] bf16 (in)          gamma [dim] bf16 (in)
  *   w     [(Hq + 2 Hkv) * D, dim] bf16, row-major (in: row n holds output feature n)
  *   q     [B, T, Hq, D] bf16 (out)       k, v  [B, T, Hkv, D] bf16 (out)
- *   workspace: caller-owned device scratch of ne_qkv_prologue_workspace_size() bytes,
- *              256-byte aligned; it receives W diag(gamma) (bf16) and is rewritten by
- *              every call.
+ *   workspace: caller-owned device scratch of ne_qkv_prologue_workspace_size(B, T, dim,
+ *              Hq, Hkv, D) bytes, 256-byte aligned; each call rewrites it with
+ *              W diag(gamma) (bf16) and the reciprocal root-mean-square of every token row
+ *              (fp32), formed by two small passes before the GEMM.
  * Arithmetic: bf16 tensor-core products with fp32 accumulation; the gain is folded into
  * the weights (W diag(gamma), rounded to bf16, formed on the device by each call), the
  * root-mean-square is fp32.  Supported: D in {32, 64, 128}, dim a multiple of 8,
  * Hq % Hkv == 0, B*T*dim and B*T*(Hq + 2 Hkv)*D below 2^31, eps >= 0.  Pointers 16-byte
  * aligned.  A call that needs a new or longer RoPE table builds it and synchronises
  * `stream` once (as the attention calls do). */
-size_t ne_qkv_prologue_workspace_size(int dim, int Hq, int Hkv, int D);
+size_t ne_qkv_prologue_workspace_size(int B, int T, int dim, int Hq, int Hkv, int D);
 ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void* q, void* k, void* v,
                           int B, int T, int dim, int Hq, int Hkv, int D, double eps,
                           double rope_theta, int rotate, void* workspace, size_t workspace_bytes,

@@ -132,6 +132,20 @@ def test_bf16_deterministic_dk_dv():
         assert np.array_equal(a[name], b[name]), name
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_gpu_pipeline_batch_repeated_runs_identical(dtype):
+    """The GPU-pipeline batch (B16 T512 Hq12 Hkv4 D64): the forward's CTAs walk several
+    work units each and the backward's key loops run over every query tile of a head
+    group.  O, LSE, dK and dV come out bit-identical over three runs (dQ is summed by
+    reduce-adds in whatever order they land and is not compared); a difference between
+    runs is a race, whatever its size."""
+    q, k, v, dO = synthetic.make_custom(16, 512, 12, 4, 64, dtype, seed=21)
+    runs = [run_gpu(q, k, v, dO) for _ in range(3)]
+    for r in runs[1:]:
+        for name in ("o", "lse", "dk", "dv"):
+            assert np.array_equal(runs[0][name], r[name]), (name, int((runs[0][name] != r[name]).sum()))
+
+
 @pytest.mark.parametrize("B,T,Hq,Hkv,D,dtype", [
     (8, 64, 64, 8, 64, torch.bfloat16),     # 512 one-tile units: S runs across several units
     (4, 320, 48, 8, 64, torch.bfloat16),    # 384 units of 8 and 2 tiles, ragged second unit

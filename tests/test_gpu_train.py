@@ -104,6 +104,17 @@ def test_train_pair_equals_regular_pair_at_the_gpu_pipeline_shape():
         assert rel(f64(a), f64(b)) <= 1e-3
 
 
+def test_train_pair_repeated_runs_identical():
+    """The bench's path at its shape (B16 T512 Hq12 Hkv4 D64 bf16): O, LSE, dK and dV are
+    bit-identical over three runs of the training pair (dQ, summed by reduce-adds in
+    whatever order they land, is not compared)."""
+    q, k, v, dO = (t.cuda() for t in synthetic.make_custom(16, 512, 12, 4, 64, torch.bfloat16, seed=22))
+    runs = [train_pair(q, k, v, dO, poison=False) for _ in range(3)]
+    for r in runs[1:]:
+        for i, name in ((0, "o"), (1, "lse"), (3, "dk"), (4, "dv")):
+            assert torch.equal(runs[0][i], r[i]), (name, int((runs[0][i] != r[i]).sum()))
+
+
 def test_train_forward_fills_the_workspace_for_the_backward():
     """The stored R Q equals the preprocess pass's, and the dQ accumulator is zero."""
     B, T, Hq, Hkv, D = 2, 300, 4, 2, 64

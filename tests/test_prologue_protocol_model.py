@@ -2,10 +2,9 @@
 (csrc/qkv_prologue.cu), run on the CPU for every tile and chunk count a CTA can get.
 
 Roles: the TMA producer (one ring over every chunk of every tile of the CTA), the UMMA
-issuer (two TMEM accumulators, tile i in accumulator i % 2), the norm warps (sum of
-squares of each chunk's x rows, 1/rms into a double-buffered slot) and the epilogue warps
-(wait for the slot and the accumulator, free both).  A stage is freed by the MMA commit
-and the norm threads together.  Each role is a coroutine running its waits and arrivals
+issuer (two TMEM accumulators, tile i in accumulator i % 2) and the epilogue warps (wait
+for the accumulator, free it).  A stage is freed by the MMA commit alone; each row's
+1/rms comes from a pass before the kernel.  Each role is a coroutine running its waits and arrivals
 (a group of threads arrives as one; MMAs and copies complete at once); a run fails on a
 deadlock, on parity aliasing, or on an arrival that lands in another phase, as in the
 other protocol models.  Kept in step with the kernel by hand.
@@ -42,11 +41,9 @@ def simulate(n_tiles, nk, rng, epilogue_frees_acc=True):
         return bars.setdefault(name, Bar(name, count))
 
     full = [bar(f"full{s}", 1) for s in range(NS)]
-    empty = [bar(f"empty{s}", 2) for s in range(NS)]             # MMA commit + norm threads
+    empty = [bar(f"empty{s}", 1) for s in range(NS)]             # the MMA commit
     acc_full = [bar(f"acc_full{i}", 1) for i in range(2)]
     acc_empty = [bar(f"acc_empty{i}", 1) for i in range(2)]
-    rn_full = [bar(f"rn_full{i}", 1) for i in range(2)]
-    rn_empty = [bar(f"rn_empty{i}", 1) for i in range(2)]
 
     def producer():
         for g in range(n_tiles * nk):
@@ -69,29 +66,14 @@ def simulate(n_tiles, nk, rng, epilogue_frees_acc=True):
                     acc_full[ab].arrive(i >> 1)
                 g += 1
 
-    def norm():
-        g = 0
-        for i in range(n_tiles):
-            for kc in range(nk):
-                s = g % NS
-                yield full[s], g // NS, f"norm: chunk {g}"
-                empty[s].arrive(g // NS)
-                g += 1
-            rb = i & 1
-            if i >= 2:
-                yield rn_empty[rb], (i >> 1) - 1, f"norm: 1/rms slot {rb} read (tile {i - 2})"
-            rn_full[rb].arrive(i >> 1)
-
     def epilogue():
         for i in range(n_tiles):
             ab = i & 1
-            yield rn_full[ab], i >> 1, f"epilogue: 1/rms of tile {i}"
-            rn_empty[ab].arrive(i >> 1)
             yield acc_full[ab], i >> 1, f"epilogue: accumulator of tile {i}"
             if epilogue_frees_acc:
                 acc_empty[ab].arrive(i >> 1)
 
-    roles = {"producer": producer(), "issuer": issuer(), "norm": norm(), "epilogue": epilogue()}
+    roles = {"producer": producer(), "issuer": issuer(), "epilogue": epilogue()}
     pending = {}
     for name in list(roles):
         try:
