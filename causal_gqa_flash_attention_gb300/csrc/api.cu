@@ -728,13 +728,11 @@ ne_status ne_qkv_prologue(const void* x, const void* gamma, const void* w, void*
     if ((s = rope_cache(dev, T, D, rope_theta, st, &rope)) != NE_OK) return s;
     CUtensorMap tx, tw;
     if ((s = map_rows_bf16(&tx, x, M, dim, 128)) != NE_OK) return s;
-    // The gain folded into the weights: W' = W diag(gamma) in the workspace.
-    cudaError_t e = ne::launch_gain_weights(w, gamma, workspace, N, dim, st);
-    if (e != cudaSuccess) return cuda_fail(e, "gain weights launch");
-    // 1/rms of every token row, after the weights in the workspace.
+    // The gain folded into the weights, W' = W diag(gamma), and the 1/rms of every token
+    // row after them in the workspace.
     float* inv_rms = reinterpret_cast<float*>(static_cast<char*>(workspace) + prologue_weight_bytes(dim, Hq, Hkv, D));
-    e = ne::launch_rms_rows(x, inv_rms, (int)M, dim, (float)eps, st);
-    if (e != cudaSuccess) return cuda_fail(e, "row rms launch");
+    cudaError_t e = ne::launch_prologue_prep(w, gamma, workspace, N, x, inv_rms, (int)M, dim, (float)eps, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prologue prep launch");
     if ((s = map_rows_bf16(&tw, workspace, N, dim, ne::prologue_tile_n())) != NE_OK) return s;
     ne::ProArgs a;
     a.q = q;

@@ -184,10 +184,11 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // (64 x prologue_tile_n()) boxes.
 int prologue_tile_n();
 cudaError_t launch_qkv_prologue(const CUtensorMap& tx, const CUtensorMap& tw, const ProArgs& a, cudaStream_t st);
-// inv_rms [M] = 1 / sqrt(mean of the squares of row m of x [M, dim] bf16 + eps); dim % 8 == 0.
-cudaError_t launch_rms_rows(const void* x, float* inv_rms, int M, int dim, float eps, cudaStream_t st);
-// wg [N, dim] = w [N, dim] times gamma [dim] along each row (bf16); dim % 8 == 0.
-cudaError_t launch_gain_weights(const void* w, const void* gamma, void* wg, long long N, int dim, cudaStream_t st);
+// The pass before the prologue GEMM: wg [N, dim] = w [N, dim] times gamma [dim] along
+// each row (bf16), and inv_rms [M] = 1 / sqrt(mean of the squares of row m of x [M, dim]
+// bf16 + eps); dim % 8 == 0.
+cudaError_t launch_prologue_prep(const void* w, const void* gamma, void* wg, long long N, const void* x,
+                                 float* inv_rms, int M, int dim, float eps, cudaStream_t st);
 // Tile rows of the key/value tensor maps the forward kernel expects.
 int fwd_kv_box_rows(bool tf32, int D);
 // Launchers: return cudaSuccess or the launch error.

@@ -7,7 +7,7 @@
 // with W [(Hq + 2 Hkv) D, dim] (query heads, then key heads, then value heads).  Since
 // 1/r_m is one factor per output row, it is applied to the fp32 accumulator in the
 // epilogue; gamma is folded into the weights once per call (W' = W diag(gamma)) and
-// 1/r_m is formed once per row, both by small passes into the caller's workspace before
+// 1/r_m is formed once per row, both by a small pass into the caller's workspace before
 // the GEMM, so x goes from TMA straight to the MMA and the GEMM's ring has one reader.
 //
 // Persistent, one CTA per SM walking 128-row x 256-column output tiles; the dim (K) axis
@@ -245,13 +245,18 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-// W' = W diag(gamma): row n, column c of the projection times the gain of input column c,
-// rounded to bf16; 8 elements (16 bytes) per thread step.
-__global__ void __launch_bounds__(256) gain_weights_kernel(const __nv_bfloat16* __restrict__ w,
-                                                           const __nv_bfloat16* __restrict__ gamma,
-                                                           __nv_bfloat16* __restrict__ wg, long long n8, int dim8) {
+// The two passes before the GEMM, in one launch: W' = W diag(gamma) (row n, column c of
+// the projection times the gain of input column c, rounded to bf16; 8 elements, 16 bytes,
+// per thread step), then inv_rms[m] = 1 / sqrt(mean_c x_mc^2 + eps) (one warp per row,
+// 16 bytes a lane at a time, the lanes' sums combined by shuffles; dim % 8 == 0).
+__global__ void __launch_bounds__(256) prologue_prep_kernel(const __nv_bfloat16* __restrict__ w,
+                                                            const __nv_bfloat16* __restrict__ gamma,
+                                                            __nv_bfloat16* __restrict__ wg, long long n8,
+                                                            const __nv_bfloat16* __restrict__ x,
+                                                            float* __restrict__ inv_rms, int M, int dim, float eps) {
     griddep_launch_dependents();
     griddep_wait();
+    const int dim8 = dim / 8;
     const uint4* w4 = reinterpret_cast<const uint4*>(w);
     const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
     uint4* o4 = reinterpret_cast<uint4*>(wg);
@@ -267,21 +272,12 @@ __global__ void __launch_bounds__(256) gain_weights_kernel(const __nv_bfloat16* 
         }
         o4[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-}
-
-// inv_rms[m] = 1 / sqrt(mean_c x_mc^2 + eps): one warp per row, 16 bytes a lane at a time
-// (dim % 8 == 0), the lanes' sums combined by shuffles.
-__global__ void __launch_bounds__(256) rms_rows_kernel(const __nv_bfloat16* __restrict__ x, float* __restrict__ inv_rms,
-                                                       int M, int dim, float eps) {
-    griddep_launch_dependents();
-    griddep_wait();
     const int lane = threadIdx.x & 31;
-    const int n16 = dim / 8;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int m = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; m < M; m += warps) {
         const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)m * dim);
         float2 ss2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        for (int c = lane; c < n16; c += 32) {
+        for (int c = lane; c < dim8; c += 32) {
             const uint4 v = __ldg(xr + c);
             const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -299,22 +295,19 @@ __global__ void __launch_bounds__(256) rms_rows_kernel(const __nv_bfloat16* __re
 
 }  // namespace
 
-cudaError_t launch_rms_rows(const void* x, float* inv_rms, int M, int dim, float eps, cudaStream_t st) {
-    long long blocks = ((long long)M + 7) / 8;
-    if (blocks > 152 * 8) blocks = 152 * 8;
-    return launch_k(rms_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, static_cast<const __nv_bfloat16*>(x),
-                    inv_rms, M, dim, eps);
-}
-
 int prologue_tile_n() { return ProCfg::BN; }
 
-cudaError_t launch_gain_weights(const void* w, const void* gamma, void* wg, long long N, int dim, cudaStream_t st) {
-    const long long n8 = N * dim / 8;
-    long long blocks = (n8 + 255) / 256;
-    if (blocks > 152 * 4) blocks = 152 * 4;
-    return launch_k(gain_weights_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+cudaError_t launch_prologue_prep(const void* w, const void* gamma, void* wg, long long N, const void* x,
+                                 float* inv_rms, int M, int dim, float eps, cudaStream_t st) {
+    // Enough threads for the rows (a warp each, eight per block), at most eight blocks
+    // per SM; the weights are walked grid-stride.
+    long long blocks = ((long long)M + 7) / 8;
+    if (blocks < (N * dim / 8 + 255) / 256) blocks = (N * dim / 8 + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    return launch_k(prologue_prep_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
                     static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(gamma),
-                    static_cast<__nv_bfloat16*>(wg), n8, dim / 8);
+                    static_cast<__nv_bfloat16*>(wg), N * dim / 8, static_cast<const __nv_bfloat16*>(x), inv_rms, M,
+                    dim, eps);
 }
 
 cudaError_t launch_qkv_prologue(const CUtensorMap& tx, const CUtensorMap& tw, const ProArgs& a, cudaStream_t st) {
