@@ -132,14 +132,19 @@ def test_bf16_deterministic_dk_dv():
         assert np.array_equal(a[name], b[name]), name
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_gpu_pipeline_batch_repeated_runs_identical(dtype):
-    """The GPU-pipeline batch (B16 T512 Hq12 Hkv4 D64): the forward's CTAs walk several
-    work units each and the backward's key loops run over every query tile of a head
-    group.  O, LSE, dK and dV come out bit-identical over three runs (dQ is summed by
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,dtype", [
+    (16, 512, 12, 4, 64, torch.bfloat16),
+    (16, 512, 12, 4, 64, torch.float32),
+    (8, 1024, 16, 4, 128, torch.bfloat16),   # head_dim 128: one Q/dO stage, dQ' staged in chunks
+    (4, 2048, 12, 4, 64, torch.float32),     # TF32 backward: stages freed by the transposes' reads
+])
+def test_repeated_runs_identical(B, T, Hq, Hkv, D, dtype):
+    """The GPU-pipeline batch (B16 T512 Hq12 Hkv4 D64) and longer or wider cases: the
+    forward's CTAs walk several work units each and the backward's key loops run over
+    every query tile of a head group.  O, LSE, dK and dV come out bit-identical over three runs (dQ is summed by
     reduce-adds in whatever order they land and is not compared); a difference between
     runs is a race, whatever its size."""
-    q, k, v, dO = synthetic.make_custom(16, 512, 12, 4, 64, dtype, seed=21)
+    q, k, v, dO = synthetic.make_custom(B, T, Hq, Hkv, D, dtype, seed=21)
     runs = [run_gpu(q, k, v, dO) for _ in range(3)]
     for r in runs[1:]:
         for name in ("o", "lse", "dk", "dv"):
