@@ -1,10 +1,13 @@
 """GPU parity of the fused RMSNorm -> QKV projection -> RoPE prologue (ne_qkv_prologue)
 against the fp64 oracle (oracle.qkv_prologue, pinned in test_oracle.py).
 
-Bound: relative Frobenius error <= 5e-3 per output (q, k, v), the bound of the bf16
-attention outputs: the products are bf16 with fp32 accumulation, W diag(gamma) (the
-gain folded into the weights) and the outputs are rounded to bf16 (about 2^-9 relative
-each).
+Bound: relative Frobenius error <= 3e-3 per output (q, k, v).  Two roundings to bf16
+(8 significant bits) set the floor: W diag(gamma) (the gain folded into the weights) and
+the output; the products accumulate in fp32 and 1/rms is fp32.  Each rounding adds a
+relative error of about 2^-9 at most per element and an RMS a little over half of that,
+so together about 1.6e-3 to 2.5e-3; every case here measures 2.3e-3 to 2.4e-3.  A wrong
+1/rms on a few percent of the rows (an error of the size a race in the kernel once made)
+lifts that to 3.5e-3 or more, which the earlier bound of 5e-3 let through.
 """
 import numpy as np
 import pytest
@@ -15,7 +18,7 @@ from causal_gqa_flash_attention_gb300 import _build, synthetic
 
 pytestmark = pytest.mark.gpu
 
-TOL = 5e-3
+TOL = 3e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
