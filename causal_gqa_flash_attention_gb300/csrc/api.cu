@@ -391,7 +391,7 @@ ne_status attn_bwd_impl(bool f32, const void* q, const void* k, const void* v, c
     if ((s = map_bthd(&tdo, dO, f32, B, T, Hq, D, q_rows)) != NE_OK) return s;
     std::memset(&tdq, 0, sizeof(tdq));
     if (!f32 && (s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
-    ne::BwdArgs a;
+    ne::BwdArgs a = {};
     a.lse = lse;
     a.delta = delta;
     a.dq_acc = dq_acc;
@@ -896,7 +896,7 @@ ne_status ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
     if ((s = map_bthd(&tdo, dO, false, B, T, Hq, D, q_rows)) != NE_OK) return s;
     std::memset(&tdq, 0, sizeof(tdq));
     if ((s = map_bthd(&tdq, dq_acc, true, B, T, Hq, D, 128)) != NE_OK) return s;
-    ne::BwdArgs a;
+    ne::BwdArgs a = {};
     a.lse = lse;
     a.delta = delta;
     a.dq_acc = dq_acc;

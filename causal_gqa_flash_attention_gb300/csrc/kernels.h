@@ -107,6 +107,7 @@ struct BwdArgs {
     unsigned long long timeout_ns;
     const int* seq_lens;     // [B] or null: padding queries and keys get zero gradients
     int dr;                  // the tensors' head_dim (bf16 32 runs the 64-wide kernel, zero-padded)
+    int group_major;         // set by the launcher: CTA order (key tile fastest) of attn_bwd_d64_kernel
 };
 
 // RMSNorm -> QKV projection -> RoPE prologue (qkv_prologue.cu), bf16 tensors.
