@@ -178,11 +178,13 @@ __global__ void __launch_bounds__(512, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Grid order: (kv head, batch row) fastest, so the first CTAs to start are every
     // group's first key tiles, the heaviest; or, when the fp32 dQ' accumulator is larger
-    // than about a third of the L2 and a group has at most 32 key tiles, key tile
-    // fastest, so the CTAs running together add into the accumulators of a few groups and
-    // their reduce-adds stay in L2 (B32 T2048: 816 -> 741 us).  With more key tiles per
-    // group that order measured slower (T8192 +2%, T16384 +1.4%): the heaviest tiles of
-    // the last groups start late, and the CTAs running together all add into one group.
+    // than about a third of the L2 and a group has at most 16 key tiles, key tile
+    // fastest, so the CTAs running together add into the accumulators of several groups
+    // and their reduce-adds stay in L2 (B32 T2048: 816 -> 741 us; B128 T512: 325 -> 299).
+    // With 64 and 128 key tiles per group that order measured slower (T8192 +2%, T16384
+    // +1.4%): the CTAs running together then all add into one or two groups, and the
+    // heaviest tiles of the last groups start late.  32 (T4096) is not measured and keeps
+    // the heaviest-first order.
     const int hkv = a.group_major ? (int)blockIdx.y : (int)blockIdx.x;
     const int b = a.group_major ? (int)blockIdx.z : (int)blockIdx.y;
     const int j = a.group_major ? (int)blockIdx.x : (int)blockIdx.z;
@@ -590,7 +592,7 @@ cudaError_t launch_bwd_d64(int B, const CUtensorMap& tq, const CUtensorMap& tk, 
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Bwd64::SMEM);
     if (e != cudaSuccess) return e;
     BwdArgs ag = a;
-    ag.group_major = (double)B * a.T * a.Hq * Bwd64::D * 4 > 48e6 && a.n_kvt <= 32 ? 1 : 0;
+    ag.group_major = (double)B * a.T * a.Hq * Bwd64::D * 4 > 48e6 && a.n_kvt <= 16 ? 1 : 0;
     const dim3 grid = ag.group_major ? dim3(a.n_kvt, a.Hkv, B) : dim3(a.Hkv, B, a.n_kvt);
     return launch_k(kfn, grid, dim3(Bwd64::THREADS), Bwd64::SMEM, st, tq, tk, tv, tdo, tdq, ag);
 }
